@@ -1,0 +1,333 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test pins one part of the oracle to a hand-worked example (the golden
+fixtures), to a closed form or invariant of the definition, to a special case
+that reduces to an independent library routine (numpy's binary16 conversion,
+numpy's rint, numpy's int64 matmul), or to brute force on tiny inputs.
+The definition pinned is the Cider README's "Quantization" table (symmetric
+per-token INT8 activations, symmetric INT8 / INT4 weights, INT32
+accumulation, C_fp16 = C_int32 * s_act * s_weight).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(json.loads(line))
+    return rows
+
+
+# --------------------------------------------------------------------------
+# binary16 conversions (pinned to numpy's independent implementation)
+# --------------------------------------------------------------------------
+
+def test_half_to_float_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.half_to_float(bits)
+    ref = bits.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_float_to_half_matches_numpy():
+    rng = np.random.default_rng(0)
+    finite = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    finite = finite[np.isfinite(finite)].astype(np.float32)
+    # midpoints between consecutive binary16 values exercise ties-to-even
+    pos = np.sort(finite[finite >= 0])
+    mids = ((pos[1:].astype(np.float64) + pos[:-1]) / 2).astype(np.float32)
+    cases = [
+        finite, mids, -mids,
+        np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(0)),
+        (rng.standard_normal(200000) * 10.0 ** rng.uniform(-9, 5, 200000)).astype(np.float32),
+        np.array([65504, 65519.996, 65520, 65536, 1e9, 2 ** -25, 3 * 2 ** -26,
+                  2 ** -24, 2 ** -14, 2 ** -14 - 2 ** -25, 0.0, -0.0], np.float32),
+    ]
+    for c in cases:
+        ours = oracle.float_to_half(c)
+        ref = c.astype(np.float16).view(np.uint16)
+        assert np.array_equal(ours, ref)
+
+
+# --------------------------------------------------------------------------
+# quantization
+# --------------------------------------------------------------------------
+
+def test_quant_hand_examples():
+    for ex in _golden("quant_hand_examples.txt"):
+        v = np.array([ex["values"]], np.float16)
+        if ex["kind"] == "int8":
+            q, s = oracle.quantize_act(v)
+            assert q[0].tolist() == ex["codes"]
+            assert float(s[0]) == ex["scale"]
+            wq, sw = oracle.quantize_weight_int8(v, 0)
+            assert wq[0].tolist() == ex["codes"] and float(sw[0]) == ex["scale"]
+        else:
+            wp, sw = oracle.pack_weight_int4(v, 0)
+            assert wp[0].tolist() == ex["bytes"]
+            assert float(sw[0]) == ex["scale"]
+            assert oracle.unpack_int4(wp, v.shape[1])[0].tolist() == ex["codes"]
+            nib = [(b >> (4 * (i % 2))) & 0xF for i, b in
+                   enumerate(np.repeat(wp[0], 2).tolist())]
+            assert nib == ex["nibbles"]
+
+
+def test_quant_unit_scale_is_rint():
+    """absmax 127 gives scale exactly 1, where the code must be the textbook
+    round-half-even of x (numpy.rint)."""
+    rng = np.random.default_rng(1)
+    x = (rng.uniform(-127, 127, (64, 300)) * 4).round() / 4  # quarter steps: many ties
+    x[:, 7] = 127.0
+    x[::2, 7] = -127.0
+    x = x.astype(np.float16)
+    q, s = oracle.quantize_act(x)
+    assert np.all(s == 1.0)
+    assert np.array_equal(q, np.rint(x.astype(np.float64)).astype(np.int8))
+
+
+def test_quant_power_of_two_scales():
+    """absmax 127 * 2^j gives scale 2^j exactly, so code = rint(x / 2^j) with
+    an exact division; also pins the group indexing of weight quantization."""
+    rng = np.random.default_rng(2)
+    N, K, gs = 6, 256, 64
+    G = K // gs
+    j = rng.integers(-6, 4, (N, G))
+    base = (rng.uniform(-127, 127, (N, K)) * 2).round() / 2
+    w = np.empty((N, K))
+    for n in range(N):
+        for g in range(G):
+            blk = base[n, g * gs:(g + 1) * gs].copy()
+            blk[(n + g) % gs] = 127.0 if (n + g) % 2 else -127.0
+            w[n, g * gs:(g + 1) * gs] = blk * 2.0 ** j[n, g]
+    w16 = w.astype(np.float16)
+    assert np.array_equal(w16.astype(np.float64), w)  # all exact in fp16
+    wq, s = oracle.quantize_weight_int8(w16, gs)
+    assert np.array_equal(s, (2.0 ** j).astype(np.float32))
+    expect = np.rint(w / np.repeat(2.0 ** j, gs, axis=1)).astype(np.int8)
+    assert np.array_equal(wq, expect)
+    # per-channel on the same rows: one scale per row = max of its groups
+    wq_pc, s_pc = oracle.quantize_weight_int8(w16, 0)
+    assert np.array_equal(s_pc, (2.0 ** j.max(axis=1)).astype(np.float32))
+
+
+def test_quant_invariants_random():
+    """Odd symmetry, the absmax element maps to +-127, the range is
+    [-127, 127], and |x - q*s| <= s * (1/2 + 127 * 2^-24) (rounding of the
+    quotient plus the final round to an integer)."""
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((50, 777)) * 10.0 ** rng.uniform(-4, 4, (50, 1))).astype(np.float16)
+    x[3] = 0
+    q, s = oracle.quantize_act(x)
+    qn, sn = oracle.quantize_act(-x)
+    assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+    assert q.min() >= -127 and q.max() <= 127
+    assert s[3] == 0 and not q[3].any()
+    xf = x.astype(np.float64)
+    amax = np.abs(xf).max(axis=1)
+    nz = amax > 0
+    arg = np.abs(xf).argmax(axis=1)
+    assert np.all(np.abs(q[np.arange(50), arg])[nz] == 127)
+    assert np.array_equal(s[nz], (amax[nz].astype(np.float32) / np.float32(127)))
+    err = np.abs(xf - q * s[:, None].astype(np.float64))
+    bound = s[:, None].astype(np.float64) * (0.5 + 127 * 2.0 ** -24)
+    assert np.all(err <= bound)
+
+
+def test_int4_invariants():
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal((9, 256)) * 0.02).astype(np.float16)
+    for gs in (0, 128, 64):
+        wp, s = oracle.pack_weight_int4(w, gs)
+        codes = oracle.unpack_int4(wp, 256)
+        assert codes.min() >= -7 and codes.max() <= 7
+        lo, hi = wp & 0xF, wp >> 4
+        assert lo.min() >= 1 and hi.min() >= 1 and lo.max() <= 15 and hi.max() <= 15
+        s2 = s.reshape(9, -1)
+        gsz = 256 if gs == 0 else gs
+        err = np.abs(w.astype(np.float64) - codes * np.repeat(s2, gsz, axis=1))
+        assert np.all(err <= np.repeat(s2, gsz, axis=1) * (0.5 + 7 * 2.0 ** -24))
+    # nibble 0 (never written by the quantizer) decodes to -8
+    assert oracle.unpack_int4(np.array([[0x80]], np.uint8), 2)[0].tolist() == [-8, 0]
+
+
+# --------------------------------------------------------------------------
+# INT32 products (brute force / numpy int64)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 16), (3, 5, 64), (17, 33, 256), (33, 9, 128)])
+def test_gemm_s32_brute_force(M, N, K):
+    rng = np.random.default_rng(M * 1000 + N)
+    q = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    w = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    acc = oracle.gemm_s32(q, w, 0)
+    brute = np.zeros((M, N), np.int64)
+    for m in range(M):
+        for n in range(N):
+            brute[m, n] = sum(int(q[m, k]) * int(w[n, k]) for k in range(K))
+    assert np.array_equal(acc, brute)
+    for gs in (16, 64):
+        if K % gs:
+            continue
+        part = oracle.gemm_s32(q, w, gs)
+        ref = np.einsum("mgk,ngk->mng", q.reshape(M, -1, gs).astype(np.int64),
+                        w.reshape(N, -1, gs).astype(np.int64))
+        assert np.array_equal(part, ref)
+        assert np.array_equal(part.sum(axis=2), acc)
+
+
+def test_gemm_s32_worst_case_no_overflow():
+    K = 12288
+    q = np.full((2, K), 127, np.int8)
+    q[1] = -127
+    w = np.full((2, K), 127, np.int8)
+    acc = oracle.gemm_s32(q, w, 0)
+    assert acc.tolist() == [[127 * 127 * K] * 2, [-127 * 127 * K] * 2]
+
+
+def test_gemm_identity_weights():
+    """wq = 127 * I (a slice): acc = 127 * q."""
+    rng = np.random.default_rng(5)
+    q = rng.integers(-127, 128, (7, 64), dtype=np.int8)
+    w = np.zeros((32, 64), np.int8)
+    w[np.arange(32), np.arange(32)] = 127
+    assert np.array_equal(oracle.gemm_s32(q, w, 0), 127 * q[:, :32].astype(np.int32))
+
+
+# --------------------------------------------------------------------------
+# dequant epilogues and the whole layer
+# --------------------------------------------------------------------------
+
+def test_epilogue_hand_examples():
+    for ex in _golden("epilogue_hand_examples.txt"):
+        x = np.array([ex["x"]], np.float16)
+        w = np.array([ex["w"]], np.float16)
+        gs = ex["group_size"]
+        q, _ = oracle.quantize_act(x)
+        wq, sw = oracle.quantize_weight_int8(w, gs)
+        part = oracle.gemm_s32(q, wq, gs)
+        assert part.reshape(-1).tolist() == ex["partials"]
+        y = oracle.w8a8_linear(x, wq, sw, gs)
+        expect = np.float16(np.inf) if ex["y"] == "inf" else np.float16(ex["y"])
+        assert y[0, 0] == expect
+
+
+def test_epilogue_pc_unit_scales_is_fp16_of_acc():
+    """s_act = s_w = 1: y = binary16 rounding of the integer accumulator,
+    which numpy's float64 -> float16 conversion gives independently."""
+    rng = np.random.default_rng(6)
+    for acc in rng.integers(-(2 ** 31) + 1, 2 ** 31 - 1, 4000).tolist() + [0, 1, -1, 2049, 16129, 65519, 65520]:
+        bits = oracle.epilogue_pc(acc, 1.0, 1.0)
+        # (float)acc first rounds to binary32, then to binary16
+        ref = np.float16(np.float32(acc)).view(np.uint16)
+        assert bits == ref
+
+
+def test_epilogue_pc_matches_float64_when_exact():
+    """With power-of-two scales every fp32 step is exact for |acc| < 2^24, so
+    y is the single binary16 rounding of acc * s_a * s_w."""
+    rng = np.random.default_rng(7)
+    for _ in range(3000):
+        acc = int(rng.integers(-(2 ** 24) + 1, 2 ** 24))
+        ea, ew = rng.integers(-20, 2, 2)
+        sa, sw = 2.0 ** int(ea), 2.0 ** int(ew)
+        ref = np.float16(acc * sa * sw).view(np.uint16)
+        assert oracle.epilogue_pc(acc, sa, sw) == ref
+
+
+def test_epilogue_pg_order_and_exact_case():
+    rng = np.random.default_rng(8)
+    # exact case: power-of-two scales, small partials -> the sum is exact
+    for _ in range(500):
+        G = int(rng.integers(1, 40))
+        P = rng.integers(-(2 ** 14), 2 ** 14, G)
+        sw = 2.0 ** rng.integers(-12, -4, G)
+        sa = 2.0 ** int(rng.integers(-8, 0))
+        ref = np.float16(float(np.sum(P * sw)) * sa).view(np.uint16)
+        assert oracle.epilogue_pg(P, sw, sa) == ref
+    # the rounded ascending-order sum is what the definition says: a group
+    # that is tiny next to a large earlier one is absorbed
+    P = np.array([1 << 24, 1, 1], np.int32)
+    sw = np.ones(3, np.float32)
+    assert oracle.epilogue_pg(P, sw, 2.0 ** -20) == np.float16(16.0).view(np.uint16)
+    P2 = np.array([1, 1, 1 << 24], np.int32)
+    assert oracle.epilogue_pg(P2, sw, 2.0 ** -20) == np.float16(np.float32(16777218.0) * 2.0 ** -20).view(np.uint16)
+
+
+def test_pg_with_one_group_equals_pc_for_exact_scales():
+    rng = np.random.default_rng(9)
+    M, N, K = 5, 7, 128
+    x = np.rint(rng.uniform(-127, 127, (M, K))).astype(np.float16)
+    x[:, 0] = 127
+    w = np.rint(rng.uniform(-127, 127, (N, K))).astype(np.float16)
+    w[:, 1] = -127
+    wq, s = oracle.quantize_weight_int8(w, 0)
+    y_pc = oracle.w8a8_linear(x, wq, s, 0)
+    y_pg = oracle.w8a8_linear(x, wq, s.reshape(N, 1), K)
+    assert np.array_equal(y_pc.view(np.uint16), y_pg.view(np.uint16))
+
+
+def test_layer_close_to_float64_product():
+    """A dropped term, a wrong sign or index, or a transposed operand moves y
+    far from x @ W^T; the quantized layer must stay within the error that
+    the two quantizations allow."""
+    rng = np.random.default_rng(10)
+    M, N, K = 9, 40, 512
+    x = rng.standard_normal((M, K))
+    x[:, [3, 100]] *= 20
+    x = x.astype(np.float16)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    xf, wf = x.astype(np.float64), w.astype(np.float64)
+    exact = xf @ wf.T
+    for gs in (0, 64, 128):
+        wq, s = oracle.quantize_weight_int8(w, gs)
+        y = oracle.w8a8_linear(x, wq, s, gs).astype(np.float64)
+        sa = np.abs(xf).max(axis=1) / 127
+        swf = np.abs(wf).max(axis=1) / 127 if gs == 0 else None
+        # |x w - q s_a wq s_w| <= sum(|x| e_w + |w| e_a + e_a e_w) with e = s/2
+        e_a = sa[:, None] / 2
+        if gs == 0:
+            e_w = np.repeat((swf / 2)[:, None], K, axis=1)
+        else:
+            e_w = np.repeat(s.astype(np.float64) / 2, gs, axis=1)
+        bound = (np.abs(xf) @ e_w.T + e_a * np.abs(wf).sum(axis=1)[None, :]
+                 + e_a * e_w.sum(axis=1)[None, :])
+        bound = bound * 1.001 + np.abs(exact) * 2.0 ** -10 + 1e-6
+        assert np.all(np.abs(y - exact) <= bound)
+
+
+def test_w4a8_layer_equals_w8a8_on_unpacked_codes():
+    rng = np.random.default_rng(11)
+    M, N, K = 4, 12, 256
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    for gs in (0, 128):
+        wp, s = oracle.pack_weight_int4(w, gs)
+        y4 = oracle.w4a8_linear(x, wp, s, gs)
+        y8 = oracle.w8a8_linear(x, oracle.unpack_int4(wp, K), s, gs)
+        assert np.array_equal(y4.view(np.uint16), y8.view(np.uint16))
+
+
+def test_gemv_is_gemm_row():
+    """The M=1 path is the same function as the GEMM: computing one row alone
+    gives the bits of that row computed inside a batch."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((6, 192)).astype(np.float16)
+    w = (rng.standard_normal((10, 192)) * 0.02).astype(np.float16)
+    wq, s = oracle.quantize_weight_int8(w, 64)
+    y = oracle.w8a8_linear(x, wq, s, 64)
+    for m in range(6):
+        assert np.array_equal(oracle.w8a8_linear(x[m:m + 1], wq, s, 64).view(np.uint16),
+                              y[m:m + 1].view(np.uint16))
