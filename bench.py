@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Benchmark of the fused quantize -> INT8 GEMM -> dequant linear layer on B300.
+
+Workload (one "step"): the W8A8 per-channel linear layer at M = 4096 tokens,
+N = 10240 outputs, K = 2560 inputs (the shape and token count of the Cider
+README's operator-latency table, "Shape [N=10240, K=2560]", row M = 4096):
+per-token INT8 quantization of x, the INT8 x INT8 -> INT32 product on the
+tensor cores, the fused fp32 dequant to fp16. Inputs are synthetic (seeded,
+N(0,1) activations with 4 outlier channels x20, N(0,0.02) weights), resident
+in HBM; weight quantization is offline and untimed. L2 is flushed (512 MiB
+write) between timed steps.
+
+Prints ONE JSON line (rank 0). `value` is whole-job TOPS (2*M*N*K per step,
+all ranks); `e2e` is the same metric through the public C-ABI call with the
+inputs copied from pinned host memory and the output copied back inside the
+timed region; `gemv` is the M = 1 decode GEMV in HBM GB/s; `roofline` is the
+dominant kernel (the tensor-core GEMM) against the measured dense bf16 peak
+(fp16 has the same nominal rate); `cpu_baseline` is the CPU oracle timed on a
+bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cider|reference]
+
+With N > 1 it runs under torchrun, one process per GPU, as independent
+replicas (the layer needs no exchange between GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M, N, K = 4096, 10240, 2560
+METRIC = "W8A8 GEMM TOPS & % INT8 peak at M=4096; M=1 INT8 GEMV HBM GB/s"
+WORKLOAD = "w8a8_per_channel_linear_M4096_N10240_K2560"
+FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("cider", "reference"), default="cider")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 1800.0, 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.out.read().splitlines() if ln.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reported CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_tops(x_np, wq, s_w, rows: int):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.w8a8_linear(x_np[:rows], wq, s_w, 0)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * N * K / dt / 1e12, dt
+
+
+def size_oracle_sample(x_np, wq, s_w, target_s: float) -> int:
+    """Rows of the workload the oracle processes in about target_s seconds
+    (calibrated on enough rows to keep every oracle thread busy)."""
+    import oracle
+    cal = max(16, 2 * oracle.get_threads())
+    _, dt = oracle_tops(x_np, wq, s_w, cal)
+    per_row = dt / cal
+    return int(max(cal, min(M, target_s / max(per_row, 1e-9))))
+
+
+def cpu_inputs():
+    import oracle
+    import synth
+    li = synth.linear_inputs(M, N, K, n_out=4, seed=0)
+    x_np = li.x.numpy()
+    wq, s_w = oracle.quantize_weight_int8(li.w.numpy(), 0)
+    return x_np, wq, s_w
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on bounded samples of the workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    x_np, wq, s_w = cpu_inputs()
+    per_step_target = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = size_oracle_sample(x_np, wq, s_w, per_step_target)
+    for _ in range(args.warmup):
+        oracle_tops(x_np, wq, s_w, rows)
+    times = [oracle_tops(x_np, wq, s_w, rows)[1] for _ in range(args.steps)]
+    t = statistics.mean(times)
+    value = 2.0 * rows * N * K / t / 1e12
+    sample = f"{rows} of {M} token rows per step, full N={N}, K={K}"
+    cores = oracle.get_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "mode": "per-channel",
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CUDA path
+# ---------------------------------------------------------------------------
+
+def run_cider(args):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import w4a8_quantized_gemm_int8_b300 as cider
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    cider.load_library()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    li = synth.linear_inputs(M, N, K, n_out=4, seed=0)
+    x = li.x.to(dev)
+    wq, s_w = cider.quantize_weight_int8(li.w.to(dev), 0)  # offline prep, untimed
+    a_img = torch.empty((M, K), dtype=torch.float16, device=dev)
+    s_a = torch.empty((M,), dtype=torch.float32, device=dev)
+    b_img = torch.empty((N, K), dtype=torch.float16, device=dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        cider.act_image(x, a_img, s_a)
+        cider.weight_image(wq, K, 8, b_img)
+        cider.gemm_images(a_img, s_a, b_img, s_w, 0, y)
+
+    # The staged calls are the kernels the fused entry point runs: same bits.
+    y_fused = cider.w8a8_linear(x, wq, s_w, 0)
+    step()
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_fused.view(torch.int16)), "staged != fused"
+    del y_fused
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        flush.zero_()
+        e = evs[i]
+        e[0].record(stream)
+        cider.act_image(x, a_img, s_a)
+        e[1].record(stream)
+        cider.weight_image(wq, K, 8, b_img)
+        e[2].record(stream)
+        cider.gemm_images(a_img, s_a, b_img, s_w, 0, y)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier()
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    widen_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    gemm_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    st, site = cider.device_status()
+    assert st == cider.CIDER_OK, f"device status {st} at {site:#x}"
+
+    flops = 2.0 * M * N * K
+    mean_step_s = statistics.mean(step_ms) / 1e3
+    mean_step_s = max_over_ranks(mean_step_s)
+    value = world * flops / mean_step_s / 1e12
+    gemm_s = statistics.mean(gemm_ms) / 1e3
+    bf16_peak, hbm_peak, peak_src = peaks()
+    achieved = flops / gemm_s / 1e12
+
+    # ---- M = 1 decode GEMV on the same weights (HBM stream) ----------------
+    x1 = x[0].contiguous()
+    y1 = torch.empty((N,), dtype=torch.float16, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        cider.int8_gemv(x1, wq, s_w, 8, 0, out=y1)
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in gev:
+        flush.zero_()
+        a.record(stream)
+        cider.int8_gemv(x1, wq, s_w, 8, 0, out=y1)
+        b.record(stream)
+    torch.cuda.synchronize()
+    gemv_s = statistics.mean([a.elapsed_time(b) for a, b in gev]) / 1e3
+    gemv_bytes = N * K + 4 * N + 2 * K + 2 * N
+    gemv_gbs = gemv_bytes / gemv_s / 1e9
+
+    # ---- end to end through the public call, host buffers ------------------
+    x_h = li.x.pin_memory()
+    y_h = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    x_d = torch.empty_like(x)
+    y_d = torch.empty_like(y)
+    ws = torch.empty(cider.workspace_bytes(M, N, K, 8, 0), dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        cider.w8a8_linear(x_d, wq, s_w, 0, out=y_d, ws=ws)
+        y_h.copy_(y_d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in eev:
+        flush.zero_()
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in eev]) / 1e3)
+    e2e_value = world * flops / e2e_s / 1e12
+    assert torch.equal(y_h.view(torch.int16), y.cpu().view(torch.int16))
+
+    # ---- INT8 library rate on this GPU (context for "% INT8 peak") ----------
+    int8_lib = None
+    try:
+        a8 = torch.randint(-127, 128, (8192, 8192), dtype=torch.int8, device=dev)
+        b8 = torch.randint(-127, 128, (8192, 8192), dtype=torch.int8, device=dev).t()
+        for _ in range(3):
+            torch._int_mm(a8, b8)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(10):
+            torch._int_mm(a8, b8)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        int8_lib = 2.0 * 8192 ** 3 / (s0.elapsed_time(s1) / 10 / 1e3) / 1e12
+        del a8, b8
+    except Exception as exc:  # the library may not offer INT8 GEMM here
+        int8_lib = f"unavailable: {type(exc).__name__}"
+
+    if rank != 0:
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        x_np, wq_np, sw_np = cpu_inputs()
+        rows = size_oracle_sample(x_np, wq_np, sw_np, args.cpu_seconds)
+        cpu_tops, cpu_dt = oracle_tops(x_np, wq_np, sw_np, rows)
+        cpu = {"value": cpu_tops, "unit": "TOPS", "cores": oracle.get_threads(), "kind": "oracle",
+               "sample": f"{rows} of {M} token rows, full N={N}, K={K} ({cpu_dt:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(step_ms), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "mode": "per-channel",
+                   "tensor_engine": "tcgen05 kind::f16 on exact fp16 integer codes",
+                   "l2": "flushed between steps (512 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "breakdown_ms": {"act_quant": statistics.mean(quant_ms),
+                         "weight_image": statistics.mean(widen_ms),
+                         "gemm": statistics.mean(gemm_ms)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+                     "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": None,
+                     "kernel": "gemm_tc_kernel<kPcF16>",
+                     "peak_source": f"{peak_src} dense bf16 burst; fp16 nominal rate equal"},
+        "int8_peak": {"torch_int_mm_8192_tops": int8_lib,
+                      "value_pct": (100.0 * value / int8_lib
+                                    if isinstance(int8_lib, float) else None)},
+        "gemv": {"value": gemv_gbs, "unit": "GB/s", "us": gemv_s * 1e6, "M": 1, "N": N, "K": K,
+                 "bytes": gemv_bytes, "roofline": {"bound": "hbm", "achieved": gemv_gbs,
+                                                    "peak": hbm_peak, "unit": "GB/s",
+                                                    "frac": gemv_gbs / hbm_peak,
+                                                    "traffic": None}},
+        "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": M * K * 2,
+                "d2h_bytes_per_step": M * N * 2},
+        "cpu_baseline": cpu,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clock_info,
+        "impl": "cider",
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cider(args)
+
+
+if __name__ == "__main__":
+    main()

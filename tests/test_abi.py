@@ -1,0 +1,66 @@
+"""Host-side checks of the C-ABI library that need no GPU: it loads, it
+exports every symbol include/cider.h declares, and argument validation that
+runs before any CUDA call answers as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import w4a8_quantized_gemm_int8_b300 as cider
+from w4a8_quantized_gemm_int8_b300 import build as cbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return cider.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "cider.h")).read()
+    return sorted(set(re.findall(r"CIDER_API\s+[\w\s\*]*?\b(cider_\w+)\s*\(", src)))
+
+
+def test_header_declares_binding_names():
+    assert _declared() == sorted(cider.ABI_FUNCTIONS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    # nothing else leaks out as a C symbol with the prefix
+    out = os.popen(f"nm -D --defined-only {cider.LIB_PATH}").read()
+    exported = sorted(set(re.findall(r" T (cider_\w+)", out)))
+    assert exported == _declared()
+
+
+def test_status_strings_and_version(lib):
+    assert cider.abi_version() == 1
+    for code, name in [(0, "CIDER_OK"), (1, "CIDER_ERR_INVALID_ARG"),
+                       (2, "CIDER_ERR_UNSUPPORTED"), (3, "CIDER_ERR_CUDA"),
+                       (4, "CIDER_ERR_TIMEOUT"), (5, "CIDER_ERR_WORKSPACE"), (99, "CIDER_ERR_UNKNOWN")]:
+        assert cider.status_string(code) == name
+
+
+def test_workspace_bytes(lib):
+    assert cider.workspace_bytes(1, 10240, 2560) == 0   # GEMV path
+    assert cider.workspace_bytes(0, 16, 16) == 0
+    assert cider.workspace_bytes(4, 16, 16, bits=3) == 0
+    n = cider.workspace_bytes(4096, 10240, 2560)
+    assert n >= 2 * 4096 * 2560 + 4 * 4096 + 2 * 10240 * 2560
+    assert n % 256 == 0
+
+
+def test_null_and_size_checks_precede_cuda(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: checks fail first
+    assert lib.cider_quantize_act(None, 4, 16, p, p, None) == 1
+    assert lib.cider_quantize_act(p, 0, 16, p, p, None) == 1
+    assert lib.cider_w8a8_gemm_pc(p, 4, 16, 16, None, p, p, p, 1 << 20, None) == 1
+    assert lib.cider_w8a8_gemm_pc(p, -1, 16, 16, p, p, p, p, 1 << 20, None) == 1
+    assert lib.cider_w8a8_gemm_pg(p, 4, 16, 128, p, p, 0, p, p, 1 << 20, None) == 1
+    assert lib.cider_int8_gemv(p, 16, 16, p, p, 5, 0, p, None) == 1
+    assert lib.cider_test_wait_timeout(0, None) == 1
+    assert lib.cider_test_gemm_s32(p, p, 4, 4, 64, 7, 0, p, p, 1 << 20, None) == 1

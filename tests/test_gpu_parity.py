@@ -1,0 +1,268 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Bars: INT8 codes, scales and INT32 accumulators bit-exact; fp16 outputs
+within 1 ulp of the oracle (the tests also count the outputs that are not
+bit-identical; the kernels follow the oracle's operation order, so the
+expected count is 0).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import w4a8_quantized_gemm_int8_b300 as cider
+from gpu_helpers import assert_f16_within_1ulp, cuda, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    cider.load_library()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+    st, site = cider.device_status()
+    assert st == cider.CIDER_OK, f"device status {st} at site {site:#x}"
+
+
+# ---------------------------------------------------------------------------
+# failure detection: a bounded device wait gives up and reports
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_reports_timeout():
+    cider.device_status()  # clear
+    cider.wait_timeout_probe(20_000_000)  # 20 ms
+    st, site = cider.device_status()
+    assert st == cider.CIDER_ERR_TIMEOUT and site == 0x901
+    st, _ = cider.device_status()
+    assert st == cider.CIDER_OK
+    # the context is still usable
+    x = torch.ones(4, 16, dtype=torch.float16, device="cuda")
+    q, s = cider.quantize_act(x)
+    assert int(q[0, 0]) == 127
+
+
+# ---------------------------------------------------------------------------
+# activation quantization
+# ---------------------------------------------------------------------------
+
+def _special_rows(K):
+    rows = [np.zeros(K), np.zeros(K)]
+    rows[1][K // 2] = -3.0
+    r = (np.arange(K) % 9 - 4) * 0.5
+    r[0] = 4.0 * 127 / 127  # absmax 4 -> scale 4/127
+    rows.append(r)
+    t = np.full(K, 0.5)
+    t[1] = 127.0  # scale 1: 0.5 ties to 0
+    rows.append(t)
+    return np.array(rows, dtype=np.float16)
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (3, 40), (5, 13), (128, 512), (257, 2560),
+                                 (64, 12288), (2, 1 << 16)])
+def test_quantize_act_bitexact(M, K):
+    x = synth.activations(M, K, 4 if K >= 64 else 0, synth.generator(M * 7 + K)).numpy()
+    x = np.concatenate([x, _special_rows(K)])
+    q, s = cider.quantize_act(cuda(torch.from_numpy(x)))
+    qo, so = oracle.quantize_act(x)
+    assert np.array_equal(host(s).view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(host(q), qo)
+
+
+def test_quantize_exhaustive_over_x_for_many_scales():
+    """For each chosen absmax a, one row holds a and every fp16 x with
+    |x| <= a (zero padded): all codes must match the oracle bit for bit."""
+    pos = np.arange(1, 0x7C00, dtype=np.int32)      # positive finite fp16 bit patterns
+    chosen = np.unique(np.concatenate([pos[::97], pos[-40:], pos[:40],
+                                       np.array([0x3C00, 0x57F0, 0x5BF0, 0x7BFF])]))
+    width = 2 * 0x7C00
+    width += (-width) % 16
+    rows = np.zeros((len(chosen), width), np.uint16)
+    for i, a in enumerate(chosen):
+        xs = np.arange(0, a + 1, dtype=np.uint16)
+        rows[i, :a + 1] = xs
+        rows[i, a + 1:2 * a + 2] = xs | 0x8000
+    x = rows.view(np.float16)
+    q, s = cider.quantize_act(cuda(torch.from_numpy(x)))
+    qo, so = oracle.quantize_act(x)
+    assert np.array_equal(host(s).view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(host(q), qo)
+
+
+# ---------------------------------------------------------------------------
+# weight preparation
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("gs", [0, 64, 128])
+def test_quantize_weight_int8_bitexact(gs):
+    w = synth.weights(300, 512, synth.generator(gs + 1)).numpy()
+    w[3] = 0
+    wq, s = cider.quantize_weight_int8(cuda(torch.from_numpy(w)), gs)
+    wqo, so = oracle.quantize_weight_int8(w, gs)
+    assert np.array_equal(host(wq), wqo)
+    assert np.array_equal(host(s).view(np.uint32), so.view(np.uint32))
+
+
+@pytest.mark.parametrize("gs", [0, 64, 128])
+def test_pack_weight_int4_bitexact(gs):
+    w = synth.weights(130, 768, synth.generator(gs + 2)).numpy()
+    w[5, :128] = 0
+    wp, s = cider.pack_weight_int4(cuda(torch.from_numpy(w)), gs)
+    wpo, so = oracle.pack_weight_int4(w, gs)
+    assert np.array_equal(host(wp), wpo)
+    assert np.array_equal(host(s).view(np.uint32), so.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# INT32 accumulators of the tensor-core engine (raw, bit-exact)
+# ---------------------------------------------------------------------------
+
+def _codes(shape, seed, lo=-127, hi=127):
+    rng = np.random.default_rng(seed)
+    return rng.integers(lo, hi + 1, shape, dtype=np.int8)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (1, 16, 64), (7, 300, 192), (130, 257, 1088),
+                                   (300, 520, 2560), (129, 256, 12288)])
+def test_gemm_s32_bitexact(M, N, K):
+    q = _codes((M, K), M + N)
+    w = _codes((N, K), K)
+    acc = cider.raw_gemm_s32(cuda(torch.from_numpy(q)), cuda(torch.from_numpy(w)), K)
+    assert np.array_equal(host(acc), oracle.gemm_s32(q, w, 0))
+
+
+def test_gemm_s32_worst_case_magnitudes():
+    """All codes +-127: each 1024-deep segment reaches 127^2 * 1024 (just
+    under 2^24) and the total reaches 127^2 * K; signs alternate by row so
+    large partial sums cancel and rebuild."""
+    M, N, K = 256, 256, 12288
+    q = np.full((M, K), 127, np.int8)
+    q[1::2] = -127
+    q[2::4, ::3] = -127
+    w = np.full((N, K), 127, np.int8)
+    w[::3, ::2] = -127
+    w[5] = 127
+    acc = cider.raw_gemm_s32(cuda(torch.from_numpy(q)), cuda(torch.from_numpy(w)), K)
+    assert np.array_equal(host(acc), oracle.gemm_s32(q, w, 0))
+
+
+@pytest.mark.parametrize("gs", [64, 128])
+def test_gemm_s32_group_partials(gs):
+    M, N, K = 140, 270, 1024
+    q = _codes((M, K), 11)
+    w = _codes((N, K), 12)
+    part = cider.raw_gemm_s32(cuda(torch.from_numpy(q)), cuda(torch.from_numpy(w)), K,
+                               group_size=gs)
+    assert np.array_equal(host(part), oracle.gemm_s32(q, w, gs))
+
+
+def test_gemm_s32_int4_weights():
+    M, N, K = 130, 300, 512
+    q = _codes((M, K), 21)
+    wp = np.random.default_rng(22).integers(0, 256, (N, K // 2), dtype=np.uint8)
+    acc = cider.raw_gemm_s32(cuda(torch.from_numpy(q)), cuda(torch.from_numpy(wp)), K, bits=4)
+    assert np.array_equal(host(acc), oracle.gemm_s32(q, oracle.unpack_int4(wp, K), 0))
+
+
+# ---------------------------------------------------------------------------
+# whole linear layers
+# ---------------------------------------------------------------------------
+
+def _layer_inputs(M, N, K, seed):
+    li = synth.linear_inputs(M, N, K, n_out=4, seed=seed)
+    return li.x.numpy(), li.w.numpy()
+
+
+LAYER_SHAPES = [(128, 256, 512), (2, 16, 64), (3, 300, 192), (130, 257, 1088), (200, 8, 2560),
+                (129, 384, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", LAYER_SHAPES)
+def test_w8a8_pc_layer(M, N, K):
+    x, w = _layer_inputs(M, N, K, seed=M + N + K)
+    wq, s = oracle.quantize_weight_int8(w, 0)
+    y = cider.w8a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                          cuda(torch.from_numpy(s)), 0)
+    ref = oracle.w8a8_linear(x, wq, s, 0)
+    assert_f16_within_1ulp(host(y), ref, "pc")
+
+
+@pytest.mark.parametrize("gs", [64, 128])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (3, 300, 1024), (130, 264, 2560)])
+def test_w8a8_pg_layer(M, N, K, gs):
+    x, w = _layer_inputs(M, N, K, seed=gs + M)
+    wq, s = oracle.quantize_weight_int8(w, gs)
+    y = cider.w8a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                          cuda(torch.from_numpy(s)), gs)
+    ref = oracle.w8a8_linear(x, wq, s, gs)
+    assert_f16_within_1ulp(host(y), ref, f"pg{gs}")
+
+
+@pytest.mark.parametrize("gs", [0, 128, 64])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (2, 300, 1024), (131, 264, 2560)])
+def test_w4a8_layer(M, N, K, gs):
+    x, w = _layer_inputs(M, N, K, seed=gs + 3 * M)
+    wp, s = oracle.pack_weight_int4(w, gs)
+    y = cider.w4a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wp)),
+                          cuda(torch.from_numpy(s)), gs)
+    ref = oracle.w4a8_linear(x, wp, s, gs)
+    assert_f16_within_1ulp(host(y), ref, f"w4 gs{gs}")
+
+
+def test_layer_edge_rows():
+    """All-zero tokens, a single non-zero, exact-scale rows, overflow to inf."""
+    M, N, K = 6, 64, 128
+    x = np.zeros((M, K), np.float16)
+    x[1, 5] = -2.0
+    x[2] = 127.0
+    x[3, ::2] = 127.0
+    x[3, 1::2] = -127.0
+    x[4] = np.linspace(-60, 60, K).astype(np.float16)
+    x[5] = 65504.0
+    w = synth.weights(N, K, synth.generator(5)).numpy()
+    w[0] = 127.0
+    w[1] = 0.0
+    for gs in (0, 64):
+        wq, s = oracle.quantize_weight_int8(w, gs)
+        y = cider.w8a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                              cuda(torch.from_numpy(s)), gs)
+        ref = oracle.w8a8_linear(x, wq, s, gs)
+        assert np.array_equal(host(y).view(np.uint16), ref.view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# M = 1 GEMV
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits,gs", [(8, 0), (8, 64), (8, 128), (4, 0), (4, 128), (4, 64)])
+@pytest.mark.parametrize("N,K", [(10240, 2560), (2560, 10240), (37, 512), (1, 12288)])
+def test_gemv_matches_oracle(bits, gs, N, K):
+    x, w = _layer_inputs(1, N, K, seed=N + bits + gs)
+    if bits == 8:
+        wq, s = oracle.quantize_weight_int8(w, gs)
+        ref = oracle.w8a8_linear(x, wq, s, gs)
+    else:
+        wq, s = oracle.pack_weight_int4(w, gs)
+        ref = oracle.w4a8_linear(x, wq, s, gs)
+    y = cider.int8_gemv(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                        cuda(torch.from_numpy(s)), bits=bits, group_size=gs)
+    assert np.array_equal(host(y).view(np.uint16), ref[0].view(np.uint16))
+
+
+@pytest.mark.parametrize("gs", [0, 64])
+def test_gemv_equals_gemm_row(gs):
+    """Routing on M never changes a result: GEMV(x[m]) is bit-identical to
+    row m of the tensor-core GEMM over the whole batch."""
+    M, N, K = 130, 1000, 2560
+    x, w = _layer_inputs(M, N, K, seed=77 + gs)
+    wq, s = oracle.quantize_weight_int8(w, gs)
+    xd, wd, sd = (cuda(torch.from_numpy(a)) for a in (x, wq, s))
+    y = host(cider.w8a8_linear(xd, wd, sd, gs))
+    for m in (0, 1, 64, 129):
+        ym = host(cider.int8_gemv(xd[m], wd, sd, bits=8, group_size=gs))
+        assert np.array_equal(ym.view(np.uint16), y[m].view(np.uint16))
+    # the public GEMM entry point at M == 1 takes the GEMV
+    y1 = host(cider.w8a8_linear(xd[5:6].contiguous(), wd, sd, gs))
+    assert np.array_equal(y1.view(np.uint16), y[5:6].view(np.uint16))

@@ -1,0 +1,304 @@
+"""B300 (sm_103a) quantized linear layers: online per-token INT8 activation
+quantization, exact INT8 x INT8 -> INT32 products on the tensor cores, fused
+dequant to fp16; W8A8 per-channel, W8A8 per-group, W4A8, and the M = 1 GEMV.
+
+This module is a thin ctypes binding over ``libcider.so`` (the C ABI in
+``include/cider.h``): it checks tensors, allocates outputs and workspace with
+torch, and passes raw device pointers and the current CUDA stream. Every
+arithmetic step runs in the library's CUDA kernels; there is no CPU path. If
+the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcider.so")
+
+# The C-ABI entry points (names as declared in include/cider.h).
+ABI_FUNCTIONS = (
+    "cider_status_string", "cider_abi_version", "cider_quantize_act",
+    "cider_quantize_weight_int8", "cider_pack_weight_int4", "cider_workspace_bytes",
+    "cider_w8a8_gemm_pc", "cider_w8a8_gemm_pg", "cider_w4a8_gemm", "cider_int8_gemv",
+    "cider_act_image", "cider_weight_image", "cider_gemm_images",
+    "cider_test_gemm_s32", "cider_device_status", "cider_test_wait_timeout",
+)
+
+CIDER_OK = 0
+CIDER_ERR_TIMEOUT = 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CiderError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def load_library():
+    """Loads libcider.so (built by ``build.py``); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m "
+                "w4a8_quantized_gemm_int8_b300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        sig = {
+            "cider_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "cider_abi_version": ([], ctypes.c_int),
+            "cider_quantize_act": ([p, i64, i64, p, p, p], ctypes.c_int),
+            "cider_quantize_weight_int8": ([p, i64, i64, i32, p, p, p], ctypes.c_int),
+            "cider_pack_weight_int4": ([p, i64, i64, i32, p, p, p], ctypes.c_int),
+            "cider_workspace_bytes": ([i64, i64, i64, i32, i32], sz),
+            "cider_w8a8_gemm_pc": ([p, i64, i64, i64, p, p, p, p, sz, p], ctypes.c_int),
+            "cider_w8a8_gemm_pg": ([p, i64, i64, i64, p, p, i32, p, p, sz, p], ctypes.c_int),
+            "cider_w4a8_gemm": ([p, i64, i64, i64, p, p, i32, p, p, sz, p], ctypes.c_int),
+            "cider_int8_gemv": ([p, i64, i64, p, p, i32, i32, p, p], ctypes.c_int),
+            "cider_act_image": ([p, i64, i64, p, p, p], ctypes.c_int),
+            "cider_weight_image": ([p, i64, i64, i32, p, p], ctypes.c_int),
+            "cider_gemm_images": ([p, p, p, p, i64, i64, i64, i32, p, p], ctypes.c_int),
+            "cider_test_gemm_s32": ([p, p, i64, i64, i64, i32, i32, p, p, sz, p], ctypes.c_int),
+            "cider_device_status": ([p, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+            "cider_test_wait_timeout": ([i64, p], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().cider_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(load_library().cider_abi_version())
+
+
+def _check(fn: str, status: int) -> None:
+    if status != CIDER_OK:
+        raise CiderError(fn, status)
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str, ndim: int | None = None) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    return t.data_ptr()
+
+
+_ws_cache: dict = {}
+
+
+def workspace_bytes(M: int, N: int, K: int, bits: int = 8, group_size: int = 0) -> int:
+    return int(load_library().cider_workspace_bytes(M, N, K, bits, group_size))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor | None:
+    """A per-device workspace buffer, grown on demand (stream-ordered reuse:
+    calls on one stream may share it)."""
+    if nbytes == 0:
+        return None
+    key = torch.device(device).index
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+# ---------------------------------------------------------------------------
+# quantization
+# ---------------------------------------------------------------------------
+
+def quantize_act(x: torch.Tensor):
+    """Per-token INT8 activation quantization: x fp16 [M,K] -> (q int8 [M,K],
+    s_a fp32 [M])."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    s = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check("cider_quantize_act", load_library().cider_quantize_act(
+        _dev(x, torch.float16, "x", 2), M, K, q.data_ptr(), s.data_ptr(), _stream()))
+    return q, s
+
+
+def quantize_weight_int8(w: torch.Tensor, group_size: int = 0):
+    """INT8 weight quantization: w fp16 [N,K] -> (wq int8 [N,K], s_w fp32
+    [N] (group_size 0) or [N, K/group_size])."""
+    N, K = w.shape
+    wq = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    shape = (N,) if group_size == 0 else (N, K // group_size)
+    s = torch.empty(shape, dtype=torch.float32, device=w.device)
+    _check("cider_quantize_weight_int8", load_library().cider_quantize_weight_int8(
+        _dev(w, torch.float16, "w", 2), N, K, group_size, wq.data_ptr(), s.data_ptr(),
+        _stream()))
+    return wq, s
+
+
+def pack_weight_int4(w: torch.Tensor, group_size: int = 0):
+    """INT4 weight quantization + packing: w fp16 [N,K] -> (wp uint8 [N,K/2],
+    s_w fp32 [N] or [N, K/group_size])."""
+    N, K = w.shape
+    wp = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    shape = (N,) if group_size == 0 else (N, K // group_size)
+    s = torch.empty(shape, dtype=torch.float32, device=w.device)
+    _check("cider_pack_weight_int4", load_library().cider_pack_weight_int4(
+        _dev(w, torch.float16, "w", 2), N, K, group_size, wp.data_ptr(), s.data_ptr(),
+        _stream()))
+    return wp, s
+
+
+# ---------------------------------------------------------------------------
+# linear layers
+# ---------------------------------------------------------------------------
+
+def w8a8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor, group_size: int = 0,
+                out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """W8A8 linear layer y = dequant(quant(x) . wq^T): per-channel for
+    group_size 0 (s_w [N]), per-group otherwise (s_w [N, K/gs]). M == 1 runs
+    the GEMV inside the library."""
+    M, K = x.shape
+    N = wq.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=x.device)
+    need = workspace_bytes(M, N, K, 8, group_size)
+    buf = ws if ws is not None else _workspace(need, x.device)
+    wsp, wsn = (buf.data_ptr(), buf.numel()) if buf is not None else (None, 0)
+    lib = load_library()
+    xp = _dev(x, torch.float16, "x", 2)
+    wp = _dev(wq, torch.int8, "wq", 2)
+    sp = _dev(s_w, torch.float32, "s_w")
+    yp = _dev(y, torch.float16, "y", 2)
+    if group_size == 0:
+        st = lib.cider_w8a8_gemm_pc(xp, M, N, K, wp, sp, yp, wsp, wsn, _stream())
+        _check("cider_w8a8_gemm_pc", st)
+    else:
+        st = lib.cider_w8a8_gemm_pg(xp, M, N, K, wp, sp, group_size, yp, wsp, wsn, _stream())
+        _check("cider_w8a8_gemm_pg", st)
+    return y
+
+
+def w4a8_linear(x: torch.Tensor, wp: torch.Tensor, s_w: torch.Tensor, group_size: int = 0,
+                out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """W4A8 linear layer with packed INT4 weights wp [N, K/2]."""
+    M, K = x.shape
+    N = wp.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=x.device)
+    need = workspace_bytes(M, N, K, 4, group_size)
+    buf = ws if ws is not None else _workspace(need, x.device)
+    wsp, wsn = (buf.data_ptr(), buf.numel()) if buf is not None else (None, 0)
+    st = load_library().cider_w4a8_gemm(
+        _dev(x, torch.float16, "x", 2), M, N, K, _dev(wp, torch.uint8, "wp", 2),
+        _dev(s_w, torch.float32, "s_w"), group_size, _dev(y, torch.float16, "y", 2), wsp, wsn,
+        _stream())
+    _check("cider_w4a8_gemm", st)
+    return y
+
+
+def int8_gemv(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
+              group_size: int = 0, out: torch.Tensor | None = None) -> torch.Tensor:
+    """M = 1 GEMV: x fp16 [K] (or [1,K]); w int8 [N,K] (bits 8) or packed
+    uint8 [N, K/2] (bits 4); returns y fp16 [N]."""
+    xv = x.reshape(-1)
+    K = xv.numel()
+    N = w.shape[0]
+    y = out if out is not None else torch.empty((N,), dtype=torch.float16, device=x.device)
+    wdt = torch.int8 if bits == 8 else torch.uint8
+    st = load_library().cider_int8_gemv(
+        _dev(xv, torch.float16, "x"), K, N, _dev(w, wdt, "w", 2), _dev(s_w, torch.float32, "s_w"),
+        bits, group_size, _dev(y, torch.float16, "y"), _stream())
+    _check("cider_int8_gemv", st)
+    return y
+
+
+def act_image(x: torch.Tensor, a_img: torch.Tensor | None = None,
+              s_a: torch.Tensor | None = None):
+    """Stage 1 of the GEMM path: x fp16 [M,K] -> (codes as fp16 integers
+    [M,K], s_a fp32 [M])."""
+    M, K = x.shape
+    a_img = a_img if a_img is not None else torch.empty((M, K), dtype=torch.float16,
+                                                        device=x.device)
+    s_a = s_a if s_a is not None else torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check("cider_act_image", load_library().cider_act_image(
+        _dev(x, torch.float16, "x", 2), M, K, _dev(a_img, torch.float16, "a_img", 2),
+        _dev(s_a, torch.float32, "s_a"), _stream()))
+    return a_img, s_a
+
+
+def weight_image(w: torch.Tensor, K: int, bits: int = 8, b_img: torch.Tensor | None = None):
+    """Stage 2: INT8 [N,K] or packed INT4 [N,K/2] codes -> fp16 integers [N,K]."""
+    N = w.shape[0]
+    b_img = b_img if b_img is not None else torch.empty((N, K), dtype=torch.float16,
+                                                        device=w.device)
+    wdt = torch.int8 if bits == 8 else torch.uint8
+    _check("cider_weight_image", load_library().cider_weight_image(
+        _dev(w, wdt, "w", 2), N, K, bits, _dev(b_img, torch.float16, "b_img", 2), _stream()))
+    return b_img
+
+
+def gemm_images(a_img: torch.Tensor, s_a: torch.Tensor, b_img: torch.Tensor,
+                s_w: torch.Tensor, group_size: int = 0,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """Stage 3: tensor-core GEMM + fused dequant on the fp16 code images."""
+    M, K = a_img.shape
+    N = b_img.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=a_img.device)
+    _check("cider_gemm_images", load_library().cider_gemm_images(
+        _dev(a_img, torch.float16, "a_img", 2), _dev(s_a, torch.float32, "s_a"),
+        _dev(b_img, torch.float16, "b_img", 2), _dev(s_w, torch.float32, "s_w"), M, N, K,
+        group_size, _dev(y, torch.float16, "y", 2), _stream()))
+    return y
+
+
+def raw_gemm_s32(q: torch.Tensor, w: torch.Tensor, K: int, bits: int = 8,
+                  group_size: int = 0) -> torch.Tensor:
+    """Test hook: raw int32 products of the tensor-core engine on INT8 codes
+    q [M,K] and weights (int8 [N,K] or packed [N,K/2]); [M,N] totals or
+    [M,N,K/gs] per-group partials."""
+    M = q.shape[0]
+    N = w.shape[0]
+    G = 1 if group_size == 0 else K // group_size
+    out = torch.empty((M, N) if group_size == 0 else (M, N, G), dtype=torch.int32,
+                      device=q.device)
+    need = workspace_bytes(max(M, 2), N, K, bits, group_size)
+    buf = _workspace(need, q.device)
+    wdt = torch.int8 if bits == 8 else torch.uint8
+    st = load_library().cider_test_gemm_s32(
+        _dev(q, torch.int8, "q", 2), _dev(w, wdt, "w", 2), M, N, K, bits, group_size,
+        out.data_ptr(), buf.data_ptr(), buf.numel(), _stream())
+    _check("cider_test_gemm_s32", st)
+    return out
+
+
+def device_status() -> tuple[int, int]:
+    """Synchronizes the current stream; returns (status, wait site) of the
+    device status word and clears it."""
+    site = ctypes.c_uint32(0)
+    st = load_library().cider_device_status(_stream(), ctypes.byref(site))
+    return int(st), int(site.value)
+
+
+def wait_timeout_probe(timeout_ns: int) -> None:
+    """Test hook: a kernel whose bounded mbarrier wait is never satisfied."""
+    _check("cider_test_wait_timeout",
+           load_library().cider_test_wait_timeout(int(timeout_ns), _stream()))

@@ -1,0 +1,337 @@
+// C ABI of the library (declared in include/cider.h): argument checks,
+// workspace carving, routing (M == 1 -> GEMV) and kernel launches.
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/cider.h"
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using namespace cider;
+
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s bound on every device-side wait
+constexpr int kMaxDevices = 64;
+int g_num_sms[kMaxDevices] = {};
+
+cider_status num_sms(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CIDER_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return CIDER_ERR_UNSUPPORTED;
+    if (g_num_sms[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return CIDER_ERR_CUDA;
+        g_num_sms[dev] = v;
+    }
+    *out = g_num_sms[dev];
+    return CIDER_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+cider_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return CIDER_OK;
+    if (e == cudaErrorInvalidValue) {
+        cudaGetLastError();  // a launcher's own argument rejection, nothing launched
+        return CIDER_ERR_UNSUPPORTED;
+    }
+    return CIDER_ERR_CUDA;
+}
+
+struct Workspace {
+    __half* a_img;
+    float* s_a;
+    __half* b_img;
+};
+
+size_t workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    return align256((size_t)M * K * 2) + align256((size_t)M * 4) + align256((size_t)N * K * 2);
+}
+
+Workspace carve(void* ws, int64_t M, int64_t N, int64_t K) {
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    Workspace w;
+    w.a_img = reinterpret_cast<__half*>(p);
+    p += align256((size_t)M * K * 2);
+    w.s_a = reinterpret_cast<float*>(p);
+    p += align256((size_t)M * 4);
+    w.b_img = reinterpret_cast<__half*>(p);
+    return w;
+}
+
+bool valid_group(int32_t gs, int64_t K, int multiple) {
+    return gs == 0 || (gs > 0 && gs % multiple == 0 && K % gs == 0);
+}
+
+// Shared body of the three GEMM entry points.
+cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const void* w, int bits,
+                         const float* s_w, int32_t gs, void* y, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    if (!x || !w || !s_w || !y) return CIDER_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || gs < 0) return CIDER_ERR_INVALID_ARG;
+    if (K % 16 != 0 || (bits == 4 && K % 32 != 0)) return CIDER_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(s_w))
+        return CIDER_ERR_UNSUPPORTED;
+    if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+
+    if (M == 1) {  // decode: the GEMV computes the same function
+        if (K > 16384 || !valid_group(gs, K, bits == 8 ? 16 : 32)) return CIDER_ERR_UNSUPPORTED;
+        GemvArgs g{static_cast<const __half*>(x), K, N, w, s_w, bits, gs,
+                   static_cast<__half*>(y)};
+        return from_cuda(launch_gemv(g, sms, stream));
+    }
+    if (!valid_group(gs, K, 64)) return CIDER_ERR_UNSUPPORTED;
+    const size_t need = workspace_bytes(M, N, K);
+    if (!ws || ws_bytes < need) return CIDER_ERR_WORKSPACE;
+    if (!aligned16(ws)) return CIDER_ERR_UNSUPPORTED;
+    unsigned long long* status = nullptr;
+    if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
+
+    Workspace wsp = carve(ws, M, N, K);
+    cudaError_t e = launch_quant_groups(static_cast<const __half*>(x), M, K, K, 127,
+                                        QuantOut::kF16, wsp.a_img, wsp.s_a, sms, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, wsp.b_img, sms, stream)
+                    : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, wsp.b_img, sms, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    GemmArgs a{};
+    a.a_img = wsp.a_img;
+    a.b_img = wsp.b_img;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.group_size = gs;
+    a.s_a = wsp.s_a;
+    a.s_w = s_w;
+    a.out = y;
+    a.mode = (gs == 0) ? GemmMode::kPcF16 : GemmMode::kPgF16;
+    a.timeout_ns = kWaitTimeoutNs;
+    a.status = status;
+    return from_cuda(launch_gemm_tc(a, sms, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cider_status_string(int status) {
+    switch (status) {
+        case CIDER_OK: return "CIDER_OK";
+        case CIDER_ERR_INVALID_ARG: return "CIDER_ERR_INVALID_ARG";
+        case CIDER_ERR_UNSUPPORTED: return "CIDER_ERR_UNSUPPORTED";
+        case CIDER_ERR_CUDA: return "CIDER_ERR_CUDA";
+        case CIDER_ERR_TIMEOUT: return "CIDER_ERR_TIMEOUT";
+        case CIDER_ERR_WORKSPACE: return "CIDER_ERR_WORKSPACE";
+        default: return "CIDER_ERR_UNKNOWN";
+    }
+}
+
+int cider_abi_version(void) { return CIDER_ABI_VERSION; }
+
+cider_status cider_quantize_act(const void* x_f16, int64_t M, int64_t K, int8_t* q, float* s_a,
+                                void* stream) {
+    if (!x_f16 || !q || !s_a) return CIDER_ERR_INVALID_ARG;
+    if (M <= 0 || K <= 0) return CIDER_ERR_INVALID_ARG;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    return from_cuda(launch_quant_groups(static_cast<const __half*>(x_f16), M, K, K, 127,
+                                         QuantOut::kInt8, q, s_a, sms,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+cider_status cider_quantize_weight_int8(const void* w_f16, int64_t N, int64_t K,
+                                        int32_t group_size, int8_t* wq, float* s_w,
+                                        void* stream) {
+    if (!w_f16 || !wq || !s_w) return CIDER_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || group_size < 0) return CIDER_ERR_INVALID_ARG;
+    if (group_size != 0 && K % group_size != 0) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    const int64_t gs = group_size ? group_size : K;
+    return from_cuda(launch_quant_groups(static_cast<const __half*>(w_f16), N, K, gs, 127,
+                                         QuantOut::kInt8, wq, s_w, sms,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+cider_status cider_pack_weight_int4(const void* w_f16, int64_t N, int64_t K, int32_t group_size,
+                                    uint8_t* wp, float* s_w, void* stream) {
+    if (!w_f16 || !wp || !s_w) return CIDER_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || group_size < 0) return CIDER_ERR_INVALID_ARG;
+    if (K % 8 != 0 || !valid_group(group_size, K, 8)) return CIDER_ERR_UNSUPPORTED;
+    if (!aligned16(w_f16) || !aligned16(wp)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    const int64_t gs = group_size ? group_size : K;
+    return from_cuda(launch_quant_groups(static_cast<const __half*>(w_f16), N, K, gs, 7,
+                                         QuantOut::kInt4, wp, s_w, sms,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bits, int32_t group_size) {
+    (void)group_size;
+    if (M <= 1 || N <= 0 || K <= 0 || (bits != 8 && bits != 4)) return 0;
+    return workspace_bytes(M, N, K);
+}
+
+cider_status cider_w8a8_gemm_pc(const void* x_f16, int64_t M, int64_t N, int64_t K,
+                                const int8_t* wq, const float* s_w, void* y_f16, void* ws,
+                                size_t ws_bytes, void* stream) {
+    return gemm_common(x_f16, M, N, K, wq, 8, s_w, 0, y_f16, ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+cider_status cider_w8a8_gemm_pg(const void* x_f16, int64_t M, int64_t N, int64_t K,
+                                const int8_t* wq, const float* s_w, int32_t group_size,
+                                void* y_f16, void* ws, size_t ws_bytes, void* stream) {
+    if (group_size <= 0) return CIDER_ERR_INVALID_ARG;
+    return gemm_common(x_f16, M, N, K, wq, 8, s_w, group_size, y_f16, ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+cider_status cider_w4a8_gemm(const void* x_f16, int64_t M, int64_t N, int64_t K,
+                             const uint8_t* wp, const float* s_w, int32_t group_size, void* y_f16,
+                             void* ws, size_t ws_bytes, void* stream) {
+    return gemm_common(x_f16, M, N, K, wp, 4, s_w, group_size, y_f16, ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, const void* w,
+                             const float* s_w, int32_t bits, int32_t group_size, void* y_f16,
+                             void* stream) {
+    if (!x_f16 || !w || !s_w || !y_f16) return CIDER_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || group_size < 0) return CIDER_ERR_INVALID_ARG;
+    if (bits != 8 && bits != 4) return CIDER_ERR_INVALID_ARG;
+    if (K > 16384 || K % (bits == 8 ? 16 : 32) != 0) return CIDER_ERR_UNSUPPORTED;
+    if (!valid_group(group_size, K, bits == 8 ? 16 : 32)) return CIDER_ERR_UNSUPPORTED;
+    if (!aligned16(x_f16) || !aligned16(w)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    GemvArgs g{static_cast<const __half*>(x_f16), K, N, w, s_w, bits, group_size,
+               static_cast<__half*>(y_f16)};
+    return from_cuda(launch_gemv(g, sms, static_cast<cudaStream_t>(stream)));
+}
+
+cider_status cider_act_image(const void* x_f16, int64_t M, int64_t K, void* a_img, float* s_a,
+                             void* stream) {
+    if (!x_f16 || !a_img || !s_a) return CIDER_ERR_INVALID_ARG;
+    if (M <= 0 || K <= 0) return CIDER_ERR_INVALID_ARG;
+    if (K % 8 != 0 || !aligned16(x_f16) || !aligned16(a_img)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    return from_cuda(launch_quant_groups(static_cast<const __half*>(x_f16), M, K, K, 127,
+                                         QuantOut::kF16, a_img, s_a, sms,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+cider_status cider_weight_image(const void* w, int64_t N, int64_t K, int32_t bits, void* b_img,
+                                void* stream) {
+    if (!w || !b_img) return CIDER_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || (bits != 8 && bits != 4)) return CIDER_ERR_INVALID_ARG;
+    if ((N * K) % 32 != 0 || !aligned16(w) || !aligned16(b_img)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(bits == 8 ? launch_widen_i8(static_cast<const int8_t*>(w), N * K,
+                                                 static_cast<__half*>(b_img), sms, s)
+                               : launch_widen_i4(static_cast<const uint8_t*>(w), N * K,
+                                                 static_cast<__half*>(b_img), sms, s));
+}
+
+cider_status cider_gemm_images(const void* a_img, const float* s_a, const void* b_img,
+                               const float* s_w, int64_t M, int64_t N, int64_t K,
+                               int32_t group_size, void* y_f16, void* stream) {
+    if (!a_img || !s_a || !b_img || !s_w || !y_f16) return CIDER_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || group_size < 0) return CIDER_ERR_INVALID_ARG;
+    if (K % 16 != 0 || !valid_group(group_size, K, 64)) return CIDER_ERR_UNSUPPORTED;
+    if (!aligned16(a_img) || !aligned16(b_img) || !aligned16(y_f16) || !aligned16(s_w))
+        return CIDER_ERR_UNSUPPORTED;
+    if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    unsigned long long* status = nullptr;
+    if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
+    GemmArgs a{};
+    a.a_img = static_cast<const __half*>(a_img);
+    a.b_img = static_cast<const __half*>(b_img);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.group_size = group_size;
+    a.s_a = s_a;
+    a.s_w = s_w;
+    a.out = y_f16;
+    a.mode = (group_size == 0) ? GemmMode::kPcF16 : GemmMode::kPgF16;
+    a.timeout_ns = kWaitTimeoutNs;
+    a.status = status;
+    return from_cuda(launch_gemm_tc(a, sms, static_cast<cudaStream_t>(stream)));
+}
+
+cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int64_t N, int64_t K,
+                                 int32_t bits, int32_t group_size, int32_t* out, void* ws,
+                                 size_t ws_bytes, void* stream) {
+    if (!q || !w || !out) return CIDER_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || group_size < 0 || (bits != 8 && bits != 4))
+        return CIDER_ERR_INVALID_ARG;
+    if (K % 32 != 0 || !valid_group(group_size, K, 64)) return CIDER_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(w) || !aligned16(out)) return CIDER_ERR_UNSUPPORTED;
+    const int64_t Mw = M < 2 ? 2 : M;
+    if (!ws || ws_bytes < workspace_bytes(Mw, N, K)) return CIDER_ERR_WORKSPACE;
+    if (!aligned16(ws)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    unsigned long long* status = nullptr;
+    if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Workspace wsp = carve(ws, Mw, N, K);
+    cudaError_t e = launch_widen_i8(q, M * K, wsp.a_img, sms, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, wsp.b_img, sms, s)
+                    : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, wsp.b_img, sms, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    GemmArgs a{};
+    a.a_img = wsp.a_img;
+    a.b_img = wsp.b_img;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.group_size = group_size;
+    a.s_a = nullptr;
+    a.s_w = nullptr;
+    a.out = out;
+    a.mode = (group_size == 0) ? GemmMode::kRawS32 : GemmMode::kRawPgS32;
+    a.timeout_ns = kWaitTimeoutNs;
+    a.status = status;
+    return from_cuda(launch_gemm_tc(a, sms, s));
+}
+
+cider_status cider_device_status(void* stream, uint32_t* site) {
+    unsigned long long v = 0;
+    if (read_and_clear_device_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CIDER_ERR_CUDA;
+    if (site) *site = static_cast<uint32_t>(v & 0xFFFFFFFFu);
+    if ((v >> 32) == kDevTimeout) return CIDER_ERR_TIMEOUT;
+    return v == 0 ? CIDER_OK : CIDER_ERR_CUDA;
+}
+
+cider_status cider_test_wait_timeout(int64_t timeout_ns, void* stream) {
+    if (timeout_ns <= 0 || timeout_ns > 10000000000ll) return CIDER_ERR_INVALID_ARG;
+    return from_cuda(launch_wait_timeout_probe((uint64_t)timeout_ns,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,522 @@
+// INT8 x INT8 -> INT32 GEMM with fused dequant, on the sm_103a tensor cores.
+//
+// What it computes (Cider README, sections "Metal Kernel Pipeline" and
+// "Quantization"): acc[m,n] = sum_k q[m,k] * wq[n,k] exactly in int32, then
+//   per-channel: y = fp16(((float)acc * s_a[m]) * s_w[n])            (C = C_int32 * s_act * s_weight)
+//   per-group:   f = sum over groups g, ascending, of (float)P_g * s_w[n,g]; y = fp16(f * s_a[m])
+// where P_g is the int32 partial over the g-th group of K.
+//
+// How (B300): tcgen05 has no integer MMA kind on sm_103a, so the codes
+// (integers in [-127, 127]) are held exactly as fp16 and multiplied with
+// tcgen05.mma kind::f16 into an fp32 accumulator in tensor memory. Every
+// product is an integer of magnitude <= 127^2, exact in fp32, and every
+// partial sum over at most 1024 consecutive k is an integer of magnitude
+// <= 127^2 * 1024 < 2^24, so the fp32 accumulator holds it exactly. K is
+// therefore cut into segments of at most 1024 (per-channel) or of one group
+// (per-group); each segment accumulates into one of two TMEM buffers, and the
+// epilogue warps fold it - converting the exact fp32 integer to int32 and
+// adding (per-channel), or rescaling and adding in fp32 in ascending group
+// order (per-group) - while the tensor core fills the other buffer.
+//
+// Kernel shape: persistent, one CTA per SM, tile 128 tokens x 256 output
+// channels, 64-deep K stages (one 128-byte swizzle row of fp16), 4-stage TMA
+// ring. Warp 0 issues TMA, warp 1 owns TMEM and issues MMAs (warps 2-3 idle),
+// warps 4..11 are the epilogue (two warps per TMEM lane quadrant, 128 columns
+// each).
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace cider {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
+constexpr int NUM_ROLE_THREADS = 128;  // warpgroup 0: TMA warp, MMA warp, two idle warps
+constexpr int NUM_THREADS = NUM_ROLE_THREADS + NUM_EPI_THREADS;
+constexpr int TMEM_COLS = 512;  // two 256-column fp32 accumulators
+constexpr int MAX_SEG_KB = 16;  // 16 x 64 = 1024 k per exact fp32 segment
+// Register split, per warpgroup (setmaxnreg acts on whole warpgroups): the
+// block is launched with LAUNCH_REGS per thread; warpgroup 0 (the TMA and MMA
+// roles) drops to ROLE_REGS and the two epilogue warpgroups (128 running sums
+// per thread) rise to EPI_REGS. The sum must not exceed the launch allocation
+// (checked at compile time below, and against the built kernel's register
+// count before the first launch).
+constexpr int LAUNCH_REGS = 168;
+constexpr int ROLE_REGS = 96;
+constexpr int EPI_REGS = 200;
+static_assert(NUM_ROLE_THREADS * ROLE_REGS + NUM_EPI_THREADS * EPI_REGS <=
+                  NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+
+struct __align__(8) Barriers {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint64_t epi_sync;  // reusable barrier of the 256 epilogue threads
+};
+
+struct SmemLayout {
+    static constexpr int a_off = 0;
+    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
+    static constexpr int scale_off = b_off + STAGES * B_STAGE_BYTES;  // float[2][BN]
+    static constexpr int bar_off = scale_off + 2 * BN * 4;
+    static constexpr int misc_off = bar_off + (int)sizeof(Barriers);  // tmem base, abort
+    static constexpr int bytes = misc_off + 16;
+    static constexpr int alloc_bytes = bytes + 1024;  // runtime 1024-byte alignment slack
+};
+
+struct Params {
+    int M, N, K;
+    int num_kb;     // k-blocks of 64
+    int seg_kb;     // k-blocks per segment
+    int num_seg;    // segments per tile
+    int G;          // columns of s_w (1 for per-channel)
+    int tiles_m, tiles_n;
+    const float* s_a;
+    const float* s_w;
+    void* out;
+    uint64_t timeout_ns;
+    unsigned long long* status;
+};
+
+// Wait sites recorded in the device status word on a timeout.
+enum : uint32_t {
+    kSiteProducerEmpty = 0x101,
+    kSiteMmaAccEmpty = 0x102,
+    kSiteMmaFull = 0x103,
+    kSiteEpiAccFull = 0x104,
+    kSiteDrain = 0x105,
+    kSiteProducerDrain = 0x106,
+    kSiteEpiSync = 0x107,
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int& tn) {
+    tm = tile % tiles_m;
+    tn = tile / tiles_m;
+}
+
+// Scale for epilogue thread `et` (0..255) in the given segment: s_w[n, g]
+// with n the et-th column of the tile; g = segment (per-group) or 0.
+__device__ __forceinline__ float load_seg_scale(const Params& p, int tn, int seg, int et) {
+    const int n = tn * BN + et;
+    if (n >= p.N || p.s_w == nullptr) return 0.0f;
+    const int g = (p.G == 1) ? 0 : seg;
+    return __ldg(p.s_w + (int64_t)n * p.G + g);
+}
+
+template <GemmMode MODE>
+__global__ void __maxnreg__(LAUNCH_REGS)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Barriers* bars = reinterpret_cast<Barriers*>(smem + SmemLayout::bar_off);
+    float* scales = reinterpret_cast<float*>(smem + SmemLayout::scale_off);
+    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_tiles = p.tiles_m * p.tiles_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->acc_full[b]), 1);
+            mbar_init(smem_u32(&bars->acc_empty[b]), NUM_EPI_THREADS);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        mbar_init(smem_u32(&bars->epi_sync), NUM_EPI_THREADS);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_base_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    // Scales of this CTA's first segment.
+    if (warp >= 4 && (int)blockIdx.x < num_tiles) {
+        int tm, tn;
+        tile_coords(blockIdx.x, p.tiles_m, tm, tn);
+        scales[threadIdx.x - NUM_ROLE_THREADS] =
+            load_seg_scale(p, tn, 0, threadIdx.x - NUM_ROLE_THREADS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_base_slot;
+
+    if (warp < 4) {
+      setmaxnreg_dec<ROLE_REGS>();  // all of warpgroup 0
+      if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                int tm, tn;
+                tile_coords(tile, p.tiles_m, tm, tn);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1, p.timeout_ns,
+                                           abort_flag, p.status, kSiteProducerEmpty))
+                        goto producer_done;
+                    const uint32_t fb = smem_u32(&bars->full[stage]);
+                    mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
+                    tma_load_2d(smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES), &tmap_a,
+                                fb, kb * BK, tm * BM);
+                    tma_load_2d(smem_u32(smem + SmemLayout::b_off + stage * B_STAGE_BYTES), &tmap_b,
+                                fb, kb * BK, tn * BN);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        producer_done:
+            if (*abort_flag) {
+                // Let every tile load already issued land before the CTA exits.
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s))
+                        mbar_wait_bounded(smem_u32(&bars->full[s]), (issued_phase >> s) & 1,
+                                          p.timeout_ns, abort_flag, p.status, kSiteProducerDrain);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32acc(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t seg_count = 0;
+            bool issued_any = false;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
+                    const uint32_t b = seg_count & 1;
+                    const uint32_t acc_phase = (seg_count >> 1) & 1;
+                    if (!mbar_wait_bounded(smem_u32(&bars->acc_empty[b]), acc_phase ^ 1,
+                                           p.timeout_ns, abort_flag, p.status, kSiteMmaAccEmpty))
+                        goto mma_done;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + b * BN;
+                    const int kb0 = seg * p.seg_kb;
+                    const int kb1 = min(p.num_kb, kb0 + p.seg_kb);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, p.timeout_ns,
+                                               abort_flag, p.status, kSiteMmaFull))
+                            goto mma_done;
+                        tc_fence_after();
+                        const uint64_t adesc = smem_desc_sw128_kmajor(
+                            smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES));
+                        const uint64_t bdesc = smem_desc_sw128_kmajor(
+                            smem_u32(smem + SmemLayout::b_off + stage * B_STAGE_BYTES));
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            // +32 bytes along K per 16-element step (encoded >> 4).
+                            tc_mma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                       (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
+                        issued_any = true;
+                        tc_commit(smem_u32(&bars->empty[stage]));
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    tc_commit(smem_u32(&bars->acc_full[b]));
+                }
+            }
+        mma_done:
+            if (*abort_flag && issued_any) {
+                // Every MMA issued so far must finish before TMEM is released.
+                tc_commit(smem_u32(&bars->drain));
+                mbar_wait_bounded(smem_u32(&bars->drain), 0, p.timeout_ns, abort_flag, p.status,
+                                  kSiteDrain);
+            }
+        }
+      }
+    } else {
+        setmaxnreg_inc<EPI_REGS>();  // all of warpgroups 1 and 2
+        // ------------------------------ epilogue ----------------------------
+        const int ewarp = warp - 4;                  // 0..7
+        const int quad = warp & 3;                   // TMEM lane quadrant this warp may access
+        const int half = ewarp >> 2;                 // column half: 0 -> [0,128), 1 -> [128,256)
+        const int et = threadIdx.x - NUM_ROLE_THREADS;  // 0..255
+        const int row_in_tile = quad * 32 + lane;
+        uint32_t seg_count = 0;
+        uint32_t epi_phase = 0;
+        uint32_t acc[128];  // int32 running sum (per-channel) or fp32 running sum (per-group)
+
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int tm, tn;
+            tile_coords(tile, p.tiles_m, tm, tn);
+            const int m = tm * BM + row_in_tile;
+            const int n_half = tn * BN + half * 128;
+
+            for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
+                const uint32_t b = seg_count & 1;
+                const uint32_t acc_phase = (seg_count >> 1) & 1;
+                const float* sc = scales + (seg_count & 1) * BN + half * 128;
+
+                // Prefetch the next segment's scale into a register.
+                float next_scale = 0.0f;
+                {
+                    int nt = tile, ns = seg + 1;
+                    if (ns == p.num_seg) {
+                        ns = 0;
+                        nt += gridDim.x;
+                    }
+                    if (nt < num_tiles) {
+                        int ntm, ntn;
+                        tile_coords(nt, p.tiles_m, ntm, ntn);
+                        next_scale = load_seg_scale(p, ntn, ns, et);
+                    }
+                }
+
+                {
+                    // Every lane waits; the warp leaves together if any lane gave up,
+                    // so the warp-wide tcgen05.ld below is always issued by all lanes.
+                    const bool ok = mbar_wait_bounded(smem_u32(&bars->acc_full[b]), acc_phase,
+                                                      p.timeout_ns, abort_flag, p.status,
+                                                      kSiteEpiAccFull);
+                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                }
+                tc_fence_after();
+
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                       b * BN + half * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // 8 chunks of 16 columns
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(t_row + c * 16, v);
+                    tmem_wait_ld();
+                    if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int part = __float2int_rn(__uint_as_float(v[j]));
+                            acc[c * 16 + j] = (seg == 0) ? (uint32_t)part
+                                                         : (uint32_t)((int)acc[c * 16 + j] + part);
+                        }
+                    } else if constexpr (MODE == GemmMode::kPgF16) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 s4 = *reinterpret_cast<const float4*>(sc + c * 16 + j);
+                            const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float prev =
+                                    (seg == 0) ? 0.0f : __uint_as_float(acc[c * 16 + j + i]);
+                                const float prod = __fmul_rn(__uint_as_float(v[j + i]), ss[i]);
+                                acc[c * 16 + j + i] = __float_as_uint(__fadd_rn(prev, prod));
+                            }
+                        }
+                    } else {  // kRawPgS32: write this group's partials directly
+                        if (m < p.M) {
+                            int32_t* out = static_cast<int32_t*>(p.out);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int n = n_half + c * 16 + j;
+                                if (n < p.N)
+                                    out[((int64_t)m * p.N + n) * p.G + seg] =
+                                        __float2int_rn(__uint_as_float(v[j]));
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars->acc_empty[b]));
+
+                // Final segment of the tile: dequantize and store.
+                if (seg == p.num_seg - 1 && m < p.M &&
+                    (MODE == GemmMode::kPcF16 || MODE == GemmMode::kPgF16 ||
+                     MODE == GemmMode::kRawS32)) {
+                    const float sa = (MODE == GemmMode::kRawS32) ? 0.0f : __ldg(p.s_a + m);
+                    const bool vec_ok = ((p.N & 7) == 0);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {  // 16 groups of 8 columns
+                        const int n0 = n_half + c * 8;
+                        if (n0 >= p.N) break;
+                        if constexpr (MODE == GemmMode::kRawS32) {
+                            int32_t* out = static_cast<int32_t*>(p.out) + (int64_t)m * p.N;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (n0 + j < p.N) out[n0 + j] = (int)acc[c * 8 + j];
+                        } else {
+                            uint32_t h2[4];
+#pragma unroll
+                            for (int j = 0; j < 8; j += 2) {
+                                float y0, y1;
+                                if constexpr (MODE == GemmMode::kPcF16) {
+                                    y0 = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[c * 8 + j]), sa),
+                                                   sc[c * 8 + j]);
+                                    y1 = __fmul_rn(
+                                        __fmul_rn(__int2float_rn((int)acc[c * 8 + j + 1]), sa),
+                                        sc[c * 8 + j + 1]);
+                                } else {
+                                    y0 = __fmul_rn(__uint_as_float(acc[c * 8 + j]), sa);
+                                    y1 = __fmul_rn(__uint_as_float(acc[c * 8 + j + 1]), sa);
+                                }
+                                const __half2 hv = __floats2half2_rn(y0, y1);
+                                h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                            }
+                            __half* out = static_cast<__half*>(p.out) + (int64_t)m * p.N + n0;
+                            if (vec_ok && n0 + 8 <= p.N) {
+                                *reinterpret_cast<uint4*>(out) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                            } else {
+                                const __half* hh = reinterpret_cast<const __half*>(h2);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    if (n0 + j < p.N) out[j] = hh[j];
+                            }
+                        }
+                    }
+                }
+
+                // Publish the next segment's scales (all epilogue threads are
+                // done with the buffer being overwritten after this barrier).
+                scales[((seg_count + 1) & 1) * BN + et] = next_scale;
+                mbar_arrive(smem_u32(&bars->epi_sync));
+                {
+                    const bool ok = mbar_wait_bounded(smem_u32(&bars->epi_sync), epi_phase,
+                                                      p.timeout_ns, abort_flag, p.status,
+                                                      kSiteEpiSync);
+                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                    epi_phase ^= 1;
+                }
+            }
+        }
+    epi_done:;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace gemm
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+template <GemmMode MODE>
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p,
+                        int grid, cudaStream_t stream) {
+    auto kern = gemm::gemm_tc_kernel<MODE>;
+    static bool attr_set = false;  // benign race: setting the same value twice
+    if (!attr_set) {
+        // The in-kernel register split assumes exactly LAUNCH_REGS per thread at
+        // launch; refuse to launch a build that differs (it could not rebalance).
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != gemm::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm::SmemLayout::alloc_bytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    kern<<<grid, gemm::NUM_THREADS, gemm::SmemLayout::alloc_bytes, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+CUresult encode_tmap_f16_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                                uint32_t box_rows, uint32_t box_cols) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t elem_strides[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+    using namespace gemm;
+    if (a.M <= 0 || a.N <= 0 || a.K <= 0 || a.K % 16 != 0) return cudaErrorInvalidValue;
+    if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2)
+        return cudaErrorInvalidValue;
+    CUtensorMap ta, tb;
+    if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS ||
+        encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN, BK) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    Params p{};
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.num_kb = (p.K + BK - 1) / BK;
+    const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
+    if (per_group) {
+        if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
+            return cudaErrorInvalidValue;
+        p.seg_kb = a.group_size / BK;
+        p.G = p.K / a.group_size;
+    } else {
+        const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        p.seg_kb = (p.num_kb + nseg - 1) / nseg;
+        p.G = 1;
+    }
+    p.num_seg = (p.num_kb + p.seg_kb - 1) / p.seg_kb;
+    p.tiles_m = (p.M + BM - 1) / BM;
+    p.tiles_n = (p.N + BN - 1) / BN;
+    p.s_a = a.s_a;
+    p.s_w = a.s_w;
+    p.out = a.out;
+    p.timeout_ns = a.timeout_ns;
+    p.status = a.status;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    switch (a.mode) {
+        case GemmMode::kPcF16: return launch_mode<GemmMode::kPcF16>(ta, tb, p, grid, stream);
+        case GemmMode::kPgF16: return launch_mode<GemmMode::kPgF16>(ta, tb, p, grid, stream);
+        case GemmMode::kRawS32: return launch_mode<GemmMode::kRawS32>(ta, tb, p, grid, stream);
+        case GemmMode::kRawPgS32: return launch_mode<GemmMode::kRawPgS32>(ta, tb, p, grid, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace cider

@@ -1,0 +1,74 @@
+// Internal launcher declarations shared by the C-ABI layer and the kernel
+// translation units (host side only; not part of the public interface).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace cider {
+
+enum class QuantOut : int { kInt8 = 0, kF16 = 1, kInt4 = 2 };
+
+// Symmetric quantization of `rows` x K fp16 values in groups of `gs`
+// consecutive elements of a row (gs == K: one group per row), scale =
+// absmax / qmax; codes written as int8, as exact fp16 integers, or as packed
+// nibbles (code + 8, two per byte). scales: [rows, K / gs].
+cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int64_t gs, int qmax,
+                                QuantOut out_kind, void* out, float* scales, int num_sms,
+                                cudaStream_t stream);
+
+// Operand images: INT8 codes / packed INT4 nibbles -> exact fp16 integers.
+cudaError_t launch_widen_i8(const int8_t* src, int64_t n, __half* dst, int num_sms,
+                            cudaStream_t stream);
+cudaError_t launch_widen_i4(const uint8_t* src, int64_t n_codes, __half* dst, int num_sms,
+                            cudaStream_t stream);
+
+// ---- tensor-core GEMM over fp16 operand images ------------------------------
+enum class GemmMode : int {
+    kPcF16 = 0,     // y = fp16(((float)acc * s_a[m]) * s_w[n])
+    kPgF16 = 1,     // f = sum_g (float)P_g * s_w[n,g] (ascending g); y = fp16(f * s_a[m])
+    kRawS32 = 2,    // out int32 [M,N] = acc
+    kRawPgS32 = 3,  // out int32 [M,N,G] = P_g
+};
+
+struct GemmArgs {
+    const __half* a_img;  // [M, K] fp16 codes (tokens)
+    const __half* b_img;  // [N, K] fp16 codes (weights)
+    int64_t M, N, K;
+    int group_size;       // 0 for per-channel / raw totals
+    const float* s_a;     // [M]
+    const float* s_w;     // [N] or [N, K/gs]
+    void* out;
+    GemmMode mode;
+    uint64_t timeout_ns;
+    unsigned long long* status;  // device status word
+};
+
+cudaError_t launch_gemm_tc(const GemmArgs& args, int num_sms, cudaStream_t stream);
+
+// ---- M = 1 GEMV (quantizes x per CTA, int32 dot products, same epilogue) ----
+struct GemvArgs {
+    const __half* x;     // [K]
+    int64_t K, N;
+    const void* w;       // int8 [N, K] or packed int4 [N, K/2]
+    const float* s_w;    // [N] or [N, K/gs]
+    int bits;            // 8 or 4
+    int group_size;      // 0, 64 or 128 (w4: 0 or 128, any multiple of 32)
+    __half* y;           // [N]
+};
+
+cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
+
+// ---- device status --------------------------------------------------------
+// Address of the current device's status word (looked up once per device).
+cudaError_t device_status_ptr(unsigned long long** ptr);
+cudaError_t read_and_clear_device_status(unsigned long long* value, cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t stream);
+
+// Host-side encoder for a 2D fp16 K-major tile map with 128-byte swizzle.
+CUresult encode_tmap_f16_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                                uint32_t box_rows, uint32_t box_cols);
+
+}  // namespace cider

@@ -1,0 +1,230 @@
+// Symmetric min-max quantization kernels (activations per token, weights per
+// output channel or per group, INT4 packing) and the operand-image kernels
+// that widen INT8 / INT4 codes to exact fp16 integers for the tensor cores.
+//
+// Definition (Cider README, section "Quantization"): activations are
+// symmetric INT8 per token; W8A8 weights symmetric INT8 per channel or per
+// group of 64/128; W4A8 weights symmetric INT4 stored with zero point 8.
+// Scale = absmax / qmax (fp32, IEEE division), code = clamp(rint(x / scale))
+// with ties to even, an all-zero block has scale 0 and codes 0.
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace cider {
+
+namespace {
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// One code: clamp(rint(x / s), -qmax, qmax); s == 0 only for all-zero blocks.
+__device__ __forceinline__ int quant_one(float x, float s, int qmax) {
+    if (s == 0.0f) return 0;
+    int q = __float2int_rn(__fdiv_rn(x, s));
+    q = q > qmax ? qmax : q;
+    q = q < -qmax ? -qmax : q;
+    return q;
+}
+
+template <QuantOut OUT>
+__device__ __forceinline__ void store_codes8(void* out, int64_t elem, const int (&q)[8]) {
+    if constexpr (OUT == QuantOut::kInt8) {
+        uint32_t lo = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
+                      ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
+        uint32_t hi = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
+                      ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
+        *reinterpret_cast<uint2*>(static_cast<int8_t*>(out) + elem) = make_uint2(lo, hi);
+    } else if constexpr (OUT == QuantOut::kF16) {
+        __half2 h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            h[i] = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+        *reinterpret_cast<uint4*>(static_cast<__half*>(out) + elem) =
+            *reinterpret_cast<const uint4*>(h);
+    } else {  // kInt4: nibble = code + 8, element 2j in the low nibble of byte j
+        uint32_t w = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w |= (uint32_t)((q[i] + 8) & 0xF) << (4 * i);
+        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(out) + elem / 2) = w;
+    }
+}
+
+template <QuantOut OUT>
+__device__ __forceinline__ void store_code1(void* out, int64_t elem, int q) {
+    if constexpr (OUT == QuantOut::kInt8) {
+        static_cast<int8_t*>(out)[elem] = (int8_t)q;
+    } else if constexpr (OUT == QuantOut::kF16) {
+        static_cast<__half*>(out)[elem] = __int2half_rn(q);
+    }
+}
+
+// One warp per (row, group). Vector path: 16-byte loads of 8 fp16 values;
+// requires K % 8 == 0 and gs % 8 == 0 (the host checks alignment).
+template <QuantOut OUT>
+__global__ void __launch_bounds__(256) quant_groups_vec_kernel(const __half* __restrict__ src,
+                                                               int64_t rows, int64_t K, int64_t gs,
+                                                               int qmax, void* __restrict__ out,
+                                                               float* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const int64_t G = K / gs;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t nvec = gs >> 3;
+    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         item < rows * G; item += nwarps) {
+        const int64_t row = item / G, g = item - row * G;
+        const int64_t base = row * K + g * gs;
+        const uint4* p = reinterpret_cast<const uint4*>(src + base);
+        __half2 hm = __float2half2_rn(0.0f);
+        for (int64_t v = lane; v < nvec; v += 32) {
+            uint4 u = __ldg(p + v);
+            const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hm = __hmax2(hm, __habs2(h[i]));
+        }
+        float amax = fmaxf(__low2float(hm), __high2float(hm));
+        amax = warp_max(amax);
+        const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
+        if (lane == 0) scales[item] = s;
+        for (int64_t v = lane; v < nvec; v += 32) {
+            uint4 u = __ldg(p + v);
+            const __half* h = reinterpret_cast<const __half*>(&u);
+            int q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = quant_one(__half2float(h[i]), s, qmax);
+            store_codes8<OUT>(out, base + v * 8, q);
+        }
+    }
+}
+
+// Scalar fallback for shapes the vector path does not take (int8 / fp16 out).
+template <QuantOut OUT>
+__global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const __half* __restrict__ src,
+                                                                  int64_t rows, int64_t K,
+                                                                  int64_t gs, int qmax,
+                                                                  void* __restrict__ out,
+                                                                  float* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const int64_t G = K / gs;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         item < rows * G; item += nwarps) {
+        const int64_t row = item / G, g = item - row * G;
+        const int64_t base = row * K + g * gs;
+        float amax = 0.0f;
+        for (int64_t k = lane; k < gs; k += 32) amax = fmaxf(amax, fabsf(__half2float(src[base + k])));
+        amax = warp_max(amax);
+        const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
+        if (lane == 0) scales[item] = s;
+        for (int64_t k = lane; k < gs; k += 32)
+            store_code1<OUT>(out, base + k, quant_one(__half2float(src[base + k]), s, qmax));
+    }
+}
+
+// INT8 codes -> exact fp16 integers (operand image), 16 codes per thread step.
+__global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t* __restrict__ src, int64_t n16,
+                                                       __half* __restrict__ dst) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        int4 u = __ldg(reinterpret_cast<const int4*>(src) + i);
+        const int8_t* b = reinterpret_cast<const int8_t*>(&u);
+        __half2 h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            h[j] = __halves2half2(__short2half_rn(b[2 * j]), __short2half_rn(b[2 * j + 1]));
+        uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
+        d[0] = *reinterpret_cast<const uint4*>(&h[0]);
+        d[1] = *reinterpret_cast<const uint4*>(&h[4]);
+    }
+}
+
+// Packed INT4 (nibble = code + 8, element 2j in the low nibble of byte j) ->
+// exact fp16 integers, 32 codes (16 bytes) per thread step.
+__global__ void __launch_bounds__(256) widen_i4_kernel(const uint8_t* __restrict__ src,
+                                                       int64_t n16, __half* __restrict__ dst) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + i);
+        const uint8_t* b = reinterpret_cast<const uint8_t*>(&u);
+        __half2 h[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            h[j] = __halves2half2(__short2half_rn((short)(b[j] & 0xF) - 8),
+                                  __short2half_rn((short)(b[j] >> 4) - 8));
+        uint4* d = reinterpret_cast<uint4*>(dst) + 4 * i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[j] = *reinterpret_cast<const uint4*>(&h[4 * j]);
+    }
+}
+
+int grid_for(int64_t work_items, int per_block, int num_sms) {
+    int64_t b = (work_items + per_block - 1) / per_block;
+    int64_t cap = (int64_t)num_sms * 16;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int64_t gs, int qmax,
+                                QuantOut out_kind, void* out, float* scales, int num_sms,
+                                cudaStream_t stream) {
+    const int64_t items = rows * (K / gs);
+    const bool vec = (K % 8 == 0) && (gs % 8 == 0) &&
+                     (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+    const int grid = grid_for(items, 8, num_sms);
+    if (vec) {
+        switch (out_kind) {
+            case QuantOut::kInt8:
+                quant_groups_vec_kernel<QuantOut::kInt8>
+                    <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
+                break;
+            case QuantOut::kF16:
+                quant_groups_vec_kernel<QuantOut::kF16>
+                    <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
+                break;
+            case QuantOut::kInt4:
+                quant_groups_vec_kernel<QuantOut::kInt4>
+                    <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
+                break;
+        }
+    } else {
+        switch (out_kind) {
+            case QuantOut::kInt8:
+                quant_groups_scalar_kernel<QuantOut::kInt8>
+                    <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
+                break;
+            case QuantOut::kF16:
+                quant_groups_scalar_kernel<QuantOut::kF16>
+                    <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
+                break;
+            case QuantOut::kInt4:
+                return cudaErrorInvalidValue;  // packing needs the vector path
+        }
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_i8(const int8_t* src, int64_t n, __half* dst, int num_sms,
+                            cudaStream_t stream) {
+    if (n % 16 != 0) return cudaErrorInvalidValue;
+    const int64_t n16 = n / 16;
+    widen_i8_kernel<<<grid_for(n16, 256, num_sms), 256, 0, stream>>>(src, n16, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_i4(const uint8_t* src, int64_t n_codes, __half* dst, int num_sms,
+                            cudaStream_t stream) {
+    if (n_codes % 32 != 0) return cudaErrorInvalidValue;
+    const int64_t n16 = n_codes / 32;
+    widen_i4_kernel<<<grid_for(n16, 256, num_sms), 256, 0, stream>>>(src, n16, dst);
+    return cudaGetLastError();
+}
+
+}  // namespace cider
