@@ -29,9 +29,7 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -47,7 +45,7 @@ FLUSH_BYTES = 512 << 20
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("cider", "reference"), default="cider")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -74,55 +72,66 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event (throttle) reasons of one GPU, polled through
+    NVML (the data nvidia-smi reports) every 2 ms from a thread while the
+    timed region runs."""
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"))
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.out = None
+    def __init__(self, torch_device_index: int):
+        self.idx = torch_device_index
+        self.samples = []
+        self.error = None
+        self._stop = None
+        self._thread = None
 
     def start(self):
+        import threading
         try:
-            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.out, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            uuid = str(torch.cuda.get_device_properties(self.idx).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self._smax = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+        except Exception as exc:  # no NVML: report why instead of clocks
+            self.error = f"{type(exc).__name__}: {exc}"
+            return
+        self._stop = threading.Event()
+
+        def poll():
+            while True:
+                try:
+                    sm = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+                    rs = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+                    self.samples.append((sm, rs))
+                except Exception as exc:
+                    self.error = f"{type(exc).__name__}: {exc}"
+                if self._stop.wait(0.002):
+                    break
+
+        self._thread = threading.Thread(target=poll, daemon=True)
+        self._thread.start()
+        while not self.samples and self.error is None:  # first sample before the region
+            time.sleep(0.001)
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.out.flush()
-        self.out.seek(0)
-        rows = [ln.strip().split(", ") for ln in self.out.read().splitlines() if ln.strip()]
-        os.unlink(self.out.name)
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for r in rows:
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if self._thread is None:
+            return {"error": self.error} if self.error else None
+        self._stop.set()
+        self._thread.join()
+        import pynvml
+        reasons = set()
+        for _, rs in self.samples:
+            for name, const in self.REASONS:
+                if rs & getattr(pynvml, const):
+                    reasons.add(name)
+        sm = [s for s, _ in self.samples]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self._smax,
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
 
 
 # ---------------------------------------------------------------------------
