@@ -163,6 +163,31 @@ CIDER_API cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, 
                              void* stream);
 
 /*
+ * cider_w8a8_gemm_pc without a caller workspace, for callers that cannot
+ * allocate device memory (for example code running under a framework that
+ * owns every device allocation through its own pool, or a latency-critical
+ * loop that must not pay cudaMalloc's implicit synchronization). The pages
+ * describe no counterpart of this entry point.
+ *   Same arguments, layouts and result as cider_w8a8_gemm_pc minus ws /
+ *   ws_bytes; M == 1 is computed by the tensor-core GEMM (no GEMV routing,
+ *   same bits). The scratch (fp16 operand images of the codes and the
+ *   token scales, 2*M*K + 4*M + 2*N*K bytes, each part rounded up to 256)
+ *   comes from one 64 MiB array compiled into the library
+ *   (CIDER_STATIC_SCRATCH_BYTES); larger problems return
+ *   CIDER_ERR_WORKSPACE and enqueue nothing. The call allocates nothing.
+ *   The first call on a device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   All calls on a device share the array: calls whose execution overlaps
+ *   on the GPU (other streams, other threads) race and must be serialized.
+ *   Every GPU that loads the library keeps the array until the process
+ *   exits.
+ */
+#define CIDER_STATIC_SCRATCH_BYTES (64u << 20)
+CIDER_API cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M, int64_t N,
+                                                  int64_t K, const int8_t* wq, const float* s_w,
+                                                  void* y_f16, void* stream);
+
+/*
  * The three stages the GEMM entry points above run, exposed so a caller can
  * time them separately or keep a weight image across calls. The tensor
  * cores of sm_103a have no integer MMA kind, so the library multiplies the

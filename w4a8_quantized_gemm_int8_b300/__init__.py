@@ -24,6 +24,7 @@ ABI_FUNCTIONS = (
     "cider_status_string", "cider_abi_version", "cider_quantize_act",
     "cider_quantize_weight_int8", "cider_pack_weight_int4", "cider_workspace_bytes",
     "cider_w8a8_gemm_pc", "cider_w8a8_gemm_pg", "cider_w4a8_gemm", "cider_int8_gemv",
+    "cider_w8a8_gemm_pc_noalloc",
     "cider_act_image", "cider_weight_image", "cider_gemm_images",
     "cider_test_gemm_s32", "cider_device_status", "cider_test_wait_timeout",
 )
@@ -64,6 +65,7 @@ def load_library():
             "cider_w8a8_gemm_pg": ([p, i64, i64, i64, p, p, i32, p, p, sz, p], ctypes.c_int),
             "cider_w4a8_gemm": ([p, i64, i64, i64, p, p, i32, p, p, sz, p], ctypes.c_int),
             "cider_int8_gemv": ([p, i64, i64, p, p, i32, i32, p, p], ctypes.c_int),
+            "cider_w8a8_gemm_pc_noalloc": ([p, i64, i64, i64, p, p, p, p], ctypes.c_int),
             "cider_act_image": ([p, i64, i64, p, p, p], ctypes.c_int),
             "cider_weight_image": ([p, i64, i64, i32, p, p], ctypes.c_int),
             "cider_gemm_images": ([p, p, p, p, i64, i64, i64, i32, p, p], ctypes.c_int),
@@ -196,6 +198,23 @@ def w8a8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor, group_size
         st = lib.cider_w8a8_gemm_pg(xp, M, N, K, wp, sp, group_size, yp, wsp, wsn, _stream())
         _check("cider_w8a8_gemm_pg", st)
     return y
+
+
+STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def w8a8_linear_noalloc(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
+                        out: torch.Tensor) -> torch.Tensor:
+    """W8A8 per-channel layer that allocates nothing: its scratch is a 64 MiB
+    array inside the library, shared by all calls on the device (calls that
+    overlap on the GPU race). ``out`` (fp16 [M,N]) must be provided."""
+    M, K = x.shape
+    N = wq.shape[0]
+    st = load_library().cider_w8a8_gemm_pc_noalloc(
+        _dev(x, torch.float16, "x", 2), M, N, K, _dev(wq, torch.int8, "wq", 2),
+        _dev(s_w, torch.float32, "s_w"), _dev(out, torch.float16, "out", 2), _stream())
+    _check("cider_w8a8_gemm_pc_noalloc", st)
+    return out
 
 
 def w4a8_linear(x: torch.Tensor, wp: torch.Tensor, s_w: torch.Tensor, group_size: int = 0,
