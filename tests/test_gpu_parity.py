@@ -91,6 +91,33 @@ def test_quantize_exhaustive_over_x_for_many_scales():
     assert np.array_equal(host(q), qo)
 
 
+def test_quantize_exhaustive_rows_up_to_16k():
+    """The same exhaustive coverage on rows of 16384 elements (the width the
+    one-pass register kernels take): for each chosen absmax a, a set of rows
+    that each hold a and a window of the fp16 values |x| <= a, both signs."""
+    pos = np.arange(1, 0x7C00, dtype=np.int32)
+    chosen = np.unique(np.concatenate([pos[::211], pos[-12:], pos[:12],
+                                       np.array([0x3C00, 0x57F0, 0x5BF0, 0x7BFF])]))
+    width, win = 16384, 8191
+    rows = []
+    for a in chosen:
+        for lo in range(0, a + 1, win):
+            xs = np.arange(lo, min(lo + win, a + 1), dtype=np.uint16)
+            r = np.zeros(width, np.uint16)
+            r[0] = a
+            r[1:1 + len(xs)] = xs
+            r[1 + win:1 + win + len(xs)] = xs | 0x8000
+            rows.append(r)
+    x = np.stack(rows).view(np.float16)
+    q, s = cider.quantize_act(cuda(torch.from_numpy(x)))
+    qo, so = oracle.quantize_act(x)
+    assert np.array_equal(host(s).view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(host(q), qo)
+    img, s2 = cider.act_image(cuda(torch.from_numpy(x)))
+    assert np.array_equal(host(s2).view(np.uint32), so.view(np.uint32))
+    assert np.array_equal(host(img).astype(np.int32), qo.astype(np.int32))
+
+
 # ---------------------------------------------------------------------------
 # weight preparation
 # ---------------------------------------------------------------------------

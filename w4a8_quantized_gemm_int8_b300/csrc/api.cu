@@ -83,8 +83,10 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
 
     if (M == 1) {  // decode: the GEMV computes the same function
         if (K > 16384 || !valid_group(gs, K, bits == 8 ? 16 : 32)) return CIDER_ERR_UNSUPPORTED;
+        unsigned long long* status = nullptr;
+        if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
         GemvArgs g{static_cast<const __half*>(x), K, N, w, s_w, bits, gs,
-                   static_cast<__half*>(y)};
+                   static_cast<__half*>(y), kWaitTimeoutNs, status};
         return from_cuda(launch_gemv(g, sms, stream));
     }
     if (!valid_group(gs, K, 64)) return CIDER_ERR_UNSUPPORTED;
@@ -217,8 +219,10 @@ cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, const void
     int sms = 0;
     cider_status st = num_sms(&sms);
     if (st != CIDER_OK) return st;
+    unsigned long long* status = nullptr;
+    if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
     GemvArgs g{static_cast<const __half*>(x_f16), K, N, w, s_w, bits, group_size,
-               static_cast<__half*>(y_f16)};
+               static_cast<__half*>(y_f16), kWaitTimeoutNs, status};
     return from_cuda(launch_gemv(g, sms, static_cast<cudaStream_t>(stream)));
 }
 

@@ -197,9 +197,10 @@ __global__ void __maxnreg__(LAUNCH_REGS)
             if (*abort_flag) {
                 // Let every tile load already issued land before the CTA exits.
                 for (int s = 0; s < STAGES; ++s)
-                    if (issued_mask & (1u << s))
-                        mbar_wait_bounded(smem_u32(&bars->full[s]), (issued_phase >> s) & 1,
-                                          p.timeout_ns, abort_flag, p.status, kSiteProducerDrain);
+                    if ((issued_mask & (1u << s)) &&
+                        !mbar_wait_drain(smem_u32(&bars->full[s]), (issued_phase >> s) & 1,
+                                         p.timeout_ns))
+                        report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
             }
         }
     } else if (warp == 1) {
@@ -250,8 +251,8 @@ __global__ void __maxnreg__(LAUNCH_REGS)
             if (*abort_flag && issued_any) {
                 // Every MMA issued so far must finish before TMEM is released.
                 tc_commit(smem_u32(&bars->drain));
-                mbar_wait_bounded(smem_u32(&bars->drain), 0, p.timeout_ns, abort_flag, p.status,
-                                  kSiteDrain);
+                if (!mbar_wait_drain(smem_u32(&bars->drain), 0, p.timeout_ns))
+                    report_device_error(p.status, kDevTimeout, kSiteDrain);
             }
         }
       }

@@ -7,44 +7,59 @@
 // matrix-vector kernel; section "Quantization" for the arithmetic.
 //
 // B300 design: the op is a stream of N*K weight bytes (N*K/2 for INT4) from
-// HBM. Each CTA first quantizes x into shared memory (x is a few KB and sits
-// in L2; its first weight loads are already in flight meanwhile), then each
-// warp walks whole weight rows with 16-byte coalesced loads, eight in flight
-// per lane and the next block issued before the current one is consumed.
-// Dot products use dp4a (4 x int8 -> int32); INT4 nibbles are widened to
-// signed bytes in registers. Per-group partials are reduced across the lanes
-// that hold one group, rescaled, and summed in ascending group order.
+// HBM, so the kernel is built to keep as many bytes in flight as HBM needs.
+// One CTA per SM owns a contiguous slice of weight rows (row-major weights
+// make the slice one contiguous byte range). A producer warp issues bulk
+// asynchronous copies (cp.async.bulk, mbarrier completion) of whole groups of
+// rows into a ring of shared-memory stages at kernel start - for the decode
+// shapes the whole slice fits, so every weight byte is requested at once -
+// while eight consumer warps quantize x into shared memory. Consumers then
+// take rows from the landed stages: dp4a (4 x int8 -> int32) over 16-byte
+// chunks, INT4 nibbles widened to signed bytes in registers. Per-group
+// scales travel in the same stage as their rows (when 16-byte aligned); the
+// per-group partials are rescaled and summed in ascending group order by one
+// lane. Every mbarrier wait is bounded and reports to the device status word.
 #include <cuda_fp16.h>
 #include <cstdint>
 
+#include "device_common.cuh"
 #include "kernels.h"
 
 namespace cider {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 8;           // 16-byte chunks in flight per lane
-constexpr int kMaxK = 16384;         // codes kept in shared memory
-constexpr int kMaxGroups = kMaxK / 32;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kMaxK = 16384;
+constexpr int kStageTarget = 16384;        // weight bytes per stage (at least one row)
+constexpr int kMaxStages = 32;
+constexpr int kUnroll = 4;          // 16-byte chunks per lane loaded before use
 
 struct Params {
     const __half* x;
     int K, N;
-    const uint8_t* w;  // row-major, K bytes (int8) or K/2 bytes (int4) per row
+    const uint8_t* w;  // row-major, row_bytes per row
     const float* s_w;
     int G;             // columns of s_w (1 for per-channel)
     int cpg;           // 16-byte chunks per group (per-group only)
     __half* y;
+    int row_bytes;
+    int rows_per_stage;
+    int stage_bytes;     // weights + staged scales, 128-byte multiple
+    int num_stages;      // ring depth
+    int scales_staged;   // per-group scales copied with their rows
+    int sw_in_smem;      // per-channel scales of the CTA's rows prefetched to shared memory
+    int codes_off, prod_off, sw_off, bar_off, stage_off;
+    uint64_t timeout_ns;
+    unsigned long long* status;
 };
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
+enum : uint32_t {
+    kSiteGemvProducerEmpty = 0x201,
+    kSiteGemvConsumerFull = 0x202,
+    kSiteGemvProducerDrain = 0x203,
+};
 
 __device__ __forceinline__ int dp4a(int a, int b, int c) { return __dp4a(a, b, c); }
 
@@ -84,38 +99,74 @@ __device__ __forceinline__ int chunk_dot(const uint4& wv, const uint4* codes, in
 }
 
 template <int BITS, bool PG>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
-    __shared__ __align__(16) int8_t codes_s[kMaxK];
-    __shared__ float prod_s[PG ? kWarps : 1][PG ? kMaxGroups : 1];
-    __shared__ float red_s[kWarps];
-    __shared__ float sa_s;
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    int8_t* codes_s = reinterpret_cast<int8_t*>(smem + p.codes_off);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* empty = full + kMaxStages;
+    float* red_s = reinterpret_cast<float*>(empty + kMaxStages);  // [kConsumerWarps]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red_s + kConsumerWarps);
+    uint8_t* stages = smem + p.stage_off;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row_bytes = (BITS == 8) ? p.K : p.K / 2;
-    const int nchunk = row_bytes / 16;
-    const int row_stride = gridDim.x * kWarps;
-    const uint4* codes = reinterpret_cast<const uint4*>(codes_s);
+    // This CTA's rows: [n0, n0 + nrows), balanced over the grid.
+    const int n0 = (int)(((int64_t)p.N * blockIdx.x) / gridDim.x);
+    const int nrows = (int)(((int64_t)p.N * (blockIdx.x + 1)) / gridDim.x) - n0;
+    const int R = p.rows_per_stage;
+    const int nst = (nrows + R - 1) / R;
+    const int NS = p.num_stages;
 
-    // Block iterator over (row, first chunk) of this warp's work.
-    int n = blockIdx.x * kWarps + warp;
-    int c0 = 0;
-    uint4 cur[kUnroll];
-    auto load_block = [&](uint4 (&dst)[kUnroll], int rn, int rc0) {
-        const uint4* row = reinterpret_cast<const uint4*>(p.w + (int64_t)rn * row_bytes);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int c = rc0 + u * 32 + lane;
-            if (c < nchunk) dst[u] = ld_stream(row + c);
+    if (threadIdx.x == kConsumers) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), kConsumerWarps);
         }
-    };
-    if (n < p.N) load_block(cur, n, 0);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
 
-    // ---- per-token quantization of x (each CTA, from L2) -------------------
+    if (warp == kConsumerWarps) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            const uint8_t* src = p.w + (int64_t)n0 * p.row_bytes;
+            const uint8_t* ssrc =
+                reinterpret_cast<const uint8_t*>(p.s_w) + (int64_t)n0 * p.G * 4;
+            int issued = 0;
+            for (int s = 0; s < nst; ++s) {
+                const int slot = s % NS;
+                const uint32_t use = (uint32_t)(s / NS);
+                if (!mbar_wait_bounded(smem_u32(&empty[slot]), (use & 1u) ^ 1u, p.timeout_ns,
+                                       abort_flag, p.status, kSiteGemvProducerEmpty))
+                    break;
+                const int rows = min(R, nrows - s * R);
+                const uint32_t wbytes = (uint32_t)rows * p.row_bytes;
+                const uint32_t sbytes = p.scales_staged ? (uint32_t)rows * p.G * 4 : 0u;
+                const uint32_t fb = smem_u32(&full[slot]);
+                uint8_t* dst = stages + (size_t)slot * p.stage_bytes;
+                mbar_arrive_expect_tx(fb, wbytes + sbytes);
+                bulk_load(smem_u32(dst), src + (int64_t)s * R * p.row_bytes, wbytes, fb);
+                if (sbytes)
+                    bulk_load(smem_u32(dst + (size_t)R * p.row_bytes),
+                              ssrc + (int64_t)s * R * p.G * 4, sbytes, fb);
+                issued = s + 1;
+            }
+            // No copy may still be landing when the CTA exits: wait for the
+            // last use of every slot (immediate unless consumers gave up).
+            for (int s = max(0, issued - NS); s < issued; ++s)
+                if (!mbar_wait_drain(smem_u32(&full[s % NS]), (uint32_t)(s / NS) & 1u,
+                                     p.timeout_ns))
+                    report_device_error(p.status, kDevTimeout, kSiteGemvProducerDrain);
+        }
+        return;
+    }
+
+    // -------------------- per-token quantization of x ------------------------
     {
         const uint4* xv = reinterpret_cast<const uint4*>(p.x);
         const int nvec = p.K / 8;
         __half2 hm = __float2half2_rn(0.0f);
-        for (int v = threadIdx.x; v < nvec; v += kThreads) {
+        for (int v = threadIdx.x; v < nvec; v += kConsumers) {
             uint4 u = __ldg(xv + v);
             const __half2* h = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
@@ -125,15 +176,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) red_s[warp] = m;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float a = red_s[0];
-            for (int w = 1; w < kWarps; ++w) a = fmaxf(a, red_s[w]);
-            sa_s = (a == 0.0f) ? 0.0f : __fdiv_rn(a, 127.0f);
-        }
-        __syncthreads();
-        const float s = sa_s;
-        for (int v = threadIdx.x; v < nvec; v += kThreads) {
+        named_bar_sync(1, kConsumers);
+        float a = red_s[0];
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) a = fmaxf(a, red_s[w]);
+        const float s = (a == 0.0f) ? 0.0f : __fdiv_rn(a, 127.0f);
+        for (int v = threadIdx.x; v < nvec; v += kConsumers) {
             uint4 u = __ldg(xv + v);
             const __half* h = reinterpret_cast<const __half*>(&u);
             uint32_t lo = 0, hi = 0;
@@ -151,73 +199,106 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
             }
             reinterpret_cast<uint2*>(codes_s)[v] = make_uint2(lo, hi);
         }
-        __syncthreads();
-    }
-    const float s_a = sa_s;
+        // Per-channel scales of this CTA's rows, into shared memory.
+        float* sw_s = reinterpret_cast<float*>(smem + p.sw_off);
+        if (!PG && p.sw_in_smem)
+            for (int i = threadIdx.x; i < nrows; i += kConsumers) sw_s[i] = __ldg(p.s_w + n0 + i);
+        named_bar_sync(1, kConsumers);
+        const float s_a = s;  // every consumer thread holds the token scale
 
-    // ---- weight stream --------------------------------------------------------
-    int lane_acc = 0;  // per-channel: this lane's share of the row's int32 sum
-    while (n < p.N) {
-        int nn = n, nc0 = c0 + kUnroll * 32;
-        if (nc0 >= nchunk) {
-            nn = n + row_stride;
-            nc0 = 0;
-        }
-        uint4 nxt[kUnroll];
-        if (nn < p.N) load_block(nxt, nn, nc0);
-
+        // ------------------------------ weight rows ---------------------------
+        const uint4* codes = reinterpret_cast<const uint4*>(codes_s);
+        const int nchunk = p.row_bytes / 16;
+        float* prod = PG ? reinterpret_cast<float*>(smem + p.prod_off) + warp * p.G : nullptr;
+        for (int st = 0; st < nst; ++st) {
+            const int slot = st % NS;
+            const uint32_t use = (uint32_t)(st / NS);
+            {
+                const bool ok = mbar_wait_bounded(smem_u32(&full[slot]), use & 1u, p.timeout_ns,
+                                                  abort_flag, p.status, kSiteGemvConsumerFull);
+                if (!__all_sync(0xffffffffu, ok)) return;
+            }
+            const uint8_t* stage = stages + (size_t)slot * p.stage_bytes;
+            const int rows = min(R, nrows - st * R);
+            // Rows of the stage go to warps round-robin on the CTA-local row index.
+            int j = (warp - (st * R) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+            for (; j < rows; j += kConsumerWarps) {
+                const int n = n0 + st * R + j;
+                const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)j * p.row_bytes);
+                if constexpr (!PG) {
+                    int acc = 0;
+                    for (int c0 = 0; c0 < nchunk; c0 += 32 * kUnroll) {  // warp-uniform
+                        uint4 wv[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int cbase = c0 + u * 32;  // warp-uniform
-            if (cbase >= nchunk) break;
-            const int c = cbase + lane;
-            int part = (c < nchunk) ? chunk_dot<BITS>(cur[u], codes, c) : 0;
-            if constexpr (!PG) {
-                lane_acc += part;
-            } else {
-                for (int o = 1; o < p.cpg; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                if ((lane % p.cpg) == 0 && c < nchunk) {
-                    const int g = c / p.cpg;
-                    prod_s[warp][g] =
-                        __fmul_rn(__int2float_rn(part), __ldg(p.s_w + (int64_t)n * p.G + g));
+                        for (int u = 0; u < kUnroll; ++u) {
+                            const int c = c0 + u * 32 + lane;
+                            if (c < nchunk) wv[u] = wrow[c];
+                        }
+#pragma unroll
+                        for (int u = 0; u < kUnroll; ++u) {
+                            const int c = c0 + u * 32 + lane;
+                            if (c < nchunk) acc += chunk_dot<BITS>(wv[u], codes, c);
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                    if (lane == 0)
+                        p.y[n] = __float2half_rn(
+                            __fmul_rn(__fmul_rn(__int2float_rn(acc), s_a),
+                                      p.sw_in_smem ? sw_s[n - n0] : __ldg(p.s_w + n)));
+                } else {
+                    const float* srow =
+                        p.scales_staged
+                            ? reinterpret_cast<const float*>(stage + (size_t)R * p.row_bytes) + j * p.G
+                            : p.s_w + (int64_t)n * p.G;
+                    for (int c0 = 0; c0 < nchunk; c0 += 32 * kUnroll) {  // warp-uniform
+                        uint4 wv[kUnroll];
+#pragma unroll
+                        for (int u = 0; u < kUnroll; ++u) {
+                            const int c = c0 + u * 32 + lane;
+                            if (c < nchunk) wv[u] = wrow[c];
+                        }
+#pragma unroll
+                        for (int u = 0; u < kUnroll; ++u) {
+                            const int c = c0 + u * 32 + lane;
+                            if (c0 + u * 32 >= nchunk) break;  // warp-uniform
+                            int part = (c < nchunk) ? chunk_dot<BITS>(wv[u], codes, c) : 0;
+                            for (int o = 1; o < p.cpg; o <<= 1)
+                                part += __shfl_xor_sync(0xffffffffu, part, o);
+                            if ((lane & (p.cpg - 1)) == 0 && c < nchunk) {
+                                const int g = c / p.cpg;
+                                prod[g] = __fmul_rn(__int2float_rn(part), srow[g]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        float f = 0.0f;
+                        for (int g = 0; g < p.G; ++g) f = __fadd_rn(f, prod[g]);
+                        p.y[n] = __float2half_rn(__fmul_rn(f, s_a));
+                    }
+                    __syncwarp();
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
         }
-
-        if (nc0 == 0) {  // row n complete
-            if constexpr (!PG) {
-                int a = lane_acc;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                if (lane == 0) {
-                    const float t = __fmul_rn(__fmul_rn(__int2float_rn(a), s_a), __ldg(p.s_w + n));
-                    p.y[n] = __float2half_rn(t);
-                }
-                lane_acc = 0;
-            } else {
-                __syncwarp();
-                if (lane == 0) {
-                    float f = 0.0f;
-                    for (int g = 0; g < p.G; ++g) f = __fadd_rn(f, prod_s[warp][g]);
-                    p.y[n] = __float2half_rn(__fmul_rn(f, s_a));
-                }
-                __syncwarp();
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) cur[u] = nxt[u];
-        n = nn;
-        c0 = nc0;
     }
 }
 
+int g_max_smem = 0;  // opt-in shared memory per block (queried once; same on every B300)
+
 template <int BITS, bool PG>
-cudaError_t launch_one(const Params& p, int num_sms, cudaStream_t stream) {
-    int grid = num_sms * 2;
-    const int rows_per_cta = kWarps;
-    const int need = (p.N + rows_per_cta - 1) / rows_per_cta;
-    if (need < grid) grid = need;
-    gemv_kernel<BITS, PG><<<grid, kThreads, 0, stream>>>(p);
+cudaError_t launch_one(const Params& p, int grid, int smem, cudaStream_t stream) {
+    auto kern = gemv_kernel<BITS, PG>;
+    static int attr_smem = 0;  // benign race: setting the same value twice
+    if (attr_smem < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             g_max_smem);
+        if (e != cudaSuccess) return e;
+        attr_smem = g_max_smem;
+    }
+    kern<<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -228,6 +309,14 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     if (a.bits != 8 && a.bits != 4) return cudaErrorInvalidValue;
     const int chunk_elems = (a.bits == 8) ? 16 : 32;
     if (a.K % chunk_elems != 0) return cudaErrorInvalidValue;
+    if (g_max_smem == 0) {
+        int dev = 0, v = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        g_max_smem = v;
+    }
     Params p{};
     p.x = a.x;
     p.K = (int)a.K;
@@ -235,6 +324,8 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     p.w = static_cast<const uint8_t*>(a.w);
     p.s_w = a.s_w;
     p.y = a.y;
+    p.timeout_ns = a.timeout_ns;
+    p.status = a.status;
     if (a.group_size == 0) {
         p.G = 1;
         p.cpg = 0;
@@ -242,13 +333,43 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
         if (a.group_size % chunk_elems != 0 || a.K % a.group_size != 0) return cudaErrorInvalidValue;
         p.G = (int)(a.K / a.group_size);
         p.cpg = a.group_size / chunk_elems;
-        if (p.cpg > 32 || (p.cpg & (p.cpg - 1)) != 0 || p.G > kMaxGroups)
-            return cudaErrorInvalidValue;
+        if (p.cpg > 32 || (p.cpg & (p.cpg - 1)) != 0) return cudaErrorInvalidValue;
     }
     const bool pg = a.group_size != 0;
+    p.row_bytes = (a.bits == 8) ? p.K : p.K / 2;
+    p.rows_per_stage = kStageTarget / p.row_bytes > 0 ? kStageTarget / p.row_bytes : 1;
+    p.scales_staged = pg && (p.G % 4 == 0) && (reinterpret_cast<uintptr_t>(a.s_w) % 16 == 0);
+    const int stage_payload =
+        p.rows_per_stage * (p.row_bytes + (p.scales_staged ? p.G * 4 : 0));
+    p.stage_bytes = (stage_payload + 127) & ~127;
+
+    const int grid = (int)(a.N < num_sms ? a.N : num_sms);
+    const int max_rows = (int)((a.N + grid - 1) / grid);
+    const int max_stages_needed = (max_rows + p.rows_per_stage - 1) / p.rows_per_stage;
+
+    // Shared memory: codes | per-warp group products | barriers | stages.
+    p.codes_off = 0;
+    p.prod_off = (p.K + 127) & ~127;
+    const int prod_bytes = pg ? ((kConsumerWarps * p.G * 4 + 127) & ~127) : 0;
+    p.sw_off = p.prod_off + prod_bytes;
+    p.sw_in_smem = !pg && max_rows <= 8192;
+    const int sw_bytes = p.sw_in_smem ? ((max_rows * 4 + 127) & ~127) : 0;
+    p.bar_off = p.sw_off + sw_bytes;
+    const int bar_bytes = 2 * kMaxStages * 8 + kConsumerWarps * 4 + 16;
+    p.stage_off = (p.bar_off + bar_bytes + 127) & ~127;
+    const int budget = g_max_smem - p.stage_off;
+    int ns = budget / p.stage_bytes;
+    if (ns > kMaxStages) ns = kMaxStages;
+    if (ns > max_stages_needed) ns = max_stages_needed;
+    if (ns < 1) return cudaErrorInvalidValue;
+    p.num_stages = ns;
+    const int smem = p.stage_off + ns * p.stage_bytes;
+
     if (a.bits == 8)
-        return pg ? launch_one<8, true>(p, num_sms, stream) : launch_one<8, false>(p, num_sms, stream);
-    return pg ? launch_one<4, true>(p, num_sms, stream) : launch_one<4, false>(p, num_sms, stream);
+        return pg ? launch_one<8, true>(p, grid, smem, stream)
+                  : launch_one<8, false>(p, grid, smem, stream);
+    return pg ? launch_one<4, true>(p, grid, smem, stream)
+              : launch_one<4, false>(p, grid, smem, stream);
 }
 
 }  // namespace cider

@@ -57,6 +57,8 @@ struct GemvArgs {
     int bits;            // 8 or 4
     int group_size;      // 0, 64 or 128 (w4: 0 or 128, any multiple of 32)
     __half* y;           // [N]
+    uint64_t timeout_ns;          // bound on every device-side wait
+    unsigned long long* status;   // device status word
 };
 
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);

@@ -8,6 +8,7 @@
 // Scale = absmax / qmax (fp32, IEEE division), code = clamp(rint(x / scale))
 // with ties to even, an all-zero block has scale 0 and codes 0.
 #include <cuda_fp16.h>
+#include <algorithm>
 #include <cstdint>
 
 #include "kernels.h"
@@ -101,6 +102,64 @@ __global__ void __launch_bounds__(256) quant_groups_vec_kernel(const __half* __r
     }
 }
 
+// One pass per row (groups of the whole row, gs == K): each row is read once
+// into registers (VPT 16-byte vectors per thread, all loads issued before any
+// use), reduced to its absmax, and quantized from the registers. WPR = 1: one
+// warp per row (K <= 256 * VPT); WPR = 8: the whole 256-thread block per row
+// (K <= 2048 * VPT). Same arithmetic as quant_groups_vec_kernel.
+template <QuantOut OUT, int VPT, int WPR>
+__global__ void __launch_bounds__(256) quant_rows_reg_kernel(const __half* __restrict__ src,
+                                                             int64_t rows, int64_t K, int qmax,
+                                                             void* __restrict__ out,
+                                                             float* __restrict__ scales) {
+    static_assert(WPR == 1 || WPR == 8, "one warp or one block per row");
+    __shared__ float red_s[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kRowsPerBlock = 8 / WPR;
+    constexpr int kThreadsPerRow = 32 * WPR;
+    const int t = (WPR == 1) ? lane : threadIdx.x;
+    const int64_t nvec = K >> 3;
+    for (int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (WPR == 1 ? warp : 0); row < rows;
+         row += (int64_t)gridDim.x * kRowsPerBlock) {
+        const uint4* p = reinterpret_cast<const uint4*>(src + row * K);
+        uint4 v[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t c = t + (int64_t)i * kThreadsPerRow;
+            v[i] = (c < nvec) ? __ldg(p + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        __half2 hm = __float2half2_rn(0.0f);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) hm = __hmax2(hm, __habs2(h[j]));
+        }
+        float amax = fmaxf(__low2float(hm), __high2float(hm));
+        amax = warp_max(amax);
+        if constexpr (WPR == 8) {
+            if (lane == 0) red_s[warp] = amax;
+            __syncthreads();
+#pragma unroll
+            for (int w = 0; w < 8; ++w) amax = fmaxf(amax, red_s[w]);
+            __syncthreads();  // red_s is reused by the next row
+        }
+        const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
+        if (t == 0) scales[row] = s;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int64_t c = t + (int64_t)i * kThreadsPerRow;
+            if (c < nvec) {
+                const __half* h = reinterpret_cast<const __half*>(&v[i]);
+                int q[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) q[j] = quant_one(__half2float(h[j]), s, qmax);
+                store_codes8<OUT>(out, row * K + c * 8, q);
+            }
+        }
+    }
+}
+
 // Scalar fallback for shapes the vector path does not take (int8 / fp16 out).
 template <QuantOut OUT>
 __global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const __half* __restrict__ src,
@@ -125,39 +184,63 @@ __global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const __half* 
     }
 }
 
-// INT8 codes -> exact fp16 integers (operand image), 16 codes per thread step.
+// INT8 codes -> exact fp16 integers (operand image), 16 codes per thread step,
+// four steps' loads in flight per thread.
 __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t* __restrict__ src, int64_t n16,
                                                        __half* __restrict__ dst) {
+    constexpr int U = 4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-        int4 u = __ldg(reinterpret_cast<const int4*>(src) + i);
-        const int8_t* b = reinterpret_cast<const int8_t*>(&u);
-        __half2 h[8];
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n16; i0 += U * stride) {
+        int4 u[U];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            h[j] = __halves2half2(__short2half_rn(b[2 * j]), __short2half_rn(b[2 * j + 1]));
-        uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
-        d[0] = *reinterpret_cast<const uint4*>(&h[0]);
-        d[1] = *reinterpret_cast<const uint4*>(&h[4]);
+        for (int k = 0; k < U; ++k) {
+            const int64_t i = i0 + k * stride;
+            if (i < n16) u[k] = __ldg(reinterpret_cast<const int4*>(src) + i);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t i = i0 + k * stride;
+            if (i >= n16) break;
+            const int8_t* b = reinterpret_cast<const int8_t*>(&u[k]);
+            __half2 h[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                h[j] = __halves2half2(__short2half_rn(b[2 * j]), __short2half_rn(b[2 * j + 1]));
+            uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
+            d[0] = *reinterpret_cast<const uint4*>(&h[0]);
+            d[1] = *reinterpret_cast<const uint4*>(&h[4]);
+        }
     }
 }
 
 // Packed INT4 (nibble = code + 8, element 2j in the low nibble of byte j) ->
-// exact fp16 integers, 32 codes (16 bytes) per thread step.
+// exact fp16 integers, 32 codes (16 bytes) per thread step, four steps' loads
+// in flight per thread.
 __global__ void __launch_bounds__(256) widen_i4_kernel(const uint8_t* __restrict__ src,
                                                        int64_t n16, __half* __restrict__ dst) {
+    constexpr int U = 4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-        uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + i);
-        const uint8_t* b = reinterpret_cast<const uint8_t*>(&u);
-        __half2 h[16];
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n16; i0 += U * stride) {
+        uint4 u[U];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            h[j] = __halves2half2(__short2half_rn((short)(b[j] & 0xF) - 8),
-                                  __short2half_rn((short)(b[j] >> 4) - 8));
-        uint4* d = reinterpret_cast<uint4*>(dst) + 4 * i;
+        for (int k = 0; k < U; ++k) {
+            const int64_t i = i0 + k * stride;
+            if (i < n16) u[k] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) d[j] = *reinterpret_cast<const uint4*>(&h[4 * j]);
+        for (int k = 0; k < U; ++k) {
+            const int64_t i = i0 + k * stride;
+            if (i >= n16) break;
+            const uint8_t* b = reinterpret_cast<const uint8_t*>(&u[k]);
+            __half2 h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                h[j] = __halves2half2(__short2half_rn((short)(b[j] & 0xF) - 8),
+                                      __short2half_rn((short)(b[j] >> 4) - 8));
+            uint4* d = reinterpret_cast<uint4*>(dst) + 4 * i;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d[j] = *reinterpret_cast<const uint4*>(&h[4 * j]);
+        }
     }
 }
 
@@ -171,6 +254,43 @@ int grid_for(int64_t work_items, int per_block, int num_sms) {
 
 }  // namespace
 
+namespace {
+
+template <QuantOut OUT>
+cudaError_t launch_rows_reg_t(const __half* src, int64_t rows, int64_t K, int qmax, void* out,
+                              float* scales, int num_sms, cudaStream_t stream) {
+    const int64_t nvec = K / 8;
+    const int64_t cap = (int64_t)num_sms * 8;  // 8 resident blocks of 256 threads per SM
+    if (nvec <= 32 * 4) {
+        const int grid = (int)std::min<int64_t>((rows + 7) / 8, cap);
+        quant_rows_reg_kernel<OUT, 4, 1><<<grid, 256, 0, stream>>>(src, rows, K, qmax, out, scales);
+    } else if (nvec <= 32 * 8) {
+        const int grid = (int)std::min<int64_t>((rows + 7) / 8, cap);
+        quant_rows_reg_kernel<OUT, 8, 1><<<grid, 256, 0, stream>>>(src, rows, K, qmax, out, scales);
+    } else if (nvec <= 32 * 16) {
+        const int grid = (int)std::min<int64_t>((rows + 7) / 8, cap);
+        quant_rows_reg_kernel<OUT, 16, 1><<<grid, 256, 0, stream>>>(src, rows, K, qmax, out, scales);
+    } else if (nvec <= 256 * 8) {
+        const int grid = (int)std::min<int64_t>(rows, cap);
+        quant_rows_reg_kernel<OUT, 8, 8><<<grid, 256, 0, stream>>>(src, rows, K, qmax, out, scales);
+    } else {
+        return cudaErrorNotSupported;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows_reg(const __half* src, int64_t rows, int64_t K, int qmax,
+                                  QuantOut out_kind, void* out, float* scales, int num_sms,
+                                  cudaStream_t stream) {
+    if (out_kind == QuantOut::kInt8)
+        return launch_rows_reg_t<QuantOut::kInt8>(src, rows, K, qmax, out, scales, num_sms, stream);
+    if (out_kind == QuantOut::kF16)
+        return launch_rows_reg_t<QuantOut::kF16>(src, rows, K, qmax, out, scales, num_sms, stream);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
 cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int64_t gs, int qmax,
                                 QuantOut out_kind, void* out, float* scales, int num_sms,
                                 cudaStream_t stream) {
@@ -179,6 +299,11 @@ cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int6
                      (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(out) % 16 == 0);
     const int grid = grid_for(items, 8, num_sms);
+    if (vec && gs == K && out_kind != QuantOut::kInt4 && K <= 16384) {
+        cudaError_t e = launch_quant_rows_reg(src, rows, K, qmax, out_kind, out, scales, num_sms,
+                                              stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     if (vec) {
         switch (out_kind) {
             case QuantOut::kInt8:
