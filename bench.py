@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemv-only", action="store_true",
                     help="run only the M = 1 GEMV leg (a small command for profilers)")
+    ap.add_argument("--step-only", action="store_true",
+                    help="run only the M = 4096 step (a small command for profilers)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -333,6 +335,13 @@ def run_cider(args):
     st, site = cider.device_status()
     assert st == cider.CIDER_OK, f"device status {st} at {site:#x}"
 
+    if args.step_only:
+        if rank == 0:
+            print(json.dumps({"step_ms": statistics.mean(step_ms),
+                              "act_quant_ms": statistics.mean(quant_ms),
+                              "weight_image_ms": statistics.mean(widen_ms),
+                              "gemm_ms": statistics.mean(gemm_ms)}))
+        return
     flops = 2.0 * M * N * K
     mean_step_s = statistics.mean(step_ms) / 1e3
     mean_step_s = max_over_ranks(mean_step_s)

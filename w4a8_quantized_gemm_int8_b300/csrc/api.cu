@@ -116,7 +116,7 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
     a.mode = (gs == 0) ? GemmMode::kPcF16 : GemmMode::kPgF16;
     a.timeout_ns = kWaitTimeoutNs;
     a.status = status;
-    return from_cuda(launch_gemm_tc(a, sms, stream));
+    return from_cuda(launch_gemm(a, sms, stream));
 }
 
 }  // namespace
@@ -281,7 +281,7 @@ cider_status cider_gemm_images(const void* a_img, const float* s_a, const void* 
     a.mode = (group_size == 0) ? GemmMode::kPcF16 : GemmMode::kPgF16;
     a.timeout_ns = kWaitTimeoutNs;
     a.status = status;
-    return from_cuda(launch_gemm_tc(a, sms, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_gemm(a, sms, static_cast<cudaStream_t>(stream)));
 }
 
 cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int64_t N, int64_t K,
@@ -320,7 +320,7 @@ cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int6
     a.mode = (group_size == 0) ? GemmMode::kRawS32 : GemmMode::kRawPgS32;
     a.timeout_ns = kWaitTimeoutNs;
     a.status = status;
-    return from_cuda(launch_gemm_tc(a, sms, s));
+    return from_cuda(launch_gemm(a, sms, s));
 }
 
 cider_status cider_device_status(void* stream, uint32_t* site) {

@@ -1,0 +1,589 @@
+// INT8 x INT8 -> INT32 GEMM with fused dequant on a pair of SMs (cta_group::2).
+//
+// Same function as gemm_tc.cu (Cider README, "Metal Kernel Pipeline" and
+// "Quantization"): acc[m,n] = sum_k q[m,k] * wq[n,k] exactly in int32, then
+//   per-channel: y = fp16(((float)acc * s_a[m]) * s_w[n])
+//   per-group:   f = sum over groups g, ascending, of (float)P_g * s_w[n,g]; y = fp16(f * s_a[m])
+// computed on exact fp16 images of the codes with tcgen05 kind::f16 and an
+// fp32 tensor-memory accumulator folded into int32 every <= 1024 k (every
+// group in per-group mode), where every partial sum is an exact integer.
+//
+// Pair design (B300): a cluster of two CTAs on two SMs computes one 256 x 256
+// tile. Each CTA loads its own 128 token rows of A and its own 128-row half of
+// the 256 weight rows of B with TMA; the even CTA's MMA thread issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), which reads A and B from
+// both CTAs' shared memory and writes each CTA's 128 x 256 fp32 accumulator
+// into that CTA's tensor memory. Per SM this halves the B-operand traffic
+// from L2 and the tensor core's shared-memory reads of B compared with a
+// 128 x 256 single-CTA tile, and frees shared memory for a deeper ring
+// (6 stages of 32 KB). Both CTAs' TMA completions land on the even CTA's
+// stage barrier; the MMA commits arrive on both CTAs' barriers (multicast);
+// both CTAs' epilogue warps release an accumulator buffer on the even CTA's
+// barrier. Persistent: each cluster walks the tile list with a stride of the
+// number of clusters. Every mbarrier wait is bounded.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace cider {
+namespace gemm2 {
+
+constexpr int BM = 128;        // token rows per CTA (256 per pair)
+constexpr int BN = 256;        // output columns per tile; each CTA loads BN / 2 weight rows
+constexpr int BK = 64;         // one 128-byte swizzle row of fp16
+constexpr int STAGES = 6;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = (BN / 2) * BK * 2;
+constexpr int STAGE_TX_BYTES = 2 * (A_STAGE_BYTES + B_STAGE_BYTES);  // both CTAs
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
+constexpr int NUM_ROLE_THREADS = 128;
+constexpr int NUM_THREADS = NUM_ROLE_THREADS + NUM_EPI_THREADS;
+constexpr int TMEM_COLS = 512;  // two 256-column fp32 accumulators
+constexpr int MAX_SEG_KB = 16;  // 16 x 64 = 1024 k per exact fp32 segment
+constexpr int LAUNCH_REGS = 168;
+constexpr int ROLE_REGS = 56;    // TMA and MMA issue need few registers
+constexpr int EPI_REGS = 224;    // 128 running sums + 64 loaded columns per thread
+constexpr int OUT_WARP_BYTES = 32 * 32 * 2;  // output staging: 32 rows x 32 fp16 per warp
+static_assert(NUM_ROLE_THREADS * ROLE_REGS + NUM_EPI_THREADS * EPI_REGS <=
+                  NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+constexpr uint16_t kPairMask = 0x3;
+
+struct __align__(8) Barriers {
+    uint64_t full[STAGES];      // even CTA: both CTAs' tile bytes landed
+    uint64_t empty[STAGES];     // each CTA: the MMAs reading the stage completed
+    uint64_t acc_full[2];       // each CTA: accumulator buffer ready
+    uint64_t acc_empty[2];      // even CTA: both CTAs' epilogues drained the buffer
+    uint64_t drain;             // even CTA: MMA drain after an abort
+    uint64_t epi_sync;          // each CTA: its 256 epilogue threads
+};
+
+struct SmemLayout {
+    static constexpr int a_off = 0;
+    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
+    static constexpr int out_off = b_off + STAGES * B_STAGE_BYTES;  // per-warp output staging
+    static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;  // float[2][BN]
+    static constexpr int bar_off = scale_off + 2 * BN * 4;
+    static constexpr int misc_off = bar_off + (int)sizeof(Barriers);  // tmem base, abort
+    static constexpr int bytes = misc_off + 16;
+    static constexpr int alloc_bytes = bytes + 1024;  // runtime 1024-byte alignment slack
+};
+
+struct Params {
+    int M, N, K;
+    int num_kb;
+    int seg_kb;
+    int num_seg;
+    int G;
+    int tiles_m, tiles_n;  // tiles of 256 x 256
+    const float* s_a;
+    const float* s_w;
+    void* out;
+    int tma_store;  // fp16 output written through tmap_y (N % 8 == 0)
+    uint64_t timeout_ns;
+    unsigned long long* status;
+};
+
+enum : uint32_t {
+    kSiteProducerEmpty = 0x301,
+    kSiteMmaAccEmpty = 0x302,
+    kSiteMmaFull = 0x303,
+    kSiteEpiAccFull = 0x304,
+    kSiteDrain = 0x305,
+    kSiteProducerDrain = 0x306,
+    kSiteEpiSync = 0x307,
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int& tn) {
+    tm = tile % tiles_m;
+    tn = tile / tiles_m;
+}
+
+__device__ __forceinline__ float load_seg_scale(const Params& p, int tn, int seg, int et) {
+    const int n = tn * BN + et;
+    if (n >= p.N || p.s_w == nullptr) return 0.0f;
+    const int g = (p.G == 1) ? 0 : seg;
+    return __ldg(p.s_w + (int64_t)n * p.G + g);
+}
+
+template <GemmMode MODE>
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_y, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Barriers* bars = reinterpret_cast<Barriers*>(smem + SmemLayout::bar_off);
+    float* scales = reinterpret_cast<float*>(smem + SmemLayout::scale_off);
+    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+    const int cluster = (int)cluster_id_x();
+    const int nclusters = (int)num_clusters_x();
+    const int num_tiles = p.tiles_m * p.tiles_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->acc_full[b]), 1);
+            mbar_init(smem_u32(&bars->acc_empty[b]), 2 * NUM_EPI_WARPS);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        mbar_init(smem_u32(&bars->epi_sync), NUM_EPI_THREADS);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        if (p.tma_store) prefetch_tmap(&tmap_y);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_base_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    if (warp >= 4 && cluster < num_tiles) {
+        int tm, tn;
+        tile_coords(cluster, p.tiles_m, tm, tn);
+        scales[threadIdx.x - NUM_ROLE_THREADS] =
+            load_seg_scale(p, tn, 0, threadIdx.x - NUM_ROLE_THREADS);
+    }
+    tc_fence_before();
+    // Both CTAs' barriers are initialised before any cross-CTA arrive or TMA.
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_base_slot;
+
+    if (warp < 4) {
+        setmaxnreg_dec<ROLE_REGS>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------ TMA producer (both CTAs) ----------
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;  // stage-uses issued
+            for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+                int tm, tn;
+                tile_coords(tile, p.tiles_m, tm, tn);
+                const int a_row = tm * (2 * BM) + (int)rank * BM;
+                const int b_row = tn * BN + (int)rank * (BN / 2);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1, p.timeout_ns,
+                                           abort_flag, p.status, kSiteProducerEmpty))
+                        goto producer_done;
+                    const uint32_t fb_local = smem_u32(&bars->full[stage]);
+                    if (rank == 0) mbar_arrive_expect_tx(fb_local, STAGE_TX_BYTES);
+                    const uint32_t fb = map_to_rank(fb_local, 0);
+                    tma_load_2d_pair(smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES),
+                                     &tmap_a, fb, kb * BK, a_row);
+                    tma_load_2d_pair(smem_u32(smem + SmemLayout::b_off + stage * B_STAGE_BYTES),
+                                     &tmap_b, fb, kb * BK, b_row);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        producer_done:
+            // The MMA commits that release the last uses of each stage arrive
+            // on this CTA's empty barriers; wait for them so that no arrive
+            // (from the other CTA) is still in flight when this CTA exits.
+            for (int u = (issued > STAGES ? issued - STAGES : 0); u < issued; ++u)
+                if (!mbar_wait_drain(smem_u32(&bars->empty[u % STAGES]),
+                                     (uint32_t)(u / STAGES) & 1u, p.timeout_ns))
+                    report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
+        } else if (warp == 1 && lane == 0 && rank == 0) {
+            // ------------------------------ MMA issuer (even CTA) -------------
+            constexpr uint32_t idesc = idesc_f16_f32acc(2 * BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t seg_count = 0;
+            bool issued_any = false;
+            for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+                for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
+                    const uint32_t b = seg_count & 1;
+                    const uint32_t acc_phase = (seg_count >> 1) & 1;
+                    if (!mbar_wait_bounded(smem_u32(&bars->acc_empty[b]), acc_phase ^ 1,
+                                           p.timeout_ns, abort_flag, p.status, kSiteMmaAccEmpty))
+                        goto mma_done;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + b * BN;
+                    const int kb0 = seg * p.seg_kb;
+                    const int kb1 = min(p.num_kb, kb0 + p.seg_kb);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, p.timeout_ns,
+                                               abort_flag, p.status, kSiteMmaFull))
+                            goto mma_done;
+                        tc_fence_after();
+                        const uint64_t adesc = smem_desc_sw128_kmajor(
+                            smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES));
+                        const uint64_t bdesc = smem_desc_sw128_kmajor(
+                            smem_u32(smem + SmemLayout::b_off + stage * B_STAGE_BYTES));
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            tc_mma_f16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                            (kb > kb0 || k > 0) ? 1u : 0u);
+                        issued_any = true;
+                        tc_commit_pair_multicast(smem_u32(&bars->empty[stage]), kPairMask);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    tc_commit_pair_multicast(smem_u32(&bars->acc_full[b]), kPairMask);
+                }
+            }
+        mma_done:
+            if (*abort_flag && issued_any) {
+                tc_commit_pair_multicast(smem_u32(&bars->drain), 0x1);
+                if (!mbar_wait_drain(smem_u32(&bars->drain), 0, p.timeout_ns))
+                    report_device_error(p.status, kDevTimeout, kSiteDrain);
+            }
+        }
+    } else {
+        setmaxnreg_inc<EPI_REGS>();
+        // ------------------------------ epilogue (both CTAs) ------------------
+        // Warp w (4..11) owns TMEM lanes 32 * (w % 4).. (its 32 token rows) and
+        // the 128 columns [128 * half, 128 * half + 128) of the tile.
+        const int ewarp = warp - 4;
+        const int quad = warp & 3;
+        const int half = ewarp >> 2;
+        const int et = threadIdx.x - NUM_ROLE_THREADS;
+        const int row_in_tile = quad * 32 + lane;
+        // Output staging for the TMA store: 32 rows x 32 fp16 (64-byte rows,
+        // 64-byte swizzle: chunk c of row r at chunk c ^ ((r >> 1) & 3)).
+        uint8_t* stage_out = smem + SmemLayout::out_off + ewarp * OUT_WARP_BYTES;
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);
+        uint32_t seg_count = 0;
+        uint32_t epi_phase = 0;
+        uint32_t sbuf = 0;  // scales buffer of the current segment
+        bool store_pending = false;
+        uint32_t acc[128];
+
+        for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+            int tm, tn;
+            tile_coords(tile, p.tiles_m, tm, tn);
+            const int m_base = tm * (2 * BM) + (int)rank * BM + quad * 32;
+            const int m = m_base + lane;
+            const int n_half = tn * BN + half * 128;
+
+            for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
+                const uint32_t b = seg_count & 1;
+                const uint32_t acc_phase = (seg_count >> 1) & 1;
+                const bool last_seg = (seg == p.num_seg - 1);
+                // Per-group scales change every segment, per-channel ones every tile.
+                const bool new_scales = (MODE == GemmMode::kPgF16) || last_seg;
+                const float* sc = scales + sbuf * BN + half * 128;
+
+                float next_scale = 0.0f;
+                if (new_scales) {
+                    int nt = tile, ns = seg + 1;
+                    if (ns == p.num_seg) {
+                        ns = 0;
+                        nt += nclusters;
+                    }
+                    if (nt < num_tiles) {
+                        int ntm, ntn;
+                        tile_coords(nt, p.tiles_m, ntm, ntn);
+                        next_scale = load_seg_scale(p, ntn, ns, et);
+                    }
+                }
+
+                {
+                    const bool ok = mbar_wait_bounded(smem_u32(&bars->acc_full[b]), acc_phase,
+                                                      p.timeout_ns, abort_flag, p.status,
+                                                      kSiteEpiAccFull);
+                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                }
+                tc_fence_after();
+
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                       b * BN + half * 128;
+                // Two batches of 64 columns: both 32-column loads in flight, one wait.
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t v[64];
+                    tmem_ld_32x32b_x32_ptr(t_row + hb * 64, v);
+                    tmem_ld_32x32b_x32_ptr(t_row + hb * 64 + 32, v + 32);
+                    tmem_wait_ld();
+                    if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
+                        // Exact fp32 integers -> int32: the fast conversion holds
+                        // below 2^22; a warp holding a larger one converts all.
+                        bool big = false;
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) big |= fabsf(__uint_as_float(v[j])) >= 4194304.0f;
+                        if (__any_sync(0xffffffffu, big)) {
+#pragma unroll
+                            for (int j = 0; j < 64; ++j) {
+                                const int part = __float2int_rn(__uint_as_float(v[j]));
+                                acc[hb * 64 + j] = (seg == 0) ? (uint32_t)part
+                                                              : (uint32_t)((int)acc[hb * 64 + j] + part);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 64; ++j) {
+                                const int part = small_float_to_int(__uint_as_float(v[j]));
+                                acc[hb * 64 + j] = (seg == 0) ? (uint32_t)part
+                                                              : (uint32_t)((int)acc[hb * 64 + j] + part);
+                            }
+                        }
+                    } else if constexpr (MODE == GemmMode::kPgF16) {
+#pragma unroll
+                        for (int j = 0; j < 64; j += 4) {
+                            const float4 s4 = *reinterpret_cast<const float4*>(sc + hb * 64 + j);
+                            const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float prev =
+                                    (seg == 0) ? 0.0f : __uint_as_float(acc[hb * 64 + j + i]);
+                                const float prod = __fmul_rn(__uint_as_float(v[j + i]), ss[i]);
+                                acc[hb * 64 + j + i] = __float_as_uint(__fadd_rn(prev, prod));
+                            }
+                        }
+                    } else {  // kRawPgS32: this group's partials, straight out
+                        if (m < p.M) {
+                            int32_t* out = static_cast<int32_t*>(p.out);
+#pragma unroll
+                            for (int j = 0; j < 64; ++j) {
+                                const int n = n_half + hb * 64 + j;
+                                if (n < p.N)
+                                    out[((int64_t)m * p.N + n) * p.G + seg] =
+                                        __float2int_rn(__uint_as_float(v[j]));
+                            }
+                        }
+                    }
+                }
+                // This warp's reads of the buffer are complete: release it on
+                // the even CTA's barrier (one arrival per warp, both CTAs).
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&bars->acc_empty[b]), 0));
+
+                if (last_seg) {
+                    if constexpr (MODE == GemmMode::kRawS32) {
+                        if (m < p.M) {
+                            int32_t* out = static_cast<int32_t*>(p.out) + (int64_t)m * p.N;
+#pragma unroll
+                            for (int j = 0; j < 128; ++j)
+                                if (n_half + j < p.N) out[n_half + j] = (int)acc[j];
+                        }
+                    } else if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kPgF16) {
+                        const float sa = (m < p.M) ? __ldg(p.s_a + m) : 0.0f;
+                        bool big = false;
+                        if constexpr (MODE == GemmMode::kPcF16) {
+#pragma unroll
+                            for (int j = 0; j < 128; ++j) {
+                                const int a = (int)acc[j];
+                                big |= (a >= 4194304 || a <= -4194304);
+                            }
+                        }
+                        const bool slow_cvt = __any_sync(0xffffffffu, big);
+                        // Four rounds of 32 columns: dequant, stage, TMA store.
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            uint32_t h2[16];
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                float y0, y1;
+                                const int c = r * 32 + j;
+                                if constexpr (MODE == GemmMode::kPcF16) {
+                                    const float f0 = slow_cvt ? __int2float_rn((int)acc[c])
+                                                              : small_int_to_float((int)acc[c]);
+                                    const float f1 = slow_cvt ? __int2float_rn((int)acc[c + 1])
+                                                              : small_int_to_float((int)acc[c + 1]);
+                                    y0 = __fmul_rn(__fmul_rn(f0, sa), sc[c]);
+                                    y1 = __fmul_rn(__fmul_rn(f1, sa), sc[c + 1]);
+                                } else {
+                                    y0 = __fmul_rn(__uint_as_float(acc[c]), sa);
+                                    y1 = __fmul_rn(__uint_as_float(acc[c + 1]), sa);
+                                }
+                                const __half2 hv = __floats2half2_rn(y0, y1);
+                                h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                            }
+                            if (p.tma_store) {
+                                // The staging buffer is free once the previous
+                                // store from it has been read out.
+                                if (store_pending && lane == 0) bulk_wait_group_read0();
+                                __syncwarp();
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    *reinterpret_cast<uint4*>(stage_out + lane * 64 +
+                                                              ((q ^ swz) << 4)) =
+                                        make_uint4(h2[4 * q], h2[4 * q + 1], h2[4 * q + 2],
+                                                   h2[4 * q + 3]);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&tmap_y, smem_u32(stage_out), n_half + r * 32,
+                                                 m_base);
+                                    bulk_commit_group();
+                                }
+                                store_pending = true;
+                            } else if (m < p.M) {
+                                __half* out = static_cast<__half*>(p.out) + (int64_t)m * p.N;
+                                const __half* hh = reinterpret_cast<const __half*>(h2);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (n_half + r * 32 + j < p.N) out[n_half + r * 32 + j] = hh[j];
+                            }
+                        }
+                    }
+                }
+
+                if (new_scales) {
+                    // Publish the next segment's scales in the other buffer; the
+                    // barrier keeps a thread from overwriting scales that another
+                    // thread still reads.
+                    scales[(sbuf ^ 1) * BN + et] = next_scale;
+                    mbar_arrive(smem_u32(&bars->epi_sync));
+                    const bool ok = mbar_wait_bounded(smem_u32(&bars->epi_sync), epi_phase,
+                                                      p.timeout_ns, abort_flag, p.status,
+                                                      kSiteEpiSync);
+                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                    epi_phase ^= 1;
+                    sbuf ^= 1;
+                }
+            }
+        }
+    epi_done:
+        // Every output store has completed before the CTA exits.
+        if (store_pending && lane == 0) bulk_wait_group0();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // Neither CTA leaves (or frees tensor memory) while the other may still
+    // arrive on its barriers or the MMAs may still write its tensor memory.
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace gemm2
+
+namespace {
+
+struct PairLaunchInfo {
+    bool checked = false;
+    bool ok = false;
+    int max_clusters = 0;
+};
+
+template <GemmMode MODE>
+cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
+                             const gemm2::Params& p, int num_sms, cudaStream_t stream) {
+    using namespace gemm2;
+    auto kern = gemm_tc2_kernel<MODE>;
+    static PairLaunchInfo info;  // benign race: every thread computes the same values
+    if (!info.checked) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemLayout::alloc_bytes);
+        if (e != cudaSuccess) return e;
+        // How many pairs fit on the GPU at once (SMs pair up within a GPC).
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = SmemLayout::alloc_bytes;
+        cfg.numAttrs = 0;  // the kernel's compile-time cluster shape (2, 1, 1) applies
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        info.max_clusters = n;
+        info.ok = n > 0;
+        info.checked = true;
+    }
+    if (!info.ok) return cudaErrorInvalidConfiguration;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int clusters = tiles < info.max_clusters ? tiles : info.max_clusters;
+    kern<<<2 * clusters, NUM_THREADS, SmemLayout::alloc_bytes, stream>>>(ta, tb, ty, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+    using namespace gemm2;
+    if (a.M <= 0 || a.N <= 0 || a.K <= 0 || a.K % 16 != 0) return cudaErrorInvalidValue;
+    if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2)
+        return cudaErrorInvalidValue;
+    CUtensorMap ta, tb, ty;
+    if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS ||
+        encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN / 2, BK) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // fp16 output through TMA stores of 32 x 32 boxes (64-byte swizzle) when
+    // the row pitch allows it (a multiple of 16 bytes); direct stores otherwise.
+    const bool f16_out = (a.mode == GemmMode::kPcF16 || a.mode == GemmMode::kPgF16);
+    const bool tma_store = f16_out && (a.N % 8 == 0) &&
+                           (reinterpret_cast<uintptr_t>(a.out) % 16 == 0);
+    memset(&ty, 0, sizeof(ty));
+    if (tma_store && encode_tmap_f16_2d(&ty, a.out, a.M, a.N, 32, 32,
+                                        CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    Params p{};
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.num_kb = (p.K + BK - 1) / BK;
+    const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
+    if (per_group) {
+        if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
+            return cudaErrorInvalidValue;
+        p.seg_kb = a.group_size / BK;
+        p.G = p.K / a.group_size;
+    } else {
+        const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        p.seg_kb = (p.num_kb + nseg - 1) / nseg;
+        p.G = 1;
+    }
+    p.num_seg = (p.num_kb + p.seg_kb - 1) / p.seg_kb;
+    p.tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
+    p.tiles_n = (p.N + BN - 1) / BN;
+    p.s_a = a.s_a;
+    p.s_w = a.s_w;
+    p.out = a.out;
+    p.tma_store = tma_store ? 1 : 0;
+    p.timeout_ns = a.timeout_ns;
+    p.status = a.status;
+    switch (a.mode) {
+        case GemmMode::kPcF16:
+            return launch_pair_mode<GemmMode::kPcF16>(ta, tb, ty, p, num_sms, stream);
+        case GemmMode::kPgF16:
+            return launch_pair_mode<GemmMode::kPgF16>(ta, tb, ty, p, num_sms, stream);
+        case GemmMode::kRawS32:
+            return launch_pair_mode<GemmMode::kRawS32>(ta, tb, ty, p, num_sms, stream);
+        case GemmMode::kRawPgS32:
+            return launch_pair_mode<GemmMode::kRawPgS32>(ta, tb, ty, p, num_sms, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+    static const int engine = [] {
+        const char* e = getenv("CIDER_GEMM_ENGINE");
+        if (e && strcmp(e, "single") == 0) return 1;
+        if (e && strcmp(e, "pair") == 0) return 2;
+        return 0;
+    }();
+    const bool pair = engine == 2 || (engine == 0 && a.M > gemm2::BM);
+    return pair ? launch_gemm_tc_pair(a, num_sms, stream) : launch_gemm_tc(a, num_sms, stream);
+}
+
+}  // namespace cider

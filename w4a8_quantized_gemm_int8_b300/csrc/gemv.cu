@@ -181,17 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
 #pragma unroll
         for (int w = 1; w < kConsumerWarps; ++w) a = fmaxf(a, red_s[w]);
         const float s = (a == 0.0f) ? 0.0f : __fdiv_rn(a, 127.0f);
+        const float r = quant_recip(s);
         for (int v = threadIdx.x; v < nvec; v += kConsumers) {
             uint4 u = __ldg(xv + v);
             const __half* h = reinterpret_cast<const __half*>(&u);
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                int q = 0;
-                if (s != 0.0f) {
-                    q = __float2int_rn(__fdiv_rn(__half2float(h[i]), s));
-                    q = q > 127 ? 127 : (q < -127 ? -127 : q);
-                }
+                const int q = quant_code(__half2float(h[i]), s, r, 127);
                 if (i < 4)
                     lo |= (uint32_t)(q & 0xFF) << (8 * i);
                 else

@@ -47,6 +47,11 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm_tc(const GemmArgs& args, int num_sms, cudaStream_t stream);
+// Same function on SM pairs (cta_group::2, 256 x 256 tiles); for M > 128.
+cudaError_t launch_gemm_tc_pair(const GemmArgs& args, int num_sms, cudaStream_t stream);
+// Picks the engine for the problem: SM pairs for M > 128, single SMs otherwise
+// (CIDER_GEMM_ENGINE=single|pair in the environment overrides).
+cudaError_t launch_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
 
 // ---- M = 1 GEMV (quantizes x per CTA, int32 dot products, same epilogue) ----
 struct GemvArgs {
@@ -68,6 +73,10 @@ cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
 cudaError_t device_status_ptr(unsigned long long** ptr);
 cudaError_t read_and_clear_device_status(unsigned long long* value, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t stream);
+
+// Host-side encoder for a 2D fp16 row-major tile map (any swizzle mode).
+CUresult encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                            uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle);
 
 // Host-side encoder for a 2D fp16 K-major tile map with 128-byte swizzle.
 CUresult encode_tmap_f16_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cstdint>
 
+#include "device_common.cuh"
 #include "kernels.h"
 
 namespace cider {
@@ -23,13 +24,10 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// One code: clamp(rint(x / s), -qmax, qmax); s == 0 only for all-zero blocks.
-__device__ __forceinline__ int quant_one(float x, float s, int qmax) {
-    if (s == 0.0f) return 0;
-    int q = __float2int_rn(__fdiv_rn(x, s));
-    q = q > qmax ? qmax : q;
-    q = q < -qmax ? -qmax : q;
-    return q;
+// One code: clamp(rint(x / s), -qmax, qmax); s == 0 only for all-zero blocks
+// (quant_code in device_common.cuh; r = quant_recip(s)).
+__device__ __forceinline__ int quant_one(float x, float s, float r, int qmax) {
+    return quant_code(x, s, r, qmax);
 }
 
 template <QuantOut OUT>
@@ -90,13 +88,14 @@ __global__ void __launch_bounds__(256) quant_groups_vec_kernel(const __half* __r
         float amax = fmaxf(__low2float(hm), __high2float(hm));
         amax = warp_max(amax);
         const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
+        const float r = quant_recip(s);
         if (lane == 0) scales[item] = s;
         for (int64_t v = lane; v < nvec; v += 32) {
             uint4 u = __ldg(p + v);
             const __half* h = reinterpret_cast<const __half*>(&u);
             int q[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = quant_one(__half2float(h[i]), s, qmax);
+            for (int i = 0; i < 8; ++i) q[i] = quant_one(__half2float(h[i]), s, r, qmax);
             store_codes8<OUT>(out, base + v * 8, q);
         }
     }
@@ -145,6 +144,7 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const __half* __res
             __syncthreads();  // red_s is reused by the next row
         }
         const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
+        const float r = quant_recip(s);
         if (t == 0) scales[row] = s;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const __half* __res
                 const __half* h = reinterpret_cast<const __half*>(&v[i]);
                 int q[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) q[j] = quant_one(__half2float(h[j]), s, qmax);
+                for (int j = 0; j < 8; ++j) q[j] = quant_one(__half2float(h[j]), s, r, qmax);
                 store_codes8<OUT>(out, row * K + c * 8, q);
             }
         }
@@ -178,9 +178,10 @@ __global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const __half* 
         for (int64_t k = lane; k < gs; k += 32) amax = fmaxf(amax, fabsf(__half2float(src[base + k])));
         amax = warp_max(amax);
         const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
+        const float r = quant_recip(s);
         if (lane == 0) scales[item] = s;
         for (int64_t k = lane; k < gs; k += 32)
-            store_code1<OUT>(out, base + k, quant_one(__half2float(src[base + k]), s, qmax));
+            store_code1<OUT>(out, base + k, quant_one(__half2float(src[base + k]), s, r, qmax));
     }
 }
 

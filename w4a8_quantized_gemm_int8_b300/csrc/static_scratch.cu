@@ -114,7 +114,7 @@ extern "C" cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M,
         a.mode = GemmMode::kPcF16;
         a.timeout_ns = kWaitTimeoutNs;
         a.status = status;
-        e = launch_gemm_tc(a, sms, s);
+        e = launch_gemm(a, sms, s);
     }
     if (e == cudaSuccess) return CIDER_OK;
     if (e == cudaErrorInvalidValue) {
