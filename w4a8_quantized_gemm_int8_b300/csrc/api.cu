@@ -97,11 +97,8 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
     if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
 
     Workspace wsp = carve(ws, M, N, K);
-    cudaError_t e = launch_quant_groups(static_cast<const __half*>(x), M, K, K, 127,
-                                        QuantOut::kF16, wsp.a_img, wsp.s_a, sms, stream);
-    if (e != cudaSuccess) return from_cuda(e);
-    e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, wsp.b_img, sms, stream)
-                    : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, wsp.b_img, sms, stream);
+    cudaError_t e = launch_operand_images(static_cast<const __half*>(x), M, K, w, bits, N,
+                                          wsp.a_img, wsp.s_a, wsp.b_img, sms, stream);
     if (e != cudaSuccess) return from_cuda(e);
     GemmArgs a{};
     a.a_img = wsp.a_img;

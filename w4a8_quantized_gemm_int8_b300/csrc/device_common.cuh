@@ -397,6 +397,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32_ptr(uint32_t taddr, uint32_t*
         : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the preceding kernel in the stream has
+// finished; grid_dep_wait() blocks until that kernel has completed and its
+// memory writes are visible (a no-op for an ordinary launch), and
+// grid_dep_launch() lets the next such kernel be scheduled early.
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Per-warp register budget changes (warp-specialized kernels). The block's
 // total must stay within what it was launched with; callers check that.
 template <uint32_t N>

@@ -152,17 +152,24 @@ __global__ void __maxnreg__(LAUNCH_REGS)
         tmem_alloc(smem_u32(tmem_base_slot), TMEM_COLS);
         tmem_relinquish();
     }
-    // Scales of this CTA's first segment.
-    if (warp >= 4 && (int)blockIdx.x < num_tiles) {
-        int tm, tn;
-        tile_coords(blockIdx.x, p.tiles_m, tm, tn);
-        scales[threadIdx.x - NUM_ROLE_THREADS] =
-            load_seg_scale(p, tn, 0, threadIdx.x - NUM_ROLE_THREADS);
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_slot;
+    // Everything above overlaps the tail of the preceding kernel (programmatic
+    // dependent launch); global memory is touched only after this wait.
+    grid_dep_wait();
+    grid_dep_launch();
+    // Scales of this CTA's first segment.
+    if (warp >= 4) {
+        if ((int)blockIdx.x < num_tiles) {
+            int tm, tn;
+            tile_coords(blockIdx.x, p.tiles_m, tm, tn);
+            scales[threadIdx.x - NUM_ROLE_THREADS] =
+                load_seg_scale(p, tn, 0, threadIdx.x - NUM_ROLE_THREADS);
+        }
+        named_bar_sync(1, NUM_EPI_THREADS);
+    }
 
     if (warp < 4) {
       setmaxnreg_dec<ROLE_REGS>();  // all of warpgroup 0
@@ -457,8 +464,7 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const gemm
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    kern<<<grid, gemm::NUM_THREADS, gemm::SmemLayout::alloc_bytes, stream>>>(ta, tb, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, gemm::NUM_THREADS, gemm::SmemLayout::alloc_bytes, stream, ta, tb, p);
 }
 
 }  // namespace

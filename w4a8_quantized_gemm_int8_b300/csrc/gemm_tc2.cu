@@ -153,17 +153,24 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
         tmem_alloc_pair(smem_u32(tmem_base_slot), TMEM_COLS);
         tmem_relinquish_pair();
     }
-    if (warp >= 4 && cluster < num_tiles) {
-        int tm, tn;
-        tile_coords(cluster, p.tiles_m, tm, tn);
-        scales[threadIdx.x - NUM_ROLE_THREADS] =
-            load_seg_scale(p, tn, 0, threadIdx.x - NUM_ROLE_THREADS);
-    }
     tc_fence_before();
     // Both CTAs' barriers are initialised before any cross-CTA arrive or TMA.
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_slot;
+    // Everything above overlaps the tail of the preceding kernel (programmatic
+    // dependent launch); global memory is touched only after this wait.
+    grid_dep_wait();
+    grid_dep_launch();
+    if (warp >= 4) {
+        if (cluster < num_tiles) {
+            int tm, tn;
+            tile_coords(cluster, p.tiles_m, tm, tn);
+            scales[threadIdx.x - NUM_ROLE_THREADS] =
+                load_seg_scale(p, tn, 0, threadIdx.x - NUM_ROLE_THREADS);
+        }
+        named_bar_sync(1, NUM_EPI_THREADS);  // first tile's scales visible to all epilogue warps
+    }
 
     if (warp < 4) {
         setmaxnreg_dec<ROLE_REGS>();
@@ -260,7 +267,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
         const int quad = warp & 3;
         const int half = ewarp >> 2;
         const int et = threadIdx.x - NUM_ROLE_THREADS;
-        const int row_in_tile = quad * 32 + lane;
         // Output staging for the TMA store: 32 rows x 32 fp16 (64-byte rows,
         // 64-byte swizzle: chunk c of row r at chunk c ^ ((r >> 1) & 3)).
         uint8_t* stage_out = smem + SmemLayout::out_off + ewarp * OUT_WARP_BYTES;
@@ -513,8 +519,7 @@ cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const
     if (!info.ok) return cudaErrorInvalidConfiguration;
     const int tiles = p.tiles_m * p.tiles_n;
     const int clusters = tiles < info.max_clusters ? tiles : info.max_clusters;
-    kern<<<2 * clusters, NUM_THREADS, SmemLayout::alloc_bytes, stream>>>(ta, tb, ty, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, 2 * clusters, NUM_THREADS, SmemLayout::alloc_bytes, stream, ta, tb, ty, p);
 }
 
 }  // namespace

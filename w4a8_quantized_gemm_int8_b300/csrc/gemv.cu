@@ -162,6 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
     }
 
     // -------------------- per-token quantization of x ------------------------
+    // The producer's copies of weights (and staged per-group scales) above may
+    // start before the preceding kernel in the stream has finished
+    // (programmatic dependent launch): weights are never written by the
+    // kernel just before a GEMV. x, per-channel scales and y are touched only
+    // after this wait.
+    grid_dep_wait();
+    grid_dep_launch();
     {
         const uint4* xv = reinterpret_cast<const uint4*>(p.x);
         const int nvec = p.K / 8;
@@ -295,8 +302,7 @@ cudaError_t launch_one(const Params& p, int grid, int smem, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         attr_smem = g_max_smem;
     }
-    kern<<<grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, kThreads, smem, stream, p);
 }
 
 }  // namespace

@@ -9,6 +9,27 @@
 
 namespace cider {
 
+// Launches `kern` with programmatic stream serialization: it may be scheduled
+// while the preceding kernel in the stream is still running (that kernel
+// allows it by executing griddepcontrol.launch_dependents); every kernel
+// launched this way executes griddepcontrol.wait before its first access to
+// memory that a preceding kernel may write.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 enum class QuantOut : int { kInt8 = 0, kF16 = 1, kInt4 = 2 };
 
 // Symmetric quantization of `rows` x K fp16 values in groups of `gs`
@@ -18,6 +39,14 @@ enum class QuantOut : int { kInt8 = 0, kF16 = 1, kInt4 = 2 };
 cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int64_t gs, int qmax,
                                 QuantOut out_kind, void* out, float* scales, int num_sms,
                                 cudaStream_t stream);
+
+// Both operand images of the tensor-core GEMM in one launch: x fp16 [M,K] ->
+// a_img (exact fp16 codes) + s_a, and weights (INT8 [N,K] or packed INT4
+// [N,K/2]) -> b_img (exact fp16 integers). Falls back to separate launches
+// for shapes the fused kernel does not take.
+cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const void* w, int bits,
+                                  int64_t N, __half* a_img, float* s_a, __half* b_img,
+                                  int num_sms, cudaStream_t stream);
 
 // Operand images: INT8 codes / packed INT4 nibbles -> exact fp16 integers.
 cudaError_t launch_widen_i8(const int8_t* src, int64_t n, __half* dst, int num_sms,

@@ -107,10 +107,10 @@ __global__ void __launch_bounds__(256) quant_groups_vec_kernel(const __half* __r
 // warp per row (K <= 256 * VPT); WPR = 8: the whole 256-thread block per row
 // (K <= 2048 * VPT). Same arithmetic as quant_groups_vec_kernel.
 template <QuantOut OUT, int VPT, int WPR>
-__global__ void __launch_bounds__(256) quant_rows_reg_kernel(const __half* __restrict__ src,
-                                                             int64_t rows, int64_t K, int qmax,
-                                                             void* __restrict__ out,
-                                                             float* __restrict__ scales) {
+__device__ __forceinline__ void quant_rows_reg_body(const __half* __restrict__ src, int64_t rows,
+                                                    int64_t K, int qmax, void* __restrict__ out,
+                                                    float* __restrict__ scales, int block,
+                                                    int nblocks) {
     static_assert(WPR == 1 || WPR == 8, "one warp or one block per row");
     __shared__ float red_s[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const __half* __res
     constexpr int kThreadsPerRow = 32 * WPR;
     const int t = (WPR == 1) ? lane : threadIdx.x;
     const int64_t nvec = K >> 3;
-    for (int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (WPR == 1 ? warp : 0); row < rows;
-         row += (int64_t)gridDim.x * kRowsPerBlock) {
+    for (int64_t row = (int64_t)block * kRowsPerBlock + (WPR == 1 ? warp : 0); row < rows;
+         row += (int64_t)nblocks * kRowsPerBlock) {
         const uint4* p = reinterpret_cast<const uint4*>(src + row * K);
         uint4 v[VPT];
 #pragma unroll
@@ -146,18 +146,43 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const __half* __res
         const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
         const float r = quant_recip(s);
         if (t == 0) scales[row] = s;
+        // Codes by the reciprocal screen (quant_code); a warp in which any
+        // lane has a value near a rounding boundary redoes that vector with
+        // the correctly rounded division (a warp-uniform branch, rarely taken).
+        // Padding vectors hold zeros, so every lane votes on every vector.
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t c = t + (int64_t)i * kThreadsPerRow;
-            if (c < nvec) {
-                const __half* h = reinterpret_cast<const __half*>(&v[i]);
-                int q[8];
+            const __half* h = reinterpret_cast<const __half*>(&v[i]);
+            int q[8];
+            bool near = false;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) q[j] = quant_one(__half2float(h[j]), s, r, qmax);
-                store_codes8<OUT>(out, row * K + c * 8, q);
+            for (int j = 0; j < 8; ++j) {
+                const float tq = __fmul_rn(__half2float(h[j]), r);
+                const float rq = rintf(tq);
+                near |= !(fabsf(tq - rq) < 0.5f - 0x1p-12f);
+                q[j] = (int)rq;
             }
+            if (__any_sync(0xffffffffu, near)) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    q[j] = (s == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(__half2float(h[j]), s));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) q[j] = max(-qmax, min(qmax, q[j]));
+            if (c < nvec) store_codes8<OUT>(out, row * K + c * 8, q);
         }
     }
+}
+
+template <QuantOut OUT, int VPT, int WPR>
+__global__ void __launch_bounds__(256) quant_rows_reg_kernel(const __half* __restrict__ src,
+                                                             int64_t rows, int64_t K, int qmax,
+                                                             void* __restrict__ out,
+                                                             float* __restrict__ scales) {
+    grid_dep_wait();
+    grid_dep_launch();
+    quant_rows_reg_body<OUT, VPT, WPR>(src, rows, K, qmax, out, scales, blockIdx.x, gridDim.x);
 }
 
 // Scalar fallback for shapes the vector path does not take (int8 / fp16 out).
@@ -187,11 +212,11 @@ __global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const __half* 
 
 // INT8 codes -> exact fp16 integers (operand image), 16 codes per thread step,
 // four steps' loads in flight per thread.
-__global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t* __restrict__ src, int64_t n16,
-                                                       __half* __restrict__ dst) {
+__device__ __forceinline__ void widen_i8_body(const int8_t* __restrict__ src, int64_t n16,
+                                              __half* __restrict__ dst, int block, int nblocks) {
     constexpr int U = 4;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n16; i0 += U * stride) {
+    const int64_t stride = (int64_t)nblocks * blockDim.x;
+    for (int64_t i0 = (int64_t)block * blockDim.x + threadIdx.x; i0 < n16; i0 += U * stride) {
         int4 u[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
@@ -217,11 +242,11 @@ __global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t* __restrict_
 // Packed INT4 (nibble = code + 8, element 2j in the low nibble of byte j) ->
 // exact fp16 integers, 32 codes (16 bytes) per thread step, four steps' loads
 // in flight per thread.
-__global__ void __launch_bounds__(256) widen_i4_kernel(const uint8_t* __restrict__ src,
-                                                       int64_t n16, __half* __restrict__ dst) {
+__device__ __forceinline__ void widen_i4_body(const uint8_t* __restrict__ src, int64_t n16,
+                                              __half* __restrict__ dst, int block, int nblocks) {
     constexpr int U = 4;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n16; i0 += U * stride) {
+    const int64_t stride = (int64_t)nblocks * blockDim.x;
+    for (int64_t i0 = (int64_t)block * blockDim.x + threadIdx.x; i0 < n16; i0 += U * stride) {
         uint4 u[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
@@ -245,6 +270,51 @@ __global__ void __launch_bounds__(256) widen_i4_kernel(const uint8_t* __restrict
     }
 }
 
+__global__ void __launch_bounds__(256) widen_i8_kernel(const int8_t* __restrict__ src, int64_t n16,
+                                                       __half* __restrict__ dst) {
+    grid_dep_wait();
+    grid_dep_launch();
+    widen_i8_body(src, n16, dst, blockIdx.x, gridDim.x);
+}
+
+__global__ void __launch_bounds__(256) widen_i4_kernel(const uint8_t* __restrict__ src,
+                                                       int64_t n16, __half* __restrict__ dst) {
+    grid_dep_wait();
+    grid_dep_launch();
+    widen_i4_body(src, n16, dst, blockIdx.x, gridDim.x);
+}
+
+// Both operand images of the tensor-core GEMM in one launch: blocks
+// [0, a_blocks) quantize the activation rows into exact fp16 codes and their
+// scales; the remaining blocks widen the weight codes (INT8 or packed INT4)
+// into exact fp16 integers. The two jobs are independent and share the GPU.
+struct ImagesArgs {
+    const __half* x;
+    int64_t M, K;
+    __half* a_img;
+    float* s_a;
+    const void* w;
+    int64_t n16;      // 16-byte weight chunks
+    __half* b_img;
+    int a_blocks;
+};
+
+template <int VPT, int WPR, int BITS>
+__global__ void __launch_bounds__(256) operand_images_kernel(const ImagesArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
+    if ((int)blockIdx.x < a.a_blocks) {
+        quant_rows_reg_body<QuantOut::kF16, VPT, WPR>(a.x, a.M, a.K, 127, a.a_img, a.s_a,
+                                                       blockIdx.x, a.a_blocks);
+    } else if constexpr (BITS == 8) {
+        widen_i8_body(static_cast<const int8_t*>(a.w), a.n16, a.b_img, blockIdx.x - a.a_blocks,
+                      gridDim.x - a.a_blocks);
+    } else {
+        widen_i4_body(static_cast<const uint8_t*>(a.w), a.n16, a.b_img, blockIdx.x - a.a_blocks,
+                      gridDim.x - a.a_blocks);
+    }
+}
+
 int grid_for(int64_t work_items, int per_block, int num_sms) {
     int64_t b = (work_items + per_block - 1) / per_block;
     int64_t cap = (int64_t)num_sms * 16;
@@ -262,22 +332,24 @@ cudaError_t launch_rows_reg_t(const __half* src, int64_t rows, int64_t K, int qm
                               float* scales, int num_sms, cudaStream_t stream) {
     const int64_t nvec = K / 8;
     const int64_t cap = (int64_t)num_sms * 8;  // 8 resident blocks of 256 threads per SM
-    if (nvec <= 32 * 4) {
-        const int grid = (int)std::min<int64_t>((rows + 7) / 8, cap);
-        quant_rows_reg_kernel<OUT, 4, 1><<<grid, 256, 0, stream>>>(src, rows, K, qmax, out, scales);
-    } else if (nvec <= 32 * 8) {
-        const int grid = (int)std::min<int64_t>((rows + 7) / 8, cap);
-        quant_rows_reg_kernel<OUT, 8, 1><<<grid, 256, 0, stream>>>(src, rows, K, qmax, out, scales);
-    } else if (nvec <= 32 * 16) {
-        const int grid = (int)std::min<int64_t>((rows + 7) / 8, cap);
-        quant_rows_reg_kernel<OUT, 16, 1><<<grid, 256, 0, stream>>>(src, rows, K, qmax, out, scales);
-    } else if (nvec <= 256 * 8) {
-        const int grid = (int)std::min<int64_t>(rows, cap);
-        quant_rows_reg_kernel<OUT, 8, 8><<<grid, 256, 0, stream>>>(src, rows, K, qmax, out, scales);
-    } else {
-        return cudaErrorNotSupported;
-    }
-    return cudaGetLastError();
+    const int g1 = (int)std::min<int64_t>((rows + 7) / 8, cap);
+    const int g8 = (int)std::min<int64_t>(rows, cap);
+    if (nvec <= 32 * 4)
+        return launch_pdl(quant_rows_reg_kernel<OUT, 4, 1>, g1, 256, 0, stream, src, rows, K, qmax,
+                          out, scales);
+    if (nvec <= 32 * 8)
+        return launch_pdl(quant_rows_reg_kernel<OUT, 8, 1>, g1, 256, 0, stream, src, rows, K, qmax,
+                          out, scales);
+    if (nvec <= 32 * 12)
+        return launch_pdl(quant_rows_reg_kernel<OUT, 12, 1>, g1, 256, 0, stream, src, rows, K,
+                          qmax, out, scales);
+    if (nvec <= 32 * 16)
+        return launch_pdl(quant_rows_reg_kernel<OUT, 16, 1>, g1, 256, 0, stream, src, rows, K,
+                          qmax, out, scales);
+    if (nvec <= 256 * 8)
+        return launch_pdl(quant_rows_reg_kernel<OUT, 8, 8>, g8, 256, 0, stream, src, rows, K, qmax,
+                          out, scales);
+    return cudaErrorNotSupported;
 }
 
 cudaError_t launch_quant_rows_reg(const __half* src, int64_t rows, int64_t K, int qmax,
@@ -341,16 +413,60 @@ cudaError_t launch_widen_i8(const int8_t* src, int64_t n, __half* dst, int num_s
                             cudaStream_t stream) {
     if (n % 16 != 0) return cudaErrorInvalidValue;
     const int64_t n16 = n / 16;
-    widen_i8_kernel<<<grid_for(n16, 256, num_sms), 256, 0, stream>>>(src, n16, dst);
-    return cudaGetLastError();
+    return launch_pdl(widen_i8_kernel, grid_for(n16, 256 * 4, num_sms), 256, 0, stream, src, n16,
+                      dst);
 }
 
 cudaError_t launch_widen_i4(const uint8_t* src, int64_t n_codes, __half* dst, int num_sms,
                             cudaStream_t stream) {
     if (n_codes % 32 != 0) return cudaErrorInvalidValue;
     const int64_t n16 = n_codes / 32;
-    widen_i4_kernel<<<grid_for(n16, 256, num_sms), 256, 0, stream>>>(src, n16, dst);
-    return cudaGetLastError();
+    return launch_pdl(widen_i4_kernel, grid_for(n16, 256 * 4, num_sms), 256, 0, stream, src, n16,
+                      dst);
+}
+
+namespace {
+
+template <int BITS>
+cudaError_t launch_images_t(const ImagesArgs& a0, int64_t nvec, int num_sms, cudaStream_t stream) {
+    ImagesArgs a = a0;
+    const int64_t b_blocks = std::min<int64_t>((a.n16 + 256 * 4 - 1) / (256 * 4), (int64_t)num_sms * 4);
+    auto go = [&](auto kern, int64_t a_blocks) {
+        a.a_blocks = (int)a_blocks;
+        return launch_pdl(kern, (unsigned)(a_blocks + b_blocks), 256, 0, stream, a);
+    };
+    const int64_t g1 = std::min<int64_t>((a.M + 7) / 8, (int64_t)num_sms * 3);
+    const int64_t g8 = std::min<int64_t>(a.M, (int64_t)num_sms * 4);
+    if (nvec <= 32 * 4) return go(operand_images_kernel<4, 1, BITS>, g1);
+    if (nvec <= 32 * 8) return go(operand_images_kernel<8, 1, BITS>, g1);
+    if (nvec <= 32 * 12) return go(operand_images_kernel<12, 1, BITS>, g1);
+    if (nvec <= 32 * 16) return go(operand_images_kernel<16, 1, BITS>, g1);
+    return go(operand_images_kernel<8, 8, BITS>, g8);
+}
+
+}  // namespace
+
+cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const void* w, int bits,
+                                  int64_t N, __half* a_img, float* s_a, __half* b_img,
+                                  int num_sms, cudaStream_t stream) {
+    const int64_t nvec = K / 8;
+    const int64_t codes_per_chunk = (bits == 8) ? 16 : 32;
+    const bool fused = (K % 8 == 0) && nvec <= 256 * 8 &&
+                       (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                       (reinterpret_cast<uintptr_t>(a_img) % 16 == 0) &&
+                       ((N * K) % codes_per_chunk == 0);
+    if (!fused) {
+        cudaError_t e = launch_quant_groups(x, M, K, K, 127, QuantOut::kF16, a_img, s_a, num_sms,
+                                            stream);
+        if (e != cudaSuccess) return e;
+        return (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, b_img, num_sms,
+                                             stream)
+                           : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, b_img, num_sms,
+                                             stream);
+    }
+    ImagesArgs a{x, M, K, a_img, s_a, w, (N * K) / codes_per_chunk, b_img, 0};
+    return (bits == 8) ? launch_images_t<8>(a, nvec, num_sms, stream)
+                       : launch_images_t<4>(a, nvec, num_sms, stream);
 }
 
 }  // namespace cider

@@ -97,9 +97,8 @@ extern "C" cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M,
     __half* b_img = reinterpret_cast<__half*>(p + a_bytes + s_bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    cudaError_t e = launch_quant_groups(static_cast<const __half*>(x_f16), M, K, K, 127,
-                                        QuantOut::kF16, a_img, s_a, sms, s);
-    if (e == cudaSuccess) e = launch_widen_i8(wq, N * K, b_img, sms, s);
+    cudaError_t e = launch_operand_images(static_cast<const __half*>(x_f16), M, K, wq, 8, N,
+                                          a_img, s_a, b_img, sms, s);
     if (e == cudaSuccess) {
         GemmArgs a{};
         a.a_img = a_img;
