@@ -55,6 +55,9 @@ def parse_args():
                     help="run only the M = 1 GEMV leg (a small command for profilers)")
     ap.add_argument("--step-only", action="store_true",
                     help="run only the M = 4096 step (a small command for profilers)")
+    ap.add_argument("--configs", action="store_true",
+                    help="time every workload of the config list (M sweeps, per-group, W4A8, "
+                         "decoder layer) through the public calls; one JSON line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -301,6 +304,96 @@ def gemv_leg(args, x, wq, s_w, y_row0, stream):
             assert torch.equal(t.view(torch.int16), y_row0.view(torch.int16)), "graph GEMV"
     del wq_copies
     return standalone, sequence, n_copies
+
+
+def run_configs(args):
+    """Every workload shape of the operator configs, timed through the public
+    calls (quant + GEMM + dequant per call; the GEMV for M = 1). Inputs are
+    drawn on the GPU from a seeded generator (timing does not depend on the
+    values), in sets rotated so that together they exceed 3x L2. Times are
+    CUDA-event means over `steps` calls after `warmup`."""
+    import torch
+    import w4a8_quantized_gemm_int8_b300 as cider
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    cider.load_library()
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+
+    def inputs(M, N, K, bits, gs, n_out):
+        x = torch.randn(M, K, generator=gen, device=dev)
+        x[:, torch.randperm(K, generator=gen, device=dev)[:n_out]] *= 20.0
+        w = (torch.randn(N, K, generator=gen, device=dev) * 0.02).half()
+        x = x.half()
+        if bits == 8:
+            wq, s = cider.quantize_weight_int8(w, gs)
+        else:
+            wq, s = cider.pack_weight_int4(w, gs)
+        return x, wq, s
+
+    def time_case(M, N, K, bits, gs, n_out=4):
+        wbytes = N * K if bits == 8 else N * K // 2
+        per_set = 2 * M * K + wbytes + 2 * M * N
+        n_sets = max(1, min(8, -(-3 * l2 // per_set) + 1))
+        sets = []
+        for _ in range(n_sets):
+            x, wq, s = inputs(M, N, K, bits, gs, n_out)
+            sets.append((x, wq, s, torch.empty((M, N), dtype=torch.float16, device=dev)))
+        ws = torch.empty(max(1, cider.workspace_bytes(M, N, K, bits, gs)), dtype=torch.uint8,
+                         device=dev)
+
+        def call(i):
+            x, wq, s, y = sets[i % n_sets]
+            if M == 1:
+                cider.int8_gemv(x[0], wq, s, bits, gs, out=y[0])
+            elif bits == 8:
+                cider.w8a8_linear(x, wq, s, gs, out=y, ws=ws)
+            else:
+                cider.w4a8_linear(x, wq, s, gs, out=y, ws=ws)
+
+        for i in range(max(args.warmup, n_sets)):
+            call(i)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e5 * args.steps))
+        for i, (a, b) in enumerate(evs):
+            a.record(stream)
+            call(i)
+            b.record(stream)
+        torch.cuda.synchronize()
+        t = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+        st, site = cider.device_status()
+        assert st == cider.CIDER_OK, f"device status {st} at {site:#x}"
+        G = 1 if gs == 0 else K // gs
+        res = {"M": M, "N": N, "K": K, "bits": bits, "gs": gs, "us": round(t * 1e6, 2),
+               "TOPS": round(2.0 * M * N * K / t / 1e12, 1)}
+        if M == 1:
+            res["GB/s"] = round((wbytes + 4 * N * G + 2 * K + 2 * N) / t / 1e9, 1)
+        del sets, ws
+        return res
+
+    out = {"per_channel_N10240_K2560": [time_case(m, 10240, 2560, 8, 0)
+                                        for m in (1, 128, 1024, 4096, 8192)]}
+    for gs in (64, 128):
+        out[f"per_group{gs}_N2560_K10240"] = [time_case(m, 2560, 10240, 8, gs)
+                                              for m in (1, 128, 1024, 4096, 8192)]
+    for (n, k) in ((10240, 2560), (2560, 10240)):
+        out[f"w4a8_gs128_N{n}_K{k}"] = [time_case(m, n, k, 4, 128) for m in (1, 1024, 8192)]
+    import synth
+    layer = []
+    for name, K_, N_ in synth.DECODER_LAYER:
+        r = time_case(2048, N_, K_, 8, 0, n_out=max(1, round(K_ * 0.01)))
+        r["linear"] = name
+        layer.append(r)
+    tot_us = sum(r["us"] for r in layer)
+    tot_ops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in layer)
+    out["decoder_layer_M2048"] = {"linears": layer, "total_us": round(tot_us, 2),
+                                  "TOPS": round(tot_ops / (tot_us * 1e-6) / 1e12, 1)}
+    print(json.dumps({"configs": out, "steps": args.steps, "warmup": args.warmup,
+                      "timing": "CUDA events per call, inputs rotating over sets > 3x L2"}))
 
 
 def run_cider(args):
@@ -564,6 +657,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.configs:
+        run_configs(args)
     else:
         run_cider(args)
 

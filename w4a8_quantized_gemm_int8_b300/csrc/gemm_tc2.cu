@@ -47,8 +47,8 @@ constexpr int NUM_THREADS = NUM_ROLE_THREADS + NUM_EPI_THREADS;
 constexpr int TMEM_COLS = 512;  // two 256-column fp32 accumulators
 constexpr int MAX_SEG_KB = 16;  // 16 x 64 = 1024 k per exact fp32 segment
 constexpr int LAUNCH_REGS = 168;
-constexpr int ROLE_REGS = 56;    // TMA and MMA issue need few registers
-constexpr int EPI_REGS = 224;    // 128 running sums + 64 loaded columns per thread
+constexpr int ROLE_REGS = 40;    // TMA and MMA issue need few registers
+constexpr int EPI_REGS = 232;    // 128 running sums + loaded columns per thread
 constexpr int OUT_WARP_BYTES = 32 * 32 * 2;  // output staging: 32 rows x 32 fp16 per warp
 static_assert(NUM_ROLE_THREADS * ROLE_REGS + NUM_EPI_THREADS * EPI_REGS <=
                   NUM_THREADS * LAUNCH_REGS,
@@ -61,15 +61,15 @@ struct __align__(8) Barriers {
     uint64_t acc_full[2];       // each CTA: accumulator buffer ready
     uint64_t acc_empty[2];      // even CTA: both CTAs' epilogues drained the buffer
     uint64_t drain;             // even CTA: MMA drain after an abort
-    uint64_t epi_sync;          // each CTA: its 256 epilogue threads
 };
 
 struct SmemLayout {
     static constexpr int a_off = 0;
     static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
     static constexpr int out_off = b_off + STAGES * B_STAGE_BYTES;  // per-warp output staging
-    static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;  // float[2][BN]
-    static constexpr int bar_off = scale_off + 2 * BN * 4;
+    // Per epilogue warp: two buffers of its 128 columns' weight scales.
+    static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;
+    static constexpr int bar_off = scale_off + NUM_EPI_WARPS * 2 * 128 * 4;
     static constexpr int misc_off = bar_off + (int)sizeof(Barriers);  // tmem base, abort
     static constexpr int bytes = misc_off + 16;
     static constexpr int alloc_bytes = bytes + 1024;  // runtime 1024-byte alignment slack
@@ -97,7 +97,6 @@ enum : uint32_t {
     kSiteEpiAccFull = 0x304,
     kSiteDrain = 0x305,
     kSiteProducerDrain = 0x306,
-    kSiteEpiSync = 0x307,
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int& tn) {
@@ -142,7 +141,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             mbar_init(smem_u32(&bars->acc_empty[b]), 2 * NUM_EPI_WARPS);
         }
         mbar_init(smem_u32(&bars->drain), 1);
-        mbar_init(smem_u32(&bars->epi_sync), NUM_EPI_THREADS);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmap_a);
@@ -162,15 +160,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     // dependent launch); global memory is touched only after this wait.
     grid_dep_wait();
     grid_dep_launch();
-    if (warp >= 4) {
-        if (cluster < num_tiles) {
-            int tm, tn;
-            tile_coords(cluster, p.tiles_m, tm, tn);
-            scales[threadIdx.x - NUM_ROLE_THREADS] =
-                load_seg_scale(p, tn, 0, threadIdx.x - NUM_ROLE_THREADS);
-        }
-        named_bar_sync(1, NUM_EPI_THREADS);  // first tile's scales visible to all epilogue warps
-    }
 
     if (warp < 4) {
         setmaxnreg_dec<ROLE_REGS>();
@@ -266,14 +255,41 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
         const int ewarp = warp - 4;
         const int quad = warp & 3;
         const int half = ewarp >> 2;
-        const int et = threadIdx.x - NUM_ROLE_THREADS;
         // Output staging for the TMA store: 32 rows x 32 fp16 (64-byte rows,
         // 64-byte swizzle: chunk c of row r at chunk c ^ ((r >> 1) & 3)).
         uint8_t* stage_out = smem + SmemLayout::out_off + ewarp * OUT_WARP_BYTES;
         const uint32_t swz = (uint32_t)((lane >> 1) & 3);
+        // This warp's weight scales: two buffers of its 128 columns. Lane l
+        // copies columns 4l..4l+3 of the next segment that needs them (the
+        // next segment in per-group mode, the next tile's last segment in
+        // per-channel mode) one segment ahead, with asynchronous copies that
+        // hold no registers; no other warp reads them.
+        float* wsc = scales + ewarp * 256;
+        uint32_t sbuf = 0;
+        auto fetch_scales = [&](int tile, int seg, uint32_t buf) {
+            int tm, tn;
+            tile_coords(tile, p.tiles_m, tm, tn);
+            const int n0 = tn * BN + half * 128 + 4 * lane;
+            const int g = (p.G == 1) ? 0 : seg;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float* dst = wsc + buf * 128 + 4 * lane + i;
+                if (p.s_w != nullptr && n0 + i < p.N)
+                    cp_async_4(smem_u32(dst), p.s_w + (int64_t)(n0 + i) * p.G + g);
+                else
+                    *dst = 0.0f;
+            }
+            cp_async_commit();
+        };
+        auto scales_ready = [&]() {
+            cp_async_wait_all();
+            __syncwarp();
+        };
+        if (cluster < num_tiles) {
+            fetch_scales(cluster, (MODE == GemmMode::kPgF16) ? 0 : p.num_seg - 1, 0);
+            scales_ready();
+        }
         uint32_t seg_count = 0;
-        uint32_t epi_phase = 0;
-        uint32_t sbuf = 0;  // scales buffer of the current segment
         bool store_pending = false;
         uint32_t acc[128];
 
@@ -288,22 +304,19 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                 const uint32_t b = seg_count & 1;
                 const uint32_t acc_phase = (seg_count >> 1) & 1;
                 const bool last_seg = (seg == p.num_seg - 1);
-                // Per-group scales change every segment, per-channel ones every tile.
-                const bool new_scales = (MODE == GemmMode::kPgF16) || last_seg;
-                const float* sc = scales + sbuf * BN + half * 128;
+                const bool uses_scales = (MODE == GemmMode::kPgF16) || last_seg;
+                const float* sc = wsc + sbuf * 128;
 
-                float next_scale = 0.0f;
-                if (new_scales) {
+                // The other buffer was last read by this warp alone, in the
+                // previous scale-consuming segment, which every lane has left.
+                if (uses_scales) {
                     int nt = tile, ns = seg + 1;
                     if (ns == p.num_seg) {
                         ns = 0;
                         nt += nclusters;
                     }
-                    if (nt < num_tiles) {
-                        int ntm, ntn;
-                        tile_coords(nt, p.tiles_m, ntm, ntn);
-                        next_scale = load_seg_scale(p, ntn, ns, et);
-                    }
+                    if (MODE != GemmMode::kPgF16) ns = p.num_seg - 1;
+                    if (nt < num_tiles) fetch_scales(nt, ns, sbuf ^ 1);
                 }
 
                 {
@@ -316,65 +329,93 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
 
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                        b * BN + half * 128;
-                // Two batches of 64 columns: both 32-column loads in flight, one wait.
+                // Batches of BW columns (32; 16 in per-group mode, which keeps
+                // more values live); the next batch's TMEM load is in flight
+                // while the current one is folded.
+                {
+                    constexpr int BW = (MODE == GemmMode::kPgF16) ? 16 : 32;
+                    constexpr int NB = 128 / BW;
+                    auto ld = [&](uint32_t col, uint32_t* r) {
+                        if constexpr (BW == 32) tmem_ld_32x32b_x32_ptr(t_row + col, r);
+                        else tmem_ld_32x32b_x16_ptr(t_row + col, r);
+                    };
+                    auto wait = [&](uint32_t* r) {
+                        if constexpr (BW == 32) tmem_wait_ld_32(r);
+                        else tmem_wait_ld_16(r);
+                    };
+                    uint32_t va[BW], vb[BW];
+                    ld(0, va);
+                    wait(va);
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t v[64];
-                    tmem_ld_32x32b_x32_ptr(t_row + hb * 64, v);
-                    tmem_ld_32x32b_x32_ptr(t_row + hb * 64 + 32, v + 32);
-                    tmem_wait_ld();
-                    if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
-                        // Exact fp32 integers -> int32: the fast conversion holds
-                        // below 2^22; a warp holding a larger one converts all.
-                        bool big = false;
+                    for (int bt = 0; bt < NB; ++bt) {
+                        uint32_t* v = (bt & 1) ? vb : va;
+                        uint32_t* vn = (bt & 1) ? va : vb;
+                        if (bt < NB - 1) ld((bt + 1) * BW, vn);
+                        const int c0 = bt * BW;
+                        if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
+                            // Exact fp32 integers -> int32: the fast conversion holds
+                            // below 2^22; a warp holding a larger one converts all.
+                            bool big = false;
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) big |= fabsf(__uint_as_float(v[j])) >= 4194304.0f;
-                        if (__any_sync(0xffffffffu, big)) {
+                            for (int j = 0; j < BW; ++j) big |= fabsf(__uint_as_float(v[j])) >= 4194304.0f;
+                            if (__any_sync(0xffffffffu, big)) {
 #pragma unroll
-                            for (int j = 0; j < 64; ++j) {
-                                const int part = __float2int_rn(__uint_as_float(v[j]));
-                                acc[hb * 64 + j] = (seg == 0) ? (uint32_t)part
-                                                              : (uint32_t)((int)acc[hb * 64 + j] + part);
+                                for (int j = 0; j < BW; ++j) {
+                                    const int part = __float2int_rn(__uint_as_float(v[j]));
+                                    acc[c0 + j] = (seg == 0) ? (uint32_t)part
+                                                             : (uint32_t)((int)acc[c0 + j] + part);
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < BW; j += 2) {
+                                    float t0, t1;
+                                    fadd2_rn(t0, t1, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                             12582912.0f, 12582912.0f);
+                                    const int p0 = __float_as_int(t0) - 0x4B400000;
+                                    const int p1 = __float_as_int(t1) - 0x4B400000;
+                                    acc[c0 + j] = (seg == 0) ? (uint32_t)p0 : (uint32_t)((int)acc[c0 + j] + p0);
+                                    acc[c0 + j + 1] =
+                                        (seg == 0) ? (uint32_t)p1 : (uint32_t)((int)acc[c0 + j + 1] + p1);
+                                }
                             }
-                        } else {
+                        } else if constexpr (MODE == GemmMode::kPgF16) {
+                            // f = f + fl(P_g * s_g), both roundings kept (ascending g).
+                            // Scalar operations on purpose: a packed f32x2 multiply
+                            // whose only use is a packed add is contracted into a
+                            // fused multiply-add by the compiler.
 #pragma unroll
-                            for (int j = 0; j < 64; ++j) {
-                                const int part = small_float_to_int(__uint_as_float(v[j]));
-                                acc[hb * 64 + j] = (seg == 0) ? (uint32_t)part
-                                                              : (uint32_t)((int)acc[hb * 64 + j] + part);
+                            for (int j = 0; j < BW; j += 2) {
+                                const float2 s2 = *reinterpret_cast<const float2*>(sc + c0 + j);
+                                const float q0 = __fmul_rn(__uint_as_float(v[j]), s2.x);
+                                const float q1 = __fmul_rn(__uint_as_float(v[j + 1]), s2.y);
+                                const float f0 = (seg == 0) ? 0.0f : __uint_as_float(acc[c0 + j]);
+                                const float f1 = (seg == 0) ? 0.0f : __uint_as_float(acc[c0 + j + 1]);
+                                acc[c0 + j] = __float_as_uint(__fadd_rn(f0, q0));
+                                acc[c0 + j + 1] = __float_as_uint(__fadd_rn(f1, q1));
+                            }
+                        } else {  // kRawPgS32: this group's partials, straight out
+                            if (m < p.M) {
+                                int32_t* out = static_cast<int32_t*>(p.out);
+#pragma unroll
+                                for (int j = 0; j < BW; ++j) {
+                                    const int n = n_half + c0 + j;
+                                    if (n < p.N)
+                                        out[((int64_t)m * p.N + n) * p.G + seg] =
+                                            __float2int_rn(__uint_as_float(v[j]));
+                                }
                             }
                         }
-                    } else if constexpr (MODE == GemmMode::kPgF16) {
-#pragma unroll
-                        for (int j = 0; j < 64; j += 4) {
-                            const float4 s4 = *reinterpret_cast<const float4*>(sc + hb * 64 + j);
-                            const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float prev =
-                                    (seg == 0) ? 0.0f : __uint_as_float(acc[hb * 64 + j + i]);
-                                const float prod = __fmul_rn(__uint_as_float(v[j + i]), ss[i]);
-                                acc[hb * 64 + j + i] = __float_as_uint(__fadd_rn(prev, prod));
-                            }
-                        }
-                    } else {  // kRawPgS32: this group's partials, straight out
-                        if (m < p.M) {
-                            int32_t* out = static_cast<int32_t*>(p.out);
-#pragma unroll
-                            for (int j = 0; j < 64; ++j) {
-                                const int n = n_half + hb * 64 + j;
-                                if (n < p.N)
-                                    out[((int64_t)m * p.N + n) * p.G + seg] =
-                                        __float2int_rn(__uint_as_float(v[j]));
-                            }
-                        }
+                        if (bt < NB - 1) wait(vn);
                     }
                 }
-                // This warp's reads of the buffer are complete: release it on
-                // the even CTA's barrier (one arrival per warp, both CTAs).
+                // This warp's reads of the buffer are complete (waited, the
+                // values are in registers): release it on the even CTA's
+                // barrier, one relaxed arrival per warp of both CTAs; the
+                // arrival orders no memory writes.
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&bars->acc_empty[b]), 0));
+                if (lane == 0)
+                    mbar_arrive_cluster_relaxed(map_to_rank(smem_u32(&bars->acc_empty[b]), 0));
 
                 if (last_seg) {
                     if constexpr (MODE == GemmMode::kRawS32) {
@@ -401,18 +442,20 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                             uint32_t h2[16];
 #pragma unroll
                             for (int j = 0; j < 32; j += 2) {
-                                float y0, y1;
                                 const int c = r * 32 + j;
+                                float y0, y1;
                                 if constexpr (MODE == GemmMode::kPcF16) {
                                     const float f0 = slow_cvt ? __int2float_rn((int)acc[c])
                                                               : small_int_to_float((int)acc[c]);
                                     const float f1 = slow_cvt ? __int2float_rn((int)acc[c + 1])
                                                               : small_int_to_float((int)acc[c + 1]);
-                                    y0 = __fmul_rn(__fmul_rn(f0, sa), sc[c]);
-                                    y1 = __fmul_rn(__fmul_rn(f1, sa), sc[c + 1]);
+                                    const float2 s2 = *reinterpret_cast<const float2*>(sc + c);
+                                    float t0, t1;
+                                    fmul2_rn(t0, t1, f0, f1, sa, sa);
+                                    fmul2_rn(y0, y1, t0, t1, s2.x, s2.y);
                                 } else {
-                                    y0 = __fmul_rn(__uint_as_float(acc[c]), sa);
-                                    y1 = __fmul_rn(__uint_as_float(acc[c + 1]), sa);
+                                    fmul2_rn(y0, y1, __uint_as_float(acc[c]), __uint_as_float(acc[c + 1]),
+                                             sa, sa);
                                 }
                                 const __half2 hv = __floats2half2_rn(y0, y1);
                                 h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
@@ -447,17 +490,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                     }
                 }
 
-                if (new_scales) {
-                    // Publish the next segment's scales in the other buffer; the
-                    // barrier keeps a thread from overwriting scales that another
-                    // thread still reads.
-                    scales[(sbuf ^ 1) * BN + et] = next_scale;
-                    mbar_arrive(smem_u32(&bars->epi_sync));
-                    const bool ok = mbar_wait_bounded(smem_u32(&bars->epi_sync), epi_phase,
-                                                      p.timeout_ns, abort_flag, p.status,
-                                                      kSiteEpiSync);
-                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
-                    epi_phase ^= 1;
+                if (uses_scales) {
+                    scales_ready();
                     sbuf ^= 1;
                 }
             }
