@@ -42,6 +42,10 @@ M, N, K = 4096, 10240, 2560
 METRIC = "W8A8 GEMM TOPS & % INT8 peak at M=4096; M=1 INT8 GEMV HBM GB/s"
 WORKLOAD = "w8a8_per_channel_linear_M4096_N10240_K2560"
 FLUSH_BYTES = 512 << 20
+# DRAM bytes (read + write) of one launch of the pair GEMM at this workload,
+# from the ncu capture summarised in profiles/; reset to None whenever the
+# kernel changes until it is captured again.
+GEMM_DRAM_BYTES_PER_LAUNCH = 127.8e6
 
 
 def parse_args():
@@ -625,7 +629,11 @@ def run_cider(args):
                          "note": "kernels timed one by one; in the step the quant and weight "
                                  "image share one launch and the GEMM prologue overlaps it"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak,
-                     "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / bf16_peak,
+                     "traffic": GEMM_DRAM_BYTES_PER_LAUNCH,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one "
+                                       "cold-cache launch (profiles/gemm_tc2_kernel_pc_M4096_"
+                                       "N10240_K2560.md)",
                      "kernel": "gemm_tc2_kernel<kPcF16> (SM pairs, cta_group::2)",
                      "peak_source": f"{peak_src} dense bf16 burst; fp16 nominal rate equal"},
         "int8_peak": {"torch_int_mm_8192_tops": int8_lib,

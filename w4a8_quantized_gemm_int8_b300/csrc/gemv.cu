@@ -99,7 +99,7 @@ __device__ __forceinline__ int chunk_dot(const uint4& wv, const uint4* codes, in
 }
 
 template <int BITS, bool PG>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     int8_t* codes_s = reinterpret_cast<int8_t*>(smem + p.codes_off);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
@@ -346,7 +346,10 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
         p.rows_per_stage * (p.row_bytes + (p.scales_staged ? p.G * 4 : 0));
     p.stage_bytes = (stage_payload + 127) & ~127;
 
-    const int grid = (int)(a.N < num_sms ? a.N : num_sms);
+    // Two CTAs per SM, each with at most half the shared memory: consecutive
+    // GEMVs (programmatic dependent launch) then overlap on every SM, the
+    // next one streaming its weights while the previous one finishes.
+    const int grid = (int)(a.N < 2 * num_sms ? a.N : 2 * num_sms);
     const int max_rows = (int)((a.N + grid - 1) / grid);
     const int max_stages_needed = (max_rows + p.rows_per_stage - 1) / p.rows_per_stage;
 
@@ -360,7 +363,7 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     p.bar_off = p.sw_off + sw_bytes;
     const int bar_bytes = 2 * kMaxStages * 8 + kConsumerWarps * 4 + 16;
     p.stage_off = (p.bar_off + bar_bytes + 127) & ~127;
-    const int budget = g_max_smem - p.stage_off;
+    const int budget = (g_max_smem / 2 - 1024) - p.stage_off;
     int ns = budget / p.stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
     if (ns > max_stages_needed) ns = max_stages_needed;
