@@ -105,8 +105,10 @@ CIDER_API cider_status cider_pack_weight_int4(const void* w_f16, int64_t N, int6
 /*
  * Bytes of device workspace the GEMM calls below need for this problem
  * (bits 8 or 4). The workspace holds the fp16 operand images of the
- * quantized activations and weights and the per-token scales. Returns 0
- * when M == 1 (the GEMV path needs none) and on invalid sizes.
+ * quantized activations and weights and the per-token scales, and for
+ * group_size > 0 a group-major copy of the per-group weight scales. Returns
+ * 0 when M == 1 (the GEMV path needs none) and on invalid sizes (including a
+ * group_size that does not divide K).
  */
 CIDER_API size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bits, int32_t group_size);
 

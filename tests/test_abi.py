@@ -52,6 +52,10 @@ def test_workspace_bytes(lib):
     n = cider.workspace_bytes(4096, 10240, 2560)
     assert n >= 2 * 4096 * 2560 + 4 * 4096 + 2 * 10240 * 2560
     assert n % 256 == 0
+    # per-group: plus the group-major copy of the scales
+    g = cider.workspace_bytes(4096, 2560, 10240, 8, 64)
+    assert g >= 2 * 4096 * 10240 + 4 * 4096 + 2 * 2560 * 10240 + 4 * 2560 * (10240 // 64)
+    assert cider.workspace_bytes(4096, 2560, 10240, 8, 100) == 0  # 100 does not divide K
 
 
 def test_null_and_size_checks_precede_cuda(lib):

@@ -46,13 +46,16 @@ struct Workspace {
     __half* a_img;
     float* s_a;
     __half* b_img;
+    float* s_wT;  // per-group scales, group-major (per-group modes only)
 };
 
-size_t workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    return align256((size_t)M * K * 2) + align256((size_t)M * 4) + align256((size_t)N * K * 2);
+// a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K] fp16 | s_wT [K/gs, N] fp32 (gs > 0)
+size_t workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t gs = 0) {
+    const size_t t = gs > 0 ? align256((size_t)(K / gs) * N * 4) : 0;
+    return align256((size_t)M * K * 2) + align256((size_t)M * 4) + align256((size_t)N * K * 2) + t;
 }
 
-Workspace carve(void* ws, int64_t M, int64_t N, int64_t K) {
+Workspace carve(void* ws, int64_t M, int64_t N, int64_t K, int64_t gs = 0) {
     uint8_t* p = static_cast<uint8_t*>(ws);
     Workspace w;
     w.a_img = reinterpret_cast<__half*>(p);
@@ -60,6 +63,8 @@ Workspace carve(void* ws, int64_t M, int64_t N, int64_t K) {
     w.s_a = reinterpret_cast<float*>(p);
     p += align256((size_t)M * 4);
     w.b_img = reinterpret_cast<__half*>(p);
+    p += align256((size_t)N * K * 2);
+    w.s_wT = gs > 0 ? reinterpret_cast<float*>(p) : nullptr;
     return w;
 }
 
@@ -90,15 +95,16 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
         return from_cuda(launch_gemv(g, sms, stream));
     }
     if (!valid_group(gs, K, 64)) return CIDER_ERR_UNSUPPORTED;
-    const size_t need = workspace_bytes(M, N, K);
+    const size_t need = workspace_bytes(M, N, K, gs);
     if (!ws || ws_bytes < need) return CIDER_ERR_WORKSPACE;
     if (!aligned16(ws)) return CIDER_ERR_UNSUPPORTED;
     unsigned long long* status = nullptr;
     if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
 
-    Workspace wsp = carve(ws, M, N, K);
+    Workspace wsp = carve(ws, M, N, K, gs);
     cudaError_t e = launch_operand_images(static_cast<const __half*>(x), M, K, w, bits, N,
-                                          wsp.a_img, wsp.s_a, wsp.b_img, sms, stream);
+                                          wsp.a_img, wsp.s_a, wsp.b_img, s_w, wsp.s_wT,
+                                          gs > 0 ? K / gs : 1, sms, stream);
     if (e != cudaSuccess) return from_cuda(e);
     GemmArgs a{};
     a.a_img = wsp.a_img;
@@ -109,6 +115,7 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
     a.group_size = gs;
     a.s_a = wsp.s_a;
     a.s_w = s_w;
+    a.s_wT = wsp.s_wT;
     a.out = y;
     a.mode = (gs == 0) ? GemmMode::kPcF16 : GemmMode::kPgF16;
     a.timeout_ns = kWaitTimeoutNs;
@@ -177,9 +184,9 @@ cider_status cider_pack_weight_int4(const void* w_f16, int64_t N, int64_t K, int
 }
 
 size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bits, int32_t group_size) {
-    (void)group_size;
     if (M <= 1 || N <= 0 || K <= 0 || (bits != 8 && bits != 4)) return 0;
-    return workspace_bytes(M, N, K);
+    if (group_size < 0 || (group_size > 0 && K % group_size != 0)) return 0;
+    return workspace_bytes(M, N, K, group_size);
 }
 
 cider_status cider_w8a8_gemm_pc(const void* x_f16, int64_t M, int64_t N, int64_t K,

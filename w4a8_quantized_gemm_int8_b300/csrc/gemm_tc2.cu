@@ -84,6 +84,7 @@ struct Params {
     int tiles_m, tiles_n;  // tiles of 256 x 256
     const float* s_a;
     const float* s_w;
+    const float* s_wT;  // optional group-major copy of per-group scales [G, N]
     void* out;
     int tma_store;  // fp16 output written through tmap_y (N % 8 == 0)
     uint64_t timeout_ns;
@@ -271,13 +272,18 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             tile_coords(tile, p.tiles_m, tm, tn);
             const int n0 = tn * BN + half * 128 + 4 * lane;
             const int g = (p.G == 1) ? 0 : seg;
+            float* dst = wsc + buf * 128 + 4 * lane;
+            if (p.s_wT != nullptr && n0 + 3 < p.N && (p.N & 3) == 0) {
+                // group-major copy: the four columns are 16 contiguous bytes
+                cp_async_16(smem_u32(dst), p.s_wT + (int64_t)g * p.N + n0);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float* dst = wsc + buf * 128 + 4 * lane + i;
-                if (p.s_w != nullptr && n0 + i < p.N)
-                    cp_async_4(smem_u32(dst), p.s_w + (int64_t)(n0 + i) * p.G + g);
-                else
-                    *dst = 0.0f;
+                for (int i = 0; i < 4; ++i) {
+                    if (p.s_w != nullptr && n0 + i < p.N)
+                        cp_async_4(smem_u32(dst + i), p.s_w + (int64_t)(n0 + i) * p.G + g);
+                    else
+                        dst[i] = 0.0f;
+                }
             }
             cp_async_commit();
         };
@@ -300,6 +306,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             const int m = m_base + lane;
             const int n_half = tn * BN + half * 128;
 
+            if constexpr (MODE == GemmMode::kPgF16) {
+#pragma unroll
+                for (int j = 0; j < 128; ++j) acc[j] = 0u;  // f = +0 before the first group
+            }
             for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
                 const uint32_t b = seg_count & 1;
                 const uint32_t acc_phase = (seg_count >> 1) & 1;
@@ -333,7 +343,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                 // more values live); the next batch's TMEM load is in flight
                 // while the current one is folded.
                 {
-                    constexpr int BW = (MODE == GemmMode::kPgF16) ? 16 : 32;
+                    constexpr int BW = 32;
                     constexpr int NB = 128 / BW;
                     auto ld = [&](uint32_t col, uint32_t* r) {
                         if constexpr (BW == 32) tmem_ld_32x32b_x32_ptr(t_row + col, r);
@@ -379,19 +389,24 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                                 }
                             }
                         } else if constexpr (MODE == GemmMode::kPgF16) {
-                            // f = f + fl(P_g * s_g), both roundings kept (ascending g).
-                            // Scalar operations on purpose: a packed f32x2 multiply
-                            // whose only use is a packed add is contracted into a
-                            // fused multiply-add by the compiler.
+                            // f = f + fl(P_g * s_g), both roundings kept (ascending g;
+                            // f starts at +0 for each tile, as 0 + q). Products are
+                            // scalar multiplies: a packed f32x2 multiply whose only use
+                            // is a packed add is contracted into a fused multiply-add.
 #pragma unroll
-                            for (int j = 0; j < BW; j += 2) {
-                                const float2 s2 = *reinterpret_cast<const float2*>(sc + c0 + j);
-                                const float q0 = __fmul_rn(__uint_as_float(v[j]), s2.x);
-                                const float q1 = __fmul_rn(__uint_as_float(v[j + 1]), s2.y);
-                                const float f0 = (seg == 0) ? 0.0f : __uint_as_float(acc[c0 + j]);
-                                const float f1 = (seg == 0) ? 0.0f : __uint_as_float(acc[c0 + j + 1]);
-                                acc[c0 + j] = __float_as_uint(__fadd_rn(f0, q0));
-                                acc[c0 + j + 1] = __float_as_uint(__fadd_rn(f1, q1));
+                            for (int j = 0; j < BW; j += 4) {
+                                const float4 s4 = *reinterpret_cast<const float4*>(sc + c0 + j);
+                                const float q0 = __fmul_rn(__uint_as_float(v[j]), s4.x);
+                                const float q1 = __fmul_rn(__uint_as_float(v[j + 1]), s4.y);
+                                const float q2 = __fmul_rn(__uint_as_float(v[j + 2]), s4.z);
+                                const float q3 = __fmul_rn(__uint_as_float(v[j + 3]), s4.w);
+                                float r0, r1, r2, r3;
+                                fadd2_rn(r0, r1, __uint_as_float(acc[c0 + j]), __uint_as_float(acc[c0 + j + 1]), q0, q1);
+                                fadd2_rn(r2, r3, __uint_as_float(acc[c0 + j + 2]), __uint_as_float(acc[c0 + j + 3]), q2, q3);
+                                acc[c0 + j] = __float_as_uint(r0);
+                                acc[c0 + j + 1] = __float_as_uint(r1);
+                                acc[c0 + j + 2] = __float_as_uint(r2);
+                                acc[c0 + j + 3] = __float_as_uint(r3);
                             }
                         } else {  // kRawPgS32: this group's partials, straight out
                             if (m < p.M) {
@@ -597,6 +612,8 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     p.tiles_n = (p.N + BN - 1) / BN;
     p.s_a = a.s_a;
     p.s_w = a.s_w;
+    p.s_wT = (per_group && a.s_wT && reinterpret_cast<uintptr_t>(a.s_wT) % 16 == 0) ? a.s_wT
+                                                                                   : nullptr;
     p.out = a.out;
     p.tma_store = tma_store ? 1 : 0;
     p.timeout_ns = a.timeout_ns;

@@ -42,11 +42,13 @@ cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int6
 
 // Both operand images of the tensor-core GEMM in one launch: x fp16 [M,K] ->
 // a_img (exact fp16 codes) + s_a, and weights (INT8 [N,K] or packed INT4
-// [N,K/2]) -> b_img (exact fp16 integers). Falls back to separate launches
-// for shapes the fused kernel does not take.
+// [N,K/2]) -> b_img (exact fp16 integers); with s_wT non-NULL also the
+// group-major copy s_wT [G,N] of per-group scales s_w [N,G]. Falls back to
+// separate launches for shapes the fused kernel does not take.
 cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const void* w, int bits,
                                   int64_t N, __half* a_img, float* s_a, __half* b_img,
-                                  int num_sms, cudaStream_t stream);
+                                  const float* s_w, float* s_wT, int64_t G, int num_sms,
+                                  cudaStream_t stream);
 
 // Operand images: INT8 codes / packed INT4 nibbles -> exact fp16 integers.
 cudaError_t launch_widen_i8(const int8_t* src, int64_t n, __half* dst, int num_sms,
@@ -69,6 +71,7 @@ struct GemmArgs {
     int group_size;       // 0 for per-channel / raw totals
     const float* s_a;     // [M]
     const float* s_w;     // [N] or [N, K/gs]
+    const float* s_wT;    // per-group scales group-major [K/gs, N] (optional; faster fetch)
     void* out;
     GemmMode mode;
     uint64_t timeout_ns;

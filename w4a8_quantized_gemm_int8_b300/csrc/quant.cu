@@ -297,7 +297,24 @@ struct ImagesArgs {
     int64_t n16;      // 16-byte weight chunks
     __half* b_img;
     int a_blocks;
+    const float* s_w;  // per-group weight scales [N, G] (NULL: nothing to transpose)
+    float* s_wT;       // their group-major copy [G, N]
+    int64_t N, G;
 };
+
+// Group-major copy of per-group scales: s_wT[g, n] = s_w[n, g] (writes
+// coalesced along n), so the GEMM epilogue fetches one group's scales for a
+// run of output channels as contiguous bytes.
+__device__ __forceinline__ void transpose_scales_body(const float* __restrict__ s_w,
+                                                      float* __restrict__ s_wT, int64_t N,
+                                                      int64_t G, int block, int nblocks) {
+    const int64_t total = N * G;
+    for (int64_t i = (int64_t)block * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)nblocks * blockDim.x) {
+        const int64_t g = i / N, n = i - g * N;
+        s_wT[i] = __ldg(s_w + n * G + g);
+    }
+}
 
 template <int VPT, int WPR, int BITS>
 __global__ void __launch_bounds__(256) operand_images_kernel(const ImagesArgs a) {
@@ -306,12 +323,13 @@ __global__ void __launch_bounds__(256) operand_images_kernel(const ImagesArgs a)
     if ((int)blockIdx.x < a.a_blocks) {
         quant_rows_reg_body<QuantOut::kF16, VPT, WPR>(a.x, a.M, a.K, 127, a.a_img, a.s_a,
                                                        blockIdx.x, a.a_blocks);
-    } else if constexpr (BITS == 8) {
-        widen_i8_body(static_cast<const int8_t*>(a.w), a.n16, a.b_img, blockIdx.x - a.a_blocks,
-                      gridDim.x - a.a_blocks);
     } else {
-        widen_i4_body(static_cast<const uint8_t*>(a.w), a.n16, a.b_img, blockIdx.x - a.a_blocks,
-                      gridDim.x - a.a_blocks);
+        const int wb = blockIdx.x - a.a_blocks, nwb = gridDim.x - a.a_blocks;
+        if constexpr (BITS == 8)
+            widen_i8_body(static_cast<const int8_t*>(a.w), a.n16, a.b_img, wb, nwb);
+        else
+            widen_i4_body(static_cast<const uint8_t*>(a.w), a.n16, a.b_img, wb, nwb);
+        if (a.s_wT) transpose_scales_body(a.s_w, a.s_wT, a.N, a.G, wb, nwb);
     }
 }
 
@@ -446,9 +464,18 @@ cudaError_t launch_images_t(const ImagesArgs& a0, int64_t nvec, int num_sms, cud
 
 }  // namespace
 
+__global__ void __launch_bounds__(256) transpose_scales_kernel(const float* __restrict__ s_w,
+                                                               float* __restrict__ s_wT, int64_t N,
+                                                               int64_t G) {
+    grid_dep_wait();
+    grid_dep_launch();
+    transpose_scales_body(s_w, s_wT, N, G, blockIdx.x, gridDim.x);
+}
+
 cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const void* w, int bits,
                                   int64_t N, __half* a_img, float* s_a, __half* b_img,
-                                  int num_sms, cudaStream_t stream) {
+                                  const float* s_w, float* s_wT, int64_t G, int num_sms,
+                                  cudaStream_t stream) {
     const int64_t nvec = K / 8;
     const int64_t codes_per_chunk = (bits == 8) ? 16 : 32;
     const bool fused = (K % 8 == 0) && nvec <= 256 * 8 &&
@@ -459,12 +486,15 @@ cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const v
         cudaError_t e = launch_quant_groups(x, M, K, K, 127, QuantOut::kF16, a_img, s_a, num_sms,
                                             stream);
         if (e != cudaSuccess) return e;
-        return (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, b_img, num_sms,
-                                             stream)
-                           : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, b_img, num_sms,
-                                             stream);
+        e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, b_img, num_sms,
+                                          stream)
+                        : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, b_img, num_sms,
+                                          stream);
+        if (e != cudaSuccess || !s_wT) return e;
+        return launch_pdl(transpose_scales_kernel, grid_for(N * G, 256, num_sms), 256, 0, stream,
+                          s_w, s_wT, N, G);
     }
-    ImagesArgs a{x, M, K, a_img, s_a, w, (N * K) / codes_per_chunk, b_img, 0};
+    ImagesArgs a{x, M, K, a_img, s_a, w, (N * K) / codes_per_chunk, b_img, 0, s_w, s_wT, N, G};
     return (bits == 8) ? launch_images_t<8>(a, nvec, num_sms, stream)
                        : launch_images_t<4>(a, nvec, num_sms, stream);
 }

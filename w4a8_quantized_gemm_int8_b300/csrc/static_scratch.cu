@@ -98,7 +98,7 @@ extern "C" cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     cudaError_t e = launch_operand_images(static_cast<const __half*>(x_f16), M, K, wq, 8, N,
-                                          a_img, s_a, b_img, sms, s);
+                                          a_img, s_a, b_img, nullptr, nullptr, 1, sms, s);
     if (e == cudaSuccess) {
         GemmArgs a{};
         a.a_img = a_img;
