@@ -49,10 +49,12 @@ struct Workspace {
     float* s_wT;  // per-group scales, group-major (per-group modes only)
 };
 
-// a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K] fp16 | s_wT [K/gs, N] fp32 (gs > 0)
+// a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K] fp16 (SM-pair engine only;
+// the single-SM engine reads the raw weight codes) | s_wT [K/gs, N] fp32 (gs > 0)
 size_t workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t gs = 0) {
+    const size_t b = gemm_uses_pair(M) ? align256((size_t)N * K * 2) : 0;
     const size_t t = gs > 0 ? align256((size_t)(K / gs) * N * 4) : 0;
-    return align256((size_t)M * K * 2) + align256((size_t)M * 4) + align256((size_t)N * K * 2) + t;
+    return align256((size_t)M * K * 2) + align256((size_t)M * 4) + b + t;
 }
 
 Workspace carve(void* ws, int64_t M, int64_t N, int64_t K, int64_t gs = 0) {
@@ -62,8 +64,11 @@ Workspace carve(void* ws, int64_t M, int64_t N, int64_t K, int64_t gs = 0) {
     p += align256((size_t)M * K * 2);
     w.s_a = reinterpret_cast<float*>(p);
     p += align256((size_t)M * 4);
-    w.b_img = reinterpret_cast<__half*>(p);
-    p += align256((size_t)N * K * 2);
+    w.b_img = nullptr;
+    if (gemm_uses_pair(M)) {
+        w.b_img = reinterpret_cast<__half*>(p);
+        p += align256((size_t)N * K * 2);
+    }
     w.s_wT = gs > 0 ? reinterpret_cast<float*>(p) : nullptr;
     return w;
 }
@@ -101,14 +106,19 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
     unsigned long long* status = nullptr;
     if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
 
+    // SM-pair engine: fp16 images of both operands. Single-SM engine (few
+    // tokens): activation image only; the GEMM widens the raw weight codes.
     Workspace wsp = carve(ws, M, N, K, gs);
-    cudaError_t e = launch_operand_images(static_cast<const __half*>(x), M, K, w, bits, N,
-                                          wsp.a_img, wsp.s_a, wsp.b_img, s_w, wsp.s_wT,
+    const bool img = wsp.b_img != nullptr;
+    cudaError_t e = launch_operand_images(static_cast<const __half*>(x), M, K, img ? w : nullptr,
+                                          bits, N, wsp.a_img, wsp.s_a, wsp.b_img, s_w, wsp.s_wT,
                                           gs > 0 ? K / gs : 1, sms, stream);
     if (e != cudaSuccess) return from_cuda(e);
     GemmArgs a{};
     a.a_img = wsp.a_img;
     a.b_img = wsp.b_img;
+    a.b_raw = img ? nullptr : w;
+    a.b_bits = bits;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -308,12 +318,16 @@ cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int6
     Workspace wsp = carve(ws, Mw, N, K);
     cudaError_t e = launch_widen_i8(q, M * K, wsp.a_img, sms, s);
     if (e != cudaSuccess) return from_cuda(e);
-    e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, wsp.b_img, sms, s)
-                    : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, wsp.b_img, sms, s);
-    if (e != cudaSuccess) return from_cuda(e);
+    if (wsp.b_img) {
+        e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, wsp.b_img, sms, s)
+                        : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, wsp.b_img, sms, s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
     GemmArgs a{};
     a.a_img = wsp.a_img;
     a.b_img = wsp.b_img;
+    a.b_raw = wsp.b_img ? nullptr : w;
+    a.b_bits = bits;
     a.M = M;
     a.N = N;
     a.K = K;

@@ -1,4 +1,5 @@
-// INT8 x INT8 -> INT32 GEMM with fused dequant, on the sm_103a tensor cores.
+// INT8 x INT8 -> INT32 GEMM with fused dequant, one SM per tile: the engine
+// for few tokens (M <= 128), and the tensor-map encoders both engines use.
 //
 // What it computes (Cider README, sections "Metal Kernel Pipeline" and
 // "Quantization"): acc[m,n] = sum_k q[m,k] * wq[n,k] exactly in int32, then
@@ -9,84 +10,100 @@
 // How (B300): tcgen05 has no integer MMA kind on sm_103a, so the codes
 // (integers in [-127, 127]) are held exactly as fp16 and multiplied with
 // tcgen05.mma kind::f16 into an fp32 accumulator in tensor memory. Every
-// product is an integer of magnitude <= 127^2, exact in fp32, and every
-// partial sum over at most 1024 consecutive k is an integer of magnitude
-// <= 127^2 * 1024 < 2^24, so the fp32 accumulator holds it exactly. K is
-// therefore cut into segments of at most 1024 (per-channel) or of one group
+// product is an integer of magnitude <= 127^2 and every partial sum over at
+// most 1024 consecutive k an integer below 127^2 * 1024 < 2^24, exact in
+// fp32. K is cut into segments of at most 1024 (per-channel) or of one group
 // (per-group); each segment accumulates into one of two TMEM buffers, and the
-// epilogue warps fold it - converting the exact fp32 integer to int32 and
-// adding (per-channel), or rescaling and adding in fp32 in ascending group
-// order (per-group) - while the tensor core fills the other buffer.
+// epilogue folds it (exact fp32 integer -> int32 and add, or rescale and add
+// in fp32 in ascending group order) while the tensor core fills the other.
 //
-// Kernel shape: persistent, one CTA per SM, tile 128 tokens x 256 output
-// channels, 64-deep K stages (one 128-byte swizzle row of fp16), 4-stage TMA
-// ring. Warp 0 issues TMA, warp 1 owns TMEM and issues MMAs (warps 2-3 idle),
-// warps 4..11 are the epilogue (two warps per TMEM lane quadrant, 128 columns
-// each).
+// Shape for few tokens: one CTA per 128-token x 64-channel tile (160 tiles at
+// N = 10240), persistent over tiles. With few tokens the weights are nearly
+// all of the bytes, so they are read as their raw codes (INT8 [N,K] or packed
+// INT4 [N,K/2]) and widened to exact fp16 on chip: TMA stages the raw bytes
+// and two converter warps write the 128-byte-swizzled fp16 operand tile that
+// the tensor core reads; no weight image is written to memory. (An fp16
+// weight image is accepted too.) Warp 0 issues TMA, warp 1 owns TMEM and
+// issues MMAs (128 x 64 x 16), warps 2-3 convert, warps 4..11 are the
+// epilogue: each owns one TMEM lane quadrant and 32 of the 64 columns, reads
+// a whole segment with one 32-column TMEM load, and writes fp16 output
+// through 64-byte-swizzled staging and TMA stores. Every wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <cstring>
 
 #include "device_common.cuh"
 #include "kernels.h"
 
 namespace cider {
-namespace gemm {
+namespace gemm1 {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BN = 64;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK * 2;
 constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int MAX_STAGES = 8;
+constexpr int NUM_CONV_WARPS = 2;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
-constexpr int NUM_ROLE_THREADS = 128;  // warpgroup 0: TMA warp, MMA warp, two idle warps
+constexpr int NUM_ROLE_THREADS = 128;  // TMA warp, MMA warp, two converter warps
 constexpr int NUM_THREADS = NUM_ROLE_THREADS + NUM_EPI_THREADS;
-constexpr int TMEM_COLS = 512;  // two 256-column fp32 accumulators
-constexpr int MAX_SEG_KB = 16;  // 16 x 64 = 1024 k per exact fp32 segment
-// Register split, per warpgroup (setmaxnreg acts on whole warpgroups): the
-// block is launched with LAUNCH_REGS per thread; warpgroup 0 (the TMA and MMA
-// roles) drops to ROLE_REGS and the two epilogue warpgroups (128 running sums
-// per thread) rise to EPI_REGS. The sum must not exceed the launch allocation
-// (checked at compile time below, and against the built kernel's register
-// count before the first launch).
-constexpr int LAUNCH_REGS = 168;
-constexpr int ROLE_REGS = 96;
-constexpr int EPI_REGS = 200;
-static_assert(NUM_ROLE_THREADS * ROLE_REGS + NUM_EPI_THREADS * EPI_REGS <=
-                  NUM_THREADS * LAUNCH_REGS,
-              "register split exceeds the launch allocation");
+constexpr int TMEM_COLS = 2 * BN;  // two 64-column fp32 accumulators
+constexpr int MAX_SEG_KB = 16;     // 16 x 64 = 1024 k per exact fp32 segment
+constexpr int COLS = BN / 2;       // columns per epilogue warp
+constexpr int OUT_WARP_BYTES = 32 * COLS * 2;
+
+// Weight operand source: 0 = fp16 image (TMA straight into the operand
+// tile); 8 / 4 = raw INT8 / packed INT4 codes, widened on chip.
+template <int BSRC>
+struct Src {
+    static constexpr bool kRaw = BSRC != 0;
+    static constexpr int kRawRowBytes = BSRC == 8 ? BK : BK / 2;  // one k-block of one row
+    static constexpr int kRawBytes = kRaw ? BN * kRawRowBytes : 0;
+    static constexpr int kStages = kRaw ? 7 : 8;
+    static constexpr int kFullTx = kRaw ? A_STAGE_BYTES : A_STAGE_BYTES + B_STAGE_BYTES;
+};
 
 struct __align__(8) Barriers {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];       // TMA of the activation (and image weight) tiles
+    uint64_t raw_full[MAX_STAGES];   // TMA of the raw weight tile
+    uint64_t conv_full[MAX_STAGES];  // converters wrote the fp16 weight tile
+    uint64_t empty[MAX_STAGES];      // the MMAs reading the stage completed
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
-    uint64_t epi_sync;  // reusable barrier of the 256 epilogue threads
 };
 
+template <int BSRC>
 struct SmemLayout {
+    static constexpr int STAGES = Src<BSRC>::kStages;
     static constexpr int a_off = 0;
     static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
-    static constexpr int scale_off = b_off + STAGES * B_STAGE_BYTES;  // float[2][BN]
-    static constexpr int bar_off = scale_off + 2 * BN * 4;
+    static constexpr int raw_off = b_off + STAGES * B_STAGE_BYTES;
+    static constexpr int out_off = raw_off + STAGES * Src<BSRC>::kRawBytes;
+    static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;  // per warp 2 x 32 floats
+    static constexpr int bar_off = scale_off + NUM_EPI_WARPS * 2 * COLS * 4;
     static constexpr int misc_off = bar_off + (int)sizeof(Barriers);  // tmem base, abort
     static constexpr int bytes = misc_off + 16;
     static constexpr int alloc_bytes = bytes + 1024;  // runtime 1024-byte alignment slack
+    static_assert(alloc_bytes <= 232448, "shared memory per block");
+    static_assert(out_off % 1024 == 0, "64-byte-swizzled staging alignment");
 };
 
 struct Params {
     int M, N, K;
-    int num_kb;     // k-blocks of 64
-    int seg_kb;     // k-blocks per segment
-    int num_seg;    // segments per tile
-    int G;          // columns of s_w (1 for per-channel)
+    int num_kb;   // k-blocks of 64
+    int seg_kb;   // k-blocks per segment
+    int num_seg;  // segments per tile
+    int G;        // columns of s_w (1 for per-channel)
     int tiles_m, tiles_n;
     const float* s_a;
     const float* s_w;
+    const float* s_wT;  // group-major copy of per-group s_w, or NULL
     void* out;
+    int tma_store;  // fp16 output written through tmap_y (N % 8 == 0)
     uint64_t timeout_ns;
     unsigned long long* status;
 };
@@ -99,7 +116,8 @@ enum : uint32_t {
     kSiteEpiAccFull = 0x104,
     kSiteDrain = 0x105,
     kSiteProducerDrain = 0x106,
-    kSiteEpiSync = 0x107,
+    kSiteConvRaw = 0x107,
+    kSiteMmaConv = 0x108,
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int& tn) {
@@ -107,26 +125,70 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int&
     tn = tile / tiles_m;
 }
 
-// Scale for epilogue thread `et` (0..255) in the given segment: s_w[n, g]
-// with n the et-th column of the tile; g = segment (per-group) or 0.
-__device__ __forceinline__ float load_seg_scale(const Params& p, int tn, int seg, int et) {
-    const int n = tn * BN + et;
-    if (n >= p.N || p.s_w == nullptr) return 0.0f;
-    const int g = (p.G == 1) ? 0 : seg;
-    return __ldg(p.s_w + (int64_t)n * p.G + g);
+// Widens one 16-byte piece of raw weight codes (INT8: 16 codes; packed INT4:
+// 32 codes) of operand row r, starting at 16-byte chunk c0 of the fp16 row
+// (8 codes per chunk), into the 128-byte-swizzled K-major tile: chunk c of
+// row r lives at byte r * 128 + ((c ^ (r & 7)) << 4). Each code u-shifted to
+// [0, 256) becomes the fp16 1024 + u by placing u under the exponent byte
+// 0x64, and an exact fp16 subtraction removes the offset.
+template <int BSRC>
+__device__ __forceinline__ void widen_piece(const uint4 raw, uint8_t* tile, int r, int c0) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    constexpr int NH = (BSRC == 8) ? 8 : 16;  // fp16 pairs produced
+    uint32_t h[NH];
+    if constexpr (BSRC == 8) {
+        const __half2 bias = __float2half2_rn(1152.0f);  // 1024 + 128
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t u = w[i] ^ 0x80808080u;  // signed byte b -> b + 128
+            const uint32_t t0 = __byte_perm(u, 0x64646464u, 0x5140);  // codes 4i, 4i+1
+            const uint32_t t1 = __byte_perm(u, 0x64646464u, 0x7362);  // codes 4i+2, 4i+3
+            __half2 v0 = __hsub2(*reinterpret_cast<const __half2*>(&t0), bias);
+            __half2 v1 = __hsub2(*reinterpret_cast<const __half2*>(&t1), bias);
+            h[2 * i] = *reinterpret_cast<uint32_t*>(&v0);
+            h[2 * i + 1] = *reinterpret_cast<uint32_t*>(&v1);
+        }
+    } else {
+        // Nibble = code + 8; element 2j is the low nibble of byte j.
+        const __half2 bias = __float2half2_rn(1032.0f);  // 1024 + 8
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = w[i] & 0x0F0F0F0Fu;            // elements 8i, 8i+2, 8i+4, 8i+6
+            const uint32_t hi = (w[i] >> 4) & 0x0F0F0F0Fu;     // elements 8i+1, 8i+3, ...
+            const uint32_t e0 = __byte_perm(lo, hi, 0x5140);   // elements 8i .. 8i+3
+            const uint32_t e1 = __byte_perm(lo, hi, 0x7362);   // elements 8i+4 .. 8i+7
+            const uint32_t t[4] = {__byte_perm(e0, 0x64646464u, 0x5140),
+                                   __byte_perm(e0, 0x64646464u, 0x7362),
+                                   __byte_perm(e1, 0x64646464u, 0x5140),
+                                   __byte_perm(e1, 0x64646464u, 0x7362)};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t[j]), bias);
+                h[4 * i + j] = *reinterpret_cast<uint32_t*>(&v);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NH / 4; ++q)
+        *reinterpret_cast<uint4*>(tile + r * 128 + (((c0 + q) ^ (r & 7)) << 4)) =
+            make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
 }
 
-template <GemmMode MODE>
-__global__ void __maxnreg__(LAUNCH_REGS)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+template <GemmMode MODE, int BSRC>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc1_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_y, const Params p) {
+    using Layout = SmemLayout<BSRC>;
+    using S = Src<BSRC>;
+    constexpr int STAGES = Layout::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Barriers* bars = reinterpret_cast<Barriers*>(smem + SmemLayout::bar_off);
-    float* scales = reinterpret_cast<float*>(smem + SmemLayout::scale_off);
-    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
+    Barriers* bars = reinterpret_cast<Barriers*>(smem + Layout::bar_off);
+    float* scales = reinterpret_cast<float*>(smem + Layout::scale_off);
+    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + Layout::misc_off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Layout::misc_off + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -135,18 +197,20 @@ __global__ void __maxnreg__(LAUNCH_REGS)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->raw_full[s]), 1);
+            mbar_init(smem_u32(&bars->conv_full[s]), NUM_CONV_WARPS);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->acc_full[b]), 1);
-            mbar_init(smem_u32(&bars->acc_empty[b]), NUM_EPI_THREADS);
+            mbar_init(smem_u32(&bars->acc_empty[b]), NUM_EPI_WARPS);
         }
         mbar_init(smem_u32(&bars->drain), 1);
-        mbar_init(smem_u32(&bars->epi_sync), NUM_EPI_THREADS);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
+        if (p.tma_store) prefetch_tmap(&tmap_y);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_base_slot), TMEM_COLS);
@@ -160,25 +224,13 @@ __global__ void __maxnreg__(LAUNCH_REGS)
     // dependent launch); global memory is touched only after this wait.
     grid_dep_wait();
     grid_dep_launch();
-    // Scales of this CTA's first segment.
-    if (warp >= 4) {
-        if ((int)blockIdx.x < num_tiles) {
-            int tm, tn;
-            tile_coords(blockIdx.x, p.tiles_m, tm, tn);
-            scales[threadIdx.x - NUM_ROLE_THREADS] =
-                load_seg_scale(p, tn, 0, threadIdx.x - NUM_ROLE_THREADS);
-        }
-        named_bar_sync(1, NUM_EPI_THREADS);
-    }
 
-    if (warp < 4) {
-      setmaxnreg_dec<ROLE_REGS>();  // all of warpgroup 0
-      if (warp == 0) {
-        // ------------------------------ TMA producer ------------------------
+    if (warp == 0) {
+        // ------------------------------ TMA producer --------------------------
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_phase = 0;
+            int issued = 0;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 int tm, tn;
                 tile_coords(tile, p.tiles_m, tm, tn);
@@ -187,13 +239,19 @@ __global__ void __maxnreg__(LAUNCH_REGS)
                                            abort_flag, p.status, kSiteProducerEmpty))
                         goto producer_done;
                     const uint32_t fb = smem_u32(&bars->full[stage]);
-                    mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
-                    tma_load_2d(smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES), &tmap_a,
+                    mbar_arrive_expect_tx(fb, S::kFullTx);
+                    tma_load_2d(smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES), &tmap_a,
                                 fb, kb * BK, tm * BM);
-                    tma_load_2d(smem_u32(smem + SmemLayout::b_off + stage * B_STAGE_BYTES), &tmap_b,
-                                fb, kb * BK, tn * BN);
-                    issued_mask |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if constexpr (S::kRaw) {
+                        const uint32_t rb = smem_u32(&bars->raw_full[stage]);
+                        mbar_arrive_expect_tx(rb, S::kRawBytes);
+                        tma_load_2d(smem_u32(smem + Layout::raw_off + stage * S::kRawBytes),
+                                    &tmap_b, rb, kb * S::kRawRowBytes, tn * BN);
+                    } else {
+                        tma_load_2d(smem_u32(smem + Layout::b_off + stage * B_STAGE_BYTES),
+                                    &tmap_b, fb, kb * BK, tn * BN);
+                    }
+                    ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -202,16 +260,20 @@ __global__ void __maxnreg__(LAUNCH_REGS)
             }
         producer_done:
             if (*abort_flag) {
-                // Let every tile load already issued land before the CTA exits.
-                for (int s = 0; s < STAGES; ++s)
-                    if ((issued_mask & (1u << s)) &&
-                        !mbar_wait_drain(smem_u32(&bars->full[s]), (issued_phase >> s) & 1,
-                                         p.timeout_ns))
-                        report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
+                // Let every tile load already issued land before the CTA exits:
+                // the last use u of each stage completes phase u / STAGES.
+                for (int u = (issued > STAGES ? issued - STAGES : 0); u < issued; ++u) {
+                    const uint32_t par = (uint32_t)(u / STAGES) & 1u;
+                    bool ok = mbar_wait_drain(smem_u32(&bars->full[u % STAGES]), par, p.timeout_ns);
+                    if (S::kRaw)
+                        ok = mbar_wait_drain(smem_u32(&bars->raw_full[u % STAGES]), par,
+                                             p.timeout_ns) && ok;
+                    if (!ok) report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
+                }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------ MMA issuer --------------------------
+        // ------------------------------ MMA issuer ----------------------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32acc(BM, BN);
             int stage = 0;
@@ -233,11 +295,15 @@ __global__ void __maxnreg__(LAUNCH_REGS)
                         if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, p.timeout_ns,
                                                abort_flag, p.status, kSiteMmaFull))
                             goto mma_done;
+                        if (S::kRaw &&
+                            !mbar_wait_bounded(smem_u32(&bars->conv_full[stage]), phase,
+                                               p.timeout_ns, abort_flag, p.status, kSiteMmaConv))
+                            goto mma_done;
                         tc_fence_after();
                         const uint64_t adesc = smem_desc_sw128_kmajor(
-                            smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES));
+                            smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES));
                         const uint64_t bdesc = smem_desc_sw128_kmajor(
-                            smem_u32(smem + SmemLayout::b_off + stage * B_STAGE_BYTES));
+                            smem_u32(smem + Layout::b_off + stage * B_STAGE_BYTES));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
                             // +32 bytes along K per 16-element step (encoded >> 4).
@@ -262,158 +328,263 @@ __global__ void __maxnreg__(LAUNCH_REGS)
                     report_device_error(p.status, kDevTimeout, kSiteDrain);
             }
         }
-      }
+    } else if (warp < 4) {
+        // ------------------------- weight converters --------------------------
+        // A stage's raw tile is BN rows of kRawRowBytes, i.e. PPR 16-byte
+        // pieces per row; piece pc covers row pc / PPR, fp16 chunks from
+        // (pc % PPR) * CPP.
+        if constexpr (S::kRaw) {
+            constexpr int PPR = S::kRawRowBytes / 16;
+            constexpr int CPP = 8 / PPR;
+            constexpr int PER_THREAD = BN * PPR / (32 * NUM_CONV_WARPS);
+            const int ct = (warp - 2) * 32 + lane;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    {
+                        const bool ok = mbar_wait_bounded(smem_u32(&bars->raw_full[stage]), phase,
+                                                          p.timeout_ns, abort_flag, p.status,
+                                                          kSiteConvRaw);
+                        if (!__all_sync(0xffffffffu, ok)) goto conv_done;
+                    }
+                    const uint4* raw =
+                        reinterpret_cast<const uint4*>(smem + Layout::raw_off + stage * S::kRawBytes);
+                    uint8_t* tile_b = smem + Layout::b_off + stage * B_STAGE_BYTES;
+                    uint4 pcs[PER_THREAD];
+#pragma unroll
+                    for (int i = 0; i < PER_THREAD; ++i) pcs[i] = raw[ct + i * 32 * NUM_CONV_WARPS];
+#pragma unroll
+                    for (int i = 0; i < PER_THREAD; ++i) {
+                        const int pc = ct + i * 32 * NUM_CONV_WARPS;
+                        widen_piece<BSRC>(pcs[i], tile_b, pc / PPR, (pc % PPR) * CPP);
+                    }
+                    // Make the generic-proxy writes visible to the tensor core.
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars->conv_full[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        conv_done:;
+        }
     } else {
-        setmaxnreg_inc<EPI_REGS>();  // all of warpgroups 1 and 2
-        // ------------------------------ epilogue ----------------------------
-        const int ewarp = warp - 4;                  // 0..7
-        const int quad = warp & 3;                   // TMEM lane quadrant this warp may access
-        const int half = ewarp >> 2;                 // column half: 0 -> [0,128), 1 -> [128,256)
-        const int et = threadIdx.x - NUM_ROLE_THREADS;  // 0..255
-        const int row_in_tile = quad * 32 + lane;
+        // ------------------------------ epilogue ------------------------------
+        // Warp w (4..11) owns TMEM lanes 32 * (w % 4) .. +31 (its 32 token
+        // rows; a warp may only access its own lane quadrant) and the 32
+        // columns [32 * half, 32 * half + 32) of the 64-column tile.
+        const int ewarp = warp - 4;
+        const int quad = warp & 3;
+        const int half = ewarp >> 2;
+        uint8_t* stage_out = smem + Layout::out_off + ewarp * OUT_WARP_BYTES;
+        const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-byte swizzle of row `lane`
+        // This warp's 32 weight scales per segment that needs them, double
+        // buffered: lane l copies column l with cp.async one segment ahead.
+        float* wsc = scales + ewarp * 2 * COLS;
+        uint32_t sbuf = 0;
+        auto fetch_scales = [&](int tile, int seg, uint32_t buf) {
+            int tm, tn;
+            tile_coords(tile, p.tiles_m, tm, tn);
+            const int n = tn * BN + half * COLS + lane;
+            const int g = (p.G == 1) ? 0 : seg;
+            float* dst = wsc + buf * COLS + lane;
+            if (p.s_w != nullptr && n < p.N) {
+                const float* src = (p.s_wT != nullptr) ? p.s_wT + (int64_t)g * p.N + n
+                                                       : p.s_w + (int64_t)n * p.G + g;
+                cp_async_4(smem_u32(dst), src);
+            } else {
+                *dst = 0.0f;
+            }
+            cp_async_commit();
+        };
+        auto scales_ready = [&]() {
+            cp_async_wait_all();
+            __syncwarp();
+        };
+        constexpr bool kPerSegScales = (MODE == GemmMode::kPgF16);
+        if ((int)blockIdx.x < num_tiles) {
+            fetch_scales(blockIdx.x, kPerSegScales ? 0 : p.num_seg - 1, 0);
+            scales_ready();
+        }
         uint32_t seg_count = 0;
-        uint32_t epi_phase = 0;
-        uint32_t acc[128];  // int32 running sum (per-channel) or fp32 running sum (per-group)
+        bool store_pending = false;
+        uint32_t acc[COLS];  // int32 running sum (per-channel) or fp32 running sum (per-group)
 
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int tm, tn;
             tile_coords(tile, p.tiles_m, tm, tn);
-            const int m = tm * BM + row_in_tile;
-            const int n_half = tn * BN + half * 128;
-
+            const int m_base = tm * BM + quad * 32;
+            const int m = m_base + lane;
+            const int n_w = tn * BN + half * COLS;
+            if constexpr (MODE == GemmMode::kPgF16) {
+#pragma unroll
+                for (int j = 0; j < COLS; ++j) acc[j] = 0u;  // f = +0 before the first group
+            }
             for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
                 const uint32_t b = seg_count & 1;
                 const uint32_t acc_phase = (seg_count >> 1) & 1;
-                const float* sc = scales + (seg_count & 1) * BN + half * 128;
-
-                // Prefetch the next segment's scale into a register.
-                float next_scale = 0.0f;
-                {
+                const bool last_seg = (seg == p.num_seg - 1);
+                const bool uses_scales = kPerSegScales || last_seg;
+                const float* sc = wsc + sbuf * COLS;
+                if (uses_scales) {
+                    // Prefetch the scales of the next segment that uses them.
                     int nt = tile, ns = seg + 1;
                     if (ns == p.num_seg) {
                         ns = 0;
                         nt += gridDim.x;
                     }
-                    if (nt < num_tiles) {
-                        int ntm, ntn;
-                        tile_coords(nt, p.tiles_m, ntm, ntn);
-                        next_scale = load_seg_scale(p, ntn, ns, et);
-                    }
+                    if (!kPerSegScales) ns = p.num_seg - 1;
+                    if (nt < num_tiles) fetch_scales(nt, ns, sbuf ^ 1);
                 }
-
                 {
-                    // Every lane waits; the warp leaves together if any lane gave up,
-                    // so the warp-wide tcgen05.ld below is always issued by all lanes.
+                    // Every lane waits; the warp leaves together if any lane gave
+                    // up, so the warp-wide tcgen05.ld is always issued by all lanes.
                     const bool ok = mbar_wait_bounded(smem_u32(&bars->acc_full[b]), acc_phase,
                                                       p.timeout_ns, abort_flag, p.status,
                                                       kSiteEpiAccFull);
                     if (!__all_sync(0xffffffffu, ok)) goto epi_done;
                 }
                 tc_fence_after();
-
-                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                       b * BN + half * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {  // 8 chunks of 16 columns
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(t_row + c * 16, v);
-                    tmem_wait_ld();
+                {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32_ptr(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                               b * BN + half * COLS,
+                                           v);
+                    tmem_wait_ld_32(v);
                     if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
+                        // Exact fp32 integers -> int32 (the short conversion is exact
+                        // below 2^22; the warp takes the long one if any lane needs it).
+                        bool big = false;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int part = __float2int_rn(__uint_as_float(v[j]));
-                            acc[c * 16 + j] = (seg == 0) ? (uint32_t)part
-                                                         : (uint32_t)((int)acc[c * 16 + j] + part);
+                        for (int j = 0; j < 32; ++j) big |= fabsf(__uint_as_float(v[j])) >= 4194304.0f;
+                        if (__any_sync(0xffffffffu, big)) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int part = __float2int_rn(__uint_as_float(v[j]));
+                                acc[j] = (seg == 0) ? (uint32_t)part : (uint32_t)((int)acc[j] + part);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int part = small_float_to_int(__uint_as_float(v[j]));
+                                acc[j] = (seg == 0) ? (uint32_t)part : (uint32_t)((int)acc[j] + part);
+                            }
                         }
                     } else if constexpr (MODE == GemmMode::kPgF16) {
+                        // f = f + fl(P_g * s_g): scalar products (a packed product
+                        // whose only use is a packed add is fused), packed adds.
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 s4 = *reinterpret_cast<const float4*>(sc + c * 16 + j);
-                            const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float prev =
-                                    (seg == 0) ? 0.0f : __uint_as_float(acc[c * 16 + j + i]);
-                                const float prod = __fmul_rn(__uint_as_float(v[j + i]), ss[i]);
-                                acc[c * 16 + j + i] = __float_as_uint(__fadd_rn(prev, prod));
-                            }
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 s4 = *reinterpret_cast<const float4*>(sc + j);
+                            const float q0 = __fmul_rn(__uint_as_float(v[j]), s4.x);
+                            const float q1 = __fmul_rn(__uint_as_float(v[j + 1]), s4.y);
+                            const float q2 = __fmul_rn(__uint_as_float(v[j + 2]), s4.z);
+                            const float q3 = __fmul_rn(__uint_as_float(v[j + 3]), s4.w);
+                            float r0, r1, r2, r3;
+                            fadd2_rn(r0, r1, __uint_as_float(acc[j]), __uint_as_float(acc[j + 1]),
+                                     q0, q1);
+                            fadd2_rn(r2, r3, __uint_as_float(acc[j + 2]),
+                                     __uint_as_float(acc[j + 3]), q2, q3);
+                            acc[j] = __float_as_uint(r0);
+                            acc[j + 1] = __float_as_uint(r1);
+                            acc[j + 2] = __float_as_uint(r2);
+                            acc[j + 3] = __float_as_uint(r3);
                         }
-                    } else {  // kRawPgS32: write this group's partials directly
+                    } else {  // kRawPgS32: this group's partials, written directly
                         if (m < p.M) {
-                            int32_t* out = static_cast<int32_t*>(p.out);
+                            int32_t* out = static_cast<int32_t*>(p.out) +
+                                           ((int64_t)m * p.N + n_w) * p.G + seg;
+                            const int valid = min(32, p.N - n_w);
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int n = n_half + c * 16 + j;
-                                if (n < p.N)
-                                    out[((int64_t)m * p.N + n) * p.G + seg] =
-                                        __float2int_rn(__uint_as_float(v[j]));
-                            }
+                            for (int j = 0; j < 32; ++j)
+                                if (j < valid)
+                                    out[(int64_t)j * p.G] = __float2int_rn(__uint_as_float(v[j]));
                         }
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(smem_u32(&bars->acc_empty[b]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[b]));
 
-                // Final segment of the tile: dequantize and store.
-                if (seg == p.num_seg - 1 && m < p.M &&
-                    (MODE == GemmMode::kPcF16 || MODE == GemmMode::kPgF16 ||
-                     MODE == GemmMode::kRawS32)) {
-                    const float sa = (MODE == GemmMode::kRawS32) ? 0.0f : __ldg(p.s_a + m);
-                    const bool vec_ok = ((p.N & 7) == 0);
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {  // 16 groups of 8 columns
-                        const int n0 = n_half + c * 8;
-                        if (n0 >= p.N) break;
-                        if constexpr (MODE == GemmMode::kRawS32) {
+                if (last_seg) {
+                    if constexpr (MODE == GemmMode::kRawS32) {
+                        if (m < p.M) {
                             int32_t* out = static_cast<int32_t*>(p.out) + (int64_t)m * p.N;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                if (n0 + j < p.N) out[n0 + j] = (int)acc[c * 8 + j];
-                        } else {
-                            uint32_t h2[4];
+                            for (int j = 0; j < 32; ++j)
+                                if (n_w + j < p.N) out[n_w + j] = (int)acc[j];
+                        }
+                    } else if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kPgF16) {
+                        const float sa = (m < p.M) ? __ldg(p.s_a + m) : 0.0f;
+                        bool big = false;
+                        if constexpr (MODE == GemmMode::kPcF16) {
 #pragma unroll
-                            for (int j = 0; j < 8; j += 2) {
-                                float y0, y1;
-                                if constexpr (MODE == GemmMode::kPcF16) {
-                                    y0 = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[c * 8 + j]), sa),
-                                                   sc[c * 8 + j]);
-                                    y1 = __fmul_rn(
-                                        __fmul_rn(__int2float_rn((int)acc[c * 8 + j + 1]), sa),
-                                        sc[c * 8 + j + 1]);
-                                } else {
-                                    y0 = __fmul_rn(__uint_as_float(acc[c * 8 + j]), sa);
-                                    y1 = __fmul_rn(__uint_as_float(acc[c * 8 + j + 1]), sa);
-                                }
-                                const __half2 hv = __floats2half2_rn(y0, y1);
-                                h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                            for (int j = 0; j < 32; ++j) {
+                                const int a = (int)acc[j];
+                                big |= (a >= 4194304 || a <= -4194304);
                             }
-                            __half* out = static_cast<__half*>(p.out) + (int64_t)m * p.N + n0;
-                            if (vec_ok && n0 + 8 <= p.N) {
-                                *reinterpret_cast<uint4*>(out) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                        }
+                        const bool slow_cvt = __any_sync(0xffffffffu, big);
+                        uint32_t h2[16];
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            float y0, y1;
+                            if constexpr (MODE == GemmMode::kPcF16) {
+                                const float f0 = slow_cvt ? __int2float_rn((int)acc[j])
+                                                          : small_int_to_float((int)acc[j]);
+                                const float f1 = slow_cvt ? __int2float_rn((int)acc[j + 1])
+                                                          : small_int_to_float((int)acc[j + 1]);
+                                const float2 s2 = *reinterpret_cast<const float2*>(sc + j);
+                                float t0, t1;
+                                fmul2_rn(t0, t1, f0, f1, sa, sa);
+                                fmul2_rn(y0, y1, t0, t1, s2.x, s2.y);
                             } else {
-                                const __half* hh = reinterpret_cast<const __half*>(h2);
-#pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    if (n0 + j < p.N) out[j] = hh[j];
+                                fmul2_rn(y0, y1, __uint_as_float(acc[j]),
+                                         __uint_as_float(acc[j + 1]), sa, sa);
                             }
+                            const __half2 hv = __floats2half2_rn(y0, y1);
+                            h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                        }
+                        if (p.tma_store) {
+                            if (m_base < p.M && n_w < p.N) {  // warp-uniform
+                                if (store_pending && lane == 0) bulk_wait_group_read0();
+                                __syncwarp();
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    *reinterpret_cast<uint4*>(stage_out + lane * 64 +
+                                                              ((q ^ swz) << 4)) =
+                                        make_uint4(h2[4 * q], h2[4 * q + 1], h2[4 * q + 2],
+                                                   h2[4 * q + 3]);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&tmap_y, smem_u32(stage_out), n_w, m_base);
+                                    bulk_commit_group();
+                                }
+                                store_pending = true;
+                            }
+                        } else if (m < p.M) {
+                            __half* out = static_cast<__half*>(p.out) + (int64_t)m * p.N;
+                            const __half* hh = reinterpret_cast<const __half*>(h2);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (n_w + j < p.N) out[n_w + j] = hh[j];
                         }
                     }
                 }
-
-                // Publish the next segment's scales (all epilogue threads are
-                // done with the buffer being overwritten after this barrier).
-                scales[((seg_count + 1) & 1) * BN + et] = next_scale;
-                mbar_arrive(smem_u32(&bars->epi_sync));
-                {
-                    const bool ok = mbar_wait_bounded(smem_u32(&bars->epi_sync), epi_phase,
-                                                      p.timeout_ns, abort_flag, p.status,
-                                                      kSiteEpiSync);
-                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
-                    epi_phase ^= 1;
+                if (uses_scales) {
+                    scales_ready();
+                    sbuf ^= 1;
                 }
             }
         }
-    epi_done:;
+    epi_done:
+        cp_async_wait_all();
+        if (store_pending && lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -425,7 +596,7 @@ __global__ void __maxnreg__(LAUNCH_REGS)
     }
 }
 
-}  // namespace gemm
+}  // namespace gemm1
 
 namespace {
 
@@ -447,62 +618,101 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-template <GemmMode MODE>
-cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p,
-                        int grid, cudaStream_t stream) {
-    auto kern = gemm::gemm_tc_kernel<MODE>;
+// Row-major 2D tile map: `rows` x `cols` elements of `elem_bytes`, boxes of
+// box_rows x box_cols, rows beyond the extent read as zero.
+CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                   const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * elem_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t elem_strides[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <GemmMode MODE, int BSRC>
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
+                        const gemm1::Params& p, int grid, cudaStream_t stream) {
+    using Layout = gemm1::SmemLayout<BSRC>;
+    auto kern = gemm1::gemm_tc1_kernel<MODE, BSRC>;
     static bool attr_set = false;  // benign race: setting the same value twice
     if (!attr_set) {
-        // The in-kernel register split assumes exactly LAUNCH_REGS per thread at
-        // launch; refuse to launch a build that differs (it could not rebalance).
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs != gemm::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 gemm::SmemLayout::alloc_bytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Layout::alloc_bytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_pdl(kern, grid, gemm::NUM_THREADS, gemm::SmemLayout::alloc_bytes, stream, ta, tb, p);
+    return launch_pdl(kern, grid, gemm1::NUM_THREADS, Layout::alloc_bytes, stream, ta, tb, ty, p);
+}
+
+template <int BSRC>
+cudaError_t launch_src(GemmMode mode, const CUtensorMap& ta, const CUtensorMap& tb,
+                       const CUtensorMap& ty, const gemm1::Params& p, int grid,
+                       cudaStream_t stream) {
+    switch (mode) {
+        case GemmMode::kPcF16:
+            return launch_mode<GemmMode::kPcF16, BSRC>(ta, tb, ty, p, grid, stream);
+        case GemmMode::kPgF16:
+            return launch_mode<GemmMode::kPgF16, BSRC>(ta, tb, ty, p, grid, stream);
+        case GemmMode::kRawS32:
+            return launch_mode<GemmMode::kRawS32, BSRC>(ta, tb, ty, p, grid, stream);
+        case GemmMode::kRawPgS32:
+            return launch_mode<GemmMode::kRawPgS32, BSRC>(ta, tb, ty, p, grid, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 CUresult encode_tmap_f16_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                                 uint32_t box_rows, uint32_t box_cols) {
-    EncodeTiledFn fn = get_encode_fn();
-    if (!fn) return CUDA_ERROR_NOT_FOUND;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t elem_strides[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, rows, cols, box_rows,
+                     box_cols, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 CUresult encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                             uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle) {
-    EncodeTiledFn fn = get_encode_fn();
-    if (!fn) return CUDA_ERROR_NOT_FOUND;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t elem_strides[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, rows, cols, box_rows,
+                     box_cols, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+}
+
+CUresult encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t box_cols) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, box_rows, box_cols,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) {
-    using namespace gemm;
+    using namespace gemm1;
     if (a.M <= 0 || a.N <= 0 || a.K <= 0 || a.K % 16 != 0) return cudaErrorInvalidValue;
     if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2)
         return cudaErrorInvalidValue;
-    CUtensorMap ta, tb;
-    if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS ||
-        encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN, BK) != CUDA_SUCCESS)
+    const int bsrc = a.b_raw ? a.b_bits : 0;
+    if (bsrc != 0 && bsrc != 8 && bsrc != 4) return cudaErrorInvalidValue;
+    if (bsrc == 0 && !a.b_img) return cudaErrorInvalidValue;
+    if (bsrc == 4 && a.K % 32 != 0) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb, ty;
+    if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    CUresult rb;
+    if (bsrc == 0) {
+        rb = encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN, BK);
+    } else {
+        // Raw codes: row n holds K bytes (INT8) or K / 2 bytes (packed INT4);
+        // a box is one k-block of BN rows, unswizzled.
+        const uint64_t row_bytes = (bsrc == 8) ? (uint64_t)a.K : (uint64_t)a.K / 2;
+        rb = encode_tmap_u8_2d(&tb, a.b_raw, a.N, row_bytes, BN, bsrc == 8 ? BK : BK / 2);
+    }
+    if (rb != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const bool f16_out = (a.mode == GemmMode::kPcF16 || a.mode == GemmMode::kPgF16);
+    const bool tma_store =
+        f16_out && (a.N % 8 == 0) && (reinterpret_cast<uintptr_t>(a.out) % 16 == 0);
+    memset(&ty, 0, sizeof(ty));
+    if (tma_store &&
+        encode_tmap_f16_2d(&ty, a.out, a.M, a.N, 32, COLS, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     Params p{};
     p.M = (int)a.M;
@@ -525,18 +735,16 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     p.tiles_n = (p.N + BN - 1) / BN;
     p.s_a = a.s_a;
     p.s_w = a.s_w;
+    p.s_wT = per_group ? a.s_wT : nullptr;
     p.out = a.out;
+    p.tma_store = tma_store ? 1 : 0;
     p.timeout_ns = a.timeout_ns;
     p.status = a.status;
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    switch (a.mode) {
-        case GemmMode::kPcF16: return launch_mode<GemmMode::kPcF16>(ta, tb, p, grid, stream);
-        case GemmMode::kPgF16: return launch_mode<GemmMode::kPgF16>(ta, tb, p, grid, stream);
-        case GemmMode::kRawS32: return launch_mode<GemmMode::kRawS32>(ta, tb, p, grid, stream);
-        case GemmMode::kRawPgS32: return launch_mode<GemmMode::kRawPgS32>(ta, tb, p, grid, stream);
-    }
-    return cudaErrorInvalidValue;
+    if (bsrc == 8) return launch_src<8>(a.mode, ta, tb, ty, p, grid, stream);
+    if (bsrc == 4) return launch_src<4>(a.mode, ta, tb, ty, p, grid, stream);
+    return launch_src<0>(a.mode, ta, tb, ty, p, grid, stream);
 }
 
 }  // namespace cider

@@ -631,15 +631,26 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+namespace {
+int engine_override() {
     static const int engine = [] {
         const char* e = getenv("CIDER_GEMM_ENGINE");
         if (e && strcmp(e, "single") == 0) return 1;
         if (e && strcmp(e, "pair") == 0) return 2;
         return 0;
     }();
-    const bool pair = engine == 2 || (engine == 0 && a.M > gemm2::BM);
-    return pair ? launch_gemm_tc_pair(a, num_sms, stream) : launch_gemm_tc(a, num_sms, stream);
+    return engine;
+}
+}  // namespace
+
+bool gemm_uses_pair(int64_t M) {
+    const int engine = engine_override();
+    return engine == 2 || (engine == 0 && M > gemm2::BM);
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+    if (gemm_uses_pair(a.M) && a.b_img) return launch_gemm_tc_pair(a, num_sms, stream);
+    return launch_gemm_tc(a, num_sms, stream);
 }
 
 }  // namespace cider

@@ -42,9 +42,10 @@ cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int6
 
 // Both operand images of the tensor-core GEMM in one launch: x fp16 [M,K] ->
 // a_img (exact fp16 codes) + s_a, and weights (INT8 [N,K] or packed INT4
-// [N,K/2]) -> b_img (exact fp16 integers); with s_wT non-NULL also the
-// group-major copy s_wT [G,N] of per-group scales s_w [N,G]. Falls back to
-// separate launches for shapes the fused kernel does not take.
+// [N,K/2]) -> b_img (exact fp16 integers; skipped when w is NULL); with s_wT
+// non-NULL also the group-major copy s_wT [G,N] of per-group scales s_w
+// [N,G]. Falls back to separate launches for shapes the fused kernel does
+// not take.
 cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const void* w, int bits,
                                   int64_t N, __half* a_img, float* s_a, __half* b_img,
                                   const float* s_w, float* s_wT, int64_t G, int num_sms,
@@ -76,6 +77,10 @@ struct GemmArgs {
     GemmMode mode;
     uint64_t timeout_ns;
     unsigned long long* status;  // device status word
+    // Raw weight codes instead of b_img (single-SM engine only): INT8 [N, K]
+    // (b_bits 8) or packed INT4 [N, K/2] (b_bits 4), widened on chip.
+    const void* b_raw;
+    int b_bits;
 };
 
 cudaError_t launch_gemm_tc(const GemmArgs& args, int num_sms, cudaStream_t stream);
@@ -84,6 +89,9 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& args, int num_sms, cudaStream_t 
 // Picks the engine for the problem: SM pairs for M > 128, single SMs otherwise
 // (CIDER_GEMM_ENGINE=single|pair in the environment overrides).
 cudaError_t launch_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
+// The engine launch_gemm takes for M tokens: true = SM pairs (needs b_img),
+// false = single SMs (takes raw weight codes).
+bool gemm_uses_pair(int64_t M);
 
 // ---- M = 1 GEMV (quantizes x per CTA, int32 dot products, same epilogue) ----
 struct GemvArgs {
@@ -109,6 +117,10 @@ cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t stream);
 // Host-side encoder for a 2D fp16 row-major tile map (any swizzle mode).
 CUresult encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                             uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle);
+
+// Host-side encoder for a 2D byte tile map (unswizzled).
+CUresult encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t box_cols);
 
 // Host-side encoder for a 2D fp16 K-major tile map with 128-byte swizzle.
 CUresult encode_tmap_f16_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

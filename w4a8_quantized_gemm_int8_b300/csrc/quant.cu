@@ -448,7 +448,8 @@ namespace {
 template <int BITS>
 cudaError_t launch_images_t(const ImagesArgs& a0, int64_t nvec, int num_sms, cudaStream_t stream) {
     ImagesArgs a = a0;
-    const int64_t b_blocks = std::min<int64_t>((a.n16 + 256 * 4 - 1) / (256 * 4), (int64_t)num_sms * 4);
+    int64_t b_blocks = std::min<int64_t>((a.n16 + 256 * 4 - 1) / (256 * 4), (int64_t)num_sms * 4);
+    if (b_blocks == 0 && a.s_wT) b_blocks = std::min<int64_t>(grid_for(a.N * a.G, 256, num_sms), num_sms);
     auto go = [&](auto kern, int64_t a_blocks) {
         a.a_blocks = (int)a_blocks;
         return launch_pdl(kern, (unsigned)(a_blocks + b_blocks), 256, 0, stream, a);
@@ -481,20 +482,24 @@ cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const v
     const bool fused = (K % 8 == 0) && nvec <= 256 * 8 &&
                        (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                        (reinterpret_cast<uintptr_t>(a_img) % 16 == 0) &&
-                       ((N * K) % codes_per_chunk == 0);
+                       (w == nullptr || (N * K) % codes_per_chunk == 0);
     if (!fused) {
         cudaError_t e = launch_quant_groups(x, M, K, K, 127, QuantOut::kF16, a_img, s_a, num_sms,
                                             stream);
         if (e != cudaSuccess) return e;
-        e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, b_img, num_sms,
-                                          stream)
-                        : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, b_img, num_sms,
-                                          stream);
-        if (e != cudaSuccess || !s_wT) return e;
+        if (w != nullptr) {
+            e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, b_img,
+                                              num_sms, stream)
+                            : launch_widen_i4(static_cast<const uint8_t*>(w), N * K, b_img,
+                                              num_sms, stream);
+            if (e != cudaSuccess) return e;
+        }
+        if (!s_wT) return e;
         return launch_pdl(transpose_scales_kernel, grid_for(N * G, 256, num_sms), 256, 0, stream,
                           s_w, s_wT, N, G);
     }
-    ImagesArgs a{x, M, K, a_img, s_a, w, (N * K) / codes_per_chunk, b_img, 0, s_w, s_wT, N, G};
+    const int64_t n16 = (w == nullptr) ? 0 : (N * K) / codes_per_chunk;
+    ImagesArgs a{x, M, K, a_img, s_a, w, n16, b_img, 0, s_w, s_wT, N, G};
     return (bits == 8) ? launch_images_t<8>(a, nvec, num_sms, stream)
                        : launch_images_t<4>(a, nvec, num_sms, stream);
 }

@@ -75,10 +75,12 @@ extern "C" cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M,
     if (!aligned16(x_f16) || !aligned16(wq) || !aligned16(s_w) || !aligned16(y_f16))
         return CIDER_ERR_UNSUPPORTED;
     if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return CIDER_ERR_UNSUPPORTED;
-    // Layout inside the array: a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K] fp16.
+    // Layout inside the array: a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K]
+    // fp16 (only for the SM-pair engine; the single-SM engine reads wq itself).
+    const bool img = gemm_uses_pair(M);
     const size_t a_bytes = round256((size_t)M * K * 2);
     const size_t s_bytes = round256((size_t)M * 4);
-    const size_t b_bytes = round256((size_t)N * K * 2);
+    const size_t b_bytes = img ? round256((size_t)N * K * 2) : 0;
     if (a_bytes + s_bytes + b_bytes > kStaticScratchBytes) return CIDER_ERR_WORKSPACE;
 
     void* base = nullptr;
@@ -94,15 +96,18 @@ extern "C" cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M,
     uint8_t* p = static_cast<uint8_t*>(base);
     __half* a_img = reinterpret_cast<__half*>(p);
     float* s_a = reinterpret_cast<float*>(p + a_bytes);
-    __half* b_img = reinterpret_cast<__half*>(p + a_bytes + s_bytes);
+    __half* b_img = img ? reinterpret_cast<__half*>(p + a_bytes + s_bytes) : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    cudaError_t e = launch_operand_images(static_cast<const __half*>(x_f16), M, K, wq, 8, N,
-                                          a_img, s_a, b_img, nullptr, nullptr, 1, sms, s);
+    cudaError_t e = launch_operand_images(static_cast<const __half*>(x_f16), M, K,
+                                          img ? wq : nullptr, 8, N, a_img, s_a, b_img, nullptr,
+                                          nullptr, 1, sms, s);
     if (e == cudaSuccess) {
         GemmArgs a{};
         a.a_img = a_img;
         a.b_img = b_img;
+        a.b_raw = img ? nullptr : wq;
+        a.b_bits = 8;
         a.M = M;
         a.N = N;
         a.K = K;
