@@ -8,13 +8,17 @@
 //
 // B300 design: the op is a stream of N*K weight bytes (N*K/2 for INT4) from
 // HBM, so the kernel is built to keep as many bytes in flight as HBM needs.
-// One CTA per SM owns a contiguous slice of weight rows (row-major weights
-// make the slice one contiguous byte range). A producer warp issues bulk
+// Two CTAs per SM, each owning a contiguous slice of weight rows (row-major
+// weights make the slice one contiguous byte range). Weights and their scales
+// are never written by the kernel just before a GEMV, so the producer warp
+// starts ahead of the wait on that kernel (programmatic dependent launch):
+// it stages the per-channel scales of its rows, then issues bulk
 // asynchronous copies (cp.async.bulk, mbarrier completion) of whole groups of
-// rows into a ring of shared-memory stages at kernel start - for the decode
-// shapes the whole slice fits, so every weight byte is requested at once -
-// while eight consumer warps quantize x into shared memory. Consumers then
-// take rows from the landed stages: dp4a (4 x int8 -> int32) over 16-byte
+// rows into a ring of shared-memory stages - two at once, the rest as soon as
+// the consumers hold x (so x's load does not queue behind the copies); for
+// the decode shapes the whole slice fits the ring. Sixteen consumer warps
+// wait for the preceding kernel, quantize x into shared memory, then take
+// rows from the landed stages: dp4a (4 x int8 -> int32) over 16-byte
 // chunks, INT4 nibbles widened to signed bytes in registers. Per-group
 // scales travel in the same stage as their rows (when 16-byte aligned); the
 // per-group partials are rescaled and summed in ascending group order by one
@@ -35,6 +39,9 @@ constexpr int kMaxK = 16384;
 constexpr int kStageTarget = 16384;        // weight bytes per stage (at least one row)
 constexpr int kMaxStages = 32;
 constexpr int kUnroll = 4;          // 16-byte chunks per lane loaded before use
+constexpr int kXVec = kMaxK / 8 / kConsumers;  // 8-element x vectors per consumer thread
+static_assert(kMaxK % (8 * kConsumers) == 0, "x vectors per thread");
+constexpr int kEarlyStages = 2;  // copies issued before x is in registers
 
 struct Params {
     const __half* x;
@@ -59,6 +66,8 @@ enum : uint32_t {
     kSiteGemvProducerEmpty = 0x201,
     kSiteGemvConsumerFull = 0x202,
     kSiteGemvProducerDrain = 0x203,
+    kSiteGemvScales = 0x204,
+    kSiteGemvX = 0x205,
 };
 
 __device__ __forceinline__ int dp4a(int a, int b, int c) { return __dp4a(a, b, c); }
@@ -106,6 +115,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
     uint64_t* empty = full + kMaxStages;
     float* red_s = reinterpret_cast<float*>(empty + kMaxStages);  // [kConsumerWarps]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red_s + kConsumerWarps);
+    uint64_t* sw_bar = reinterpret_cast<uint64_t*>(red_s + kConsumerWarps) + 1;
+    uint64_t* x_bar = sw_bar + 1;
     uint8_t* stages = smem + p.stage_off;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -121,19 +132,33 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), kConsumerWarps);
         }
+        mbar_init(smem_u32(sw_bar), 1);
+        mbar_init(smem_u32(x_bar), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
+    float* sw_s = reinterpret_cast<float*>(smem + p.sw_off);
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
+        // Per-channel scales of the CTA's rows first: a small latency-bound
+        // load that must not queue behind the bulk copies.
+        if (!PG && p.sw_in_smem)
+            for (int i = lane; i < nrows; i += 32) sw_s[i] = __ldg(p.s_w + n0 + i);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sw_bar));
         if (lane == 0) {
             const uint8_t* src = p.w + (int64_t)n0 * p.row_bytes;
             const uint8_t* ssrc =
                 reinterpret_cast<const uint8_t*>(p.s_w) + (int64_t)n0 * p.G * 4;
             int issued = 0;
             for (int s = 0; s < nst; ++s) {
+                // Past the first kEarlyStages copies, wait until the consumers
+                // hold x: its load must not queue behind this CTA's bulk copies.
+                if (s == kEarlyStages && !mbar_wait_bounded(smem_u32(x_bar), 0, p.timeout_ns,
+                                                            abort_flag, p.status, kSiteGemvX))
+                    break;
                 const int slot = s % NS;
                 const uint32_t use = (uint32_t)(s / NS);
                 if (!mbar_wait_bounded(smem_u32(&empty[slot]), (use & 1u) ^ 1u, p.timeout_ns,
@@ -172,42 +197,52 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
     {
         const uint4* xv = reinterpret_cast<const uint4*>(p.x);
         const int nvec = p.K / 8;
-        __half2 hm = __float2half2_rn(0.0f);
-        for (int v = threadIdx.x; v < nvec; v += kConsumers) {
-            uint4 u = __ldg(xv + v);
-            const __half2* h = reinterpret_cast<const __half2*>(&u);
+        uint4 xr[kXVec];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) hm = __hmax2(hm, __habs2(h[i]));
+        for (int i = 0; i < kXVec; ++i) {
+            const int v = threadIdx.x + i * kConsumers;
+            xr[i] = (v < nvec) ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        __half2 hm = __float2half2_rn(0.0f);
+#pragma unroll
+        for (int i = 0; i < kXVec; ++i) {
+            const __half2* h = reinterpret_cast<const __half2*>(&xr[i]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) hm = __hmax2(hm, __habs2(h[j]));
         }
         float m = fmaxf(__low2float(hm), __high2float(hm));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) red_s[warp] = m;
         named_bar_sync(1, kConsumers);
+        if (threadIdx.x == 0) mbar_arrive(smem_u32(x_bar));  // x is in registers: copies may go on
         float a = red_s[0];
 #pragma unroll
         for (int w = 1; w < kConsumerWarps; ++w) a = fmaxf(a, red_s[w]);
         const float s = (a == 0.0f) ? 0.0f : __fdiv_rn(a, 127.0f);
         const float r = quant_recip(s);
-        for (int v = threadIdx.x; v < nvec; v += kConsumers) {
-            uint4 u = __ldg(xv + v);
-            const __half* h = reinterpret_cast<const __half*>(&u);
+#pragma unroll
+        for (int i = 0; i < kXVec; ++i) {
+            const int v = threadIdx.x + i * kConsumers;
+            if (v >= nvec) break;
+            const __half* h = reinterpret_cast<const __half*>(&xr[i]);
             uint32_t lo = 0, hi = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int q = quant_code(__half2float(h[i]), s, r, 127);
-                if (i < 4)
-                    lo |= (uint32_t)(q & 0xFF) << (8 * i);
+            for (int j = 0; j < 8; ++j) {
+                const int q = quant_code(__half2float(h[j]), s, r, 127);
+                if (j < 4)
+                    lo |= (uint32_t)(q & 0xFF) << (8 * j);
                 else
-                    hi |= (uint32_t)(q & 0xFF) << (8 * (i - 4));
+                    hi |= (uint32_t)(q & 0xFF) << (8 * (j - 4));
             }
             reinterpret_cast<uint2*>(codes_s)[v] = make_uint2(lo, hi);
         }
-        // Per-channel scales of this CTA's rows, into shared memory.
-        float* sw_s = reinterpret_cast<float*>(smem + p.sw_off);
-        if (!PG && p.sw_in_smem)
-            for (int i = threadIdx.x; i < nrows; i += kConsumers) sw_s[i] = __ldg(p.s_w + n0 + i);
         named_bar_sync(1, kConsumers);
+        if (!PG && p.sw_in_smem) {
+            const bool ok = mbar_wait_bounded(smem_u32(sw_bar), 0, p.timeout_ns, abort_flag,
+                                              p.status, kSiteGemvScales);
+            if (!__all_sync(0xffffffffu, ok)) return;
+        }
         const float s_a = s;  // every consumer thread holds the token scale
 
         // ------------------------------ weight rows ---------------------------
@@ -361,7 +396,7 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     p.sw_in_smem = !pg && max_rows <= 8192;
     const int sw_bytes = p.sw_in_smem ? ((max_rows * 4 + 127) & ~127) : 0;
     p.bar_off = p.sw_off + sw_bytes;
-    const int bar_bytes = 2 * kMaxStages * 8 + kConsumerWarps * 4 + 16;
+    const int bar_bytes = 2 * kMaxStages * 8 + kConsumerWarps * 4 + 32;  // + abort flag, 2 barriers
     p.stage_off = (p.bar_off + bar_bytes + 127) & ~127;
     const int budget = (g_max_smem / 2 - 1024) - p.stage_off;
     int ns = budget / p.stage_bytes;
