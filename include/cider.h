@@ -131,7 +131,9 @@ CIDER_API cider_status cider_w8a8_gemm_pc(const void* x_f16, int64_t M, int64_t 
  * group's int32 partial is rescaled and summed in ascending group order, the
  * token scale applied last. README "W8A8 Quantization Granularity" (one
  * scale per 64 / 128 elements), "Quantization" table.
- * group_size: a multiple of 64 dividing K (64 and 128 are the pages' sizes).
+ * group_size: a multiple of 64 dividing K, at most 1024 for M > 1 (a group's
+ * partial must stay exact in the tensor core's fp32 accumulator); 64 and 128
+ * are the pages' sizes. Larger groups give CIDER_ERR_UNSUPPORTED.
  */
 CIDER_API cider_status cider_w8a8_gemm_pg(const void* x_f16, int64_t M, int64_t N, int64_t K,
                                 const int8_t* wq, const float* s_w, int32_t group_size,
@@ -142,7 +144,8 @@ CIDER_API cider_status cider_w8a8_gemm_pg(const void* x_f16, int64_t M, int64_t 
  * cider_pack_weight_int4) are unpacked to INT8 codes before the product
  * (README "Modes", W4A8 compute path "Unpack -> TensorOps"), then the
  * per-channel (group_size 0, s_w [N]) or per-group (s_w [N, K/gs]) layer.
- * K % 32 == 0; group_size 0 or a multiple of 64 dividing K.
+ * K % 32 == 0; group_size 0 or a multiple of 64 dividing K (at most 1024
+ * for M > 1).
  */
 CIDER_API cider_status cider_w4a8_gemm(const void* x_f16, int64_t M, int64_t N, int64_t K,
                              const uint8_t* wp, const float* s_w, int32_t group_size, void* y_f16,
@@ -205,7 +208,7 @@ CIDER_API cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M, 
  * cider_gemm_images: the tensor-core GEMM with the fused dequant epilogue on
  *   the two images: y [M,N] fp16 from a_img [M,K], s_a [M], b_img [N,K] and
  *   s_w ([N] for group_size 0, else [N, K/gs], gs a multiple of 64 dividing
- *   K). K % 16 == 0; any M >= 1 (no GEMV routing).
+ *   K, at most 1024). K % 16 == 0; any M >= 1 (no GEMV routing).
  */
 CIDER_API cider_status cider_act_image(const void* x_f16, int64_t M, int64_t K, void* a_img,
                                        float* s_a, void* stream);

@@ -99,7 +99,9 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
                    static_cast<__half*>(y), kWaitTimeoutNs, status};
         return from_cuda(launch_gemv(g, sms, stream));
     }
-    if (!valid_group(gs, K, 64)) return CIDER_ERR_UNSUPPORTED;
+    // A group's partial sum must stay exact in the tensor core's fp32
+    // accumulator: at most 1024 products of magnitude <= 127^2.
+    if (!valid_group(gs, K, 64) || gs > 1024) return CIDER_ERR_UNSUPPORTED;
     const size_t need = workspace_bytes(M, N, K, gs);
     if (!ws || ws_bytes < need) return CIDER_ERR_WORKSPACE;
     if (!aligned16(ws)) return CIDER_ERR_UNSUPPORTED;
@@ -273,7 +275,8 @@ cider_status cider_gemm_images(const void* a_img, const float* s_a, const void* 
                                int32_t group_size, void* y_f16, void* stream) {
     if (!a_img || !s_a || !b_img || !s_w || !y_f16) return CIDER_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || group_size < 0) return CIDER_ERR_INVALID_ARG;
-    if (K % 16 != 0 || !valid_group(group_size, K, 64)) return CIDER_ERR_UNSUPPORTED;
+    if (K % 16 != 0 || !valid_group(group_size, K, 64) || group_size > 1024)
+        return CIDER_ERR_UNSUPPORTED;
     if (!aligned16(a_img) || !aligned16(b_img) || !aligned16(y_f16) || !aligned16(s_w))
         return CIDER_ERR_UNSUPPORTED;
     if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return CIDER_ERR_UNSUPPORTED;
@@ -304,7 +307,8 @@ cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int6
     if (!q || !w || !out) return CIDER_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || group_size < 0 || (bits != 8 && bits != 4))
         return CIDER_ERR_INVALID_ARG;
-    if (K % 32 != 0 || !valid_group(group_size, K, 64)) return CIDER_ERR_UNSUPPORTED;
+    if (K % 32 != 0 || !valid_group(group_size, K, 64) || group_size > 1024)
+        return CIDER_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(w) || !aligned16(out)) return CIDER_ERR_UNSUPPORTED;
     const int64_t Mw = M < 2 ? 2 : M;
     if (!ws || ws_bytes < workspace_bytes(Mw, N, K)) return CIDER_ERR_WORKSPACE;

@@ -13,21 +13,23 @@
 // product is an integer of magnitude <= 127^2 and every partial sum over at
 // most 1024 consecutive k an integer below 127^2 * 1024 < 2^24, exact in
 // fp32. K is cut into segments of at most 1024 (per-channel) or of one group
-// (per-group); each segment accumulates into one of two TMEM buffers, and the
-// epilogue folds it (exact fp32 integer -> int32 and add, or rescale and add
-// in fp32 in ascending group order) while the tensor core fills the other.
+// (per-group); each segment accumulates into one of eight TMEM buffers, and
+// the epilogue folds it (exact fp32 integer -> int32 and add, or rescale and
+// add in fp32 in ascending group order) while the tensor core fills the others.
 //
-// Shape for few tokens: one CTA per 128-token x 64-channel tile (160 tiles at
-// N = 10240), persistent over tiles. With few tokens the weights are nearly
-// all of the bytes, so they are read as their raw codes (INT8 [N,K] or packed
-// INT4 [N,K/2]) and widened to exact fp16 on chip: TMA stages the raw bytes
-// and two converter warps write the 128-byte-swizzled fp16 operand tile that
-// the tensor core reads; no weight image is written to memory. (An fp16
-// weight image is accepted too.) Warp 0 issues TMA, warp 1 owns TMEM and
-// issues MMAs (128 x 64 x 16), warps 2-3 convert, warps 4..11 are the
-// epilogue: each owns one TMEM lane quadrant and 32 of the 64 columns, reads
-// a whole segment with one 32-column TMEM load, and writes fp16 output
-// through 64-byte-swizzled staging and TMA stores. Every wait is bounded.
+// Shape for few tokens: one CTA per 128-token tile of 128 output channels
+// (per-channel; 80 tiles at N = 10240) or 64 (per-group), persistent over
+// tiles. With few tokens the weights are nearly all of the bytes, so they
+// are read as their raw codes (INT8 [N,K] or packed INT4 [N,K/2]) and
+// widened to exact fp16 on chip: TMA stages the raw bytes and two converter
+// warps write the 128-byte-swizzled fp16 operand tile that the tensor core
+// reads; no weight image is written to memory. (An fp16 weight image is
+// accepted too.) Warp 0 issues TMA, warp 1 owns TMEM and issues MMAs
+// (128 x BN x 16), warps 2-3 convert, warps 4..11 are the epilogue: each owns
+// one TMEM lane quadrant and half of the tile's columns, reads them 32 at a
+// time, and writes fp16 output through 64-byte-swizzled staging and TMA
+// stores. Weight scales are fetched by cp.async several segments ahead.
+// Every wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -40,30 +42,51 @@ namespace cider {
 namespace gemm1 {
 
 constexpr int BM = 128;
-constexpr int BN = 64;
 constexpr int BK = 64;
 constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int B_STAGE_BYTES = BN * BK * 2;
 constexpr int MAX_STAGES = 8;
 constexpr int NUM_CONV_WARPS = 2;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
 constexpr int NUM_ROLE_THREADS = 128;  // TMA warp, MMA warp, two converter warps
 constexpr int NUM_THREADS = NUM_ROLE_THREADS + NUM_EPI_THREADS;
-constexpr int TMEM_COLS = 2 * BN;  // two 64-column fp32 accumulators
-constexpr int MAX_SEG_KB = 16;     // 16 x 64 = 1024 k per exact fp32 segment
-constexpr int COLS = BN / 2;       // columns per epilogue warp
-constexpr int OUT_WARP_BYTES = 32 * COLS * 2;
+constexpr int TMEM_COLS = 512;    // all of TMEM: 512 / BN fp32 accumulators
+constexpr int MAX_ACC = 8;
+constexpr int MAX_SEG_KB = 16;    // 16 x 64 = 1024 k per exact fp32 segment
+constexpr int OUT_WARP_BYTES = 32 * 32 * 2;  // one 32 x 32 fp16 store box per warp
+constexpr int SMEM_LIMIT = 232448;           // opt-in shared memory per block
 
-// Weight operand source: 0 = fp16 image (TMA straight into the operand
-// tile); 8 / 4 = raw INT8 / packed INT4 codes, widened on chip.
-template <int BSRC>
-struct Src {
+// Per-instantiation shape. BSRC: weight operand source, 0 = fp16 image (TMA
+// straight into the operand tile), 8 / 4 = raw INT8 / packed INT4 codes
+// widened on chip. BN: tile width in output channels. An MMA of 128 rows
+// costs the same issue time for any N up to 128, so per-channel tiles are
+// 128 wide; per-group tiles stay 64 wide so that a short K (few tiles) still
+// spreads over the SMs and the per-group fold stays light.
+template <int BSRC, int BN>
+struct Cfg {
     static constexpr bool kRaw = BSRC != 0;
+    static constexpr int kCols = BN / 2;        // columns per epilogue warp
+    static constexpr int kChunks = kCols / 32;  // 32-column TMEM loads per warp and segment
+    // Per-group tiles hold kGroups groups' partials side by side in one TMEM
+    // buffer (one accumulator of BN columns per group), so the tensor core and
+    // the epilogue hand over once per kGroups groups, not once per group.
+    static constexpr int kGroups = (BN == 64) ? 4 : 1;
+    static constexpr int kBufCols = kGroups * BN;
+    static constexpr int kNumAcc = TMEM_COLS / kBufCols;
+    static constexpr int kScaleDepth = 2;  // scale sets (one per segment) in flight per warp
+    static constexpr int kBStageBytes = BN * BK * 2;
     static constexpr int kRawRowBytes = BSRC == 8 ? BK : BK / 2;  // one k-block of one row
     static constexpr int kRawBytes = kRaw ? BN * kRawRowBytes : 0;
-    static constexpr int kStages = kRaw ? 7 : 8;
-    static constexpr int kFullTx = kRaw ? A_STAGE_BYTES : A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int kFullTx = kRaw ? A_STAGE_BYTES : A_STAGE_BYTES + kBStageBytes;
+    static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes + kRawBytes;
+    static constexpr int kScaleFloats = kScaleDepth * kGroups * kCols;  // per epilogue warp
+    static constexpr int kFixedBytes = NUM_EPI_WARPS * OUT_WARP_BYTES +
+                                       NUM_EPI_WARPS * kScaleFloats * 4 + 512 + 16 + 1024;
+    static constexpr int kStages = (SMEM_LIMIT - kFixedBytes) / kStageBytes < MAX_STAGES
+                                       ? (SMEM_LIMIT - kFixedBytes) / kStageBytes
+                                       : MAX_STAGES;
+    static_assert(kNumAcc >= 2 && kNumAcc <= MAX_ACC && kChunks >= 1, "tile width");
+    static_assert(kStages >= 4, "pipeline depth");
 };
 
 struct __align__(8) Barriers {
@@ -71,24 +94,26 @@ struct __align__(8) Barriers {
     uint64_t raw_full[MAX_STAGES];   // TMA of the raw weight tile
     uint64_t conv_full[MAX_STAGES];  // converters wrote the fp16 weight tile
     uint64_t empty[MAX_STAGES];      // the MMAs reading the stage completed
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t acc_full[MAX_ACC];
+    uint64_t acc_empty[MAX_ACC];
     uint64_t drain;
 };
+static_assert(sizeof(Barriers) <= 512, "barrier area");
 
-template <int BSRC>
+template <int BSRC, int BN>
 struct SmemLayout {
-    static constexpr int STAGES = Src<BSRC>::kStages;
+    using C = Cfg<BSRC, BN>;
+    static constexpr int STAGES = C::kStages;
     static constexpr int a_off = 0;
     static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
-    static constexpr int raw_off = b_off + STAGES * B_STAGE_BYTES;
-    static constexpr int out_off = raw_off + STAGES * Src<BSRC>::kRawBytes;
-    static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;  // per warp 2 x 32 floats
-    static constexpr int bar_off = scale_off + NUM_EPI_WARPS * 2 * COLS * 4;
-    static constexpr int misc_off = bar_off + (int)sizeof(Barriers);  // tmem base, abort
+    static constexpr int raw_off = b_off + STAGES * C::kBStageBytes;
+    static constexpr int out_off = raw_off + STAGES * C::kRawBytes;
+    static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;
+    static constexpr int bar_off = scale_off + NUM_EPI_WARPS * C::kScaleFloats * 4;
+    static constexpr int misc_off = bar_off + 512;  // tmem base, abort
     static constexpr int bytes = misc_off + 16;
     static constexpr int alloc_bytes = bytes + 1024;  // runtime 1024-byte alignment slack
-    static_assert(alloc_bytes <= 232448, "shared memory per block");
+    static_assert(alloc_bytes <= SMEM_LIMIT, "shared memory per block");
     static_assert(out_off % 1024 == 0, "64-byte-swizzled staging alignment");
 };
 
@@ -97,6 +122,7 @@ struct Params {
     int num_kb;   // k-blocks of 64
     int seg_kb;   // k-blocks per segment
     int num_seg;  // segments per tile
+    int group_kb; // k-blocks per group (per-group; = seg_kb for per-channel)
     int G;        // columns of s_w (1 for per-channel)
     int tiles_m, tiles_n;
     const float* s_a;
@@ -174,14 +200,17 @@ __device__ __forceinline__ void widen_piece(const uint4 raw, uint8_t* tile, int 
             make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
 }
 
-template <GemmMode MODE, int BSRC>
+template <GemmMode MODE, int BSRC, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc1_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_y, const Params p) {
-    using Layout = SmemLayout<BSRC>;
-    using S = Src<BSRC>;
+    using Layout = SmemLayout<BSRC, BN>;
+    using C = Cfg<BSRC, BN>;
     constexpr int STAGES = Layout::STAGES;
+    constexpr int NUM_ACC = C::kNumAcc;
+    constexpr int COLS = C::kCols;
+    constexpr int SD = C::kScaleDepth;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -201,7 +230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(smem_u32(&bars->conv_full[s]), NUM_CONV_WARPS);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NUM_ACC; ++b) {
             mbar_init(smem_u32(&bars->acc_full[b]), 1);
             mbar_init(smem_u32(&bars->acc_empty[b]), NUM_EPI_WARPS);
         }
@@ -239,16 +268,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                            abort_flag, p.status, kSiteProducerEmpty))
                         goto producer_done;
                     const uint32_t fb = smem_u32(&bars->full[stage]);
-                    mbar_arrive_expect_tx(fb, S::kFullTx);
+                    mbar_arrive_expect_tx(fb, C::kFullTx);
                     tma_load_2d(smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES), &tmap_a,
                                 fb, kb * BK, tm * BM);
-                    if constexpr (S::kRaw) {
+                    if constexpr (C::kRaw) {
                         const uint32_t rb = smem_u32(&bars->raw_full[stage]);
-                        mbar_arrive_expect_tx(rb, S::kRawBytes);
-                        tma_load_2d(smem_u32(smem + Layout::raw_off + stage * S::kRawBytes),
-                                    &tmap_b, rb, kb * S::kRawRowBytes, tn * BN);
+                        mbar_arrive_expect_tx(rb, C::kRawBytes);
+                        tma_load_2d(smem_u32(smem + Layout::raw_off + stage * C::kRawBytes),
+                                    &tmap_b, rb, kb * C::kRawRowBytes, tn * BN);
                     } else {
-                        tma_load_2d(smem_u32(smem + Layout::b_off + stage * B_STAGE_BYTES),
+                        tma_load_2d(smem_u32(smem + Layout::b_off + stage * C::kBStageBytes),
                                     &tmap_b, fb, kb * BK, tn * BN);
                     }
                     ++issued;
@@ -265,7 +294,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int u = (issued > STAGES ? issued - STAGES : 0); u < issued; ++u) {
                     const uint32_t par = (uint32_t)(u / STAGES) & 1u;
                     bool ok = mbar_wait_drain(smem_u32(&bars->full[u % STAGES]), par, p.timeout_ns);
-                    if (S::kRaw)
+                    if (C::kRaw)
                         ok = mbar_wait_drain(smem_u32(&bars->raw_full[u % STAGES]), par,
                                              p.timeout_ns) && ok;
                     if (!ok) report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
@@ -282,20 +311,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool issued_any = false;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
-                    const uint32_t b = seg_count & 1;
-                    const uint32_t acc_phase = (seg_count >> 1) & 1;
+                    const uint32_t b = seg_count % NUM_ACC;
+                    const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
                     if (!mbar_wait_bounded(smem_u32(&bars->acc_empty[b]), acc_phase ^ 1,
                                            p.timeout_ns, abort_flag, p.status, kSiteMmaAccEmpty))
                         goto mma_done;
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + b * BN;
                     const int kb0 = seg * p.seg_kb;
                     const int kb1 = min(p.num_kb, kb0 + p.seg_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
+                        // Group j of the segment accumulates into its own BN columns.
+                        const int j = (kb - kb0) / p.group_kb;
+                        const int gkb0 = kb0 + j * p.group_kb;
+                        const uint32_t d_tmem = tmem_base + b * C::kBufCols + j * BN;
                         if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, p.timeout_ns,
                                                abort_flag, p.status, kSiteMmaFull))
                             goto mma_done;
-                        if (S::kRaw &&
+                        if (C::kRaw &&
                             !mbar_wait_bounded(smem_u32(&bars->conv_full[stage]), phase,
                                                p.timeout_ns, abort_flag, p.status, kSiteMmaConv))
                             goto mma_done;
@@ -303,12 +335,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t adesc = smem_desc_sw128_kmajor(
                             smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES));
                         const uint64_t bdesc = smem_desc_sw128_kmajor(
-                            smem_u32(smem + Layout::b_off + stage * B_STAGE_BYTES));
+                            smem_u32(smem + Layout::b_off + stage * C::kBStageBytes));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
                             // +32 bytes along K per 16-element step (encoded >> 4).
                             tc_mma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                                       (kb > kb0 || k > 0) ? 1u : 0u);
+                                       (kb > gkb0 || k > 0) ? 1u : 0u);
                         }
                         issued_any = true;
                         tc_commit(smem_u32(&bars->empty[stage]));
@@ -333,8 +365,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // A stage's raw tile is BN rows of kRawRowBytes, i.e. PPR 16-byte
         // pieces per row; piece pc covers row pc / PPR, fp16 chunks from
         // (pc % PPR) * CPP.
-        if constexpr (S::kRaw) {
-            constexpr int PPR = S::kRawRowBytes / 16;
+        if constexpr (C::kRaw) {
+            constexpr int PPR = C::kRawRowBytes / 16;
             constexpr int CPP = 8 / PPR;
             constexpr int PER_THREAD = BN * PPR / (32 * NUM_CONV_WARPS);
             const int ct = (warp - 2) * 32 + lane;
@@ -349,8 +381,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!__all_sync(0xffffffffu, ok)) goto conv_done;
                     }
                     const uint4* raw =
-                        reinterpret_cast<const uint4*>(smem + Layout::raw_off + stage * S::kRawBytes);
-                    uint8_t* tile_b = smem + Layout::b_off + stage * B_STAGE_BYTES;
+                        reinterpret_cast<const uint4*>(smem + Layout::raw_off + stage * C::kRawBytes);
+                    uint8_t* tile_b = smem + Layout::b_off + stage * C::kBStageBytes;
                     uint4 pcs[PER_THREAD];
 #pragma unroll
                     for (int i = 0; i < PER_THREAD; ++i) pcs[i] = raw[ct + i * 32 * NUM_CONV_WARPS];
@@ -374,41 +406,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ------------------------------ epilogue ------------------------------
         // Warp w (4..11) owns TMEM lanes 32 * (w % 4) .. +31 (its 32 token
-        // rows; a warp may only access its own lane quadrant) and the 32
-        // columns [32 * half, 32 * half + 32) of the 64-column tile.
+        // rows; a warp may only access its own lane quadrant) and the COLS
+        // columns [COLS * half, COLS * half + COLS) of the tile, read 32 at a
+        // time.
         const int ewarp = warp - 4;
         const int quad = warp & 3;
         const int half = ewarp >> 2;
         uint8_t* stage_out = smem + Layout::out_off + ewarp * OUT_WARP_BYTES;
         const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-byte swizzle of row `lane`
-        // This warp's 32 weight scales per segment that needs them, double
-        // buffered: lane l copies column l with cp.async one segment ahead.
-        float* wsc = scales + ewarp * 2 * COLS;
-        uint32_t sbuf = 0;
-        auto fetch_scales = [&](int tile, int seg, uint32_t buf) {
-            int tm, tn;
-            tile_coords(tile, p.tiles_m, tm, tn);
-            const int n = tn * BN + half * COLS + lane;
-            const int g = (p.G == 1) ? 0 : seg;
-            float* dst = wsc + buf * COLS + lane;
-            if (p.s_w != nullptr && n < p.N) {
-                const float* src = (p.s_wT != nullptr) ? p.s_wT + (int64_t)g * p.N + n
-                                                       : p.s_w + (int64_t)n * p.G + g;
-                cp_async_4(smem_u32(dst), src);
-            } else {
-                *dst = 0.0f;
-            }
-            cp_async_commit();
-        };
-        auto scales_ready = [&]() {
-            cp_async_wait_all();
-            __syncwarp();
-        };
+        // Weight scales, SD sets per warp in flight: a "use" is one segment
+        // (per-group: the scales of its kGroups groups) or the last segment of
+        // a tile (per-channel); lanes copy their columns with cp.async, one
+        // commit group per use, SD - 1 uses ahead of the one being folded.
         constexpr bool kPerSegScales = (MODE == GemmMode::kPgF16);
-        if ((int)blockIdx.x < num_tiles) {
-            fetch_scales(blockIdx.x, kPerSegScales ? 0 : p.num_seg - 1, 0);
-            scales_ready();
-        }
+        constexpr int GS = C::kGroups;
+        constexpr int SET = GS * COLS;  // floats per use: [group][column]
+        float* wsc = scales + ewarp * C::kScaleFloats;
+        int f_tile = blockIdx.x, f_seg = kPerSegScales ? 0 : p.num_seg - 1;  // next use to fetch
+        uint32_t f_slot = 0, u_slot = 0;
+        auto fetch_next = [&]() {
+            if (f_tile < num_tiles) {
+                int tm, tn;
+                tile_coords(f_tile, p.tiles_m, tm, tn);
+                float* dst = wsc + f_slot * SET;
+#pragma unroll
+                for (int j = 0; j < GS; ++j) {
+                    const int g = (p.G == 1) ? 0 : f_seg * GS + j;
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        const int n = tn * BN + half * COLS + c * 32 + lane;
+                        float* d = dst + j * COLS + c * 32 + lane;
+                        if (p.s_w != nullptr && n < p.N && g < p.G) {
+                            const float* src = (p.s_wT != nullptr) ? p.s_wT + (int64_t)g * p.N + n
+                                                                   : p.s_w + (int64_t)n * p.G + g;
+                            cp_async_4(smem_u32(d), src);
+                        } else {
+                            *d = 0.0f;
+                        }
+                    }
+                }
+                if (kPerSegScales && f_seg + 1 < p.num_seg) {
+                    ++f_seg;
+                } else {
+                    f_seg = kPerSegScales ? 0 : p.num_seg - 1;
+                    f_tile += gridDim.x;
+                }
+            }
+            cp_async_commit();  // possibly empty: one group per use keeps the count
+            f_slot = (f_slot + 1 == SD) ? 0 : f_slot + 1;
+        };
+        for (int i = 0; i < SD - 1; ++i) fetch_next();
         uint32_t seg_count = 0;
         bool store_pending = false;
         uint32_t acc[COLS];  // int32 running sum (per-channel) or fp32 running sum (per-group)
@@ -424,20 +471,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int j = 0; j < COLS; ++j) acc[j] = 0u;  // f = +0 before the first group
             }
             for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
-                const uint32_t b = seg_count & 1;
-                const uint32_t acc_phase = (seg_count >> 1) & 1;
+                const uint32_t b = seg_count % NUM_ACC;
+                const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
                 const bool last_seg = (seg == p.num_seg - 1);
                 const bool uses_scales = kPerSegScales || last_seg;
-                const float* sc = wsc + sbuf * COLS;
+                const float* sc = wsc + u_slot * SET;
                 if (uses_scales) {
-                    // Prefetch the scales of the next segment that uses them.
-                    int nt = tile, ns = seg + 1;
-                    if (ns == p.num_seg) {
-                        ns = 0;
-                        nt += gridDim.x;
-                    }
-                    if (!kPerSegScales) ns = p.num_seg - 1;
-                    if (nt < num_tiles) fetch_scales(nt, ns, sbuf ^ 1);
+                    __syncwarp();  // every lane is done reading the slot refilled next
+                    fetch_next();
+                    cp_async_wait_group<SD - 1>();  // this use's group has landed
+                    __syncwarp();
                 }
                 {
                     // Every lane waits; the warp leaves together if any lane gave
@@ -449,136 +492,154 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 {
+                  // Groups of this segment (per-group), in ascending order.
+                  const int ng = (MODE == GemmMode::kPgF16 || MODE == GemmMode::kRawPgS32)
+                                     ? min(GS, p.G - seg * GS)
+                                     : 1;
+                  for (int j = 0; j < ng; ++j) {  // warp-uniform
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32_ptr(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                               b * BN + half * COLS,
+                                               b * C::kBufCols + j * BN + half * COLS + c * 32,
                                            v);
                     tmem_wait_ld_32(v);
+                    uint32_t* ac = acc + c * 32;
                     if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
                         // Exact fp32 integers -> int32 (the short conversion is exact
                         // below 2^22; the warp takes the long one if any lane needs it).
                         bool big = false;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) big |= fabsf(__uint_as_float(v[j])) >= 4194304.0f;
+                        for (int i = 0; i < 32; ++i) big |= fabsf(__uint_as_float(v[i])) >= 4194304.0f;
                         if (__any_sync(0xffffffffu, big)) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int part = __float2int_rn(__uint_as_float(v[j]));
-                                acc[j] = (seg == 0) ? (uint32_t)part : (uint32_t)((int)acc[j] + part);
+                            for (int i = 0; i < 32; ++i) {
+                                const int part = __float2int_rn(__uint_as_float(v[i]));
+                                ac[i] = (seg == 0) ? (uint32_t)part : (uint32_t)((int)ac[i] + part);
                             }
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int part = small_float_to_int(__uint_as_float(v[j]));
-                                acc[j] = (seg == 0) ? (uint32_t)part : (uint32_t)((int)acc[j] + part);
+                            for (int i = 0; i < 32; ++i) {
+                                const int part = small_float_to_int(__uint_as_float(v[i]));
+                                ac[i] = (seg == 0) ? (uint32_t)part : (uint32_t)((int)ac[i] + part);
                             }
                         }
                     } else if constexpr (MODE == GemmMode::kPgF16) {
                         // f = f + fl(P_g * s_g): scalar products (a packed product
                         // whose only use is a packed add is fused), packed adds.
+                        const float* scc = sc + j * COLS + c * 32;
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 s4 = *reinterpret_cast<const float4*>(sc + j);
-                            const float q0 = __fmul_rn(__uint_as_float(v[j]), s4.x);
-                            const float q1 = __fmul_rn(__uint_as_float(v[j + 1]), s4.y);
-                            const float q2 = __fmul_rn(__uint_as_float(v[j + 2]), s4.z);
-                            const float q3 = __fmul_rn(__uint_as_float(v[j + 3]), s4.w);
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 s4 = *reinterpret_cast<const float4*>(scc + i);
+                            const float q0 = __fmul_rn(__uint_as_float(v[i]), s4.x);
+                            const float q1 = __fmul_rn(__uint_as_float(v[i + 1]), s4.y);
+                            const float q2 = __fmul_rn(__uint_as_float(v[i + 2]), s4.z);
+                            const float q3 = __fmul_rn(__uint_as_float(v[i + 3]), s4.w);
                             float r0, r1, r2, r3;
-                            fadd2_rn(r0, r1, __uint_as_float(acc[j]), __uint_as_float(acc[j + 1]),
+                            fadd2_rn(r0, r1, __uint_as_float(ac[i]), __uint_as_float(ac[i + 1]),
                                      q0, q1);
-                            fadd2_rn(r2, r3, __uint_as_float(acc[j + 2]),
-                                     __uint_as_float(acc[j + 3]), q2, q3);
-                            acc[j] = __float_as_uint(r0);
-                            acc[j + 1] = __float_as_uint(r1);
-                            acc[j + 2] = __float_as_uint(r2);
-                            acc[j + 3] = __float_as_uint(r3);
+                            fadd2_rn(r2, r3, __uint_as_float(ac[i + 2]),
+                                     __uint_as_float(ac[i + 3]), q2, q3);
+                            ac[i] = __float_as_uint(r0);
+                            ac[i + 1] = __float_as_uint(r1);
+                            ac[i + 2] = __float_as_uint(r2);
+                            ac[i + 3] = __float_as_uint(r3);
                         }
                     } else {  // kRawPgS32: this group's partials, written directly
-                        if (m < p.M) {
+                        const int n_c = n_w + c * 32;
+                        if (m < p.M && n_c < p.N) {
                             int32_t* out = static_cast<int32_t*>(p.out) +
-                                           ((int64_t)m * p.N + n_w) * p.G + seg;
-                            const int valid = min(32, p.N - n_w);
+                                           ((int64_t)m * p.N + n_c) * p.G + seg * GS + j;
+                            const int valid = min(32, p.N - n_c);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (j < valid)
-                                    out[(int64_t)j * p.G] = __float2int_rn(__uint_as_float(v[j]));
+                            for (int i = 0; i < 32; ++i)
+                                if (i < valid)
+                                    out[(int64_t)i * p.G] = __float2int_rn(__uint_as_float(v[i]));
                         }
                     }
+                    }
+                  }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[b]));
 
                 if (last_seg) {
-                    if constexpr (MODE == GemmMode::kRawS32) {
-                        if (m < p.M) {
-                            int32_t* out = static_cast<int32_t*>(p.out) + (int64_t)m * p.N;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (n_w + j < p.N) out[n_w + j] = (int)acc[j];
-                        }
-                    } else if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kPgF16) {
-                        const float sa = (m < p.M) ? __ldg(p.s_a + m) : 0.0f;
-                        bool big = false;
-                        if constexpr (MODE == GemmMode::kPcF16) {
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        const uint32_t* ac = acc + c * 32;
+                        const int n_c = n_w + c * 32;
+                        if constexpr (MODE == GemmMode::kRawS32) {
+                            if (m < p.M) {
+                                int32_t* out = static_cast<int32_t*>(p.out) + (int64_t)m * p.N;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int a = (int)acc[j];
-                                big |= (a >= 4194304 || a <= -4194304);
+                                for (int j = 0; j < 32; ++j)
+                                    if (n_c + j < p.N) out[n_c + j] = (int)ac[j];
                             }
-                        }
-                        const bool slow_cvt = __any_sync(0xffffffffu, big);
-                        uint32_t h2[16];
-#pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            float y0, y1;
+                        } else if constexpr (MODE == GemmMode::kPcF16 ||
+                                             MODE == GemmMode::kPgF16) {
+                            const float sa = (m < p.M) ? __ldg(p.s_a + m) : 0.0f;
+                            bool big = false;
                             if constexpr (MODE == GemmMode::kPcF16) {
-                                const float f0 = slow_cvt ? __int2float_rn((int)acc[j])
-                                                          : small_int_to_float((int)acc[j]);
-                                const float f1 = slow_cvt ? __int2float_rn((int)acc[j + 1])
-                                                          : small_int_to_float((int)acc[j + 1]);
-                                const float2 s2 = *reinterpret_cast<const float2*>(sc + j);
-                                float t0, t1;
-                                fmul2_rn(t0, t1, f0, f1, sa, sa);
-                                fmul2_rn(y0, y1, t0, t1, s2.x, s2.y);
-                            } else {
-                                fmul2_rn(y0, y1, __uint_as_float(acc[j]),
-                                         __uint_as_float(acc[j + 1]), sa, sa);
-                            }
-                            const __half2 hv = __floats2half2_rn(y0, y1);
-                            h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
-                        }
-                        if (p.tma_store) {
-                            if (m_base < p.M && n_w < p.N) {  // warp-uniform
-                                if (store_pending && lane == 0) bulk_wait_group_read0();
-                                __syncwarp();
 #pragma unroll
-                                for (int q = 0; q < 4; ++q)
-                                    *reinterpret_cast<uint4*>(stage_out + lane * 64 +
-                                                              ((q ^ swz) << 4)) =
-                                        make_uint4(h2[4 * q], h2[4 * q + 1], h2[4 * q + 2],
-                                                   h2[4 * q + 3]);
-                                fence_proxy_async_smem();
-                                __syncwarp();
-                                if (lane == 0) {
-                                    tma_store_2d(&tmap_y, smem_u32(stage_out), n_w, m_base);
-                                    bulk_commit_group();
+                                for (int j = 0; j < 32; ++j) {
+                                    const int a = (int)ac[j];
+                                    big |= (a >= 4194304 || a <= -4194304);
                                 }
-                                store_pending = true;
                             }
-                        } else if (m < p.M) {
-                            __half* out = static_cast<__half*>(p.out) + (int64_t)m * p.N;
-                            const __half* hh = reinterpret_cast<const __half*>(h2);
+                            const bool slow_cvt = __any_sync(0xffffffffu, big);
+                            const float* scc = sc + c * 32;
+                            uint32_t h2[16];
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (n_w + j < p.N) out[n_w + j] = hh[j];
+                            for (int j = 0; j < 32; j += 2) {
+                                float y0, y1;
+                                if constexpr (MODE == GemmMode::kPcF16) {
+                                    const float f0 = slow_cvt ? __int2float_rn((int)ac[j])
+                                                              : small_int_to_float((int)ac[j]);
+                                    const float f1 = slow_cvt ? __int2float_rn((int)ac[j + 1])
+                                                              : small_int_to_float((int)ac[j + 1]);
+                                    const float2 s2 = *reinterpret_cast<const float2*>(scc + j);
+                                    float t0, t1;
+                                    fmul2_rn(t0, t1, f0, f1, sa, sa);
+                                    fmul2_rn(y0, y1, t0, t1, s2.x, s2.y);
+                                } else {
+                                    fmul2_rn(y0, y1, __uint_as_float(ac[j]),
+                                             __uint_as_float(ac[j + 1]), sa, sa);
+                                }
+                                const __half2 hv = __floats2half2_rn(y0, y1);
+                                h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                            }
+                            if (p.tma_store) {
+                                if (m_base < p.M && n_c < p.N) {  // warp-uniform
+                                    // The staging box is reused: the previous store
+                                    // must have read it.
+                                    if (store_pending && lane == 0) bulk_wait_group_read0();
+                                    __syncwarp();
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q)
+                                        *reinterpret_cast<uint4*>(stage_out + lane * 64 +
+                                                                  ((q ^ swz) << 4)) =
+                                            make_uint4(h2[4 * q], h2[4 * q + 1], h2[4 * q + 2],
+                                                       h2[4 * q + 3]);
+                                    fence_proxy_async_smem();
+                                    __syncwarp();
+                                    if (lane == 0) {
+                                        tma_store_2d(&tmap_y, smem_u32(stage_out), n_c, m_base);
+                                        bulk_commit_group();
+                                    }
+                                    store_pending = true;
+                                }
+                            } else if (m < p.M) {
+                                __half* out = static_cast<__half*>(p.out) + (int64_t)m * p.N;
+                                const __half* hh = reinterpret_cast<const __half*>(h2);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (n_c + j < p.N) out[n_c + j] = hh[j];
+                            }
                         }
                     }
                 }
-                if (uses_scales) {
-                    scales_ready();
-                    sbuf ^= 1;
-                }
+                if (uses_scales) u_slot = (u_slot + 1 == SD) ? 0 : u_slot + 1;
             }
         }
     epi_done:
@@ -633,11 +694,11 @@ CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_by
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <GemmMode MODE, int BSRC>
+template <GemmMode MODE, int BSRC, int BN>
 cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                         const gemm1::Params& p, int grid, cudaStream_t stream) {
-    using Layout = gemm1::SmemLayout<BSRC>;
-    auto kern = gemm1::gemm_tc1_kernel<MODE, BSRC>;
+    using Layout = gemm1::SmemLayout<BSRC, BN>;
+    auto kern = gemm1::gemm_tc1_kernel<MODE, BSRC, BN>;
     static bool attr_set = false;  // benign race: setting the same value twice
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -648,19 +709,20 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     return launch_pdl(kern, grid, gemm1::NUM_THREADS, Layout::alloc_bytes, stream, ta, tb, ty, p);
 }
 
+// Per-channel modes run 128-wide tiles, per-group modes 64-wide ones.
 template <int BSRC>
 cudaError_t launch_src(GemmMode mode, const CUtensorMap& ta, const CUtensorMap& tb,
                        const CUtensorMap& ty, const gemm1::Params& p, int grid,
                        cudaStream_t stream) {
     switch (mode) {
         case GemmMode::kPcF16:
-            return launch_mode<GemmMode::kPcF16, BSRC>(ta, tb, ty, p, grid, stream);
+            return launch_mode<GemmMode::kPcF16, BSRC, 128>(ta, tb, ty, p, grid, stream);
         case GemmMode::kPgF16:
-            return launch_mode<GemmMode::kPgF16, BSRC>(ta, tb, ty, p, grid, stream);
+            return launch_mode<GemmMode::kPgF16, BSRC, 64>(ta, tb, ty, p, grid, stream);
         case GemmMode::kRawS32:
-            return launch_mode<GemmMode::kRawS32, BSRC>(ta, tb, ty, p, grid, stream);
+            return launch_mode<GemmMode::kRawS32, BSRC, 128>(ta, tb, ty, p, grid, stream);
         case GemmMode::kRawPgS32:
-            return launch_mode<GemmMode::kRawPgS32, BSRC>(ta, tb, ty, p, grid, stream);
+            return launch_mode<GemmMode::kRawPgS32, BSRC, 64>(ta, tb, ty, p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -694,6 +756,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     if (bsrc != 0 && bsrc != 8 && bsrc != 4) return cudaErrorInvalidValue;
     if (bsrc == 0 && !a.b_img) return cudaErrorInvalidValue;
     if (bsrc == 4 && a.K % 32 != 0) return cudaErrorInvalidValue;
+    const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
+    const int BN = per_group ? 64 : 128;  // tile width of the mode's kernel
     CUtensorMap ta, tb, ty;
     if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
@@ -712,22 +776,24 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         f16_out && (a.N % 8 == 0) && (reinterpret_cast<uintptr_t>(a.out) % 16 == 0);
     memset(&ty, 0, sizeof(ty));
     if (tma_store &&
-        encode_tmap_f16_2d(&ty, a.out, a.M, a.N, 32, COLS, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+        encode_tmap_f16_2d(&ty, a.out, a.M, a.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     Params p{};
     p.M = (int)a.M;
     p.N = (int)a.N;
     p.K = (int)a.K;
     p.num_kb = (p.K + BK - 1) / BK;
-    const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
     if (per_group) {
         if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
             return cudaErrorInvalidValue;
-        p.seg_kb = a.group_size / BK;
+        p.group_kb = a.group_size / BK;
+        if (p.group_kb > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
+        p.seg_kb = p.group_kb * Cfg<0, 64>::kGroups;  // groups per segment of the per-group kernel
         p.G = p.K / a.group_size;
     } else {
         const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
         p.seg_kb = (p.num_kb + nseg - 1) / nseg;
+        p.group_kb = p.seg_kb;
         p.G = 1;
     }
     p.num_seg = (p.num_kb + p.seg_kb - 1) / p.seg_kb;

@@ -600,6 +600,7 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     if (per_group) {
         if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
             return cudaErrorInvalidValue;
+        if (a.group_size / BK > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
         p.seg_kb = a.group_size / BK;
         p.G = p.K / a.group_size;
     } else {
