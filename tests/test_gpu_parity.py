@@ -259,6 +259,24 @@ def test_layer_edge_rows():
         assert np.array_equal(host(y).view(np.uint16), ref.view(np.uint16))
 
 
+def test_group_size_limit_of_tensor_core_paths():
+    """A group partial over more than 1024 products could leave the range
+    where the tensor core's fp32 accumulator is exact (127^2 * 1024 < 2^24):
+    the tensor-core paths take groups of up to 1024 and refuse larger ones
+    instead of rounding."""
+    M, N, K = 4, 32, 4096
+    x, w = _layer_inputs(M, N, K, seed=77)
+    wq, s = oracle.quantize_weight_int8(w, 1024)
+    y = cider.w8a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                          cuda(torch.from_numpy(s)), 1024)
+    assert_f16_within_1ulp(host(y), oracle.w8a8_linear(x, wq, s, 1024), "gs1024")
+    wq, s = oracle.quantize_weight_int8(w, 2048)
+    with pytest.raises(cider.CiderError) as e:
+        cider.w8a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                          cuda(torch.from_numpy(s)), 2048)
+    assert e.value.status == cider.CIDER_ERR_UNSUPPORTED
+
+
 # ---------------------------------------------------------------------------
 # M = 1 GEMV
 # ---------------------------------------------------------------------------

@@ -30,6 +30,9 @@ ABI_FUNCTIONS = (
 )
 
 CIDER_OK = 0
+CIDER_ERR_INVALID_ARG = 1
+CIDER_ERR_UNSUPPORTED = 2
+CIDER_ERR_CUDA = 3
 CIDER_ERR_TIMEOUT = 4
 
 _lock = threading.Lock()
