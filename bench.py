@@ -15,7 +15,8 @@ same step after a 512 MiB L2-flush write is reported beside it.
 Prints ONE JSON line (rank 0). `value` is whole-job TOPS (2*M*N*K per step,
 all ranks); `e2e` is the same metric through the public C-ABI call with the
 inputs copied from pinned host memory and the output copied back inside the
-timed region; `gemv` is the M = 1 decode GEMV in HBM GB/s; `roofline` is the
+timed region (steps pipelined as a serving loop runs them: copy-in, layer and
+copy-out of consecutive steps overlap on three streams); `gemv` is the M = 1 decode GEMV in HBM GB/s; `roofline` is the
 dominant kernel (the tensor-core GEMM) against the measured dense bf16 peak
 (fp16 has the same nominal rate); `cpu_baseline` is the CPU oracle timed on a
 bounded sample of the same workload.
@@ -46,6 +47,9 @@ FLUSH_BYTES = 512 << 20
 # from the ncu capture summarised in profiles/; reset to None whenever the
 # kernel changes until it is captured again.
 GEMM_DRAM_BYTES_PER_LAUNCH = 127.8e6
+# dram__bytes_read.sum + dram__bytes_write.sum of one cold gemv_kernel<8, false> launch at
+# N10240 K2560 (ncu; the algorithmic bytes are 26.28 MB).
+GEMV_DRAM_BYTES_PER_LAUNCH = 26.30e6
 
 
 def parse_args():
@@ -555,31 +559,55 @@ def run_cider(args):
     gemv_seq_gbs = gemv_bytes / gemv_seq_s / 1e9
 
     # ---- end to end through the public call, host buffers ------------------
+    # Steps run as a serving loop runs them: the copy-in of step i + 1 and the
+    # copy-out of step i - 1 overlap the layer of step i (three streams,
+    # double-buffered device tensors). Every step's input crosses PCIe from
+    # pinned host memory and its output back inside the timed region; L2 is
+    # flushed before every layer.
     x_h = li.x.pin_memory()
-    y_h = torch.empty((M, N), dtype=torch.float16).pin_memory()
-    x_d = torch.empty_like(x)
-    y_d = torch.empty_like(y)
+    y_h = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(x) for _ in range(2)]
+    y_d = [torch.empty_like(y) for _ in range(2)]
     ws = torch.empty(cider.workspace_bytes(M, N, K, 8, 0), dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        x_d.copy_(x_h, non_blocking=True)
-        cider.w8a8_linear(x_d, wq, s_w, 0, out=y_d, ws=ws)
-        y_h.copy_(y_d, non_blocking=True)
+    def ev():
+        return torch.cuda.Event()
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for a, b in eev:
-        flush.zero_()
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks(statistics.mean([a.elapsed_time(b) for a, b in eev]) / 1e3)
+    ev_in, ev_done, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def e2e_run(n):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        s_in.wait_event(start)
+        for i in range(n):
+            k = i % 2
+            if i >= 2:
+                s_in.wait_event(ev_done[k])   # x_d[k] read by step i - 2's layer
+            with torch.cuda.stream(s_in):
+                x_d[k].copy_(x_h, non_blocking=True)
+                ev_in[k].record(s_in)
+            stream.wait_event(ev_in[k])
+            if i >= 2:
+                stream.wait_event(ev_out[k])  # y_d[k] copied out by step i - 2
+            flush.zero_()
+            cider.w8a8_linear(x_d[k], wq, s_w, 0, out=y_d[k], ws=ws)
+            ev_done[k].record(stream)
+            s_out.wait_event(ev_done[k])
+            with torch.cuda.stream(s_out):
+                y_h[k].copy_(y_d[k], non_blocking=True)
+                ev_out[k].record(s_out)
+        stream.wait_event(ev_out[(n - 1) % 2])
+        if n >= 2:
+            stream.wait_event(ev_out[(n - 2) % 2])
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / 1e3 / n
+
+    e2e_run(max(2, args.warmup))
+    e2e_s = max_over_ranks(e2e_run(args.steps))
     e2e_value = world * flops / e2e_s / 1e12
-    assert torch.equal(y_h.view(torch.int16), y.cpu().view(torch.int16))
+    assert torch.equal(y_h[(args.steps - 1) % 2].view(torch.int16), y.cpu().view(torch.int16))
 
     # ---- INT8 library rate on this GPU (context for "% INT8 peak") ----------
     int8_lib = None
@@ -644,13 +672,19 @@ def run_cider(args):
                  "l2": f"cold: {n_copies} rotating weight copies ({n_copies * N * K >> 20} MiB > 3x L2)",
                  "timing": "standalone launch, events around each",
                  "roofline": {"bound": "hbm", "achieved": gemv_gbs, "peak": hbm_peak,
-                              "unit": "GB/s", "frac": gemv_gbs / hbm_peak, "traffic": None},
+                              "unit": "GB/s", "frac": gemv_gbs / hbm_peak,
+                              "traffic": GEMV_DRAM_BYTES_PER_LAUNCH,
+                              "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write."
+                                                "sum, one cold launch (profiles/gemv_kernel_pc_"
+                                                "M1_N10240_K2560.md)"},
                  "sequence": {"value": gemv_seq_gbs, "unit": "GB/s", "us": gemv_seq_s * 1e6,
                               "timing": f"CUDA graph of {n_copies} back-to-back GEMVs (one per "
                                         "weight copy), total time / launches",
                               "frac": gemv_seq_gbs / hbm_peak}},
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": M * K * 2,
-                "d2h_bytes_per_step": M * N * 2},
+                "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_s * 1e3,
+                "timing": "steps pipelined on three streams (copy-in, layer, copy-out), "
+                          "total time / steps"},
         "cpu_baseline": cpu,
         "gpu_launches": 2 * args.steps,
         "clocks": clock_info,

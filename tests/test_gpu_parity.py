@@ -152,7 +152,9 @@ def _codes(shape, seed, lo=-127, hi=127):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (1, 16, 64), (7, 300, 192), (130, 257, 1088),
-                                   (300, 520, 2560), (129, 256, 12288)])
+                                   (300, 520, 2560), (129, 256, 12288),
+                                   # K not a multiple of the 64-deep k-block (zero-filled tail)
+                                   (5, 33, 96), (64, 130, 224), (150, 40, 224)])
 def test_gemm_s32_bitexact(M, N, K):
     q = _codes((M, K), M + N)
     w = _codes((N, K), K)
@@ -175,9 +177,25 @@ def test_gemm_s32_worst_case_magnitudes():
     assert np.array_equal(host(acc), oracle.gemm_s32(q, w, 0))
 
 
+def test_gemm_s32_worst_case_small_m():
+    """The worst-case magnitudes on the few-token engine, whose weights are
+    widened on chip from raw INT8 codes."""
+    M, N, K = 96, 200, 12288
+    q = np.full((M, K), -127, np.int8)
+    q[::2] = 127
+    q[1::4, ::5] = 127
+    w = np.full((N, K), 127, np.int8)
+    w[::2, ::3] = -127
+    acc = cider.raw_gemm_s32(cuda(torch.from_numpy(q)), cuda(torch.from_numpy(w)), K)
+    assert np.array_equal(host(acc), oracle.gemm_s32(q, w, 0))
+
+
 @pytest.mark.parametrize("gs", [64, 128])
-def test_gemm_s32_group_partials(gs):
-    M, N, K = 140, 270, 1024
+@pytest.mark.parametrize("M,K", [(140, 1024), (40, 1152), (3, 1152)])
+def test_gemm_s32_group_partials(gs, M, K):
+    """Per-group partials; K = 1152 gives a group count that is not a
+    multiple of the four groups the few-token engine folds per round."""
+    N = 270
     q = _codes((M, K), 11)
     w = _codes((N, K), 12)
     part = cider.raw_gemm_s32(cuda(torch.from_numpy(q)), cuda(torch.from_numpy(w)), K,
@@ -185,8 +203,8 @@ def test_gemm_s32_group_partials(gs):
     assert np.array_equal(host(part), oracle.gemm_s32(q, w, gs))
 
 
-def test_gemm_s32_int4_weights():
-    M, N, K = 130, 300, 512
+@pytest.mark.parametrize("M,N,K", [(130, 300, 512), (40, 300, 96), (1, 77, 224)])
+def test_gemm_s32_int4_weights(M, N, K):
     q = _codes((M, K), 21)
     wp = np.random.default_rng(22).integers(0, 256, (N, K // 2), dtype=np.uint8)
     acc = cider.raw_gemm_s32(cuda(torch.from_numpy(q)), cuda(torch.from_numpy(wp)), K, bits=4)
@@ -203,7 +221,7 @@ def _layer_inputs(M, N, K, seed):
 
 
 LAYER_SHAPES = [(128, 256, 512), (2, 16, 64), (3, 300, 192), (130, 257, 1088), (200, 8, 2560),
-                (129, 384, 4096)]
+                (129, 384, 4096), (4, 40, 80), (150, 72, 208)]
 
 
 @pytest.mark.parametrize("M,N,K", LAYER_SHAPES)
@@ -217,7 +235,8 @@ def test_w8a8_pc_layer(M, N, K):
 
 
 @pytest.mark.parametrize("gs", [64, 128])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (3, 300, 1024), (130, 264, 2560)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (3, 300, 1024), (130, 264, 2560),
+                                   (5, 260, 1152)])
 def test_w8a8_pg_layer(M, N, K, gs):
     x, w = _layer_inputs(M, N, K, seed=gs + M)
     wq, s = oracle.quantize_weight_int8(w, gs)
