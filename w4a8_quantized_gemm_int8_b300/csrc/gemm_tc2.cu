@@ -34,54 +34,85 @@ namespace cider {
 namespace gemm2 {
 
 constexpr int BM = 128;        // token rows per CTA (256 per pair)
-constexpr int BN = 256;        // output columns per tile; each CTA loads BN / 2 weight rows
 constexpr int BK = 64;         // one 128-byte swizzle row of fp16
-constexpr int STAGES = 6;
+constexpr int MAX_STAGES = 8;
 constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int B_STAGE_BYTES = (BN / 2) * BK * 2;
-constexpr int STAGE_TX_BYTES = 2 * (A_STAGE_BYTES + B_STAGE_BYTES);  // both CTAs
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
 constexpr int NUM_ROLE_THREADS = 128;
 constexpr int NUM_THREADS = NUM_ROLE_THREADS + NUM_EPI_THREADS;
-constexpr int TMEM_COLS = 512;  // two 256-column fp32 accumulators
+constexpr int TMEM_COLS = 512;  // two accumulator buffers of 256 columns
 constexpr int MAX_SEG_KB = 16;  // 16 x 64 = 1024 k per exact fp32 segment
 constexpr int LAUNCH_REGS = 168;
 constexpr int ROLE_REGS = 40;    // TMA and MMA issue need few registers
-constexpr int EPI_REGS = 232;    // 128 running sums + loaded columns per thread
+constexpr int EPI_REGS = 232;    // running sums + loaded columns per thread
 constexpr int OUT_WARP_BYTES = 32 * 32 * 2;  // output staging: 32 rows x 32 fp16 per warp
+constexpr int SMEM_LIMIT = 232448;           // opt-in shared memory per block
 static_assert(NUM_ROLE_THREADS * ROLE_REGS + NUM_EPI_THREADS * EPI_REGS <=
                   NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch allocation");
 constexpr uint16_t kPairMask = 0x3;
 
-struct __align__(8) Barriers {
-    uint64_t full[STAGES];      // even CTA: both CTAs' tile bytes landed
-    uint64_t empty[STAGES];     // each CTA: the MMAs reading the stage completed
-    uint64_t acc_full[2];       // each CTA: accumulator buffer ready
-    uint64_t acc_empty[2];      // even CTA: both CTAs' epilogues drained the buffer
-    uint64_t drain;             // even CTA: MMA drain after an abort
+// Per-instantiation tile shape. BN: output columns per pair tile (each CTA
+// loads BN / 2 weight rows). All modes run 256-wide tiles, where the MMA
+// issues at its full rate. The kernel also takes 128-wide tiles that keep two
+// groups' partials side by side in one 256-column TMEM buffer (one hand-over
+// per two groups, 64 columns per epilogue warp); measured on B300 they were
+// slower for group size 128 (M = 4096: 380 vs 316 us) and only 10 % faster
+// for group size 64, so they are not launched.
+template <int BN>
+struct Cfg {
+    static constexpr int kGroups = (BN == 128) ? 2 : 1;
+    static constexpr int kBufCols = kGroups * BN;  // one TMEM accumulator buffer
+    static constexpr int kCols = BN / 2;           // columns per epilogue warp and group
+    static constexpr int kChunks = kCols / 32;     // 32-column TMEM loads per warp and group
+    static constexpr int kScaleSet = kGroups * kCols;  // scale floats per warp and segment
+    static constexpr int kBStageBytes = (BN / 2) * BK * 2;
+    static constexpr int kStageTx = 2 * (A_STAGE_BYTES + kBStageBytes);  // both CTAs
+    static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
+    static constexpr int kFixedBytes =
+        NUM_EPI_WARPS * OUT_WARP_BYTES + NUM_EPI_WARPS * 2 * kScaleSet * 4 + 256 + 16 + 1024;
+    static constexpr int kStages = (SMEM_LIMIT - kFixedBytes) / kStageBytes < MAX_STAGES
+                                       ? (SMEM_LIMIT - kFixedBytes) / kStageBytes
+                                       : MAX_STAGES;
+    static_assert(2 * kBufCols == TMEM_COLS, "two accumulator buffers fill TMEM");
+    static_assert(kStages >= 4, "pipeline depth");
 };
 
+struct __align__(8) Barriers {
+    uint64_t full[MAX_STAGES];   // even CTA: both CTAs' tile bytes landed
+    uint64_t empty[MAX_STAGES];  // each CTA: the MMAs reading the stage completed
+    uint64_t acc_full[2];        // each CTA: accumulator buffer ready
+    uint64_t acc_empty[2];       // even CTA: both CTAs' epilogues drained the buffer
+    uint64_t drain;              // even CTA: MMA drain after an abort
+};
+static_assert(sizeof(Barriers) <= 256, "barrier area");
+
+template <int BN>
 struct SmemLayout {
+    using C = Cfg<BN>;
+    static constexpr int STAGES = C::kStages;
     static constexpr int a_off = 0;
     static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
-    static constexpr int out_off = b_off + STAGES * B_STAGE_BYTES;  // per-warp output staging
-    // Per epilogue warp: two buffers of its 128 columns' weight scales.
+    static constexpr int out_off = b_off + STAGES * C::kBStageBytes;  // per-warp output staging
+    // Per epilogue warp: two sets of its columns' weight scales.
     static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;
-    static constexpr int bar_off = scale_off + NUM_EPI_WARPS * 2 * 128 * 4;
-    static constexpr int misc_off = bar_off + (int)sizeof(Barriers);  // tmem base, abort
+    static constexpr int bar_off = scale_off + NUM_EPI_WARPS * 2 * C::kScaleSet * 4;
+    static constexpr int misc_off = bar_off + 256;  // tmem base, abort
     static constexpr int bytes = misc_off + 16;
     static constexpr int alloc_bytes = bytes + 1024;  // runtime 1024-byte alignment slack
+    static_assert(alloc_bytes <= SMEM_LIMIT, "shared memory per block");
+    static_assert(out_off % 1024 == 0, "64-byte-swizzled staging alignment");
 };
 
 struct Params {
     int M, N, K;
     int num_kb;
-    int seg_kb;
+    int seg_kb;    // k-blocks per segment (one TMEM buffer)
     int num_seg;
+    int group_kb;  // k-blocks per group (per-group; = seg_kb for per-channel)
     int G;
-    int tiles_m, tiles_n;  // tiles of 256 x 256
+    int tiles_m, tiles_n;  // tiles of 256 x BN
     const float* s_a;
     const float* s_w;
     const float* s_wT;  // optional group-major copy of per-group scales [G, N]
@@ -105,18 +136,16 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int&
     tn = tile / tiles_m;
 }
 
-__device__ __forceinline__ float load_seg_scale(const Params& p, int tn, int seg, int et) {
-    const int n = tn * BN + et;
-    if (n >= p.N || p.s_w == nullptr) return 0.0f;
-    const int g = (p.G == 1) ? 0 : seg;
-    return __ldg(p.s_w + (int64_t)n * p.G + g);
-}
-
-template <GemmMode MODE>
+template <GemmMode MODE, int BN>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_y, const Params p) {
+    using C = Cfg<BN>;
+    using SmemLayout = gemm2::SmemLayout<BN>;
+    constexpr int STAGES = SmemLayout::STAGES;
+    constexpr int COLS = C::kCols;
+    constexpr int GS = C::kGroups;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -179,11 +208,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                                            abort_flag, p.status, kSiteProducerEmpty))
                         goto producer_done;
                     const uint32_t fb_local = smem_u32(&bars->full[stage]);
-                    if (rank == 0) mbar_arrive_expect_tx(fb_local, STAGE_TX_BYTES);
+                    if (rank == 0) mbar_arrive_expect_tx(fb_local, C::kStageTx);
                     const uint32_t fb = map_to_rank(fb_local, 0);
                     tma_load_2d_pair(smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES),
                                      &tmap_a, fb, kb * BK, a_row);
-                    tma_load_2d_pair(smem_u32(smem + SmemLayout::b_off + stage * B_STAGE_BYTES),
+                    tma_load_2d_pair(smem_u32(smem + SmemLayout::b_off + stage * C::kBStageBytes),
                                      &tmap_b, fb, kb * BK, b_row);
                     ++issued;
                     if (++stage == STAGES) {
@@ -215,10 +244,16 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                                            p.timeout_ns, abort_flag, p.status, kSiteMmaAccEmpty))
                         goto mma_done;
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + b * BN;
                     const int kb0 = seg * p.seg_kb;
                     const int kb1 = min(p.num_kb, kb0 + p.seg_kb);
+                    uint32_t d_tmem = tmem_base + b * C::kBufCols;
+                    int gkb0 = kb0;  // first k-block of the current group
                     for (int kb = kb0; kb < kb1; ++kb) {
+                        // Group j of the segment accumulates into its own BN columns.
+                        if (kb - gkb0 == p.group_kb) {
+                            gkb0 = kb;
+                            d_tmem += BN;
+                        }
                         if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, p.timeout_ns,
                                                abort_flag, p.status, kSiteMmaFull))
                             goto mma_done;
@@ -226,11 +261,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                         const uint64_t adesc = smem_desc_sw128_kmajor(
                             smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES));
                         const uint64_t bdesc = smem_desc_sw128_kmajor(
-                            smem_u32(smem + SmemLayout::b_off + stage * B_STAGE_BYTES));
+                            smem_u32(smem + SmemLayout::b_off + stage * C::kBStageBytes));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
                             tc_mma_f16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                                            (kb > kb0 || k > 0) ? 1u : 0u);
+                                            (kb > gkb0 || k > 0) ? 1u : 0u);
                         issued_any = true;
                         tc_commit_pair_multicast(smem_u32(&bars->empty[stage]), kPairMask);
                         if (++stage == STAGES) {
@@ -252,7 +287,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
         setmaxnreg_inc<EPI_REGS>();
         // ------------------------------ epilogue (both CTAs) ------------------
         // Warp w (4..11) owns TMEM lanes 32 * (w % 4).. (its 32 token rows) and
-        // the 128 columns [128 * half, 128 * half + 128) of the tile.
+        // the COLS columns [COLS * half, COLS * half + COLS) of each group's
+        // accumulator, read 32 at a time.
         const int ewarp = warp - 4;
         const int quad = warp & 3;
         const int half = ewarp >> 2;
@@ -260,29 +296,35 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
         // 64-byte swizzle: chunk c of row r at chunk c ^ ((r >> 1) & 3)).
         uint8_t* stage_out = smem + SmemLayout::out_off + ewarp * OUT_WARP_BYTES;
         const uint32_t swz = (uint32_t)((lane >> 1) & 3);
-        // This warp's weight scales: two buffers of its 128 columns. Lane l
-        // copies columns 4l..4l+3 of the next segment that needs them (the
-        // next segment in per-group mode, the next tile's last segment in
-        // per-channel mode) one segment ahead, with asynchronous copies that
-        // hold no registers; no other warp reads them.
-        float* wsc = scales + ewarp * 256;
+        // This warp's weight scales: two sets, each [group][COLS columns] of
+        // one segment. Lane l copies columns FPL * l .. FPL * l + FPL - 1 of
+        // the next segment that needs them (the next segment in per-group
+        // mode, the next tile's last segment in per-channel mode) one segment
+        // ahead, with asynchronous copies that hold no registers; no other
+        // warp reads them.
+        constexpr int FPL = COLS / 32;  // scale floats per lane and group
+        float* wsc = scales + ewarp * 2 * C::kScaleSet;
         uint32_t sbuf = 0;
-        auto fetch_scales = [&](int tile, int seg, uint32_t buf) {
-            int tm, tn;
-            tile_coords(tile, p.tiles_m, tm, tn);
-            const int n0 = tn * BN + half * 128 + 4 * lane;
-            const int g = (p.G == 1) ? 0 : seg;
-            float* dst = wsc + buf * 128 + 4 * lane;
-            if (p.s_wT != nullptr && n0 + 3 < p.N && (p.N & 3) == 0) {
-                // group-major copy: the four columns are 16 contiguous bytes
-                cp_async_16(smem_u32(dst), p.s_wT + (int64_t)g * p.N + n0);
-            } else {
+        auto fetch_scales = [&](int tn, int seg, uint32_t buf) {
+            const int n0 = tn * BN + half * COLS + FPL * lane;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (p.s_w != nullptr && n0 + i < p.N)
-                        cp_async_4(smem_u32(dst + i), p.s_w + (int64_t)(n0 + i) * p.G + g);
+            for (int j = 0; j < GS; ++j) {
+                const int g = (p.G == 1) ? 0 : seg * GS + j;
+                float* dst = wsc + buf * C::kScaleSet + j * COLS + FPL * lane;
+                if (p.s_wT != nullptr && g < p.G && n0 + FPL - 1 < p.N && (p.N % FPL) == 0) {
+                    // group-major copy: the lane's columns are contiguous bytes
+                    if constexpr (FPL == 4)
+                        cp_async_16(smem_u32(dst), p.s_wT + (int64_t)g * p.N + n0);
                     else
-                        dst[i] = 0.0f;
+                        cp_async_8(smem_u32(dst), p.s_wT + (int64_t)g * p.N + n0);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < FPL; ++i) {
+                        if (p.s_w != nullptr && g < p.G && n0 + i < p.N)
+                            cp_async_4(smem_u32(dst + i), p.s_w + (int64_t)(n0 + i) * p.G + g);
+                        else
+                            dst[i] = 0.0f;
+                    }
                 }
             }
             cp_async_commit();
@@ -292,41 +334,40 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             __syncwarp();
         };
         if (cluster < num_tiles) {
-            fetch_scales(cluster, (MODE == GemmMode::kPgF16) ? 0 : p.num_seg - 1, 0);
+            fetch_scales(cluster / p.tiles_m, (MODE == GemmMode::kPgF16) ? 0 : p.num_seg - 1, 0);
             scales_ready();
         }
         uint32_t seg_count = 0;
         bool store_pending = false;
-        uint32_t acc[128];
+        uint32_t acc[COLS];
 
         for (int tile = cluster; tile < num_tiles; tile += nclusters) {
             int tm, tn;
             tile_coords(tile, p.tiles_m, tm, tn);
             const int m_base = tm * (2 * BM) + (int)rank * BM + quad * 32;
             const int m = m_base + lane;
-            const int n_half = tn * BN + half * 128;
+            const int n_half = tn * BN + half * COLS;
 
             if constexpr (MODE == GemmMode::kPgF16) {
 #pragma unroll
-                for (int j = 0; j < 128; ++j) acc[j] = 0u;  // f = +0 before the first group
+                for (int j = 0; j < COLS; ++j) acc[j] = 0u;  // f = +0 before the first group
             }
             for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
                 const uint32_t b = seg_count & 1;
                 const uint32_t acc_phase = (seg_count >> 1) & 1;
                 const bool last_seg = (seg == p.num_seg - 1);
                 const bool uses_scales = (MODE == GemmMode::kPgF16) || last_seg;
-                const float* sc = wsc + sbuf * 128;
+                const float* sc = wsc + sbuf * C::kScaleSet;
 
-                // The other buffer was last read by this warp alone, in the
+                // The other set was last read by this warp alone, in the
                 // previous scale-consuming segment, which every lane has left.
                 if (uses_scales) {
-                    int nt = tile, ns = seg + 1;
-                    if (ns == p.num_seg) {
-                        ns = 0;
-                        nt += nclusters;
+                    if (MODE == GemmMode::kPgF16 && seg + 1 < p.num_seg) {
+                        fetch_scales(tn, seg + 1, sbuf ^ 1);
+                    } else if (tile + nclusters < num_tiles) {
+                        fetch_scales((tile + nclusters) / p.tiles_m,
+                                     (MODE == GemmMode::kPgF16) ? 0 : p.num_seg - 1, sbuf ^ 1);
                     }
-                    if (MODE != GemmMode::kPgF16) ns = p.num_seg - 1;
-                    if (nt < num_tiles) fetch_scales(nt, ns, sbuf ^ 1);
                 }
 
                 {
@@ -338,46 +379,46 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                 tc_fence_after();
 
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                       b * BN + half * 128;
-                // Batches of BW columns (32; 16 in per-group mode, which keeps
-                // more values live); the next batch's TMEM load is in flight
-                // while the current one is folded.
+                                       b * C::kBufCols + half * COLS;
+                // Batches of 32 columns over the segment's groups (ascending)
+                // and the warp's column chunks; the next batch's TMEM load is
+                // in flight while the current one is folded.
                 {
-                    constexpr int BW = 32;
-                    constexpr int NB = 128 / BW;
-                    auto ld = [&](uint32_t col, uint32_t* r) {
-                        if constexpr (BW == 32) tmem_ld_32x32b_x32_ptr(t_row + col, r);
-                        else tmem_ld_32x32b_x16_ptr(t_row + col, r);
+                    constexpr int MAXB = GS * C::kChunks;
+                    const int ng = (MODE == GemmMode::kPgF16 || MODE == GemmMode::kRawPgS32)
+                                       ? min(GS, p.G - seg * GS)
+                                       : 1;
+                    const int nb = ng * C::kChunks;
+                    auto col_of = [&](int bt) {
+                        return (uint32_t)((bt / C::kChunks) * BN + (bt % C::kChunks) * 32);
                     };
-                    auto wait = [&](uint32_t* r) {
-                        if constexpr (BW == 32) tmem_wait_ld_32(r);
-                        else tmem_wait_ld_16(r);
-                    };
-                    uint32_t va[BW], vb[BW];
-                    ld(0, va);
-                    wait(va);
+                    uint32_t va[32], vb[32];
+                    tmem_ld_32x32b_x32_ptr(t_row, va);
+                    tmem_wait_ld_32(va);
 #pragma unroll
-                    for (int bt = 0; bt < NB; ++bt) {
+                    for (int bt = 0; bt < MAXB; ++bt) {
+                        if (bt >= nb) break;  // warp-uniform
                         uint32_t* v = (bt & 1) ? vb : va;
                         uint32_t* vn = (bt & 1) ? va : vb;
-                        if (bt < NB - 1) ld((bt + 1) * BW, vn);
-                        const int c0 = bt * BW;
+                        if (bt + 1 < nb) tmem_ld_32x32b_x32_ptr(t_row + col_of(bt + 1), vn);
+                        const int jg = bt / C::kChunks;          // group within the segment
+                        const int c0 = (bt % C::kChunks) * 32;   // column within the warp's span
                         if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
                             // Exact fp32 integers -> int32: the fast conversion holds
                             // below 2^22; a warp holding a larger one converts all.
                             bool big = false;
 #pragma unroll
-                            for (int j = 0; j < BW; ++j) big |= fabsf(__uint_as_float(v[j])) >= 4194304.0f;
+                            for (int j = 0; j < 32; ++j) big |= fabsf(__uint_as_float(v[j])) >= 4194304.0f;
                             if (__any_sync(0xffffffffu, big)) {
 #pragma unroll
-                                for (int j = 0; j < BW; ++j) {
+                                for (int j = 0; j < 32; ++j) {
                                     const int part = __float2int_rn(__uint_as_float(v[j]));
                                     acc[c0 + j] = (seg == 0) ? (uint32_t)part
                                                              : (uint32_t)((int)acc[c0 + j] + part);
                                 }
                             } else {
 #pragma unroll
-                                for (int j = 0; j < BW; j += 2) {
+                                for (int j = 0; j < 32; j += 2) {
                                     float t0, t1;
                                     fadd2_rn(t0, t1, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
                                              12582912.0f, 12582912.0f);
@@ -393,9 +434,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                             // f starts at +0 for each tile, as 0 + q). Products are
                             // scalar multiplies: a packed f32x2 multiply whose only use
                             // is a packed add is contracted into a fused multiply-add.
+                            const float* scc = sc + jg * COLS + c0;
 #pragma unroll
-                            for (int j = 0; j < BW; j += 4) {
-                                const float4 s4 = *reinterpret_cast<const float4*>(sc + c0 + j);
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 s4 = *reinterpret_cast<const float4*>(scc + j);
                                 const float q0 = __fmul_rn(__uint_as_float(v[j]), s4.x);
                                 const float q1 = __fmul_rn(__uint_as_float(v[j + 1]), s4.y);
                                 const float q2 = __fmul_rn(__uint_as_float(v[j + 2]), s4.z);
@@ -409,18 +451,18 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                                 acc[c0 + j + 3] = __float_as_uint(r3);
                             }
                         } else {  // kRawPgS32: this group's partials, straight out
-                            if (m < p.M) {
-                                int32_t* out = static_cast<int32_t*>(p.out);
+                            const int n_c = n_half + c0;
+                            if (m < p.M && n_c < p.N) {
+                                int32_t* out = static_cast<int32_t*>(p.out) +
+                                               ((int64_t)m * p.N + n_c) * p.G + seg * GS + jg;
+                                const int valid = min(32, p.N - n_c);
 #pragma unroll
-                                for (int j = 0; j < BW; ++j) {
-                                    const int n = n_half + c0 + j;
-                                    if (n < p.N)
-                                        out[((int64_t)m * p.N + n) * p.G + seg] =
-                                            __float2int_rn(__uint_as_float(v[j]));
-                                }
+                                for (int j = 0; j < 32; ++j)
+                                    if (j < valid)
+                                        out[(int64_t)j * p.G] = __float2int_rn(__uint_as_float(v[j]));
                             }
                         }
-                        if (bt < NB - 1) wait(vn);
+                        if (bt + 1 < nb) tmem_wait_ld_32(vn);
                     }
                 }
                 // This warp's reads of the buffer are complete (waited, the
@@ -437,7 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                         if (m < p.M) {
                             int32_t* out = static_cast<int32_t*>(p.out) + (int64_t)m * p.N;
 #pragma unroll
-                            for (int j = 0; j < 128; ++j)
+                            for (int j = 0; j < COLS; ++j)
                                 if (n_half + j < p.N) out[n_half + j] = (int)acc[j];
                         }
                     } else if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kPgF16) {
@@ -445,15 +487,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                         bool big = false;
                         if constexpr (MODE == GemmMode::kPcF16) {
 #pragma unroll
-                            for (int j = 0; j < 128; ++j) {
+                            for (int j = 0; j < COLS; ++j) {
                                 const int a = (int)acc[j];
                                 big |= (a >= 4194304 || a <= -4194304);
                             }
                         }
                         const bool slow_cvt = __any_sync(0xffffffffu, big);
-                        // Four rounds of 32 columns: dequant, stage, TMA store.
+                        // Rounds of 32 columns: dequant, stage, TMA store.
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
+                        for (int r = 0; r < C::kChunks; ++r) {
                             uint32_t h2[16];
 #pragma unroll
                             for (int j = 0; j < 32; j += 2) {
@@ -538,11 +580,12 @@ struct PairLaunchInfo {
     int max_clusters = 0;
 };
 
-template <GemmMode MODE>
+template <GemmMode MODE, int BN>
 cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                              const gemm2::Params& p, int num_sms, cudaStream_t stream) {
     using namespace gemm2;
-    auto kern = gemm_tc2_kernel<MODE>;
+    using SmemLayout = gemm2::SmemLayout<BN>;
+    auto kern = gemm_tc2_kernel<MODE, BN>;
     static PairLaunchInfo info;  // benign race: every thread computes the same values
     if (!info.checked) {
         cudaFuncAttributes fa;
@@ -578,6 +621,9 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     if (a.M <= 0 || a.N <= 0 || a.K <= 0 || a.K % 16 != 0) return cudaErrorInvalidValue;
     if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2)
         return cudaErrorInvalidValue;
+    const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
+    constexpr int BN = 256;  // tile width of every mode's kernel
+    constexpr int GS = Cfg<BN>::kGroups;
     CUtensorMap ta, tb, ty;
     if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS ||
         encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN / 2, BK) != CUDA_SUCCESS)
@@ -596,16 +642,17 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     p.N = (int)a.N;
     p.K = (int)a.K;
     p.num_kb = (p.K + BK - 1) / BK;
-    const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
     if (per_group) {
         if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
             return cudaErrorInvalidValue;
         if (a.group_size / BK > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
-        p.seg_kb = a.group_size / BK;
+        p.group_kb = a.group_size / BK;
+        p.seg_kb = p.group_kb * GS;
         p.G = p.K / a.group_size;
     } else {
         const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
         p.seg_kb = (p.num_kb + nseg - 1) / nseg;
+        p.group_kb = p.seg_kb;
         p.G = 1;
     }
     p.num_seg = (p.num_kb + p.seg_kb - 1) / p.seg_kb;
@@ -621,13 +668,13 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     p.status = a.status;
     switch (a.mode) {
         case GemmMode::kPcF16:
-            return launch_pair_mode<GemmMode::kPcF16>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kPcF16, 256>(ta, tb, ty, p, num_sms, stream);
         case GemmMode::kPgF16:
-            return launch_pair_mode<GemmMode::kPgF16>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kPgF16, 256>(ta, tb, ty, p, num_sms, stream);
         case GemmMode::kRawS32:
-            return launch_pair_mode<GemmMode::kRawS32>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kRawS32, 256>(ta, tb, ty, p, num_sms, stream);
         case GemmMode::kRawPgS32:
-            return launch_pair_mode<GemmMode::kRawPgS32>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kRawPgS32, 256>(ta, tb, ty, p, num_sms, stream);
     }
     return cudaErrorInvalidValue;
 }
