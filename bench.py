@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("cider", "reference"), default="cider")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustain-s", type=float, default=2.0,
+                    help="seconds of back-to-back steps for the sustained figure")
     ap.add_argument("--gemv-only", action="store_true",
                     help="run only the M = 1 GEMV leg (a small command for profilers)")
     ap.add_argument("--step-only", action="store_true",
@@ -547,6 +549,23 @@ def run_cider(args):
     flops = 2.0 * M * N * K
     mean_step_s = statistics.mean(step_ms) / 1e3
     mean_step_s = max_over_ranks(mean_step_s)
+
+    # ---- sustained: the same step back to back for about 2 s ---------------
+    # (the power cap can lower the SM clock of a long dense run below the
+    # short timed region's).
+    n_sus = max(args.steps, int(args.sustain_s / mean_step_s))
+    sus_clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    sus_clocks.start()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for i in range(n_sus):
+        step_i(i)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    sus_clock_info = sus_clocks.stop()
+    sus_s = max_over_ranks(s0.elapsed_time(s1) / 1e3 / n_sus)
     value = world * flops / mean_step_s / 1e12
     gemm_s = statistics.mean(gemm_ms) / 1e3
     bf16_peak, hbm_peak, peak_src = peaks()
@@ -681,6 +700,9 @@ def run_cider(args):
                               "timing": f"CUDA graph of {n_copies} back-to-back GEMVs (one per "
                                         "weight copy), total time / launches",
                               "frac": gemv_seq_gbs / hbm_peak}},
+        "sustained": {"value": world * flops / sus_s / 1e12, "unit": "TOPS",
+                      "seconds": sus_s * n_sus, "steps": n_sus, "ms_per_step": sus_s * 1e3,
+                      "clocks": sus_clock_info},
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": M * K * 2,
                 "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_s * 1e3,
                 "timing": "steps pipelined on three streams (copy-in, layer, copy-out), "

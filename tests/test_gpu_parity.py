@@ -296,6 +296,24 @@ def test_group_size_limit_of_tensor_core_paths():
     assert e.value.status == cider.CIDER_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("gs", [0, 64])
+def test_column_shards_reproduce_the_full_layer(gs):
+    """The output-channel split, each shard run on the GPU from its own weight
+    rows (as each rank of a column-parallel run does), concatenates to the
+    unsplit layer bit for bit."""
+    M, N, K, world = 130, 700, 1024, 3
+    x, w = _layer_inputs(M, N, K, seed=91)
+    wq, s = oracle.quantize_weight_int8(w, gs)
+    xd, wd, sd = cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)), cuda(torch.from_numpy(s))
+    full = cider.w8a8_linear(xd, wd, sd, gs)
+    parts = []
+    for r in range(world):
+        n0, n1 = cider.column_shard(N, world, r)
+        parts.append(cider.w8a8_linear(xd, wd[n0:n1], sd[n0:n1], gs))
+    y = torch.cat(parts, dim=1)
+    assert torch.equal(y.view(torch.int16), full.view(torch.int16))
+
+
 # ---------------------------------------------------------------------------
 # M = 1 GEMV
 # ---------------------------------------------------------------------------

@@ -324,3 +324,55 @@ def wait_timeout_probe(timeout_ns: int) -> None:
     """Test hook: a kernel whose bounded mbarrier wait is never satisfied."""
     _check("cider_test_wait_timeout",
            load_library().cider_test_wait_timeout(int(timeout_ns), _stream()))
+
+
+# ---------------------------------------------------------------------------
+# column-parallel split (several GPUs, one process each)
+# ---------------------------------------------------------------------------
+
+def column_shard(N: int, world: int, rank: int, align: int = 128) -> tuple[int, int]:
+    """Output channels [n0, n1) that rank `rank` of `world` owns when the
+    layer is split by output channel (its weight rows and scale rows): a
+    contiguous range, balanced in units of `align` channels (the GEMM's tile
+    width), the remainder going to the first ranks; the last rank also takes
+    the ragged end. Output channels are independent, so the split needs no
+    reduction, only a gather of the columns when a consumer needs all of y."""
+    if N <= 0 or world <= 0 or not 0 <= rank < world or align <= 0:
+        raise ValueError("column_shard: bad N / world / rank / align")
+    units = (N + align - 1) // align
+    base, extra = divmod(units, world)
+    u0 = rank * base + min(rank, extra)
+    u1 = u0 + base + (1 if rank < extra else 0)
+    return min(N, u0 * align), min(N, u1 * align)
+
+
+def gather_columns(y_shard: torch.Tensor, N: int, world: int, align: int = 128,
+                   group=None) -> torch.Tensor:
+    """All-gathers the column shards of y ([M, n1 - n0] on every rank, split
+    by column_shard) into the full [M, N] on every rank (torch.distributed;
+    shards are padded to the widest for the collective)."""
+    import torch.distributed as dist
+    M = y_shard.shape[0]
+    widths = [column_shard(N, world, r, align) for r in range(world)]
+    wmax = max(n1 - n0 for n0, n1 in widths)
+    pad = torch.zeros((M, wmax), dtype=y_shard.dtype, device=y_shard.device)
+    pad[:, :y_shard.shape[1]] = y_shard
+    parts = [torch.empty_like(pad) for _ in range(world)]
+    dist.all_gather(parts, pad.contiguous(), group=group)
+    return torch.cat([parts[r][:, :n1 - n0] for r, (n0, n1) in enumerate(widths)], dim=1)
+
+
+def column_parallel_w8a8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
+                                group_size: int = 0, world: int = 1, rank: int = 0,
+                                group=None) -> torch.Tensor:
+    """The W8A8 layer split by output channel over `world` ranks: this rank
+    runs its weight rows (column_shard) through w8a8_linear and the shards
+    are all-gathered into the full y. wq / s_w are the full tensors; only this
+    rank's rows are read."""
+    N = wq.shape[0]
+    n0, n1 = column_shard(N, world, rank)
+    if n1 > n0:
+        y = w8a8_linear(x, wq[n0:n1], s_w[n0:n1], group_size)
+    else:  # more ranks than 128-channel tiles: nothing to compute here
+        y = torch.empty((x.shape[0], 0), dtype=torch.float16, device=x.device)
+    return y if world == 1 else gather_columns(y, N, world, group=group)
