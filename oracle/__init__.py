@@ -66,6 +66,14 @@ def _load():
             lib.oracle_epilogue_pg.restype = ctypes.c_uint16
             lib.oracle_w8a8_linear.argtypes = [p, i64, i64, i64, p, p, i32, p]
             lib.oracle_w4a8_linear.argtypes = [p, i64, i64, i64, p, p, i32, p]
+            lib.oracle_bf16_to_float_array.argtypes = [p, i64, p]
+            lib.oracle_bf16_to_float_array.restype = None
+            lib.oracle_float_to_bf16_array.argtypes = [p, i64, p]
+            lib.oracle_float_to_bf16_array.restype = None
+            lib.oracle_quantize_act_ex.argtypes = [p, i32, i64, i64, p, p]
+            lib.oracle_quantize_act_ex.restype = None
+            lib.oracle_w8a8_linear_ex.argtypes = [p, i32, i64, i64, i64, p, p, i32, p, i32]
+            lib.oracle_w4a8_linear_ex.argtypes = [p, i32, i64, i64, i64, p, p, i32, p, i32]
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_set_threads.restype = None
             lib.oracle_get_threads.restype = ctypes.c_int
@@ -75,6 +83,24 @@ def _load():
 
 def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
+
+
+_DTYPES = {"f16": 0, "bf16": 1}
+
+
+def _bits(x, dtype: str) -> np.ndarray:
+    """Activation bits: fp16 arrays (or uint16 bits) for "f16"; uint16 bit
+    patterns for "bf16" (numpy has no bfloat16)."""
+    if dtype == "f16":
+        return _f16_bits(x)
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.uint16:
+        raise TypeError(f"bf16 values are passed as uint16 bit patterns, got {a.dtype}")
+    return a
+
+
+def _out(y_bits: np.ndarray, dtype: str) -> np.ndarray:
+    return y_bits.view(np.float16) if dtype == "f16" else y_bits
 
 
 def _f16_bits(x) -> np.ndarray:
@@ -109,6 +135,36 @@ def float_to_half(vals) -> np.ndarray:
     out = np.empty(v.shape, np.uint16)
     _load().oracle_float_to_half_array(_ptr(v), v.size, _ptr(out))
     return out.reshape(np.shape(vals))
+
+
+def bf16_to_float(bits) -> np.ndarray:
+    """bfloat16 bit patterns -> exact float32 values (the upper half of a
+    binary32 encoding)."""
+    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16)).ravel()
+    out = np.empty(b.shape, np.float32)
+    _load().oracle_bf16_to_float_array(_ptr(b), b.size, _ptr(out))
+    return out.reshape(np.shape(bits))
+
+
+def float_to_bf16(vals) -> np.ndarray:
+    """float32 values -> bfloat16 bits, round to nearest, ties to even."""
+    v = np.ascontiguousarray(np.asarray(vals, dtype=np.float32)).ravel()
+    out = np.empty(v.shape, np.uint16)
+    _load().oracle_float_to_bf16_array(_ptr(v), v.size, _ptr(out))
+    return out.reshape(np.shape(vals))
+
+
+def quantize_act_bf16(x_bits):
+    """Per-token symmetric INT8 quantization of bf16 activations (uint16 bit
+    patterns): the same formulas as quantize_act on the exact fp32 values
+    (README "Quantization" table, row "Activations"; README roadmap,
+    "automatic dtype handling (float16/bfloat16)")."""
+    xb = _bits(x_bits, "bf16")
+    M, K = xb.shape
+    q = np.empty((M, K), np.int8)
+    s = np.empty((M,), np.float32)
+    _load().oracle_quantize_act_ex(_ptr(xb), 1, M, K, _ptr(q), _ptr(s))
+    return q, s
 
 
 def quantize_act(x):
@@ -204,32 +260,41 @@ def epilogue_pg(partials, s_w_row, s_act: float) -> int:
     return int(_load().oracle_epilogue_pg(_ptr(p), _ptr(s), p.size, float(s_act)))
 
 
-def w8a8_linear(x, wq, s_w, group_size: int = 0) -> np.ndarray:
-    """W8A8 linear layer y = dequant(quant(x) . wq^T) in fp16 (README "Metal
-    Kernel Pipeline", prefill steps 1-2; "Quantization" table)."""
-    xb = _f16_bits(x)
+def w8a8_linear(x, wq, s_w, group_size: int = 0, x_dtype: str = "f16",
+                y_dtype: str | None = None) -> np.ndarray:
+    """W8A8 linear layer y = dequant(quant(x) . wq^T) (README "Metal Kernel
+    Pipeline", prefill steps 1-2; "Quantization" table). x and y are fp16 by
+    default; "bf16" takes / returns bfloat16 uint16 bit patterns (README
+    roadmap, "automatic dtype handling (float16/bfloat16)"); y_dtype defaults
+    to x_dtype."""
+    y_dtype = y_dtype or x_dtype
+    xb = _bits(x, x_dtype)
     M, K = xb.shape
     wq = np.ascontiguousarray(wq, dtype=np.int8)
     N = wq.shape[0]
     s = np.ascontiguousarray(s_w, dtype=np.float32)
     y = np.empty((M, N), np.uint16)
-    rc = _load().oracle_w8a8_linear(_ptr(xb), M, N, K, _ptr(wq), _ptr(s), group_size, _ptr(y))
+    rc = _load().oracle_w8a8_linear_ex(_ptr(xb), _DTYPES[x_dtype], M, N, K, _ptr(wq), _ptr(s),
+                                       group_size, _ptr(y), _DTYPES[y_dtype])
     if rc:
         raise ValueError("unsupported shape / group_size")
-    return y.view(np.float16)
+    return _out(y, y_dtype)
 
 
-def w4a8_linear(x, wp, s_w, group_size: int = 0) -> np.ndarray:
+def w4a8_linear(x, wp, s_w, group_size: int = 0, x_dtype: str = "f16",
+                y_dtype: str | None = None) -> np.ndarray:
     """W4A8 linear layer: INT4 nibbles unpacked to INT8, then the W8A8 layer
     (README "Modes" table, W4A8 "Unpack -> TensorOps"; "Metal Kernel
-    Pipeline", W4A8 note)."""
-    xb = _f16_bits(x)
+    Pipeline", W4A8 note). Dtypes as in w8a8_linear."""
+    y_dtype = y_dtype or x_dtype
+    xb = _bits(x, x_dtype)
     M, K = xb.shape
     wp = np.ascontiguousarray(wp, dtype=np.uint8)
     N = wp.shape[0]
     s = np.ascontiguousarray(s_w, dtype=np.float32)
     y = np.empty((M, N), np.uint16)
-    rc = _load().oracle_w4a8_linear(_ptr(xb), M, N, K, _ptr(wp), _ptr(s), group_size, _ptr(y))
+    rc = _load().oracle_w4a8_linear_ex(_ptr(xb), _DTYPES[x_dtype], M, N, K, _ptr(wp), _ptr(s),
+                                       group_size, _ptr(y), _DTYPES[y_dtype])
     if rc:
         raise ValueError("unsupported shape / group_size")
-    return y.view(np.float16)
+    return _out(y, y_dtype)

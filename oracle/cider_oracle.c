@@ -36,6 +36,11 @@
  *  - per-group output: f = 0; for g ascending: f = f + (float)P_g * s_w[n,g]
  *    (a rounded product, then a rounded sum); y = fp16_rn(f * s_act);
  *  - fp16 rounding is round-to-nearest-even, overflow gives +-inf.
+ *  - bf16 activations / outputs (the README roadmap's "automatic dtype
+ *    handling (float16/bfloat16)"): a bf16 value is the binary32 value with
+ *    the same upper 16 bits; quantization reads it exactly as fp32 and
+ *    applies the same formulas; a bf16 output is the fp32 result rounded to
+ *    nearest even at 8 significant bits, overflow gives +-inf.
  *
  * Build: plain C11, -O2 -ffp-contract=off -fno-fast-math (every float
  * operation is a single IEEE binary32 operation, as written). OpenMP only
@@ -108,6 +113,81 @@ uint16_t oracle_float_to_half(float f)
     return (uint16_t)(sign | out);
 }
 
+/* ------------------------------------------------------------------------ */
+/* bfloat16 <-> binary32, from the format definition.                        */
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits: the    */
+/* upper half of a binary32 encoding.                                        */
+/* ------------------------------------------------------------------------ */
+
+float oracle_bf16_to_float(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+/* Round a binary32 value to the nearest bfloat16, ties to even. */
+uint16_t oracle_float_to_bf16(float f)
+{
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    if (isnan(f))
+        return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs((double)f);
+    if (a == 0.0)
+        return sign;
+    if (isinf(f))
+        return (uint16_t)(sign | 0x7F80u);
+    int e2;
+    (void)frexp(a, &e2);         /* a = m * 2^e2, m in [0.5, 1) */
+    int unbiased = e2 - 1;       /* a in [2^unbiased, 2^(unbiased+1)) */
+    if (unbiased < -126)
+        unbiased = -126;         /* subnormal binade shares the 2^-133 step */
+    double quantum = ldexp(1.0, unbiased - 7);
+    double n = rint(a / quantum); /* exact quotient; rint rounds ties to even */
+    uint32_t out;
+    if (unbiased == -126 && n < 128.0) {
+        out = (uint32_t)n;       /* subnormal (or exactly the smallest normal) */
+    } else {
+        int expo = unbiased + 127;
+        if (n >= 256.0) {        /* rounding carried into the next binade */
+            n = 128.0;
+            expo += 1;
+        }
+        if (expo >= 255)
+            return (uint16_t)(sign | 0x7F80u);
+        out = ((uint32_t)expo << 7) | ((uint32_t)n - 128u);
+    }
+    return (uint16_t)(sign | out);
+}
+
+/* Element types of activations and outputs. */
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+
+static float elem_to_float(uint16_t v, int dtype)
+{
+    return dtype == ORACLE_BF16 ? oracle_bf16_to_float(v) : oracle_half_to_float(v);
+}
+
+static uint16_t float_to_elem(float f, int dtype)
+{
+    return dtype == ORACLE_BF16 ? oracle_float_to_bf16(f) : oracle_float_to_half(f);
+}
+
+void oracle_bf16_to_float_array(const uint16_t* b, int64_t n, float* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_bf16_to_float(b[i]);
+}
+
+void oracle_float_to_bf16_array(const float* f, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_float_to_bf16(f[i]);
+}
+
 void oracle_half_to_float_array(const uint16_t* h, int64_t n, float* out)
 {
     for (int64_t i = 0; i < n; ++i)
@@ -124,13 +204,14 @@ void oracle_float_to_half_array(const float* f, int64_t n, uint16_t* out)
 /* Symmetric min-max quantization of one block of fp16 values.               */
 /* ------------------------------------------------------------------------ */
 
-/* Quantizes the n contiguous values v[0..n) with the given qmax.
-   Writes the codes to out[0..n) and returns the fp32 scale. */
-static float quantize_block(const uint16_t* v, int64_t n, float qmax, int8_t* out)
+/* Quantizes the n contiguous values v[0..n) (fp16 or bf16 bit patterns)
+   with the given qmax. Writes the codes to out[0..n) and returns the fp32
+   scale. */
+static float quantize_block_t(const uint16_t* v, int64_t n, float qmax, int8_t* out, int dtype)
 {
     float absmax = 0.0f;
     for (int64_t k = 0; k < n; ++k) {
-        float a = fabsf(oracle_half_to_float(v[k]));
+        float a = fabsf(elem_to_float(v[k], dtype));
         if (a > absmax)
             absmax = a;
     }
@@ -141,7 +222,7 @@ static float quantize_block(const uint16_t* v, int64_t n, float qmax, int8_t* ou
     }
     float scale = absmax / qmax;
     for (int64_t k = 0; k < n; ++k) {
-        float x = oracle_half_to_float(v[k]);
+        float x = elem_to_float(v[k], dtype);
         float r = rintf(x / scale);
         if (r > qmax)
             r = qmax;
@@ -152,12 +233,24 @@ static float quantize_block(const uint16_t* v, int64_t n, float qmax, int8_t* ou
     return scale;
 }
 
-/* Per-token activation quantization: x fp16 [M,K] -> q int8 [M,K], s [M]. */
-void oracle_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s)
+static float quantize_block(const uint16_t* v, int64_t n, float qmax, int8_t* out)
+{
+    return quantize_block_t(v, n, qmax, out, ORACLE_F16);
+}
+
+/* Per-token activation quantization: x [M,K] (fp16, or bf16 with x_dtype 1)
+   -> q int8 [M,K], s [M]. */
+void oracle_quantize_act_ex(const uint16_t* x, int32_t x_dtype, int64_t M, int64_t K, int8_t* q,
+                            float* s)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t m = 0; m < M; ++m)
-        s[m] = quantize_block(x + m * K, K, 127.0f, q + m * K);
+        s[m] = quantize_block_t(x + m * K, K, 127.0f, q + m * K, x_dtype);
+}
+
+void oracle_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s)
+{
+    oracle_quantize_act_ex(x, ORACLE_F16, M, K, q, s);
 }
 
 /* INT8 weight quantization: w fp16 [N,K] -> wq int8 [N,K].
@@ -253,33 +346,47 @@ int oracle_gemm_s32(const int8_t* q, const int8_t* wq, int64_t M, int64_t N, int
 /* Dequant epilogues.                                                        */
 /* ------------------------------------------------------------------------ */
 
-/* Per-channel: C_fp16 = C_int32 * s_act * s_weight, left to right. */
-uint16_t oracle_epilogue_pc(int32_t acc, float s_act, float s_weight)
+/* Per-channel: C_fp16 = C_int32 * s_act * s_weight, left to right (the
+   output rounded to fp16, or to bf16 with y_dtype 1). */
+uint16_t oracle_epilogue_pc_ex(int32_t acc, float s_act, float s_weight, int32_t y_dtype)
 {
     float t = (float)acc * s_act;
     t = t * s_weight;
-    return oracle_float_to_half(t);
+    return float_to_elem(t, y_dtype);
+}
+
+uint16_t oracle_epilogue_pc(int32_t acc, float s_act, float s_weight)
+{
+    return oracle_epilogue_pc_ex(acc, s_act, s_weight, ORACLE_F16);
 }
 
 /* Per-group: each group's int32 partial is rescaled by its weight scale and
    summed in ascending group order; the token scale is applied last. */
-uint16_t oracle_epilogue_pg(const int32_t* partials, const float* s_weight_row, int64_t G,
-                            float s_act)
+uint16_t oracle_epilogue_pg_ex(const int32_t* partials, const float* s_weight_row, int64_t G,
+                               float s_act, int32_t y_dtype)
 {
     float f = 0.0f;
     for (int64_t g = 0; g < G; ++g)
         f = f + (float)partials[g] * s_weight_row[g];
-    return oracle_float_to_half(f * s_act);
+    return float_to_elem(f * s_act, y_dtype);
+}
+
+uint16_t oracle_epilogue_pg(const int32_t* partials, const float* s_weight_row, int64_t G,
+                            float s_act)
+{
+    return oracle_epilogue_pg_ex(partials, s_weight_row, G, s_act, ORACLE_F16);
 }
 
 /* ------------------------------------------------------------------------ */
 /* Whole linear layers: per-token quantize -> INT32 product -> dequant.      */
 /* ------------------------------------------------------------------------ */
 
-/* y fp16 [M,N] from x fp16 [M,K] and INT8 weights wq [N,K] with scales s_w
-   ([N] for group_size 0, [N, K/gs] otherwise). Returns 0 on success. */
-int oracle_w8a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const int8_t* wq,
-                       const float* s_w, int32_t group_size, uint16_t* y)
+/* y [M,N] from x [M,K] and INT8 weights wq [N,K] with scales s_w ([N] for
+   group_size 0, [N, K/gs] otherwise); x and y are fp16 (dtype 0) or bf16
+   (dtype 1). Returns 0 on success. */
+int oracle_w8a8_linear_ex(const uint16_t* x, int32_t x_dtype, int64_t M, int64_t N, int64_t K,
+                          const int8_t* wq, const float* s_w, int32_t group_size, uint16_t* y,
+                          int32_t y_dtype)
 {
     if (group_size < 0 || (group_size > 0 && K % group_size != 0))
         return 1;
@@ -296,7 +403,7 @@ int oracle_w8a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const
             rc = 2;
             continue;
         }
-        float s_act = quantize_block(x + m * K, K, 127.0f, q);
+        float s_act = quantize_block_t(x + m * K, K, 127.0f, q, x_dtype);
         for (int64_t n = 0; n < N; ++n) {
             const int8_t* wrow = wq + n * K;
             for (int64_t g = 0; g < G; ++g) {
@@ -306,9 +413,9 @@ int oracle_w8a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const
                 part[g] = acc;
             }
             if (group_size == 0)
-                y[m * N + n] = oracle_epilogue_pc(part[0], s_act, s_w[n]);
+                y[m * N + n] = oracle_epilogue_pc_ex(part[0], s_act, s_w[n], y_dtype);
             else
-                y[m * N + n] = oracle_epilogue_pg(part, s_w + n * G, G, s_act);
+                y[m * N + n] = oracle_epilogue_pg_ex(part, s_w + n * G, G, s_act, y_dtype);
         }
         free(q);
         free(part);
@@ -316,10 +423,17 @@ int oracle_w8a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const
     return rc;
 }
 
+int oracle_w8a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const int8_t* wq,
+                       const float* s_w, int32_t group_size, uint16_t* y)
+{
+    return oracle_w8a8_linear_ex(x, ORACLE_F16, M, N, K, wq, s_w, group_size, y, ORACLE_F16);
+}
+
 /* W4A8: unpack the INT4 nibbles to INT8 codes, then the same layer as W8A8
    (per-output-channel scales for group_size 0, per-group otherwise). */
-int oracle_w4a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const uint8_t* wp,
-                       const float* s_w, int32_t group_size, uint16_t* y)
+int oracle_w4a8_linear_ex(const uint16_t* x, int32_t x_dtype, int64_t M, int64_t N, int64_t K,
+                          const uint8_t* wp, const float* s_w, int32_t group_size, uint16_t* y,
+                          int32_t y_dtype)
 {
     if (K % 2 != 0)
         return 1;
@@ -327,9 +441,15 @@ int oracle_w4a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const
     if (!wq)
         return 2;
     oracle_unpack_int4(wp, N, K, wq);
-    int rc = oracle_w8a8_linear(x, M, N, K, wq, s_w, group_size, y);
+    int rc = oracle_w8a8_linear_ex(x, x_dtype, M, N, K, wq, s_w, group_size, y, y_dtype);
     free(wq);
     return rc;
+}
+
+int oracle_w4a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const uint8_t* wp,
+                       const float* s_w, int32_t group_size, uint16_t* y)
+{
+    return oracle_w4a8_linear_ex(x, ORACLE_F16, M, N, K, wp, s_w, group_size, y, ORACLE_F16);
 }
 
 void oracle_set_threads(int n)

@@ -331,3 +331,79 @@ def test_gemv_is_gemm_row():
     for m in range(6):
         assert np.array_equal(oracle.w8a8_linear(x[m:m + 1], wq, s, 64).view(np.uint16),
                               y[m:m + 1].view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# bfloat16 activations and outputs (README roadmap: float16/bfloat16 dtypes)
+# ---------------------------------------------------------------------------
+
+def test_bf16_to_float_all_patterns():
+    """Every bf16 bit pattern against torch's independent conversion (NaNs
+    only need to stay NaN)."""
+    import torch
+    b = np.arange(65536, dtype=np.uint16)
+    f = oracle.bf16_to_float(b)
+    ref = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).float().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(f), nan)
+    assert np.array_equal(f[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_float_to_bf16_hand_examples():
+    """Worked roundings at 8 significant bits, ties to even, overflow."""
+    cases = [
+        (1.0, 0x3F80), (-2.0, 0xC000), (0.0, 0x0000), (-0.0, 0x8000),
+        (1.0 + 2.0 ** -8, 0x3F80),          # halfway between 1 and 1 + 2^-7: even (1)
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),      # halfway between 1 + 2^-7 and 1 + 2^-6: even
+        (1.0 + 2.0 ** -8 + 2.0 ** -20, 0x3F81),  # just above the tie: up
+        (3.3895313892515355e38, 0x7F7F),   # largest finite bf16
+        (3.4028234663852886e38, 0x7F80),   # largest fp32 rounds past it to inf
+        (2.0 ** -133, 0x0001),              # smallest bf16 subnormal
+        (2.0 ** -134, 0x0000),              # halfway to it: even (0)
+        (float("inf"), 0x7F80), (float("-inf"), 0xFF80),
+    ]
+    for v, want in cases:
+        got = int(oracle.float_to_bf16(np.float32(v)))
+        assert got == want, (v, hex(got), hex(want))
+
+
+def test_float_to_bf16_matches_torch_random():
+    import torch
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal(200000).astype(np.float32)
+         * np.float32(10.0) ** rng.integers(-40, 38, 200000).astype(np.float32))
+    got = oracle.float_to_bf16(v)
+    ref = torch.from_numpy(v).bfloat16().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_quant_equals_fp16_quant_on_shared_values():
+    """Values exact in both formats (small integers and binary fractions)
+    give the same codes and scales from bf16 and fp16 inputs."""
+    rng = np.random.default_rng(8)
+    x32 = (rng.integers(-256, 257, (5, 96)) / np.float32(8.0)).astype(np.float32)
+    q16, s16 = oracle.quantize_act(x32.astype(np.float16))
+    qbf, sbf = oracle.quantize_act_bf16(oracle.float_to_bf16(x32))
+    assert np.array_equal(q16, qbf) and np.array_equal(s16, sbf)
+
+
+def test_bf16_layer_epilogue_against_numpy_float32():
+    """bf16 in / bf16 out layer: codes from the exact bf16 values, int32
+    products from numpy int64, the fp32 epilogue restated in numpy float32
+    (IEEE single) and rounded by torch's bf16 conversion."""
+    import torch
+    rng = np.random.default_rng(9)
+    M, N, K = 4, 6, 64
+    x_bits = oracle.float_to_bf16(rng.standard_normal((M, K)).astype(np.float32) * 3)
+    wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    s_w = (rng.random(N).astype(np.float32) * np.float32(0.01) + np.float32(1e-4))
+    y = oracle.w8a8_linear(x_bits, wq, s_w, 0, x_dtype="bf16")
+    q, s_a = oracle.quantize_act_bf16(x_bits)
+    acc = (q.astype(np.int64) @ wq.astype(np.int64).T).astype(np.int32)
+    t = (acc.astype(np.float32) * s_a[:, None]).astype(np.float32)
+    t = (t * s_w[None, :]).astype(np.float32)
+    ref = torch.from_numpy(t).bfloat16().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(y, ref)
+    # fp16 output from the same bf16 input: the same fp32 values rounded to fp16.
+    y16 = oracle.w8a8_linear(x_bits, wq, s_w, 0, x_dtype="bf16", y_dtype="f16")
+    assert np.array_equal(y16.view(np.uint16), t.astype(np.float16).view(np.uint16))
