@@ -62,7 +62,13 @@ typedef enum cider_status {
     CIDER_ERR_WORKSPACE = 5    /* workspace pointer missing or smaller than required */
 } cider_status;
 
-#define CIDER_ABI_VERSION 1
+#define CIDER_ABI_VERSION 2
+
+/* Element types of activations and layer outputs (README roadmap: automatic
+ * dtype handling, float16 / bfloat16). Both convert exactly to fp32; an
+ * output is the fp32 epilogue value rounded to nearest even in that type. */
+#define CIDER_DTYPE_F16 0
+#define CIDER_DTYPE_BF16 1
 
 /* Human-readable name of a status code (static string, never NULL). */
 CIDER_API const char* cider_status_string(int status);
@@ -163,6 +169,30 @@ CIDER_API cider_status cider_w4a8_gemm(const void* x_f16, int64_t M, int64_t N, 
  * bits 4: K % 32 == 0, group_size 0 or a multiple of 32 likewise.
  * Needs no workspace.
  */
+/*
+ * The linear layer for either activation / output element type: as
+ * cider_w8a8_gemm_pc (bits 8, group_size 0), cider_w8a8_gemm_pg (bits 8,
+ * group_size > 0) or cider_w4a8_gemm (bits 4), with x [M,K] of element type
+ * x_dtype and y [M,N] written as y_dtype (CIDER_DTYPE_F16 or
+ * CIDER_DTYPE_BF16; any combination). The quantization reads each element's
+ * exact fp32 value; the epilogue is the same fp32 arithmetic, rounded to the
+ * output type. M == 1 runs the GEMV. Same workspace, alignment and shape
+ * rules as the fp16 entry points; an unknown dtype or bits gives
+ * CIDER_ERR_INVALID_ARG.
+ */
+CIDER_API cider_status cider_linear(const void* x, int32_t x_dtype, int64_t M, int64_t N,
+                                    int64_t K, const void* w, int32_t bits, const float* s_w,
+                                    int32_t group_size, void* y, int32_t y_dtype, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/*
+ * cider_quantize_act for either element type of x (CIDER_DTYPE_F16 or
+ * CIDER_DTYPE_BF16): per-token INT8 codes q [M,K] and scales s_a [M] of the
+ * exact fp32 values.
+ */
+CIDER_API cider_status cider_quantize_act_ex(const void* x, int32_t x_dtype, int64_t M, int64_t K,
+                                             int8_t* q, float* s_a, void* stream);
+
 CIDER_API cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, const void* w,
                              const float* s_w, int32_t bits, int32_t group_size, void* y_f16,
                              void* stream);

@@ -220,7 +220,7 @@ static float quantize_block_t(const uint16_t* v, int64_t n, float qmax, int8_t* 
             out[k] = 0;
         return 0.0f;
     }
-    float scale = absmax / qmax;
+    float scale = absmax / qmax; /* never 0 here: absmax >= 2^-133 (bf16), 2^-24 (fp16) */
     for (int64_t k = 0; k < n; ++k) {
         float x = elem_to_float(v[k], dtype);
         float r = rintf(x / scale);

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert cider.abi_version() == 1
+    assert cider.abi_version() == 2
     for code, name in [(0, "CIDER_OK"), (1, "CIDER_ERR_INVALID_ARG"),
                        (2, "CIDER_ERR_UNSUPPORTED"), (3, "CIDER_ERR_CUDA"),
                        (4, "CIDER_ERR_TIMEOUT"), (5, "CIDER_ERR_WORKSPACE"), (99, "CIDER_ERR_UNKNOWN")]:
@@ -68,3 +68,15 @@ def test_null_and_size_checks_precede_cuda(lib):
     assert lib.cider_int8_gemv(p, 16, 16, p, p, 5, 0, p, None) == 1
     assert lib.cider_test_wait_timeout(0, None) == 1
     assert lib.cider_test_gemm_s32(p, p, 4, 4, 64, 7, 0, p, p, 1 << 20, None) == 1
+
+
+def test_element_type_checks_precede_cuda(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: checks fail first
+    # unknown activation / output element types, unknown weight width
+    assert lib.cider_linear(p, 2, 4, 16, 16, p, 8, p, 0, p, 0, p, 1 << 20, None) == 1
+    assert lib.cider_linear(p, 0, 4, 16, 16, p, 8, p, 0, p, -1, p, 1 << 20, None) == 1
+    assert lib.cider_linear(p, 1, 4, 16, 16, p, 5, p, 0, p, 1, p, 1 << 20, None) == 1
+    assert lib.cider_linear(None, 1, 4, 16, 16, p, 8, p, 0, p, 1, p, 1 << 20, None) == 1
+    assert lib.cider_quantize_act_ex(p, 3, 4, 16, p, p, None) == 1
+    assert lib.cider_quantize_act_ex(None, 1, 4, 16, p, p, None) == 1
+    assert lib.cider_quantize_act_ex(p, 1, 0, 16, p, p, None) == 1

@@ -407,3 +407,16 @@ def test_bf16_layer_epilogue_against_numpy_float32():
     # fp16 output from the same bf16 input: the same fp32 values rounded to fp16.
     y16 = oracle.w8a8_linear(x_bits, wq, s_w, 0, x_dtype="bf16", y_dtype="f16")
     assert np.array_equal(y16.view(np.uint16), t.astype(np.float16).view(np.uint16))
+
+
+def test_bf16_subnormal_scale_closed_form():
+    """bf16 reaches values whose scale absmax / 127 is an fp32 subnormal: with
+    u = 2^-149, absmax = 3 * 2^-133 = 196608 u gives s = rint(196608 / 127) u
+    = 1548 u, and the codes are rint(x / s): 65536 / 1548 = 42.3 -> 42,
+    196608 / 1548 = 127.0 -> 127."""
+    u = 2.0 ** -149
+    x = oracle.float_to_bf16(np.array([2.0 ** -133, -2.0 ** -133, 0.0, 3 * 2.0 ** -133],
+                                      dtype=np.float32))
+    q, s = oracle.quantize_act_bf16(x.reshape(1, 4))
+    assert float(s[0]) == 1548 * u
+    assert q.tolist() == [[42, -42, 0, 127]]

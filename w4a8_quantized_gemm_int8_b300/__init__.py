@@ -24,12 +24,16 @@ ABI_FUNCTIONS = (
     "cider_status_string", "cider_abi_version", "cider_quantize_act",
     "cider_quantize_weight_int8", "cider_pack_weight_int4", "cider_workspace_bytes",
     "cider_w8a8_gemm_pc", "cider_w8a8_gemm_pg", "cider_w4a8_gemm", "cider_int8_gemv",
+    "cider_linear", "cider_quantize_act_ex",
     "cider_w8a8_gemm_pc_noalloc",
     "cider_act_image", "cider_weight_image", "cider_gemm_images",
     "cider_test_gemm_s32", "cider_device_status", "cider_test_wait_timeout",
 )
 
 CIDER_OK = 0
+CIDER_DTYPE_F16 = 0
+CIDER_DTYPE_BF16 = 1
+_DTYPE_CODES = {torch.float16: CIDER_DTYPE_F16, torch.bfloat16: CIDER_DTYPE_BF16}
 CIDER_ERR_INVALID_ARG = 1
 CIDER_ERR_UNSUPPORTED = 2
 CIDER_ERR_CUDA = 3
@@ -68,6 +72,9 @@ def load_library():
             "cider_w8a8_gemm_pg": ([p, i64, i64, i64, p, p, i32, p, p, sz, p], ctypes.c_int),
             "cider_w4a8_gemm": ([p, i64, i64, i64, p, p, i32, p, p, sz, p], ctypes.c_int),
             "cider_int8_gemv": ([p, i64, i64, p, p, i32, i32, p, p], ctypes.c_int),
+            "cider_linear": ([p, i32, i64, i64, i64, p, i32, p, i32, p, i32, p, sz, p],
+                             ctypes.c_int),
+            "cider_quantize_act_ex": ([p, i32, i64, i64, p, p, p], ctypes.c_int),
             "cider_w8a8_gemm_pc_noalloc": ([p, i64, i64, i64, p, p, p, p], ctypes.c_int),
             "cider_act_image": ([p, i64, i64, p, p, p], ctypes.c_int),
             "cider_weight_image": ([p, i64, i64, i32, p, p], ctypes.c_int),
@@ -201,6 +208,47 @@ def w8a8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor, group_size
         st = lib.cider_w8a8_gemm_pg(xp, M, N, K, wp, sp, group_size, yp, wsp, wsn, _stream())
         _check("cider_w8a8_gemm_pg", st)
     return y
+
+
+def linear(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
+           group_size: int = 0, out_dtype: torch.dtype | None = None,
+           out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """The quantized linear layer for fp16 or bf16 activations x [M,K]:
+    w int8 [N,K] (bits 8) or packed uint8 [N,K/2] (bits 4), per-channel
+    (group_size 0, s_w [N]) or per-group (s_w [N, K/gs]); y [M,N] in
+    out_dtype (fp16 or bf16; default: x's dtype). M == 1 runs the GEMV."""
+    if x.dtype not in _DTYPE_CODES:
+        raise ValueError(f"x must be float16 or bfloat16, got {x.dtype}")
+    out_dtype = out_dtype or x.dtype
+    if out_dtype not in _DTYPE_CODES:
+        raise ValueError(f"out_dtype must be float16 or bfloat16, got {out_dtype}")
+    M, K = x.shape
+    N = w.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=x.device)
+    need = workspace_bytes(M, N, K, bits, group_size)
+    buf = ws if ws is not None else _workspace(need, x.device)
+    wsp, wsn = (buf.data_ptr(), buf.numel()) if buf is not None else (None, 0)
+    wdt = torch.int8 if bits == 8 else torch.uint8
+    st = load_library().cider_linear(
+        _dev(x, x.dtype, "x", 2), _DTYPE_CODES[x.dtype], M, N, K, _dev(w, wdt, "w", 2), bits,
+        _dev(s_w, torch.float32, "s_w"), group_size, _dev(y, out_dtype, "y", 2),
+        _DTYPE_CODES[out_dtype], wsp, wsn, _stream())
+    _check("cider_linear", st)
+    return y
+
+
+def quantize_act_any(x: torch.Tensor):
+    """Per-token INT8 quantization of fp16 or bf16 activations: (q int8
+    [M,K], s_a fp32 [M])."""
+    if x.dtype not in _DTYPE_CODES:
+        raise ValueError(f"x must be float16 or bfloat16, got {x.dtype}")
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    s = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check("cider_quantize_act_ex", load_library().cider_quantize_act_ex(
+        _dev(x, x.dtype, "x", 2), _DTYPE_CODES[x.dtype], M, K, q.data_ptr(), s.data_ptr(),
+        _stream()))
+    return q, s
 
 
 STATIC_SCRATCH_BYTES = 64 << 20

@@ -78,9 +78,15 @@ bool valid_group(int32_t gs, int64_t K, int multiple) {
 }
 
 // Shared body of the three GEMM entry points.
-cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const void* w, int bits,
-                         const float* s_w, int32_t gs, void* y, void* ws, size_t ws_bytes,
-                         cudaStream_t stream) {
+bool valid_dtype(int32_t d) { return d == CIDER_DTYPE_F16 || d == CIDER_DTYPE_BF16; }
+
+ElemType elem(int32_t d) { return d == CIDER_DTYPE_BF16 ? ElemType::kBF16 : ElemType::kF16; }
+
+// Shared body of the layer entry points (x / y element types: CIDER_DTYPE_*).
+cider_status gemm_common(const void* x, int32_t x_dtype, int64_t M, int64_t N, int64_t K,
+                         const void* w, int bits, const float* s_w, int32_t gs, void* y,
+                         int32_t y_dtype, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!valid_dtype(x_dtype) || !valid_dtype(y_dtype)) return CIDER_ERR_INVALID_ARG;
     if (!x || !w || !s_w || !y) return CIDER_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || gs < 0) return CIDER_ERR_INVALID_ARG;
     if (K % 16 != 0 || (bits == 4 && K % 32 != 0)) return CIDER_ERR_UNSUPPORTED;
@@ -95,8 +101,8 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
         if (K > 16384 || !valid_group(gs, K, bits == 8 ? 16 : 32)) return CIDER_ERR_UNSUPPORTED;
         unsigned long long* status = nullptr;
         if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
-        GemvArgs g{static_cast<const __half*>(x), K, N, w, s_w, bits, gs,
-                   static_cast<__half*>(y), kWaitTimeoutNs, status};
+        GemvArgs g{x, K, N, w, s_w, bits, gs, y, kWaitTimeoutNs, status,
+                   x_dtype == CIDER_DTYPE_BF16, y_dtype == CIDER_DTYPE_BF16};
         return from_cuda(launch_gemv(g, sms, stream));
     }
     // A group's partial sum must stay exact in the tensor core's fp32
@@ -112,7 +118,7 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
     // tokens): activation image only; the GEMM widens the raw weight codes.
     Workspace wsp = carve(ws, M, N, K, gs);
     const bool img = wsp.b_img != nullptr;
-    cudaError_t e = launch_operand_images(static_cast<const __half*>(x), M, K, img ? w : nullptr,
+    cudaError_t e = launch_operand_images(x, elem(x_dtype), M, K, img ? w : nullptr,
                                           bits, N, wsp.a_img, wsp.s_a, wsp.b_img, s_w, wsp.s_wT,
                                           gs > 0 ? K / gs : 1, sms, stream);
     if (e != cudaSuccess) return from_cuda(e);
@@ -132,6 +138,7 @@ cider_status gemm_common(const void* x, int64_t M, int64_t N, int64_t K, const v
     a.mode = (gs == 0) ? GemmMode::kPcF16 : GemmMode::kPgF16;
     a.timeout_ns = kWaitTimeoutNs;
     a.status = status;
+    a.out_bf16 = (y_dtype == CIDER_DTYPE_BF16);
     return from_cuda(launch_gemm(a, sms, stream));
 }
 
@@ -160,7 +167,7 @@ cider_status cider_quantize_act(const void* x_f16, int64_t M, int64_t K, int8_t*
     int sms = 0;
     cider_status st = num_sms(&sms);
     if (st != CIDER_OK) return st;
-    return from_cuda(launch_quant_groups(static_cast<const __half*>(x_f16), M, K, K, 127,
+    return from_cuda(launch_quant_groups(x_f16, ElemType::kF16, M, K, K, 127,
                                          QuantOut::kInt8, q, s_a, sms,
                                          static_cast<cudaStream_t>(stream)));
 }
@@ -175,7 +182,7 @@ cider_status cider_quantize_weight_int8(const void* w_f16, int64_t N, int64_t K,
     cider_status st = num_sms(&sms);
     if (st != CIDER_OK) return st;
     const int64_t gs = group_size ? group_size : K;
-    return from_cuda(launch_quant_groups(static_cast<const __half*>(w_f16), N, K, gs, 127,
+    return from_cuda(launch_quant_groups(w_f16, ElemType::kF16, N, K, gs, 127,
                                          QuantOut::kInt8, wq, s_w, sms,
                                          static_cast<cudaStream_t>(stream)));
 }
@@ -190,7 +197,7 @@ cider_status cider_pack_weight_int4(const void* w_f16, int64_t N, int64_t K, int
     cider_status st = num_sms(&sms);
     if (st != CIDER_OK) return st;
     const int64_t gs = group_size ? group_size : K;
-    return from_cuda(launch_quant_groups(static_cast<const __half*>(w_f16), N, K, gs, 7,
+    return from_cuda(launch_quant_groups(w_f16, ElemType::kF16, N, K, gs, 7,
                                          QuantOut::kInt4, wp, s_w, sms,
                                          static_cast<cudaStream_t>(stream)));
 }
@@ -204,7 +211,8 @@ size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bits, int3
 cider_status cider_w8a8_gemm_pc(const void* x_f16, int64_t M, int64_t N, int64_t K,
                                 const int8_t* wq, const float* s_w, void* y_f16, void* ws,
                                 size_t ws_bytes, void* stream) {
-    return gemm_common(x_f16, M, N, K, wq, 8, s_w, 0, y_f16, ws, ws_bytes,
+    return gemm_common(x_f16, CIDER_DTYPE_F16, M, N, K, wq, 8, s_w, 0, y_f16, CIDER_DTYPE_F16,
+                       ws, ws_bytes,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -212,15 +220,36 @@ cider_status cider_w8a8_gemm_pg(const void* x_f16, int64_t M, int64_t N, int64_t
                                 const int8_t* wq, const float* s_w, int32_t group_size,
                                 void* y_f16, void* ws, size_t ws_bytes, void* stream) {
     if (group_size <= 0) return CIDER_ERR_INVALID_ARG;
-    return gemm_common(x_f16, M, N, K, wq, 8, s_w, group_size, y_f16, ws, ws_bytes,
+    return gemm_common(x_f16, CIDER_DTYPE_F16, M, N, K, wq, 8, s_w, group_size, y_f16,
+                       CIDER_DTYPE_F16, ws, ws_bytes,
                        static_cast<cudaStream_t>(stream));
 }
 
 cider_status cider_w4a8_gemm(const void* x_f16, int64_t M, int64_t N, int64_t K,
                              const uint8_t* wp, const float* s_w, int32_t group_size, void* y_f16,
                              void* ws, size_t ws_bytes, void* stream) {
-    return gemm_common(x_f16, M, N, K, wp, 4, s_w, group_size, y_f16, ws, ws_bytes,
+    return gemm_common(x_f16, CIDER_DTYPE_F16, M, N, K, wp, 4, s_w, group_size, y_f16,
+                       CIDER_DTYPE_F16, ws, ws_bytes,
                        static_cast<cudaStream_t>(stream));
+}
+
+cider_status cider_linear(const void* x, int32_t x_dtype, int64_t M, int64_t N, int64_t K,
+                          const void* w, int32_t bits, const float* s_w, int32_t group_size,
+                          void* y, int32_t y_dtype, void* ws, size_t ws_bytes, void* stream) {
+    if (bits != 8 && bits != 4) return CIDER_ERR_INVALID_ARG;
+    return gemm_common(x, x_dtype, M, N, K, w, bits, s_w, group_size, y, y_dtype, ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+cider_status cider_quantize_act_ex(const void* x, int32_t x_dtype, int64_t M, int64_t K,
+                                   int8_t* q, float* s_a, void* stream) {
+    if (!x || !q || !s_a) return CIDER_ERR_INVALID_ARG;
+    if (M <= 0 || K <= 0 || !valid_dtype(x_dtype)) return CIDER_ERR_INVALID_ARG;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    return from_cuda(launch_quant_groups(x, elem(x_dtype), M, K, K, 127, QuantOut::kInt8, q, s_a,
+                                         sms, static_cast<cudaStream_t>(stream)));
 }
 
 cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, const void* w,
@@ -237,8 +266,7 @@ cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, const void
     if (st != CIDER_OK) return st;
     unsigned long long* status = nullptr;
     if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
-    GemvArgs g{static_cast<const __half*>(x_f16), K, N, w, s_w, bits, group_size,
-               static_cast<__half*>(y_f16), kWaitTimeoutNs, status};
+    GemvArgs g{x_f16, K, N, w, s_w, bits, group_size, y_f16, kWaitTimeoutNs, status, 0, 0};
     return from_cuda(launch_gemv(g, sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -250,7 +278,7 @@ cider_status cider_act_image(const void* x_f16, int64_t M, int64_t K, void* a_im
     int sms = 0;
     cider_status st = num_sms(&sms);
     if (st != CIDER_OK) return st;
-    return from_cuda(launch_quant_groups(static_cast<const __half*>(x_f16), M, K, K, 127,
+    return from_cuda(launch_quant_groups(x_f16, ElemType::kF16, M, K, K, 127,
                                          QuantOut::kF16, a_img, s_a, sms,
                                          static_cast<cudaStream_t>(stream)));
 }

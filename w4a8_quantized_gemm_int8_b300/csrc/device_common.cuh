@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 namespace cider {
@@ -59,6 +60,44 @@ __device__ __forceinline__ int quant_code(float x, float s, float r, int qmax) {
 
 // The reciprocal quant_code expects (0 for an all-zero block).
 __device__ __forceinline__ float quant_recip(float s) { return s == 0.0f ? 0.0f : __frcp_rn(s); }
+
+// ----------------------------------------------------------------------------
+// 16-bit floating-point element types of activations and outputs: fp16
+// (__half) and bfloat16 (__nv_bfloat16). Both convert exactly to fp32.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float elem_to_float(__half v) { return __half2float(v); }
+__device__ __forceinline__ float elem_to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// Largest |value| of the eight elements of a 16-byte vector (exact).
+template <typename T>
+__device__ __forceinline__ float vec8_absmax(const uint4& u);
+template <>
+__device__ __forceinline__ float vec8_absmax<__half>(const uint4& u) {
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+    __half2 m = __habs2(h[0]);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) m = __hmax2(m, __habs2(h[i]));
+    return fmaxf(__low2float(m), __high2float(m));
+}
+template <>
+__device__ __forceinline__ float vec8_absmax<__nv_bfloat16>(const uint4& u) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    __nv_bfloat162 m = __habs2(h[0]);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) m = __hmax2(m, __habs2(h[i]));
+    return fmaxf(__low2float(m), __high2float(m));
+}
+
+// Two fp32 values rounded (to nearest even) to a packed pair of output
+// elements, the first in the low half.
+__device__ __forceinline__ uint32_t pack2_rn(float a, float b, bool bf16) {
+    if (bf16) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&v);
+    }
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 // ----------------------------------------------------------------------------
 // mbarrier

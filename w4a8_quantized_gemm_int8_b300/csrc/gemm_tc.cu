@@ -130,6 +130,7 @@ struct Params {
     const float* s_wT;  // group-major copy of per-group s_w, or NULL
     void* out;
     int tma_store;  // fp16 output written through tmap_y (N % 8 == 0)
+    int out_bf16;   // output elements are bfloat16 instead of fp16
     uint64_t timeout_ns;
     unsigned long long* status;
 };
@@ -606,8 +607,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     fmul2_rn(y0, y1, __uint_as_float(ac[j]),
                                              __uint_as_float(ac[j + 1]), sa, sa);
                                 }
-                                const __half2 hv = __floats2half2_rn(y0, y1);
-                                h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                                h2[j / 2] = pack2_rn(y0, y1, p.out_bf16 != 0);
                             }
                             if (p.tma_store) {
                                 if (m_base < p.M && n_c < p.N) {  // warp-uniform
@@ -630,8 +630,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     store_pending = true;
                                 }
                             } else if (m < p.M) {
-                                __half* out = static_cast<__half*>(p.out) + (int64_t)m * p.N;
-                                const __half* hh = reinterpret_cast<const __half*>(h2);
+                                uint16_t* out = static_cast<uint16_t*>(p.out) + (int64_t)m * p.N;
+                                const uint16_t* hh = reinterpret_cast<const uint16_t*>(h2);
 #pragma unroll
                                 for (int j = 0; j < 32; ++j)
                                     if (n_c + j < p.N) out[n_c + j] = hh[j];
@@ -804,6 +804,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     p.s_wT = per_group ? a.s_wT : nullptr;
     p.out = a.out;
     p.tma_store = tma_store ? 1 : 0;
+    p.out_bf16 = a.out_bf16;
     p.timeout_ns = a.timeout_ns;
     p.status = a.status;
     const int tiles = p.tiles_m * p.tiles_n;

@@ -118,6 +118,7 @@ struct Params {
     const float* s_wT;  // optional group-major copy of per-group scales [G, N]
     void* out;
     int tma_store;  // fp16 output written through tmap_y (N % 8 == 0)
+    int out_bf16;   // output elements are bfloat16 instead of fp16
     uint64_t timeout_ns;
     unsigned long long* status;
 };
@@ -514,8 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                                     fmul2_rn(y0, y1, __uint_as_float(acc[c]), __uint_as_float(acc[c + 1]),
                                              sa, sa);
                                 }
-                                const __half2 hv = __floats2half2_rn(y0, y1);
-                                h2[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                                h2[j / 2] = pack2_rn(y0, y1, p.out_bf16 != 0);
                             }
                             if (p.tma_store) {
                                 // The staging buffer is free once the previous
@@ -537,8 +537,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                                 }
                                 store_pending = true;
                             } else if (m < p.M) {
-                                __half* out = static_cast<__half*>(p.out) + (int64_t)m * p.N;
-                                const __half* hh = reinterpret_cast<const __half*>(h2);
+                                uint16_t* out = static_cast<uint16_t*>(p.out) + (int64_t)m * p.N;
+                                const uint16_t* hh = reinterpret_cast<const uint16_t*>(h2);
 #pragma unroll
                                 for (int j = 0; j < 32; ++j)
                                     if (n_half + r * 32 + j < p.N) out[n_half + r * 32 + j] = hh[j];
@@ -664,6 +664,7 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
                                                                                    : nullptr;
     p.out = a.out;
     p.tma_store = tma_store ? 1 : 0;
+    p.out_bf16 = a.out_bf16;
     p.timeout_ns = a.timeout_ns;
     p.status = a.status;
     switch (a.mode) {

@@ -44,13 +44,14 @@ static_assert(kMaxK % (8 * kConsumers) == 0, "x vectors per thread");
 constexpr int kEarlyStages = 2;  // copies issued before x is in registers
 
 struct Params {
-    const __half* x;
+    const void* x;     // fp16 or bf16 (kernel template parameter)
     int K, N;
     const uint8_t* w;  // row-major, row_bytes per row
     const float* s_w;
     int G;             // columns of s_w (1 for per-channel)
     int cpg;           // 16-byte chunks per group (per-group only)
-    __half* y;
+    void* y;           // fp16, or bf16 with y_bf16
+    int y_bf16;
     int row_bytes;
     int rows_per_stage;
     int stage_bytes;     // weights + staged scales, 128-byte multiple
@@ -107,7 +108,15 @@ __device__ __forceinline__ int chunk_dot(const uint4& wv, const uint4* codes, in
     }
 }
 
-template <int BITS, bool PG>
+// One output element, rounded to nearest even as fp16 or bf16.
+__device__ __forceinline__ void store_y(const Params& p, int n, float v) {
+    if (p.y_bf16)
+        static_cast<__nv_bfloat16*>(p.y)[n] = __float2bfloat16_rn(v);
+    else
+        static_cast<__half*>(p.y)[n] = __float2half_rn(v);
+}
+
+template <typename T, int BITS, bool PG>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     int8_t* codes_s = reinterpret_cast<int8_t*>(smem + p.codes_off);
@@ -203,14 +212,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
             const int v = threadIdx.x + i * kConsumers;
             xr[i] = (v < nvec) ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
         }
-        __half2 hm = __float2half2_rn(0.0f);
+        float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kXVec; ++i) {
-            const __half2* h = reinterpret_cast<const __half2*>(&xr[i]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) hm = __hmax2(hm, __habs2(h[j]));
-        }
-        float m = fmaxf(__low2float(hm), __high2float(hm));
+        for (int i = 0; i < kXVec; ++i) m = fmaxf(m, vec8_absmax<T>(xr[i]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) red_s[warp] = m;
@@ -225,11 +229,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
         for (int i = 0; i < kXVec; ++i) {
             const int v = threadIdx.x + i * kConsumers;
             if (v >= nvec) break;
-            const __half* h = reinterpret_cast<const __half*>(&xr[i]);
+            const T* h = reinterpret_cast<const T*>(&xr[i]);
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int q = quant_code(__half2float(h[j]), s, r, 127);
+                const int q = quant_code(elem_to_float(h[j]), s, r, 127);
                 if (j < 4)
                     lo |= (uint32_t)(q & 0xFF) << (8 * j);
                 else
@@ -282,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
                     if (lane == 0)
-                        p.y[n] = __float2half_rn(
-                            __fmul_rn(__fmul_rn(__int2float_rn(acc), s_a),
-                                      p.sw_in_smem ? sw_s[n - n0] : __ldg(p.s_w + n)));
+                        store_y(p, n,
+                                __fmul_rn(__fmul_rn(__int2float_rn(acc), s_a),
+                                          p.sw_in_smem ? sw_s[n - n0] : __ldg(p.s_w + n)));
                 } else {
                     const float* srow =
                         p.scales_staged
@@ -314,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
                     if (lane == 0) {
                         float f = 0.0f;
                         for (int g = 0; g < p.G; ++g) f = __fadd_rn(f, prod[g]);
-                        p.y[n] = __float2half_rn(__fmul_rn(f, s_a));
+                        store_y(p, n, __fmul_rn(f, s_a));
                     }
                     __syncwarp();
                 }
@@ -327,9 +331,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
 
 int g_max_smem = 0;  // opt-in shared memory per block (queried once; same on every B300)
 
-template <int BITS, bool PG>
+template <typename T, int BITS, bool PG>
 cudaError_t launch_one(const Params& p, int grid, int smem, cudaStream_t stream) {
-    auto kern = gemv_kernel<BITS, PG>;
+    auto kern = gemv_kernel<T, BITS, PG>;
     static int attr_smem = 0;  // benign race: setting the same value twice
     if (attr_smem < smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -338,6 +342,16 @@ cudaError_t launch_one(const Params& p, int grid, int smem, cudaStream_t stream)
         attr_smem = g_max_smem;
     }
     return launch_pdl(kern, grid, kThreads, smem, stream, p);
+}
+
+template <typename T>
+cudaError_t launch_bits(const Params& p, int bits, bool pg, int grid, int smem,
+                        cudaStream_t stream) {
+    if (bits == 8)
+        return pg ? launch_one<T, 8, true>(p, grid, smem, stream)
+                  : launch_one<T, 8, false>(p, grid, smem, stream);
+    return pg ? launch_one<T, 4, true>(p, grid, smem, stream)
+              : launch_one<T, 4, false>(p, grid, smem, stream);
 }
 
 }  // namespace
@@ -362,6 +376,7 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     p.w = static_cast<const uint8_t*>(a.w);
     p.s_w = a.s_w;
     p.y = a.y;
+    p.y_bf16 = a.y_bf16;
     p.timeout_ns = a.timeout_ns;
     p.status = a.status;
     if (a.group_size == 0) {
@@ -405,12 +420,8 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     if (ns < 1) return cudaErrorInvalidValue;
     p.num_stages = ns;
     const int smem = p.stage_off + ns * p.stage_bytes;
-
-    if (a.bits == 8)
-        return pg ? launch_one<8, true>(p, grid, smem, stream)
-                  : launch_one<8, false>(p, grid, smem, stream);
-    return pg ? launch_one<4, true>(p, grid, smem, stream)
-              : launch_one<4, false>(p, grid, smem, stream);
+    return a.x_bf16 ? launch_bits<__nv_bfloat16>(p, a.bits, pg, grid, smem, stream)
+                    : launch_bits<__half>(p, a.bits, pg, grid, smem, stream);
 }
 
 }  // namespace cider

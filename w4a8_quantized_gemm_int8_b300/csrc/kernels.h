@@ -32,13 +32,16 @@ cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t sm
 
 enum class QuantOut : int { kInt8 = 0, kF16 = 1, kInt4 = 2 };
 
-// Symmetric quantization of `rows` x K fp16 values in groups of `gs`
-// consecutive elements of a row (gs == K: one group per row), scale =
+// 16-bit floating-point element type of activations (and of layer outputs).
+enum class ElemType : int { kF16 = 0, kBF16 = 1 };
+
+// Symmetric quantization of `rows` x K fp16 (or bf16) values in groups of
+// `gs` consecutive elements of a row (gs == K: one group per row), scale =
 // absmax / qmax; codes written as int8, as exact fp16 integers, or as packed
 // nibbles (code + 8, two per byte). scales: [rows, K / gs].
-cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int64_t gs, int qmax,
-                                QuantOut out_kind, void* out, float* scales, int num_sms,
-                                cudaStream_t stream);
+cudaError_t launch_quant_groups(const void* src, ElemType src_type, int64_t rows, int64_t K,
+                                int64_t gs, int qmax, QuantOut out_kind, void* out,
+                                float* scales, int num_sms, cudaStream_t stream);
 
 // Both operand images of the tensor-core GEMM in one launch: x fp16 [M,K] ->
 // a_img (exact fp16 codes) + s_a, and weights (INT8 [N,K] or packed INT4
@@ -46,7 +49,8 @@ cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int6
 // non-NULL also the group-major copy s_wT [G,N] of per-group scales s_w
 // [N,G]. Falls back to separate launches for shapes the fused kernel does
 // not take.
-cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const void* w, int bits,
+cudaError_t launch_operand_images(const void* x, ElemType x_type, int64_t M, int64_t K,
+                                  const void* w, int bits,
                                   int64_t N, __half* a_img, float* s_a, __half* b_img,
                                   const float* s_w, float* s_wT, int64_t G, int num_sms,
                                   cudaStream_t stream);
@@ -81,6 +85,7 @@ struct GemmArgs {
     // (b_bits 8) or packed INT4 [N, K/2] (b_bits 4), widened on chip.
     const void* b_raw;
     int b_bits;
+    int out_bf16;  // fp16-output modes: write bfloat16 instead of fp16
 };
 
 cudaError_t launch_gemm_tc(const GemmArgs& args, int num_sms, cudaStream_t stream);
@@ -95,15 +100,17 @@ bool gemm_uses_pair(int64_t M);
 
 // ---- M = 1 GEMV (quantizes x per CTA, int32 dot products, same epilogue) ----
 struct GemvArgs {
-    const __half* x;     // [K]
+    const void* x;       // [K] fp16, or bf16 with x_bf16
     int64_t K, N;
     const void* w;       // int8 [N, K] or packed int4 [N, K/2]
     const float* s_w;    // [N] or [N, K/gs]
     int bits;            // 8 or 4
     int group_size;      // 0, 64 or 128 (w4: 0 or 128, any multiple of 32)
-    __half* y;           // [N]
+    void* y;             // [N] fp16, or bf16 with y_bf16
     uint64_t timeout_ns;          // bound on every device-side wait
     unsigned long long* status;   // device status word
+    int x_bf16;
+    int y_bf16;
 };
 
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);

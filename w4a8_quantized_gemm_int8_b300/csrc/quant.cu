@@ -62,10 +62,10 @@ __device__ __forceinline__ void store_code1(void* out, int64_t elem, int q) {
     }
 }
 
-// One warp per (row, group). Vector path: 16-byte loads of 8 fp16 values;
-// requires K % 8 == 0 and gs % 8 == 0 (the host checks alignment).
-template <QuantOut OUT>
-__global__ void __launch_bounds__(256) quant_groups_vec_kernel(const __half* __restrict__ src,
+// One warp per (row, group). Vector path: 16-byte loads of 8 fp16 (or bf16)
+// values; requires K % 8 == 0 and gs % 8 == 0 (the host checks alignment).
+template <typename T, QuantOut OUT>
+__global__ void __launch_bounds__(256) quant_groups_vec_kernel(const T* __restrict__ src,
                                                                int64_t rows, int64_t K, int64_t gs,
                                                                int qmax, void* __restrict__ out,
                                                                float* __restrict__ scales) {
@@ -78,24 +78,18 @@ __global__ void __launch_bounds__(256) quant_groups_vec_kernel(const __half* __r
         const int64_t row = item / G, g = item - row * G;
         const int64_t base = row * K + g * gs;
         const uint4* p = reinterpret_cast<const uint4*>(src + base);
-        __half2 hm = __float2half2_rn(0.0f);
-        for (int64_t v = lane; v < nvec; v += 32) {
-            uint4 u = __ldg(p + v);
-            const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) hm = __hmax2(hm, __habs2(h[i]));
-        }
-        float amax = fmaxf(__low2float(hm), __high2float(hm));
+        float amax = 0.0f;
+        for (int64_t v = lane; v < nvec; v += 32) amax = fmaxf(amax, vec8_absmax<T>(__ldg(p + v)));
         amax = warp_max(amax);
         const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
         const float r = quant_recip(s);
         if (lane == 0) scales[item] = s;
         for (int64_t v = lane; v < nvec; v += 32) {
             uint4 u = __ldg(p + v);
-            const __half* h = reinterpret_cast<const __half*>(&u);
+            const T* h = reinterpret_cast<const T*>(&u);
             int q[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = quant_one(__half2float(h[i]), s, r, qmax);
+            for (int i = 0; i < 8; ++i) q[i] = quant_one(elem_to_float(h[i]), s, r, qmax);
             store_codes8<OUT>(out, base + v * 8, q);
         }
     }
@@ -106,8 +100,8 @@ __global__ void __launch_bounds__(256) quant_groups_vec_kernel(const __half* __r
 // use), reduced to its absmax, and quantized from the registers. WPR = 1: one
 // warp per row (K <= 256 * VPT); WPR = 8: the whole 256-thread block per row
 // (K <= 2048 * VPT). Same arithmetic as quant_groups_vec_kernel.
-template <QuantOut OUT, int VPT, int WPR>
-__device__ __forceinline__ void quant_rows_reg_body(const __half* __restrict__ src, int64_t rows,
+template <typename T, QuantOut OUT, int VPT, int WPR>
+__device__ __forceinline__ void quant_rows_reg_body(const T* __restrict__ src, int64_t rows,
                                                     int64_t K, int qmax, void* __restrict__ out,
                                                     float* __restrict__ scales, int block,
                                                     int nblocks) {
@@ -127,14 +121,9 @@ __device__ __forceinline__ void quant_rows_reg_body(const __half* __restrict__ s
             const int64_t c = t + (int64_t)i * kThreadsPerRow;
             v[i] = (c < nvec) ? __ldg(p + c) : make_uint4(0u, 0u, 0u, 0u);
         }
-        __half2 hm = __float2half2_rn(0.0f);
+        float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) hm = __hmax2(hm, __habs2(h[j]));
-        }
-        float amax = fmaxf(__low2float(hm), __high2float(hm));
+        for (int i = 0; i < VPT; ++i) amax = fmaxf(amax, vec8_absmax<T>(v[i]));
         amax = warp_max(amax);
         if constexpr (WPR == 8) {
             if (lane == 0) red_s[warp] = amax;
@@ -153,12 +142,12 @@ __device__ __forceinline__ void quant_rows_reg_body(const __half* __restrict__ s
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int64_t c = t + (int64_t)i * kThreadsPerRow;
-            const __half* h = reinterpret_cast<const __half*>(&v[i]);
+            const T* h = reinterpret_cast<const T*>(&v[i]);
             int q[8];
             bool near = false;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float tq = __fmul_rn(__half2float(h[j]), r);
+                const float tq = __fmul_rn(elem_to_float(h[j]), r);
                 const float rq = rintf(tq);
                 near |= !(fabsf(tq - rq) < 0.5f - 0x1p-12f);
                 q[j] = (int)rq;
@@ -166,7 +155,7 @@ __device__ __forceinline__ void quant_rows_reg_body(const __half* __restrict__ s
             if (__any_sync(0xffffffffu, near)) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    q[j] = (s == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(__half2float(h[j]), s));
+                    q[j] = (s == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(elem_to_float(h[j]), s));
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) q[j] = max(-qmax, min(qmax, q[j]));
@@ -175,19 +164,19 @@ __device__ __forceinline__ void quant_rows_reg_body(const __half* __restrict__ s
     }
 }
 
-template <QuantOut OUT, int VPT, int WPR>
-__global__ void __launch_bounds__(256) quant_rows_reg_kernel(const __half* __restrict__ src,
+template <typename T, QuantOut OUT, int VPT, int WPR>
+__global__ void __launch_bounds__(256) quant_rows_reg_kernel(const T* __restrict__ src,
                                                              int64_t rows, int64_t K, int qmax,
                                                              void* __restrict__ out,
                                                              float* __restrict__ scales) {
     grid_dep_wait();
     grid_dep_launch();
-    quant_rows_reg_body<OUT, VPT, WPR>(src, rows, K, qmax, out, scales, blockIdx.x, gridDim.x);
+    quant_rows_reg_body<T, OUT, VPT, WPR>(src, rows, K, qmax, out, scales, blockIdx.x, gridDim.x);
 }
 
 // Scalar fallback for shapes the vector path does not take (int8 / fp16 out).
-template <QuantOut OUT>
-__global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const __half* __restrict__ src,
+template <typename T, QuantOut OUT>
+__global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const T* __restrict__ src,
                                                                   int64_t rows, int64_t K,
                                                                   int64_t gs, int qmax,
                                                                   void* __restrict__ out,
@@ -200,13 +189,13 @@ __global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const __half* 
         const int64_t row = item / G, g = item - row * G;
         const int64_t base = row * K + g * gs;
         float amax = 0.0f;
-        for (int64_t k = lane; k < gs; k += 32) amax = fmaxf(amax, fabsf(__half2float(src[base + k])));
+        for (int64_t k = lane; k < gs; k += 32) amax = fmaxf(amax, fabsf(elem_to_float(src[base + k])));
         amax = warp_max(amax);
         const float s = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, (float)qmax);
         const float r = quant_recip(s);
         if (lane == 0) scales[item] = s;
         for (int64_t k = lane; k < gs; k += 32)
-            store_code1<OUT>(out, base + k, quant_one(__half2float(src[base + k]), s, r, qmax));
+            store_code1<OUT>(out, base + k, quant_one(elem_to_float(src[base + k]), s, r, qmax));
     }
 }
 
@@ -289,7 +278,7 @@ __global__ void __launch_bounds__(256) widen_i4_kernel(const uint8_t* __restrict
 // scales; the remaining blocks widen the weight codes (INT8 or packed INT4)
 // into exact fp16 integers. The two jobs are independent and share the GPU.
 struct ImagesArgs {
-    const __half* x;
+    const void* x;  // fp16 or bf16 [M, K] (kernel template parameter)
     int64_t M, K;
     __half* a_img;
     float* s_a;
@@ -316,12 +305,13 @@ __device__ __forceinline__ void transpose_scales_body(const float* __restrict__ 
     }
 }
 
-template <int VPT, int WPR, int BITS>
+template <typename T, int VPT, int WPR, int BITS>
 __global__ void __launch_bounds__(256) operand_images_kernel(const ImagesArgs a) {
     grid_dep_wait();
     grid_dep_launch();
     if ((int)blockIdx.x < a.a_blocks) {
-        quant_rows_reg_body<QuantOut::kF16, VPT, WPR>(a.x, a.M, a.K, 127, a.a_img, a.s_a,
+        quant_rows_reg_body<T, QuantOut::kF16, VPT, WPR>(static_cast<const T*>(a.x), a.M, a.K, 127,
+                                                         a.a_img, a.s_a,
                                                        blockIdx.x, a.a_blocks);
     } else {
         const int wb = blockIdx.x - a.a_blocks, nwb = gridDim.x - a.a_blocks;
@@ -345,79 +335,81 @@ int grid_for(int64_t work_items, int per_block, int num_sms) {
 
 namespace {
 
-template <QuantOut OUT>
-cudaError_t launch_rows_reg_t(const __half* src, int64_t rows, int64_t K, int qmax, void* out,
+template <typename T, QuantOut OUT>
+cudaError_t launch_rows_reg_t(const T* src, int64_t rows, int64_t K, int qmax, void* out,
                               float* scales, int num_sms, cudaStream_t stream) {
     const int64_t nvec = K / 8;
     const int64_t cap = (int64_t)num_sms * 8;  // 8 resident blocks of 256 threads per SM
     const int g1 = (int)std::min<int64_t>((rows + 7) / 8, cap);
     const int g8 = (int)std::min<int64_t>(rows, cap);
     if (nvec <= 32 * 4)
-        return launch_pdl(quant_rows_reg_kernel<OUT, 4, 1>, g1, 256, 0, stream, src, rows, K, qmax,
-                          out, scales);
+        return launch_pdl(quant_rows_reg_kernel<T, OUT, 4, 1>, g1, 256, 0, stream, src, rows, K,
+                          qmax, out, scales);
     if (nvec <= 32 * 8)
-        return launch_pdl(quant_rows_reg_kernel<OUT, 8, 1>, g1, 256, 0, stream, src, rows, K, qmax,
-                          out, scales);
+        return launch_pdl(quant_rows_reg_kernel<T, OUT, 8, 1>, g1, 256, 0, stream, src, rows, K,
+                          qmax, out, scales);
     if (nvec <= 32 * 12)
-        return launch_pdl(quant_rows_reg_kernel<OUT, 12, 1>, g1, 256, 0, stream, src, rows, K,
+        return launch_pdl(quant_rows_reg_kernel<T, OUT, 12, 1>, g1, 256, 0, stream, src, rows, K,
                           qmax, out, scales);
     if (nvec <= 32 * 16)
-        return launch_pdl(quant_rows_reg_kernel<OUT, 16, 1>, g1, 256, 0, stream, src, rows, K,
+        return launch_pdl(quant_rows_reg_kernel<T, OUT, 16, 1>, g1, 256, 0, stream, src, rows, K,
                           qmax, out, scales);
     if (nvec <= 256 * 8)
-        return launch_pdl(quant_rows_reg_kernel<OUT, 8, 8>, g8, 256, 0, stream, src, rows, K, qmax,
-                          out, scales);
+        return launch_pdl(quant_rows_reg_kernel<T, OUT, 8, 8>, g8, 256, 0, stream, src, rows, K,
+                          qmax, out, scales);
     return cudaErrorNotSupported;
 }
 
-cudaError_t launch_quant_rows_reg(const __half* src, int64_t rows, int64_t K, int qmax,
+template <typename T>
+cudaError_t launch_quant_rows_reg(const T* src, int64_t rows, int64_t K, int qmax,
                                   QuantOut out_kind, void* out, float* scales, int num_sms,
                                   cudaStream_t stream) {
     if (out_kind == QuantOut::kInt8)
-        return launch_rows_reg_t<QuantOut::kInt8>(src, rows, K, qmax, out, scales, num_sms, stream);
+        return launch_rows_reg_t<T, QuantOut::kInt8>(src, rows, K, qmax, out, scales, num_sms,
+                                                     stream);
     if (out_kind == QuantOut::kF16)
-        return launch_rows_reg_t<QuantOut::kF16>(src, rows, K, qmax, out, scales, num_sms, stream);
+        return launch_rows_reg_t<T, QuantOut::kF16>(src, rows, K, qmax, out, scales, num_sms,
+                                                    stream);
     return cudaErrorNotSupported;
 }
 
-}  // namespace
-
-cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int64_t gs, int qmax,
-                                QuantOut out_kind, void* out, float* scales, int num_sms,
-                                cudaStream_t stream) {
+template <typename T>
+cudaError_t launch_quant_groups_t(const T* src, int64_t rows, int64_t K, int64_t gs, int qmax,
+                                  QuantOut out_kind, void* out, float* scales, int num_sms,
+                                  cudaStream_t stream) {
     const int64_t items = rows * (K / gs);
     const bool vec = (K % 8 == 0) && (gs % 8 == 0) &&
                      (reinterpret_cast<uintptr_t>(src) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(out) % 16 == 0);
     const int grid = grid_for(items, 8, num_sms);
     if (vec && gs == K && out_kind != QuantOut::kInt4 && K <= 16384) {
-        cudaError_t e = launch_quant_rows_reg(src, rows, K, qmax, out_kind, out, scales, num_sms,
-                                              stream);
+        cudaError_t e = launch_quant_rows_reg<T>(src, rows, K, qmax, out_kind, out, scales,
+                                                 num_sms, stream);
         if (e != cudaErrorNotSupported) return e;
     }
     if (vec) {
         switch (out_kind) {
             case QuantOut::kInt8:
-                quant_groups_vec_kernel<QuantOut::kInt8>
+                quant_groups_vec_kernel<T, QuantOut::kInt8>
                     <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
                 break;
             case QuantOut::kF16:
-                quant_groups_vec_kernel<QuantOut::kF16>
+                quant_groups_vec_kernel<T, QuantOut::kF16>
                     <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
                 break;
             case QuantOut::kInt4:
-                quant_groups_vec_kernel<QuantOut::kInt4>
+                quant_groups_vec_kernel<T, QuantOut::kInt4>
                     <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
                 break;
         }
     } else {
         switch (out_kind) {
             case QuantOut::kInt8:
-                quant_groups_scalar_kernel<QuantOut::kInt8>
+                quant_groups_scalar_kernel<T, QuantOut::kInt8>
                     <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
                 break;
             case QuantOut::kF16:
-                quant_groups_scalar_kernel<QuantOut::kF16>
+                quant_groups_scalar_kernel<T, QuantOut::kF16>
                     <<<grid, 256, 0, stream>>>(src, rows, K, gs, qmax, out, scales);
                 break;
             case QuantOut::kInt4:
@@ -425,6 +417,18 @@ cudaError_t launch_quant_groups(const __half* src, int64_t rows, int64_t K, int6
         }
     }
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_groups(const void* src, ElemType src_type, int64_t rows, int64_t K,
+                                int64_t gs, int qmax, QuantOut out_kind, void* out,
+                                float* scales, int num_sms, cudaStream_t stream) {
+    if (src_type == ElemType::kBF16)
+        return launch_quant_groups_t(static_cast<const __nv_bfloat16*>(src), rows, K, gs, qmax,
+                                     out_kind, out, scales, num_sms, stream);
+    return launch_quant_groups_t(static_cast<const __half*>(src), rows, K, gs, qmax, out_kind,
+                                 out, scales, num_sms, stream);
 }
 
 cudaError_t launch_widen_i8(const int8_t* src, int64_t n, __half* dst, int num_sms,
@@ -445,7 +449,7 @@ cudaError_t launch_widen_i4(const uint8_t* src, int64_t n_codes, __half* dst, in
 
 namespace {
 
-template <int BITS>
+template <typename T, int BITS>
 cudaError_t launch_images_t(const ImagesArgs& a0, int64_t nvec, int num_sms, cudaStream_t stream) {
     ImagesArgs a = a0;
     int64_t b_blocks = std::min<int64_t>((a.n16 + 256 * 4 - 1) / (256 * 4), (int64_t)num_sms * 4);
@@ -456,11 +460,11 @@ cudaError_t launch_images_t(const ImagesArgs& a0, int64_t nvec, int num_sms, cud
     };
     const int64_t g1 = std::min<int64_t>((a.M + 7) / 8, (int64_t)num_sms * 3);
     const int64_t g8 = std::min<int64_t>(a.M, (int64_t)num_sms * 4);
-    if (nvec <= 32 * 4) return go(operand_images_kernel<4, 1, BITS>, g1);
-    if (nvec <= 32 * 8) return go(operand_images_kernel<8, 1, BITS>, g1);
-    if (nvec <= 32 * 12) return go(operand_images_kernel<12, 1, BITS>, g1);
-    if (nvec <= 32 * 16) return go(operand_images_kernel<16, 1, BITS>, g1);
-    return go(operand_images_kernel<8, 8, BITS>, g8);
+    if (nvec <= 32 * 4) return go(operand_images_kernel<T, 4, 1, BITS>, g1);
+    if (nvec <= 32 * 8) return go(operand_images_kernel<T, 8, 1, BITS>, g1);
+    if (nvec <= 32 * 12) return go(operand_images_kernel<T, 12, 1, BITS>, g1);
+    if (nvec <= 32 * 16) return go(operand_images_kernel<T, 16, 1, BITS>, g1);
+    return go(operand_images_kernel<T, 8, 8, BITS>, g8);
 }
 
 }  // namespace
@@ -473,7 +477,8 @@ __global__ void __launch_bounds__(256) transpose_scales_kernel(const float* __re
     transpose_scales_body(s_w, s_wT, N, G, blockIdx.x, gridDim.x);
 }
 
-cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const void* w, int bits,
+cudaError_t launch_operand_images(const void* x, ElemType x_type, int64_t M, int64_t K,
+                                  const void* w, int bits,
                                   int64_t N, __half* a_img, float* s_a, __half* b_img,
                                   const float* s_w, float* s_wT, int64_t G, int num_sms,
                                   cudaStream_t stream) {
@@ -484,8 +489,8 @@ cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const v
                        (reinterpret_cast<uintptr_t>(a_img) % 16 == 0) &&
                        (w == nullptr || (N * K) % codes_per_chunk == 0);
     if (!fused) {
-        cudaError_t e = launch_quant_groups(x, M, K, K, 127, QuantOut::kF16, a_img, s_a, num_sms,
-                                            stream);
+        cudaError_t e = launch_quant_groups(x, x_type, M, K, K, 127, QuantOut::kF16, a_img, s_a,
+                                            num_sms, stream);
         if (e != cudaSuccess) return e;
         if (w != nullptr) {
             e = (bits == 8) ? launch_widen_i8(static_cast<const int8_t*>(w), N * K, b_img,
@@ -500,8 +505,11 @@ cudaError_t launch_operand_images(const __half* x, int64_t M, int64_t K, const v
     }
     const int64_t n16 = (w == nullptr) ? 0 : (N * K) / codes_per_chunk;
     ImagesArgs a{x, M, K, a_img, s_a, w, n16, b_img, 0, s_w, s_wT, N, G};
-    return (bits == 8) ? launch_images_t<8>(a, nvec, num_sms, stream)
-                       : launch_images_t<4>(a, nvec, num_sms, stream);
+    if (x_type == ElemType::kBF16)
+        return (bits == 8) ? launch_images_t<__nv_bfloat16, 8>(a, nvec, num_sms, stream)
+                           : launch_images_t<__nv_bfloat16, 4>(a, nvec, num_sms, stream);
+    return (bits == 8) ? launch_images_t<__half, 8>(a, nvec, num_sms, stream)
+                       : launch_images_t<__half, 4>(a, nvec, num_sms, stream);
 }
 
 }  // namespace cider

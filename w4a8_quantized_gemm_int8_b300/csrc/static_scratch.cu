@@ -99,7 +99,7 @@ extern "C" cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M,
     __half* b_img = img ? reinterpret_cast<__half*>(p + a_bytes + s_bytes) : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    cudaError_t e = launch_operand_images(static_cast<const __half*>(x_f16), M, K,
+    cudaError_t e = launch_operand_images(x_f16, ElemType::kF16, M, K,
                                           img ? wq : nullptr, 8, N, a_img, s_a, b_img, nullptr,
                                           nullptr, 1, sms, s);
     if (e == cudaSuccess) {
