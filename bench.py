@@ -400,8 +400,19 @@ def run_configs(args):
         layer.append(r)
     tot_us = sum(r["us"] for r in layer)
     tot_ops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in layer)
+    # The same layer with the linears that share an input fused into one call
+    # each (weights concatenated along N at prep time): q|k|v and gate|up.
+    fused = []
+    for name, K_, N_ in (("qkv", 4096, 6144), ("o", 4096, 4096), ("gate_up", 4096, 24576),
+                         ("down", 12288, 4096)):
+        r = time_case(2048, N_, K_, 8, 0, n_out=max(1, round(K_ * 0.01)))
+        r["linear"] = name
+        fused.append(r)
+    fused_us = sum(r["us"] for r in fused)
     out["decoder_layer_M2048"] = {"linears": layer, "total_us": round(tot_us, 2),
-                                  "TOPS": round(tot_ops / (tot_us * 1e-6) / 1e12, 1)}
+                                  "TOPS": round(tot_ops / (tot_us * 1e-6) / 1e12, 1),
+                                  "fused": {"linears": fused, "total_us": round(fused_us, 2),
+                                            "TOPS": round(tot_ops / (fused_us * 1e-6) / 1e12, 1)}}
     print(json.dumps({"configs": out, "steps": args.steps, "warmup": args.warmup,
                       "timing": "CUDA events per call, inputs rotating over sets > 3x L2"}))
 

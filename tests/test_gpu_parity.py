@@ -314,6 +314,26 @@ def test_column_shards_reproduce_the_full_layer(gs):
     assert torch.equal(y.view(torch.int16), full.view(torch.int16))
 
 
+@pytest.mark.parametrize("gs", [0, 64])
+@pytest.mark.parametrize("M", [1, 40, 300])
+def test_concatenated_linears_equal_separate_calls(M, gs):
+    """q|k|v-style fusion: one call on the weights stacked along N gives, in
+    each linear's columns, exactly that linear's own output."""
+    K = 1024
+    x, _ = _layer_inputs(M, 8, K, seed=M + 500)
+    xd = cuda(torch.from_numpy(x))
+    lins = []
+    for i, N in enumerate((384, 128, 136)):
+        w = synth.weights(N, K, synth.generator(600 + i)).numpy()
+        wq, s = oracle.quantize_weight_int8(w, gs)
+        lins.append((cuda(torch.from_numpy(wq)), cuda(torch.from_numpy(s))))
+    wcat, scat, sizes = cider.concat_linears(lins)
+    parts = cider.split_columns(cider.w8a8_linear(xd, wcat, scat, gs), sizes)
+    for (wq, s), y in zip(lins, parts):
+        ref = cider.w8a8_linear(xd, wq, s, gs)
+        assert torch.equal(y.contiguous().view(torch.int16), ref.view(torch.int16))
+
+
 # ---------------------------------------------------------------------------
 # M = 1 GEMV
 # ---------------------------------------------------------------------------

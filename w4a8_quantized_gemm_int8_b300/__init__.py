@@ -375,6 +375,32 @@ def wait_timeout_probe(timeout_ns: int) -> None:
 
 
 # ---------------------------------------------------------------------------
+# linears that read the same input (q/k/v, gate/up): one call
+# ---------------------------------------------------------------------------
+
+def concat_linears(weights):
+    """Offline, at weight-prep time: stacks the weight rows and scale rows of
+    linears that read the same input (e.g. q, k, v) into one layer, so one
+    call quantizes the input once and runs one GEMM with N = sum of the N's.
+    Output channels are independent, so each linear's columns of the fused
+    output equal that linear's own output bit for bit. `weights` is a list of
+    (w, s_w) with the same K, bit width and group size. Returns (w, s_w,
+    sizes); split_columns(y, sizes) recovers the per-linear outputs."""
+    ws = [w for w, _ in weights]
+    ss = [s for _, s in weights]
+    if len({w.shape[1] for w in ws}) != 1 or len({w.dtype for w in ws}) != 1:
+        raise ValueError("concat_linears: the linears must share K and the weight format")
+    if len({tuple(s.shape[1:]) for s in ss}) != 1:
+        raise ValueError("concat_linears: the linears must share the scale granularity")
+    return torch.cat(ws, 0).contiguous(), torch.cat(ss, 0).contiguous(), [w.shape[0] for w in ws]
+
+
+def split_columns(y: torch.Tensor, sizes):
+    """The per-linear outputs of a fused call (column views of y)."""
+    return list(torch.split(y, list(sizes), dim=1))
+
+
+# ---------------------------------------------------------------------------
 # column-parallel split (several GPUs, one process each)
 # ---------------------------------------------------------------------------
 
