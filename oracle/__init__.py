@@ -74,6 +74,7 @@ def _load():
             lib.oracle_quantize_act_ex.restype = None
             lib.oracle_w8a8_linear_ex.argtypes = [p, i32, i64, i64, i64, p, p, i32, p, i32]
             lib.oracle_w4a8_linear_ex.argtypes = [p, i32, i64, i64, i64, p, p, i32, p, i32]
+            lib.oracle_a16_gemv.argtypes = [p, i32, i64, i64, p, i32, p, i32, p]
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_set_threads.restype = None
             lib.oracle_get_threads.restype = ctypes.c_int
@@ -298,3 +299,23 @@ def w4a8_linear(x, wp, s_w, group_size: int = 0, x_dtype: str = "f16",
     if rc:
         raise ValueError("unsupported shape / group_size")
     return _out(y, y_dtype)
+
+
+def a16_gemv(x, w, s_w, bits: int = 8, group_size: int = 0, x_dtype: str = "f16") -> np.ndarray:
+    """A16 decode matrix-vector product with weight-only dequantization
+    (README "Metal Kernel Pipeline", decode: "on-the-fly weight
+    dequantization (no activation quantization needed)"): y[n] = sum over
+    groups of s_w[n,g] * sum_k x[k] * code[n,k], accumulated in float64 and
+    returned unrounded (float64 [N]). x: fp16 [K] or bf16 bits; w: int8
+    [N,K] (bits 8) or packed uint8 [N,K/2] (bits 4)."""
+    xb = _bits(np.asarray(x).reshape(-1), x_dtype)
+    K = xb.size
+    w = np.ascontiguousarray(w, dtype=np.int8 if bits == 8 else np.uint8)
+    N = w.shape[0]
+    s = np.ascontiguousarray(s_w, dtype=np.float32)
+    y = np.empty((N,), np.float64)
+    rc = _load().oracle_a16_gemv(_ptr(xb), _DTYPES[x_dtype], K, N, _ptr(w), bits, _ptr(s),
+                                 group_size, _ptr(y))
+    if rc:
+        raise ValueError("unsupported bits / group_size")
+    return y

@@ -452,6 +452,49 @@ int oracle_w4a8_linear(const uint16_t* x, int64_t M, int64_t N, int64_t K, const
     return oracle_w4a8_linear_ex(x, ORACLE_F16, M, N, K, wp, s_w, group_size, y, ORACLE_F16);
 }
 
+/* ------------------------------------------------------------------------ */
+/* A16 decode matrix-vector product (weight-only dequantization).           */
+/* README "Metal Kernel Pipeline", decode: a matrix-vector kernel "with      */
+/* on-the-fly weight dequantization (no activation quantization needed)".    */
+/* The activations are used as they are; each weight is dequantized as code  */
+/* times its scale. The oracle returns the value of                          */
+/*   y[n] = sum_g s_w[n,g] * sum_{k in g} x[k] * wq[n,k]                      */
+/* accumulated in binary64 (each x*wq product is exact in binary64; the sums */
+/* are far more precise than any binary32 evaluation), unrounded: a GPU      */
+/* evaluation in binary32 is compared with it under an error bound.          */
+/* w: INT8 codes [N,K] (bits 8) or packed INT4 [N,K/2] (bits 4); s_w [N] for */
+/* group_size 0 or [N, K/gs]; x fp16 (dtype 0) or bf16 (dtype 1).            */
+/* ------------------------------------------------------------------------ */
+int oracle_a16_gemv(const uint16_t* x, int32_t x_dtype, int64_t K, int64_t N, const void* w,
+                    int32_t bits, const float* s_w, int32_t group_size, double* y)
+{
+    if ((bits != 8 && bits != 4) || group_size < 0 || (group_size > 0 && K % group_size != 0) ||
+        (bits == 4 && K % 2 != 0))
+        return 1;
+    int64_t gs = group_size ? group_size : K;
+    int64_t G = K / gs;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        double total = 0.0;
+        for (int64_t g = 0; g < G; ++g) {
+            double part = 0.0;
+            for (int64_t k = g * gs; k < (g + 1) * gs; ++k) {
+                int code;
+                if (bits == 8) {
+                    code = ((const int8_t*)w)[n * K + k];
+                } else {
+                    uint8_t b = ((const uint8_t*)w)[n * (K / 2) + k / 2];
+                    code = (int)((k % 2) ? (b >> 4) : (b & 0x0F)) - 8;
+                }
+                part += (double)elem_to_float(x[k], x_dtype) * (double)code;
+            }
+            total += (double)s_w[n * G + g] * part;
+        }
+        y[n] = total;
+    }
+    return 0;
+}
+
 void oracle_set_threads(int n)
 {
 #ifdef _OPENMP

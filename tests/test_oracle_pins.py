@@ -420,3 +420,47 @@ def test_bf16_subnormal_scale_closed_form():
     q, s = oracle.quantize_act_bf16(x.reshape(1, 4))
     assert float(s[0]) == 1548 * u
     assert q.tolist() == [[42, -42, 0, 127]]
+
+
+# ---------------------------------------------------------------------------
+# A16 decode matrix-vector product (weight-only dequantization)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits,gs", [(8, 0), (8, 64), (4, 0), (4, 128)])
+def test_a16_gemv_against_numpy_float64(bits, gs):
+    """Independent restatement: dequantize the weights in numpy float64
+    (code * scale) and take numpy's float64 matrix-vector product."""
+    rng = np.random.default_rng(bits * 10 + gs)
+    N, K = 37, 512
+    x = (rng.standard_normal(K) * 3).astype(np.float16)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float16)
+    if bits == 8:
+        wq, s = oracle.quantize_weight_int8(w, gs)
+        codes = wq.astype(np.float64)
+        wdev = wq
+    else:
+        wdev, s = oracle.pack_weight_int4(w, gs)
+        codes = oracle.unpack_int4(wdev, K).astype(np.float64)
+    G = 1 if gs == 0 else K // gs
+    scale = np.repeat(np.asarray(s, np.float64).reshape(N, G), K // G, axis=1)
+    ref = (codes * scale) @ x.astype(np.float64)
+    y = oracle.a16_gemv(x, wdev, s, bits, gs)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_a16_gemv_hand_examples():
+    """One non-zero product per row: the value is exactly x * code * scale."""
+    K = 64
+    x = np.zeros(K, np.float16)
+    x[5] = 1.5
+    x[9] = -0.25
+    wq = np.zeros((3, K), np.int8)
+    wq[0, 5] = 100          # 1.5 * 100 * s0
+    wq[1, 9] = -127         # -0.25 * -127 * s1
+    wq[2, 5], wq[2, 9] = 2, 4  # 1.5 * 2 - 0.25 * 4 = 2
+    s = np.array([0.5, 2.0, 0.125], np.float32)
+    y = oracle.a16_gemv(x, wq, s, 8, 0)
+    assert y.tolist() == [75.0, 63.5, 0.25]
+    # bf16 input reads the same exact values
+    xb = oracle.float_to_bf16(x.astype(np.float32))
+    assert oracle.a16_gemv(xb, wq, s, 8, 0, x_dtype="bf16").tolist() == [75.0, 63.5, 0.25]
