@@ -343,7 +343,7 @@ def run_configs(args):
             wq, s = cider.pack_weight_int4(w, gs)
         return x, wq, s
 
-    def time_case(M, N, K, bits, gs, n_out=4):
+    def time_case(M, N, K, bits, gs, n_out=4, a16=False):
         wbytes = N * K if bits == 8 else N * K // 2
         per_set = 2 * M * K + wbytes + 2 * M * N
         n_sets = max(1, min(8, -(-3 * l2 // per_set) + 1))
@@ -356,7 +356,9 @@ def run_configs(args):
 
         def call(i):
             x, wq, s, y = sets[i % n_sets]
-            if M == 1:
+            if M == 1 and a16:
+                cider.a16_gemv(x[0], wq, s, bits, gs, out=y[0])
+            elif M == 1:
                 cider.int8_gemv(x[0], wq, s, bits, gs, out=y[0])
             elif bits == 8:
                 cider.w8a8_linear(x, wq, s, gs, out=y, ws=ws)
@@ -392,6 +394,10 @@ def run_configs(args):
                                               for m in (1, 128, 1024, 4096, 8192)]
     for (n, k) in ((10240, 2560), (2560, 10240)):
         out[f"w4a8_gs128_N{n}_K{k}"] = [time_case(m, n, k, 4, 128) for m in (1, 1024, 8192)]
+    # The A16 decode product (activations unquantized, weights dequantized).
+    out["a16_decode_M1"] = [dict(time_case(1, n, k, b, g, a16=True), mode="a16")
+                            for (n, k, b, g) in ((10240, 2560, 8, 0), (2560, 10240, 8, 64),
+                                                 (10240, 2560, 4, 128))]
     import synth
     layer = []
     for name, K_, N_ in synth.DECODER_LAYER:

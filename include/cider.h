@@ -193,6 +193,20 @@ CIDER_API cider_status cider_linear(const void* x, int32_t x_dtype, int64_t M, i
 CIDER_API cider_status cider_quantize_act_ex(const void* x, int32_t x_dtype, int64_t M, int64_t K,
                                              int8_t* q, float* s_a, void* stream);
 
+/*
+ * A16 decode matrix-vector product (README "Metal Kernel Pipeline", decode:
+ * a matrix-vector kernel "with on-the-fly weight dequantization (no
+ * activation quantization needed)"): y[n] = sum_g s_w[n,g] * sum_{k in g}
+ * x[k] * code[n,k], with x [K] used as it is (fp16 or bf16, x_dtype), the
+ * weight codes dequantized on the fly, fp32 accumulation, y [N] written as
+ * y_dtype. A floating-point sum: its result agrees with the exact value
+ * within the fp32 accumulation bound, not bit for bit with another order.
+ * Weights, scales and limits as cider_int8_gemv. Needs no workspace.
+ */
+CIDER_API cider_status cider_a16_gemv(const void* x, int32_t x_dtype, int64_t K, int64_t N,
+                                      const void* w, int32_t bits, const float* s_w,
+                                      int32_t group_size, void* y, int32_t y_dtype, void* stream);
+
 CIDER_API cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, const void* w,
                              const float* s_w, int32_t bits, int32_t group_size, void* y_f16,
                              void* stream);

@@ -80,3 +80,12 @@ def test_element_type_checks_precede_cuda(lib):
     assert lib.cider_quantize_act_ex(p, 3, 4, 16, p, p, None) == 1
     assert lib.cider_quantize_act_ex(None, 1, 4, 16, p, p, None) == 1
     assert lib.cider_quantize_act_ex(p, 1, 0, 16, p, p, None) == 1
+
+
+def test_a16_gemv_checks_precede_cuda(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: checks fail first
+    assert lib.cider_a16_gemv(None, 0, 64, 16, p, 8, p, 0, p, 0, None) == 1
+    assert lib.cider_a16_gemv(p, 0, 0, 16, p, 8, p, 0, p, 0, None) == 1
+    assert lib.cider_a16_gemv(p, 0, 64, 16, p, 6, p, 0, p, 0, None) == 1
+    assert lib.cider_a16_gemv(p, 2, 64, 16, p, 8, p, 0, p, 0, None) == 1
+    assert lib.cider_a16_gemv(p, 0, 64, 16, p, 8, p, 0, p, 3, None) == 1

@@ -24,7 +24,7 @@ ABI_FUNCTIONS = (
     "cider_status_string", "cider_abi_version", "cider_quantize_act",
     "cider_quantize_weight_int8", "cider_pack_weight_int4", "cider_workspace_bytes",
     "cider_w8a8_gemm_pc", "cider_w8a8_gemm_pg", "cider_w4a8_gemm", "cider_int8_gemv",
-    "cider_linear", "cider_quantize_act_ex",
+    "cider_linear", "cider_quantize_act_ex", "cider_a16_gemv",
     "cider_w8a8_gemm_pc_noalloc",
     "cider_act_image", "cider_weight_image", "cider_gemm_images",
     "cider_test_gemm_s32", "cider_device_status", "cider_test_wait_timeout",
@@ -75,6 +75,7 @@ def load_library():
             "cider_linear": ([p, i32, i64, i64, i64, p, i32, p, i32, p, i32, p, sz, p],
                              ctypes.c_int),
             "cider_quantize_act_ex": ([p, i32, i64, i64, p, p, p], ctypes.c_int),
+            "cider_a16_gemv": ([p, i32, i64, i64, p, i32, p, i32, p, i32, p], ctypes.c_int),
             "cider_w8a8_gemm_pc_noalloc": ([p, i64, i64, i64, p, p, p, p], ctypes.c_int),
             "cider_act_image": ([p, i64, i64, p, p, p], ctypes.c_int),
             "cider_weight_image": ([p, i64, i64, i32, p, p], ctypes.c_int),
@@ -234,6 +235,27 @@ def linear(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
         _dev(s_w, torch.float32, "s_w"), group_size, _dev(y, out_dtype, "y", 2),
         _DTYPE_CODES[out_dtype], wsp, wsn, _stream())
     _check("cider_linear", st)
+    return y
+
+
+def a16_gemv(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
+             group_size: int = 0, out_dtype: torch.dtype | None = None,
+             out: torch.Tensor | None = None) -> torch.Tensor:
+    """A16 decode product: x fp16/bf16 [K] (or [1,K]) used as it is against
+    the dequantized weights (code * scale), fp32 accumulation; y [N]."""
+    xv = x.reshape(-1)
+    if xv.dtype not in _DTYPE_CODES:
+        raise ValueError(f"x must be float16 or bfloat16, got {xv.dtype}")
+    out_dtype = out_dtype or xv.dtype
+    K = xv.numel()
+    N = w.shape[0]
+    y = out if out is not None else torch.empty((N,), dtype=out_dtype, device=x.device)
+    wdt = torch.int8 if bits == 8 else torch.uint8
+    st = load_library().cider_a16_gemv(
+        _dev(xv, xv.dtype, "x"), _DTYPE_CODES[xv.dtype], K, N, _dev(w, wdt, "w", 2), bits,
+        _dev(s_w, torch.float32, "s_w"), group_size, _dev(y, out_dtype, "y"),
+        _DTYPE_CODES[out_dtype], _stream())
+    _check("cider_a16_gemv", st)
     return y
 
 

@@ -270,6 +270,26 @@ cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, const void
     return from_cuda(launch_gemv(g, sms, static_cast<cudaStream_t>(stream)));
 }
 
+cider_status cider_a16_gemv(const void* x, int32_t x_dtype, int64_t K, int64_t N, const void* w,
+                            int32_t bits, const float* s_w, int32_t group_size, void* y,
+                            int32_t y_dtype, void* stream) {
+    if (!x || !w || !s_w || !y) return CIDER_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || group_size < 0) return CIDER_ERR_INVALID_ARG;
+    if (bits != 8 && bits != 4) return CIDER_ERR_INVALID_ARG;
+    if (!valid_dtype(x_dtype) || !valid_dtype(y_dtype)) return CIDER_ERR_INVALID_ARG;
+    if (K > 16384 || K % (bits == 8 ? 16 : 32) != 0) return CIDER_ERR_UNSUPPORTED;
+    if (!valid_group(group_size, K, bits == 8 ? 16 : 32)) return CIDER_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    unsigned long long* status = nullptr;
+    if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
+    GemvArgs g{x, K, N, w, s_w, bits, group_size, y, kWaitTimeoutNs, status,
+               x_dtype == CIDER_DTYPE_BF16, y_dtype == CIDER_DTYPE_BF16, 1};
+    return from_cuda(launch_gemv(g, sms, static_cast<cudaStream_t>(stream)));
+}
+
 cider_status cider_act_image(const void* x_f16, int64_t M, int64_t K, void* a_img, float* s_a,
                              void* stream) {
     if (!x_f16 || !a_img || !s_a) return CIDER_ERR_INVALID_ARG;

@@ -108,6 +108,59 @@ __device__ __forceinline__ int chunk_dot(const uint4& wv, const uint4* codes, in
     }
 }
 
+// ---- A16 mode: activations used as they are, weights dequantized ---------
+// Two activations of type T packed in 32 bits -> fp32 (exact).
+__device__ __forceinline__ float2 to_f2(uint32_t v, __half) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+__device__ __forceinline__ float2 to_f2(uint32_t v, __nv_bfloat16) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
+
+// Signed byte j of w -> fp32 (exact): the byte offset by 128 is placed under
+// the exponent of 2^23 and the offset 2^23 + 128 subtracted.
+__device__ __forceinline__ float byte_to_float(uint32_t w_biased, int j) {
+    return __int_as_float((int)__byte_perm(w_biased, 0x4B000000u, 0x7540u | (uint32_t)j)) -
+           8388736.0f;
+}
+
+// acc + the four codes of `w` (signed bytes, element order) times the four
+// activations packed in x01, x23.
+template <typename T>
+__device__ __forceinline__ float dot4_f32(uint32_t w, uint32_t x01, uint32_t x23, float acc) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float2 a = to_f2(x01, T()), b = to_f2(x23, T());
+    acc = fmaf(a.x, byte_to_float(u, 0), acc);
+    acc = fmaf(a.y, byte_to_float(u, 1), acc);
+    acc = fmaf(b.x, byte_to_float(u, 2), acc);
+    return fmaf(b.y, byte_to_float(u, 3), acc);
+}
+
+// fp32 dot product of one 16-byte weight chunk (16 INT8 or 32 INT4 codes)
+// with the matching activations xs (16-byte vectors of 8 elements of T).
+template <typename T, int BITS>
+__device__ __forceinline__ float chunk_dot_a16(const uint4& wv, const uint4* xs, int c) {
+    if constexpr (BITS == 8) {
+        const uint4 x0 = xs[2 * c], x1 = xs[2 * c + 1];
+        float acc = dot4_f32<T>(wv.x, x0.x, x0.y, 0.0f);
+        acc = dot4_f32<T>(wv.y, x0.z, x0.w, acc);
+        acc = dot4_f32<T>(wv.z, x1.x, x1.y, acc);
+        return dot4_f32<T>(wv.w, x1.z, x1.w, acc);
+    } else {
+        const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 xv = xs[4 * c + i];
+            int e0, e1;
+            widen_nibbles(wd[i], e0, e1);
+            acc = dot4_f32<T>((uint32_t)e0, xv.x, xv.y, acc);
+            acc = dot4_f32<T>((uint32_t)e1, xv.z, xv.w, acc);
+        }
+        return acc;
+    }
+}
+
 // One output element, rounded to nearest even as fp16 or bf16.
 __device__ __forceinline__ void store_y(const Params& p, int n, float v) {
     if (p.y_bf16)
@@ -116,7 +169,10 @@ __device__ __forceinline__ void store_y(const Params& p, int n, float v) {
         static_cast<__half*>(p.y)[n] = __float2half_rn(v);
 }
 
-template <typename T, int BITS, bool PG>
+// A16 = false: the INT8 GEMV (x quantized per token, int32 dot products).
+// A16 = true: the A16 decode product, y = sum_g s_w[n,g] sum_k x[k] code[n,k]
+// with x used as it is and fp32 accumulation (no activation quantization).
+template <typename T, int BITS, bool PG, bool A16>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     int8_t* codes_s = reinterpret_cast<int8_t*>(smem + p.codes_off);
@@ -212,9 +268,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
             const int v = threadIdx.x + i * kConsumers;
             xr[i] = (v < nvec) ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float m = 0.0f;
+        if constexpr (A16) {
+            // The activations go to shared memory as they are.
 #pragma unroll
-        for (int i = 0; i < kXVec; ++i) m = fmaxf(m, vec8_absmax<T>(xr[i]));
+            for (int i = 0; i < kXVec; ++i) {
+                const int v = threadIdx.x + i * kConsumers;
+                if (v < nvec) reinterpret_cast<uint4*>(codes_s)[v] = xr[i];
+            }
+        }
+        float m = 0.0f;
+        if constexpr (!A16) {
+#pragma unroll
+            for (int i = 0; i < kXVec; ++i) m = fmaxf(m, vec8_absmax<T>(xr[i]));
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) red_s[warp] = m;
@@ -227,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
         const float r = quant_recip(s);
 #pragma unroll
         for (int i = 0; i < kXVec; ++i) {
+            if constexpr (A16) break;
             const int v = threadIdx.x + i * kConsumers;
             if (v >= nvec) break;
             const T* h = reinterpret_cast<const T*>(&xr[i]);
@@ -268,7 +335,26 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
             for (; j < rows; j += kConsumerWarps) {
                 const int n = n0 + st * R + j;
                 const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)j * p.row_bytes);
-                if constexpr (!PG) {
+                if constexpr (A16 && !PG) {
+                    float acc = 0.0f;
+                    for (int c0 = 0; c0 < nchunk; c0 += 32 * kUnroll) {  // warp-uniform
+                        uint4 wv[kUnroll];
+#pragma unroll
+                        for (int u = 0; u < kUnroll; ++u) {
+                            const int c = c0 + u * 32 + lane;
+                            if (c < nchunk) wv[u] = wrow[c];
+                        }
+#pragma unroll
+                        for (int u = 0; u < kUnroll; ++u) {
+                            const int c = c0 + u * 32 + lane;
+                            if (c < nchunk) acc += chunk_dot_a16<T, BITS>(wv[u], codes, c);
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                    if (lane == 0)
+                        store_y(p, n, acc * (p.sw_in_smem ? sw_s[n - n0] : __ldg(p.s_w + n)));
+                } else if constexpr (!PG) {
                     int acc = 0;
                     for (int c0 = 0; c0 < nchunk; c0 += 32 * kUnroll) {  // warp-uniform
                         uint4 wv[kUnroll];
@@ -305,12 +391,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
                         for (int u = 0; u < kUnroll; ++u) {
                             const int c = c0 + u * 32 + lane;
                             if (c0 + u * 32 >= nchunk) break;  // warp-uniform
-                            int part = (c < nchunk) ? chunk_dot<BITS>(wv[u], codes, c) : 0;
-                            for (int o = 1; o < p.cpg; o <<= 1)
-                                part += __shfl_xor_sync(0xffffffffu, part, o);
-                            if ((lane & (p.cpg - 1)) == 0 && c < nchunk) {
-                                const int g = c / p.cpg;
-                                prod[g] = __fmul_rn(__int2float_rn(part), srow[g]);
+                            if constexpr (A16) {
+                                float part = (c < nchunk) ? chunk_dot_a16<T, BITS>(wv[u], codes, c)
+                                                          : 0.0f;
+                                for (int o = 1; o < p.cpg; o <<= 1)
+                                    part += __shfl_xor_sync(0xffffffffu, part, o);
+                                if ((lane & (p.cpg - 1)) == 0 && c < nchunk)
+                                    prod[c / p.cpg] = part * srow[c / p.cpg];
+                            } else {
+                                int part = (c < nchunk) ? chunk_dot<BITS>(wv[u], codes, c) : 0;
+                                for (int o = 1; o < p.cpg; o <<= 1)
+                                    part += __shfl_xor_sync(0xffffffffu, part, o);
+                                if ((lane & (p.cpg - 1)) == 0 && c < nchunk) {
+                                    const int g = c / p.cpg;
+                                    prod[g] = __fmul_rn(__int2float_rn(part), srow[g]);
+                                }
                             }
                         }
                     }
@@ -318,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
                     if (lane == 0) {
                         float f = 0.0f;
                         for (int g = 0; g < p.G; ++g) f = __fadd_rn(f, prod[g]);
-                        store_y(p, n, __fmul_rn(f, s_a));
+                        store_y(p, n, A16 ? f : __fmul_rn(f, s_a));
                     }
                     __syncwarp();
                 }
@@ -331,9 +426,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
 
 int g_max_smem = 0;  // opt-in shared memory per block (queried once; same on every B300)
 
-template <typename T, int BITS, bool PG>
+template <typename T, int BITS, bool PG, bool A16>
 cudaError_t launch_one(const Params& p, int grid, int smem, cudaStream_t stream) {
-    auto kern = gemv_kernel<T, BITS, PG>;
+    auto kern = gemv_kernel<T, BITS, PG, A16>;
     static int attr_smem = 0;  // benign race: setting the same value twice
     if (attr_smem < smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -344,14 +439,14 @@ cudaError_t launch_one(const Params& p, int grid, int smem, cudaStream_t stream)
     return launch_pdl(kern, grid, kThreads, smem, stream, p);
 }
 
-template <typename T>
+template <typename T, bool A16>
 cudaError_t launch_bits(const Params& p, int bits, bool pg, int grid, int smem,
                         cudaStream_t stream) {
     if (bits == 8)
-        return pg ? launch_one<T, 8, true>(p, grid, smem, stream)
-                  : launch_one<T, 8, false>(p, grid, smem, stream);
-    return pg ? launch_one<T, 4, true>(p, grid, smem, stream)
-              : launch_one<T, 4, false>(p, grid, smem, stream);
+        return pg ? launch_one<T, 8, true, A16>(p, grid, smem, stream)
+                  : launch_one<T, 8, false, A16>(p, grid, smem, stream);
+    return pg ? launch_one<T, 4, true, A16>(p, grid, smem, stream)
+              : launch_one<T, 4, false, A16>(p, grid, smem, stream);
 }
 
 }  // namespace
@@ -405,7 +500,8 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
 
     // Shared memory: codes | per-warp group products | barriers | stages.
     p.codes_off = 0;
-    p.prod_off = (p.K + 127) & ~127;
+    // x area: INT8 codes (K bytes), or the activations themselves in A16 mode
+    p.prod_off = ((a.a16 ? 2 * p.K : p.K) + 127) & ~127;
     const int prod_bytes = pg ? ((kConsumerWarps * p.G * 4 + 127) & ~127) : 0;
     p.sw_off = p.prod_off + prod_bytes;
     p.sw_in_smem = !pg && max_rows <= 8192;
@@ -420,8 +516,11 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     if (ns < 1) return cudaErrorInvalidValue;
     p.num_stages = ns;
     const int smem = p.stage_off + ns * p.stage_bytes;
-    return a.x_bf16 ? launch_bits<__nv_bfloat16>(p, a.bits, pg, grid, smem, stream)
-                    : launch_bits<__half>(p, a.bits, pg, grid, smem, stream);
+    if (a.a16)
+        return a.x_bf16 ? launch_bits<__nv_bfloat16, true>(p, a.bits, pg, grid, smem, stream)
+                        : launch_bits<__half, true>(p, a.bits, pg, grid, smem, stream);
+    return a.x_bf16 ? launch_bits<__nv_bfloat16, false>(p, a.bits, pg, grid, smem, stream)
+                    : launch_bits<__half, false>(p, a.bits, pg, grid, smem, stream);
 }
 
 }  // namespace cider

@@ -111,6 +111,7 @@ struct GemvArgs {
     unsigned long long* status;   // device status word
     int x_bf16;
     int y_bf16;
+    int a16;     // A16 decode product: x used as it is, weights dequantized, fp32 sums
 };
 
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
