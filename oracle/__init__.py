@@ -75,6 +75,8 @@ def _load():
             lib.oracle_w8a8_linear_ex.argtypes = [p, i32, i64, i64, i64, p, p, i32, p, i32]
             lib.oracle_w4a8_linear_ex.argtypes = [p, i32, i64, i64, i64, p, p, i32, p, i32]
             lib.oracle_a16_gemv.argtypes = [p, i32, i64, i64, p, i32, p, i32, p]
+            lib.oracle_quantize_weight_pct.argtypes = [p, i32, i64, i64, i32, ctypes.c_double,
+                                                       ctypes.c_float, p, p]
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_set_threads.restype = None
             lib.oracle_get_threads.restype = ctypes.c_int
@@ -319,3 +321,29 @@ def a16_gemv(x, w, s_w, bits: int = 8, group_size: int = 0, x_dtype: str = "f16"
     if rc:
         raise ValueError("unsupported bits / group_size")
     return y
+
+
+def quantize_weight_clipped(w, group_size: int = 0, clip_percentile: float = 99.9,
+                            bits: int = 8, w_dtype: str = "f16"):
+    """Weight quantization with percentile-clipped scales (README "LLM
+    Quantization" note: "the 99th percentile method (clip_percentile=99.9)"):
+    per block (output channel, or group of ``group_size``), the clip value is
+    the ``clip_percentile``-th percentile of |w| (linear interpolation between
+    order statistics), scale = clip / qmax, codes = clamp(rint(w / scale)).
+    bits 8: returns (wq int8 [N,K], s_w); bits 4: (packed uint8 [N,K/2],
+    s_w), nibble = code + 8, element 2j in the low nibble."""
+    wb = _bits(w, w_dtype)
+    N, K = wb.shape
+    G = 1 if group_size == 0 else K // group_size
+    codes = np.empty((N, K), np.int8)
+    s = np.empty((N, G), np.float32)
+    qmax = 127.0 if bits == 8 else 7.0
+    rc = _load().oracle_quantize_weight_pct(_ptr(wb), _DTYPES[w_dtype], N, K, group_size,
+                                            float(clip_percentile), qmax, _ptr(codes), _ptr(s))
+    if rc:
+        raise ValueError("unsupported K / group_size / percentile")
+    s = s[:, 0].copy() if group_size == 0 else s
+    if bits == 8:
+        return codes, s
+    nib = (codes.astype(np.int16) + 8).astype(np.uint8)
+    return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8), s

@@ -238,6 +238,80 @@ static float quantize_block(const uint16_t* v, int64_t n, float qmax, int8_t* ou
     return quantize_block_t(v, n, qmax, out, ORACLE_F16);
 }
 
+/* ------------------------------------------------------------------------ */
+/* Percentile-clipped weight scales (README "LLM Quantization" note: besides */
+/* min-max, "the 99th percentile method (clip_percentile=99.9)").           */
+/* Reading: the clip value c of a block is the p-th percentile of its |w|,  */
+/* by linear interpolation between order statistics (sorted |w| q[0..n),     */
+/* position h = (n - 1) * p / 100, c = q[i] + (h - i) * (q[i+1] - q[i]),     */
+/* i = floor(h), evaluated in binary64 and rounded to binary32); then        */
+/* scale = c / qmax and code = clamp(rint(w / scale)) as for min-max, values */
+/* beyond c saturating at +-qmax. p = 100 gives c = absmax (min-max).        */
+/* ------------------------------------------------------------------------ */
+
+static int cmp_float(const void* a, const void* b)
+{
+    float x = *(const float*)a, y = *(const float*)b;
+    return (x > y) - (x < y);
+}
+
+static float quantize_block_pct(const uint16_t* v, int64_t n, float qmax, double pct,
+                                int8_t* out, int dtype)
+{
+    float* q = (float*)malloc((size_t)n * sizeof(float));
+    if (!q)
+        return -1.0f;
+    for (int64_t k = 0; k < n; ++k)
+        q[k] = fabsf(elem_to_float(v[k], dtype));
+    qsort(q, (size_t)n, sizeof(float), cmp_float);
+    double h = (double)(n - 1) * pct / 100.0;
+    int64_t i = (int64_t)floor(h);
+    double c = (i + 1 < n) ? (double)q[i] + (h - (double)i) * ((double)q[i + 1] - (double)q[i])
+                           : (double)q[n - 1];
+    free(q);
+    float clip = (float)c;
+    if (clip == 0.0f) {
+        for (int64_t k = 0; k < n; ++k)
+            out[k] = 0;
+        return 0.0f;
+    }
+    float scale = clip / qmax;
+    for (int64_t k = 0; k < n; ++k) {
+        float r = rintf(elem_to_float(v[k], dtype) / scale);
+        if (r > qmax)
+            r = qmax;
+        if (r < -qmax)
+            r = -qmax;
+        out[k] = (int8_t)r;
+    }
+    return scale;
+}
+
+/* Codes [N,K] (int8, in [-qmax, qmax]) and scales [N, K/gs] of weights w
+   (fp16, or bf16 with w_dtype 1) with percentile-clipped scales; qmax 127
+   (INT8) or 7 (INT4, packed by the caller). */
+int oracle_quantize_weight_pct(const uint16_t* w, int32_t w_dtype, int64_t N, int64_t K,
+                               int32_t group_size, double pct, float qmax, int8_t* codes,
+                               float* s_w)
+{
+    if (group_size < 0 || (group_size > 0 && K % group_size != 0) || !(pct > 0.0) ||
+        pct > 100.0)
+        return 1;
+    int64_t gs = group_size ? group_size : K;
+    int64_t G = K / gs;
+    int rc = 0;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < G; ++g) {
+            float sc = quantize_block_pct(w + n * K + g * gs, gs, qmax, pct,
+                                          codes + n * K + g * gs, w_dtype);
+            if (sc < 0.0f)
+                rc = 2;
+            s_w[n * G + g] = sc;
+        }
+    return rc;
+}
+
 /* Per-token activation quantization: x [M,K] (fp16, or bf16 with x_dtype 1)
    -> q int8 [M,K], s [M]. */
 void oracle_quantize_act_ex(const uint16_t* x, int32_t x_dtype, int64_t M, int64_t K, int8_t* q,

@@ -464,3 +464,40 @@ def test_a16_gemv_hand_examples():
     # bf16 input reads the same exact values
     xb = oracle.float_to_bf16(x.astype(np.float32))
     assert oracle.a16_gemv(xb, wq, s, 8, 0, x_dtype="bf16").tolist() == [75.0, 63.5, 0.25]
+
+
+# ---------------------------------------------------------------------------
+# percentile-clipped weight scales (clip_percentile)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("gs", [0, 64])
+@pytest.mark.parametrize("bits", [8, 4])
+def test_clip_percentile_100_is_min_max(gs, bits):
+    w = (np.random.default_rng(30 + gs + bits).standard_normal((9, 256)) * 0.02).astype(np.float16)
+    got = oracle.quantize_weight_clipped(w, gs, 100.0, bits)
+    ref = oracle.quantize_weight_int8(w, gs) if bits == 8 else oracle.pack_weight_int4(w, gs)
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+@pytest.mark.parametrize("pct", [99.9, 99.0, 50.0, 1.0])
+def test_clip_value_matches_numpy_percentile(pct):
+    """The scale is numpy's linear-interpolation percentile of |w| (float64,
+    rounded to float32) divided by qmax; codes saturate beyond the clip."""
+    rng = np.random.default_rng(int(pct * 10))
+    w = (rng.standard_normal((7, 1024)) * 0.05).astype(np.float16)
+    wq, s = oracle.quantize_weight_clipped(w, 128, pct, 8)
+    a = np.abs(w.astype(np.float64)).reshape(7, 8, 128)
+    clip = np.percentile(a, pct, axis=2, method="linear").astype(np.float32)
+    assert np.array_equal(s, clip / np.float32(127.0))
+    x = w.astype(np.float32).reshape(7, 8, 128) / s[:, :, None]
+    ref = np.clip(np.rint(x), -127, 127).astype(np.int8).reshape(7, 1024)
+    assert np.array_equal(wq, ref)
+
+
+def test_clip_percentile_hand_example():
+    """|w| = 1..5 (one block of 8 with three zeros): the 50th percentile of
+    [0, 0, 0, 1, 2, 3, 4, 5] sits at position 3.5 -> 1.5; scale 1.5 / 127."""
+    w = np.array([[0, 1, -2, 3, 0, -4, 5, 0]], np.float16)
+    wq, s = oracle.quantize_weight_clipped(w, 0, 50.0, 8)
+    assert s[0] == np.float32(1.5) / np.float32(127.0)
+    assert wq.tolist() == [[0, 85, -127, 127, 0, -127, 127, 0]]
