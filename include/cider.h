@@ -109,6 +109,26 @@ CIDER_API cider_status cider_pack_weight_int4(const void* w_f16, int64_t N, int6
                                     uint8_t* wp, float* s_w, void* stream);
 
 /*
+ * Weight preparation with percentile-clipped scales (README "LLM
+ * Quantization" note: besides min-max, "the 99th percentile method
+ * (clip_percentile=99.9)"). Per block (output channel for group_size 0,
+ * else each group of group_size along K) the clip value is the
+ * clip_percentile-th percentile of |w| by linear interpolation between order
+ * statistics (position (n - 1) * p / 100 in the sorted |w|), scale = clip /
+ * qmax (127 for bits 8, 7 for bits 4), codes clamp(rint(w / scale)): values
+ * beyond the clip saturate. clip_percentile 100 equals min-max.
+ *   w [N,K] fp16 (w_dtype CIDER_DTYPE_F16) or bf16; wq out: int8 [N,K] (bits
+ *   8) or packed uint8 [N,K/2] (bits 4, nibble = code + 8, element 2j low);
+ *   s_w out [N] or [N, K/gs] fp32.
+ * clip_percentile in (0, 100]; block size a multiple of 8 and <= 16384;
+ * w and wq 16-byte aligned.
+ */
+CIDER_API cider_status cider_quantize_weight_clipped(const void* w, int32_t w_dtype, int64_t N,
+                                                     int64_t K, int32_t group_size, int32_t bits,
+                                                     double clip_percentile, void* wq,
+                                                     float* s_w, void* stream);
+
+/*
  * Bytes of device workspace the GEMM calls below need for this problem
  * (bits 8 or 4). The workspace holds the fp16 operand images of the
  * quantized activations and weights and the per-token scales, and for

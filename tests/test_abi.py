@@ -89,3 +89,12 @@ def test_a16_gemv_checks_precede_cuda(lib):
     assert lib.cider_a16_gemv(p, 0, 64, 16, p, 6, p, 0, p, 0, None) == 1
     assert lib.cider_a16_gemv(p, 2, 64, 16, p, 8, p, 0, p, 0, None) == 1
     assert lib.cider_a16_gemv(p, 0, 64, 16, p, 8, p, 0, p, 3, None) == 1
+
+
+def test_clipped_weight_prep_checks_precede_cuda(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: checks fail first
+    assert lib.cider_quantize_weight_clipped(p, 0, 4, 64, 0, 8, 0.0, p, p, None) == 1
+    assert lib.cider_quantize_weight_clipped(p, 0, 4, 64, 0, 8, 100.5, p, p, None) == 1
+    assert lib.cider_quantize_weight_clipped(p, 0, 4, 64, 0, 5, 99.9, p, p, None) == 1
+    assert lib.cider_quantize_weight_clipped(None, 0, 4, 64, 0, 8, 99.9, p, p, None) == 1
+    assert lib.cider_quantize_weight_clipped(p, 0, 4, 64, 60, 8, 99.9, p, p, None) == 2

@@ -24,7 +24,7 @@ ABI_FUNCTIONS = (
     "cider_status_string", "cider_abi_version", "cider_quantize_act",
     "cider_quantize_weight_int8", "cider_pack_weight_int4", "cider_workspace_bytes",
     "cider_w8a8_gemm_pc", "cider_w8a8_gemm_pg", "cider_w4a8_gemm", "cider_int8_gemv",
-    "cider_linear", "cider_quantize_act_ex", "cider_a16_gemv",
+    "cider_linear", "cider_quantize_act_ex", "cider_a16_gemv", "cider_quantize_weight_clipped",
     "cider_w8a8_gemm_pc_noalloc",
     "cider_act_image", "cider_weight_image", "cider_gemm_images",
     "cider_test_gemm_s32", "cider_device_status", "cider_test_wait_timeout",
@@ -76,6 +76,8 @@ def load_library():
                              ctypes.c_int),
             "cider_quantize_act_ex": ([p, i32, i64, i64, p, p, p], ctypes.c_int),
             "cider_a16_gemv": ([p, i32, i64, i64, p, i32, p, i32, p, i32, p], ctypes.c_int),
+            "cider_quantize_weight_clipped": ([p, i32, i64, i64, i32, i32, ctypes.c_double, p,
+                                               p, p], ctypes.c_int),
             "cider_w8a8_gemm_pc_noalloc": ([p, i64, i64, i64, p, p, p, p], ctypes.c_int),
             "cider_act_image": ([p, i64, i64, p, p, p], ctypes.c_int),
             "cider_weight_image": ([p, i64, i64, i32, p, p], ctypes.c_int),
@@ -257,6 +259,24 @@ def a16_gemv(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
         _DTYPE_CODES[out_dtype], _stream())
     _check("cider_a16_gemv", st)
     return y
+
+
+def quantize_weight_clipped(w: torch.Tensor, group_size: int = 0, clip_percentile: float = 99.9,
+                            bits: int = 8):
+    """Weight preparation with percentile-clipped scales (fp16 or bf16 w
+    [N,K]): returns (int8 [N,K] or packed uint8 [N,K/2], s_w fp32 [N] or
+    [N, K/gs])."""
+    if w.dtype not in _DTYPE_CODES:
+        raise ValueError(f"w must be float16 or bfloat16, got {w.dtype}")
+    N, K = w.shape
+    G = 1 if group_size == 0 else K // group_size
+    wq = torch.empty((N, K) if bits == 8 else (N, K // 2),
+                     dtype=torch.int8 if bits == 8 else torch.uint8, device=w.device)
+    s = torch.empty((N,) if group_size == 0 else (N, G), dtype=torch.float32, device=w.device)
+    _check("cider_quantize_weight_clipped", load_library().cider_quantize_weight_clipped(
+        _dev(w, w.dtype, "w", 2), _DTYPE_CODES[w.dtype], N, K, group_size, bits,
+        float(clip_percentile), wq.data_ptr(), s.data_ptr(), _stream()))
+    return wq, s
 
 
 def quantize_act_any(x: torch.Tensor):

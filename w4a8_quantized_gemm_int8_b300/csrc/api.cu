@@ -202,6 +202,24 @@ cider_status cider_pack_weight_int4(const void* w_f16, int64_t N, int64_t K, int
                                          static_cast<cudaStream_t>(stream)));
 }
 
+cider_status cider_quantize_weight_clipped(const void* w, int32_t w_dtype, int64_t N, int64_t K,
+                                           int32_t group_size, int32_t bits,
+                                           double clip_percentile, void* wq, float* s_w,
+                                           void* stream) {
+    if (!w || !wq || !s_w) return CIDER_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || group_size < 0 || !valid_dtype(w_dtype)) return CIDER_ERR_INVALID_ARG;
+    if (bits != 8 && bits != 4) return CIDER_ERR_INVALID_ARG;
+    if (!(clip_percentile > 0.0) || clip_percentile > 100.0) return CIDER_ERR_INVALID_ARG;
+    const int64_t gs = group_size ? group_size : K;
+    if (K % gs != 0 || gs % 8 != 0 || gs > 16384) return CIDER_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(wq)) return CIDER_ERR_UNSUPPORTED;
+    if (N * (K / gs) > INT32_MAX) return CIDER_ERR_UNSUPPORTED;
+    return from_cuda(launch_quant_groups_pct(w, elem(w_dtype), N, K, gs, bits == 8 ? 127 : 7,
+                                             clip_percentile,
+                                             bits == 8 ? QuantOut::kInt8 : QuantOut::kInt4, wq,
+                                             s_w, static_cast<cudaStream_t>(stream)));
+}
+
 size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bits, int32_t group_size) {
     if (M <= 1 || N <= 0 || K <= 0 || (bits != 8 && bits != 4)) return 0;
     if (group_size < 0 || (group_size > 0 && K % group_size != 0)) return 0;

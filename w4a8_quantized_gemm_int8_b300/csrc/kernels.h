@@ -43,6 +43,14 @@ cudaError_t launch_quant_groups(const void* src, ElemType src_type, int64_t rows
                                 int64_t gs, int qmax, QuantOut out_kind, void* out,
                                 float* scales, int num_sms, cudaStream_t stream);
 
+// Weight quantization with percentile-clipped scales (offline preparation):
+// per block of gs elements (gs % 8 == 0, gs <= 16384), clip = the pct-th
+// percentile of |w| (linear interpolation between order statistics), scale
+// = clip / qmax; codes as int8 or packed nibbles (out_kind kInt8 / kInt4).
+cudaError_t launch_quant_groups_pct(const void* src, ElemType src_type, int64_t rows, int64_t K,
+                                    int64_t gs, int qmax, double pct, QuantOut out_kind,
+                                    void* out, float* scales, cudaStream_t stream);
+
 // Both operand images of the tensor-core GEMM in one launch: x fp16 [M,K] ->
 // a_img (exact fp16 codes) + s_a, and weights (INT8 [N,K] or packed INT4
 // [N,K/2]) -> b_img (exact fp16 integers; skipped when w is NULL); with s_wT

@@ -199,6 +199,68 @@ __global__ void __launch_bounds__(256) quant_groups_scalar_kernel(const T* __res
     }
 }
 
+// Percentile-clipped scales (weight preparation, offline): one block per
+// (row, group). The |w| of the group, as fp32 bit patterns (which order like
+// the values for non-negative numbers), are sorted in shared memory with a
+// bitonic network (padding sorts last); the clip value is the pct-th
+// percentile by linear interpolation between order statistics (position
+// (n - 1) pct / 100, in fp64, rounded to fp32); scale = clip / qmax and codes
+// clamp(rint(w / scale)). Requires gs % 8 == 0 (8-element vectors).
+template <typename T, QuantOut OUT>
+__global__ void __launch_bounds__(256) quant_groups_pct_kernel(const T* __restrict__ src,
+                                                               int64_t rows, int64_t K,
+                                                               int64_t gs, int qmax, double pct,
+                                                               int npad, void* __restrict__ out,
+                                                               float* __restrict__ scales) {
+    extern __shared__ uint32_t keys[];
+    __shared__ float clip_s;
+    const int64_t G = K / gs;
+    const int64_t item = blockIdx.x;
+    if (item >= rows * G) return;
+    const int64_t row = item / G, g = item - row * G;
+    const int64_t base = row * K + g * gs;
+    for (int i = threadIdx.x; i < npad; i += blockDim.x)
+        keys[i] = (i < gs) ? __float_as_uint(fabsf(elem_to_float(src[base + i]))) : 0xFFFFFFFFu;
+    __syncthreads();
+    for (int k = 2; k <= npad; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < npad; i += blockDim.x) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const uint32_t a = keys[i], b = keys[ixj];
+                    if ((a > b) == ((i & k) == 0)) {
+                        keys[i] = b;
+                        keys[ixj] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (threadIdx.x == 0) {
+        const double h = (double)(gs - 1) * pct / 100.0;
+        const int64_t i = (int64_t)floor(h);
+        const double lo = (double)__uint_as_float(keys[i]);
+        const double c =
+            (i + 1 < gs) ? lo + (h - (double)i) * ((double)__uint_as_float(keys[i + 1]) - lo) : lo;
+        clip_s = (float)c;
+    }
+    __syncthreads();
+    const float clip = clip_s;
+    const float s = (clip == 0.0f) ? 0.0f : __fdiv_rn(clip, (float)qmax);
+    if (threadIdx.x == 0) scales[item] = s;
+    for (int64_t v = threadIdx.x; v < gs / 8; v += blockDim.x) {
+        int q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float x = elem_to_float(src[base + 8 * v + j]);
+            int c = (s == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(x, s));
+            q[j] = max(-qmax, min(qmax, c));
+        }
+        store_codes8<OUT>(out, base + 8 * v, q);
+    }
+}
+
 // INT8 codes -> exact fp16 integers (operand image), 16 codes per thread step,
 // four steps' loads in flight per thread.
 __device__ __forceinline__ void widen_i8_body(const int8_t* __restrict__ src, int64_t n16,
@@ -429,6 +491,39 @@ cudaError_t launch_quant_groups(const void* src, ElemType src_type, int64_t rows
                                      out_kind, out, scales, num_sms, stream);
     return launch_quant_groups_t(static_cast<const __half*>(src), rows, K, gs, qmax, out_kind,
                                  out, scales, num_sms, stream);
+}
+
+cudaError_t launch_quant_groups_pct(const void* src, ElemType src_type, int64_t rows, int64_t K,
+                                    int64_t gs, int qmax, double pct, QuantOut out_kind,
+                                    void* out, float* scales, cudaStream_t stream) {
+    if (gs <= 0 || K % gs != 0 || gs % 8 != 0 || gs > 16384 || !(pct > 0.0) || pct > 100.0 ||
+        out_kind == QuantOut::kF16)
+        return cudaErrorInvalidValue;
+    const int64_t items = rows * (K / gs);
+    if (items <= 0 || items > INT32_MAX) return cudaErrorInvalidValue;
+    int npad = 1;
+    while (npad < gs) npad <<= 1;
+    const size_t smem = (size_t)npad * 4;
+    if (src_type == ElemType::kBF16) {
+        const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(src);
+        auto k8 = quant_groups_pct_kernel<__nv_bfloat16, QuantOut::kInt8>;
+        auto k4 = quant_groups_pct_kernel<__nv_bfloat16, QuantOut::kInt4>;
+        auto kern = (out_kind == QuantOut::kInt8) ? k8 : k4;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)items, 256, smem, stream>>>(p, rows, K, gs, qmax, pct, npad, out, scales);
+        return cudaGetLastError();
+    }
+    const __half* p = static_cast<const __half*>(src);
+    auto k8 = quant_groups_pct_kernel<__half, QuantOut::kInt8>;
+    auto k4 = quant_groups_pct_kernel<__half, QuantOut::kInt4>;
+    auto kern = (out_kind == QuantOut::kInt8) ? k8 : k4;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)items, 256, smem, stream>>>(p, rows, K, gs, qmax, pct, npad, out, scales);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_widen_i8(const int8_t* src, int64_t n, __half* dst, int num_sms,
