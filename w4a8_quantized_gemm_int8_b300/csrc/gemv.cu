@@ -14,7 +14,7 @@
 // starts ahead of the wait on that kernel (programmatic dependent launch):
 // it stages the per-channel scales of its rows, then issues bulk
 // asynchronous copies (cp.async.bulk, mbarrier completion) of whole groups of
-// rows into a ring of shared-memory stages - two at once, the rest as soon as
+// rows into a ring of shared-memory stages - one at once, the rest as soon as
 // the consumers hold x (so x's load does not queue behind the copies); for
 // the decode shapes the whole slice fits the ring. Sixteen consumer warps
 // wait for the preceding kernel, quantize x into shared memory, then take
@@ -41,7 +41,7 @@ constexpr int kMaxStages = 32;
 constexpr int kUnroll = 4;          // 16-byte chunks per lane loaded before use
 constexpr int kXVec = kMaxK / 8 / kConsumers;  // 8-element x vectors per consumer thread
 static_assert(kMaxK % (8 * kConsumers) == 0, "x vectors per thread");
-constexpr int kEarlyStages = 2;  // copies issued before x is in registers
+constexpr int kEarlyStages = 1;  // copies issued before x is in registers
 
 struct Params {
     const void* x;     // fp16 or bf16 (kernel template parameter)
