@@ -59,7 +59,7 @@ def _rank_main(rank, world, port, gs, out):
 @pytest.mark.parametrize("gs", [0, 64])
 def test_gathered_shards_equal_the_unsplit_layer(gs):
     world = 3
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), gs, out), nprocs=world, join=True)
         res = dict(out)
