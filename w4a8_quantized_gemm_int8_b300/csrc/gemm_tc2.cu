@@ -41,7 +41,8 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
 constexpr int NUM_ROLE_THREADS = 128;
 constexpr int NUM_THREADS = NUM_ROLE_THREADS + NUM_EPI_THREADS;
-constexpr int TMEM_COLS = 512;  // two accumulator buffers of 256 columns
+constexpr int TMEM_COLS = 512;  // accumulator buffers: 2 x 256 or 4 x 128 columns
+constexpr int MAX_ACC = 4;       // accumulator buffers at most
 constexpr int MAX_SEG_KB = 16;  // 16 x 64 = 1024 k per exact fp32 segment
 constexpr int LAUNCH_REGS = 168;
 constexpr int ROLE_REGS = 40;    // TMA and MMA issue need few registers
@@ -52,18 +53,25 @@ static_assert(NUM_ROLE_THREADS * ROLE_REGS + NUM_EPI_THREADS * EPI_REGS <=
                   NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch allocation");
 constexpr uint16_t kPairMask = 0x3;
+// Per-group modes: tile width and groups per accumulator buffer.
+constexpr int PG_BN = 256;
+constexpr int PG_GPB = 1;
 
 // Per-instantiation tile shape. BN: output columns per pair tile (each CTA
-// loads BN / 2 weight rows). All modes run 256-wide tiles, where the MMA
-// issues at its full rate. The kernel also takes 128-wide tiles that keep two
-// groups' partials side by side in one 256-column TMEM buffer (one hand-over
-// per two groups, 64 columns per epilogue warp); measured on B300 they were
-// slower for group size 128 (M = 4096: 380 vs 316 us) and only 10 % faster
-// for group size 64, so they are not launched.
-template <int BN>
+// loads BN / 2 weight rows); GPB: groups whose partials sit side by side in
+// one TMEM accumulator buffer (TMEM_COLS / (GPB * BN) buffers in flight).
+// All modes run 256-wide tiles with one group per buffer (two buffers), where
+// the MMA issues at its full rate. Measured on B300 (public call, per-group
+// N2560 K10240, M = 4096, gs 64 / gs 128; all shapes bit-exact):
+//   BN 256, GPB 1 (two buffers):   493 / 316 us  (launched)
+//   BN 128, GPB 2 (two buffers):   475 / 382 us
+//   BN 128, GPB 1 (four buffers):  551 / 420 us
+// and at M = 1024 and 8192 the launched shape is the fastest of the three.
+template <int BN, int GPB>
 struct Cfg {
-    static constexpr int kGroups = (BN == 128) ? 2 : 1;
+    static constexpr int kGroups = GPB;            // groups side by side in one buffer
     static constexpr int kBufCols = kGroups * BN;  // one TMEM accumulator buffer
+    static constexpr int kNumAcc = TMEM_COLS / kBufCols;  // buffers in flight
     static constexpr int kCols = BN / 2;           // columns per epilogue warp and group
     static constexpr int kChunks = kCols / 32;     // 32-column TMEM loads per warp and group
     static constexpr int kScaleSet = kGroups * kCols;  // scale floats per warp and segment
@@ -75,22 +83,24 @@ struct Cfg {
     static constexpr int kStages = (SMEM_LIMIT - kFixedBytes) / kStageBytes < MAX_STAGES
                                        ? (SMEM_LIMIT - kFixedBytes) / kStageBytes
                                        : MAX_STAGES;
-    static_assert(2 * kBufCols == TMEM_COLS, "two accumulator buffers fill TMEM");
+    static_assert(kNumAcc * kBufCols == TMEM_COLS && kNumAcc >= 2 && kNumAcc <= MAX_ACC &&
+                      (kNumAcc & (kNumAcc - 1)) == 0,
+                  "accumulator buffers fill TMEM");
     static_assert(kStages >= 4, "pipeline depth");
 };
 
 struct __align__(8) Barriers {
     uint64_t full[MAX_STAGES];   // even CTA: both CTAs' tile bytes landed
     uint64_t empty[MAX_STAGES];  // each CTA: the MMAs reading the stage completed
-    uint64_t acc_full[2];        // each CTA: accumulator buffer ready
-    uint64_t acc_empty[2];       // even CTA: both CTAs' epilogues drained the buffer
+    uint64_t acc_full[MAX_ACC];   // each CTA: accumulator buffer ready
+    uint64_t acc_empty[MAX_ACC];  // even CTA: both CTAs' epilogues drained the buffer
     uint64_t drain;              // even CTA: MMA drain after an abort
 };
 static_assert(sizeof(Barriers) <= 256, "barrier area");
 
-template <int BN>
+template <int BN, int GPB>
 struct SmemLayout {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, GPB>;
     static constexpr int STAGES = C::kStages;
     static constexpr int a_off = 0;
     static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
@@ -137,13 +147,13 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int&
     tn = tile / tiles_m;
 }
 
-template <GemmMode MODE, int BN>
+template <GemmMode MODE, int BN, int GPB>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_y, const Params p) {
-    using C = Cfg<BN>;
-    using SmemLayout = gemm2::SmemLayout<BN>;
+    using C = Cfg<BN, GPB>;
+    using SmemLayout = gemm2::SmemLayout<BN, GPB>;
     constexpr int STAGES = SmemLayout::STAGES;
     constexpr int COLS = C::kCols;
     constexpr int GS = C::kGroups;
@@ -167,7 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             mbar_init(smem_u32(&bars->full[s]), 1);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kNumAcc; ++b) {
             mbar_init(smem_u32(&bars->acc_full[b]), 1);
             mbar_init(smem_u32(&bars->acc_empty[b]), 2 * NUM_EPI_WARPS);
         }
@@ -239,8 +249,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             bool issued_any = false;
             for (int tile = cluster; tile < num_tiles; tile += nclusters) {
                 for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
-                    const uint32_t b = seg_count & 1;
-                    const uint32_t acc_phase = (seg_count >> 1) & 1;
+                    const uint32_t b = seg_count % C::kNumAcc;
+                    const uint32_t acc_phase = (seg_count / C::kNumAcc) & 1;
                     if (!mbar_wait_bounded(smem_u32(&bars->acc_empty[b]), acc_phase ^ 1,
                                            p.timeout_ns, abort_flag, p.status, kSiteMmaAccEmpty))
                         goto mma_done;
@@ -354,8 +364,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                 for (int j = 0; j < COLS; ++j) acc[j] = 0u;  // f = +0 before the first group
             }
             for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
-                const uint32_t b = seg_count & 1;
-                const uint32_t acc_phase = (seg_count >> 1) & 1;
+                const uint32_t b = seg_count % C::kNumAcc;
+                const uint32_t acc_phase = (seg_count / C::kNumAcc) & 1;
                 const bool last_seg = (seg == p.num_seg - 1);
                 const bool uses_scales = (MODE == GemmMode::kPgF16) || last_seg;
                 const float* sc = wsc + sbuf * C::kScaleSet;
@@ -547,6 +557,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                     }
                 }
 
+                // After the release: whatever the epilogue does between the
+                // accumulator-ready wait and the release delays the MMAs two
+                // segments on (two buffers). Waiting here for the next set was
+                // 11 % faster at group size 64 than waiting for it right before
+                // its use, and a four-set ring fetched three segments ahead
+                // gained nothing over two sets.
                 if (uses_scales) {
                     scales_ready();
                     sbuf ^= 1;
@@ -580,12 +596,12 @@ struct PairLaunchInfo {
     int max_clusters = 0;
 };
 
-template <GemmMode MODE, int BN>
+template <GemmMode MODE, int BN, int GPB>
 cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                              const gemm2::Params& p, int num_sms, cudaStream_t stream) {
     using namespace gemm2;
-    using SmemLayout = gemm2::SmemLayout<BN>;
-    auto kern = gemm_tc2_kernel<MODE, BN>;
+    using SmemLayout = gemm2::SmemLayout<BN, GPB>;
+    auto kern = gemm_tc2_kernel<MODE, BN, GPB>;
     static PairLaunchInfo info;  // benign race: every thread computes the same values
     if (!info.checked) {
         cudaFuncAttributes fa;
@@ -622,8 +638,9 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2)
         return cudaErrorInvalidValue;
     const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
-    constexpr int BN = 256;  // tile width of every mode's kernel
-    constexpr int GS = Cfg<BN>::kGroups;
+    // Tile width and groups per accumulator buffer of the mode's kernel.
+    const int BN = per_group ? PG_BN : 256;
+    const int GS = per_group ? PG_GPB : 1;
     CUtensorMap ta, tb, ty;
     if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS ||
         encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN / 2, BK) != CUDA_SUCCESS)
@@ -669,13 +686,15 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     p.status = a.status;
     switch (a.mode) {
         case GemmMode::kPcF16:
-            return launch_pair_mode<GemmMode::kPcF16, 256>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kPcF16, 256, 1>(ta, tb, ty, p, num_sms, stream);
         case GemmMode::kPgF16:
-            return launch_pair_mode<GemmMode::kPgF16, 256>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kPgF16, PG_BN, PG_GPB>(ta, tb, ty, p, num_sms,
+                                                                     stream);
         case GemmMode::kRawS32:
-            return launch_pair_mode<GemmMode::kRawS32, 256>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kRawS32, 256, 1>(ta, tb, ty, p, num_sms, stream);
         case GemmMode::kRawPgS32:
-            return launch_pair_mode<GemmMode::kRawPgS32, 256>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kRawPgS32, PG_BN, PG_GPB>(ta, tb, ty, p, num_sms,
+                                                                        stream);
     }
     return cudaErrorInvalidValue;
 }
