@@ -29,3 +29,32 @@ def cuda(t: torch.Tensor) -> torch.Tensor:
 
 def host(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy()
+
+
+def every_pair_rows(top: int, max_elems: int = 1 << 26):
+    """Batches of uint16 rows covering every pair (x, a) of a 16-bit float
+    format: for each positive finite bit pattern a in 1..top (ascending), one
+    row holding every pattern 0..a and its negation (sign bit set), so that a
+    is the row's absmax and every |x| <= a occurs with both signs; zero
+    padded to the batch width (a multiple of 16). Each batch holds at most
+    max_elems elements (the last absmax of a batch sets its width)."""
+    a = 1
+    while a <= top:
+        width = 2 * (a + 1)
+        width += (-width) % 16
+        n = 1
+        while a + n <= top:
+            w = 2 * (a + n + 1)
+            w += (-w) % 16
+            if (n + 1) * w > max_elems:
+                break
+            n += 1
+            width = w
+        rows = np.zeros((n, width), np.uint16)
+        for i in range(n):
+            v = a + i
+            xs = np.arange(v + 1, dtype=np.uint16)
+            rows[i, :v + 1] = xs
+            rows[i, v + 1:2 * v + 2] = xs | 0x8000
+        yield rows
+        a += n

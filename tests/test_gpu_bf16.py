@@ -10,7 +10,7 @@ import torch
 import oracle
 import synth
 import w4a8_quantized_gemm_int8_b300 as cider
-from gpu_helpers import cuda, host
+from gpu_helpers import cuda, every_pair_rows, host
 
 pytestmark = pytest.mark.gpu
 
@@ -73,6 +73,18 @@ def test_quantize_bf16_exhaustive_rows_up_to_16k():
     qo, so = oracle.quantize_act_bf16(xb)
     assert np.array_equal(host(s).view(np.uint32), so.view(np.uint32))
     assert np.array_equal(host(q), qo)
+
+
+def test_quantize_act_bf16_every_pair():
+    """Every finite bf16 x against every positive finite bf16 absmax a with
+    |x| <= a, both signs of x (about 10^9 pairs, one row per a): codes and
+    scales bit for bit."""
+    for rows in every_pair_rows(0x7F7F):
+        q, s = cider.quantize_act_any(_to_gpu_bf16(rows))
+        qo, so = oracle.quantize_act_bf16(rows)
+        assert np.array_equal(host(s).view(np.uint32), so.view(np.uint32)), rows.shape
+        assert np.array_equal(host(q), qo), rows.shape
+        del q, s
 
 
 def _weights(N, K, seed):

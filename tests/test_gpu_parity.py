@@ -12,7 +12,7 @@ import torch
 import oracle
 import synth
 import w4a8_quantized_gemm_int8_b300 as cider
-from gpu_helpers import assert_f16_within_1ulp, cuda, host
+from gpu_helpers import assert_f16_within_1ulp, cuda, every_pair_rows, host
 
 pytestmark = pytest.mark.gpu
 
@@ -116,6 +116,24 @@ def test_quantize_exhaustive_rows_up_to_16k():
     img, s2 = cider.act_image(cuda(torch.from_numpy(x)))
     assert np.array_equal(host(s2).view(np.uint32), so.view(np.uint32))
     assert np.array_equal(host(img).astype(np.int32), qo.astype(np.int32))
+
+
+def test_quantize_act_every_fp16_pair():
+    """Every finite fp16 x against every positive finite fp16 absmax a with
+    |x| <= a, both signs of x (about 10^9 pairs, one row per a, rows 11584
+    to 63488 elements wide): codes, scales and the fp16 operand image bit for
+    bit."""
+    for rows in every_pair_rows(0x7BFF):
+        x = rows.view(np.float16)
+        xd = cuda(torch.from_numpy(x))
+        q, s = cider.quantize_act(xd)
+        qo, so = oracle.quantize_act(x)
+        assert np.array_equal(host(s).view(np.uint32), so.view(np.uint32)), rows.shape
+        assert np.array_equal(host(q), qo), rows.shape
+        img, s2 = cider.act_image(xd)
+        assert np.array_equal(host(s2).view(np.uint32), so.view(np.uint32)), rows.shape
+        assert np.array_equal(host(img).astype(np.int32), qo.astype(np.int32)), rows.shape
+        del xd, q, s, img, s2
 
 
 # ---------------------------------------------------------------------------
