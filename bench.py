@@ -167,6 +167,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
 
 
+REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def clocks_rejected(info, low_frac: float = 0.9) -> bool:
+    """True when a clock record disqualifies its timed region: a hardware
+    or thermal slowdown was active, or the median SM clock sat below
+    low_frac of the maximum with no reason active (a clock held low by
+    someone else). sw_power_cap alone is kept. A missing record (no NVML)
+    rejects nothing."""
+    if not info or "sm_mhz" not in info:
+        return False
+    reasons = set(info.get("reasons", ()))
+    if reasons & set(REJECT_REASONS):
+        return True
+    return not reasons and info["sm_mhz"] < low_frac * info["sm_max_mhz"]
+
+
 def replica_max(v: float, world: int, device=None) -> float:
     """The slowest replica's time: the whole job's step time when N
     independent replicas run one per GPU (max over ranks of the process
@@ -497,20 +514,30 @@ def run_cider(args):
         step_i(i)
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    torch.cuda._sleep(int(2e5 * args.steps))  # host runs ahead of the GPU (see the GEMV leg)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        step_i(i)
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    clock_info = clocks.stop()
-    barrier()
-    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    def timed_region():
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(args.steps)]
+        clocks = ClockSampler(local)
+        barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        torch.cuda._sleep(int(2e5 * args.steps))  # host runs ahead of the GPU (see the GEMV leg)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step_i(i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        info = clocks.stop()
+        barrier()
+        return [e[0].elapsed_time(e[1]) for e in evs], info
+
+    step_ms, clock_info = timed_region()
+    # A region that saw a hardware or thermal slowdown, or clocks held low
+    # with no reason given, is measured once more (every rank together).
+    if max_over_ranks(1.0 if clocks_rejected(clock_info) else 0.0) > 0:
+        first = clock_info
+        step_ms, clock_info = timed_region()
+        clock_info = dict(clock_info or {}, remeasured_after=first)
     st, site = cider.device_status()
     assert st == cider.CIDER_OK, f"device status {st} at {site:#x}"
 
