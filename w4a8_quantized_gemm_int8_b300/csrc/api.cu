@@ -5,6 +5,7 @@
 
 #include "../../include/cider.h"
 #include "device_common.cuh"
+#include "host_once.h"
 #include "kernels.h"
 
 namespace {
@@ -12,21 +13,16 @@ namespace {
 using namespace cider;
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s bound on every device-side wait
-constexpr int kMaxDevices = 64;
-int g_num_sms[kMaxDevices] = {};
+PerDevice<int> g_num_sms;
 
 cider_status num_sms(int* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CIDER_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return CIDER_ERR_UNSUPPORTED;
-    if (g_num_sms[dev] == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return CIDER_ERR_CUDA;
-        g_num_sms[dev] = v;
-    }
-    *out = g_num_sms[dev];
-    return CIDER_OK;
+    const cudaError_t e = g_num_sms.get(dev, [dev](int& v) {
+        return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    }, out);
+    return e == cudaSuccess ? CIDER_OK : CIDER_ERR_CUDA;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -36,6 +36,7 @@
 #include <cstring>
 
 #include "device_common.cuh"
+#include "host_once.h"
 #include "kernels.h"
 
 namespace cider {
@@ -699,13 +700,12 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
                         const gemm1::Params& p, int grid, cudaStream_t stream) {
     using Layout = gemm1::SmemLayout<BSRC, BN>;
     auto kern = gemm1::gemm_tc1_kernel<MODE, BSRC, BN>;
-    static bool attr_set = false;  // benign race: setting the same value twice
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Layout::alloc_bytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static PerDevice<int> attr;  // the shared-memory opt-in, once per device
+    const cudaError_t e = attr.get([&](int&) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Layout::alloc_bytes);
+    });
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, gemm1::NUM_THREADS, Layout::alloc_bytes, stream, ta, tb, ty, p);
 }
 

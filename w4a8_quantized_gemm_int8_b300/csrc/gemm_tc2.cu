@@ -28,6 +28,7 @@
 #include <cstring>
 
 #include "device_common.cuh"
+#include "host_once.h"
 #include "kernels.h"
 
 namespace cider {
@@ -592,43 +593,37 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
 
 namespace {
 
-struct PairLaunchInfo {
-    bool checked = false;
-    bool ok = false;
-    int max_clusters = 0;
-};
-
 template <GemmMode MODE, int BN, int GPB>
 cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                              const gemm2::Params& p, int num_sms, cudaStream_t stream) {
     using namespace gemm2;
     using SmemLayout = gemm2::SmemLayout<BN, GPB>;
     auto kern = gemm_tc2_kernel<MODE, BN, GPB>;
-    static PairLaunchInfo info;  // benign race: every thread computes the same values
-    if (!info.checked) {
+    // Once per device: the register count the role/epilogue split assumes,
+    // the shared-memory opt-in, and how many pairs fit on the GPU at once
+    // (SMs pair up within a GPC).
+    static PerDevice<int> max_clusters_of;
+    int max_clusters = 0;
+    const cudaError_t e = max_clusters_of.get([&](int& n) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-        if (e != cudaSuccess) return e;
+        cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+        if (r != cudaSuccess) return r;
         if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SmemLayout::alloc_bytes);
-        if (e != cudaSuccess) return e;
-        // How many pairs fit on the GPU at once (SMs pair up within a GPC).
+        if (r != cudaSuccess) return r;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
         cfg.blockDim = dim3(NUM_THREADS, 1, 1);
         cfg.dynamicSmemBytes = SmemLayout::alloc_bytes;
         cfg.numAttrs = 0;  // the kernel's compile-time cluster shape (2, 1, 1) applies
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        info.max_clusters = n;
-        info.ok = n > 0;
-        info.checked = true;
-    }
-    if (!info.ok) return cudaErrorInvalidConfiguration;
+        r = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (r != cudaSuccess) return r;
+        return n > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+    }, &max_clusters);
+    if (e != cudaSuccess) return e;
     const int tiles = p.tiles_m * p.tiles_n;
-    const int clusters = tiles < info.max_clusters ? tiles : info.max_clusters;
+    const int clusters = tiles < max_clusters ? tiles : max_clusters;
     return launch_pdl(kern, 2 * clusters, NUM_THREADS, SmemLayout::alloc_bytes, stream, ta, tb, ty, p);
 }
 

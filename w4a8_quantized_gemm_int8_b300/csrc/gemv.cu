@@ -27,6 +27,7 @@
 #include <cstdint>
 
 #include "device_common.cuh"
+#include "host_once.h"
 #include "kernels.h"
 
 namespace cider {
@@ -424,29 +425,27 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
     }
 }
 
-int g_max_smem = 0;  // opt-in shared memory per block (queried once; same on every B300)
+PerDevice<int> g_max_smem;  // opt-in shared memory per block, per device
 
 template <typename T, int BITS, bool PG, bool A16>
-cudaError_t launch_one(const Params& p, int grid, int smem, cudaStream_t stream) {
+cudaError_t launch_one(const Params& p, int grid, int smem, int max_smem, cudaStream_t stream) {
     auto kern = gemv_kernel<T, BITS, PG, A16>;
-    static int attr_smem = 0;  // benign race: setting the same value twice
-    if (attr_smem < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             g_max_smem);
-        if (e != cudaSuccess) return e;
-        attr_smem = g_max_smem;
-    }
+    static PerDevice<int> attr;  // opt-in to the device's whole per-block shared memory
+    const cudaError_t e = attr.get([&](int&) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    });
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, kThreads, smem, stream, p);
 }
 
 template <typename T, bool A16>
-cudaError_t launch_bits(const Params& p, int bits, bool pg, int grid, int smem,
+cudaError_t launch_bits(const Params& p, int bits, bool pg, int grid, int smem, int max_smem,
                         cudaStream_t stream) {
     if (bits == 8)
-        return pg ? launch_one<T, 8, true, A16>(p, grid, smem, stream)
-                  : launch_one<T, 8, false, A16>(p, grid, smem, stream);
-    return pg ? launch_one<T, 4, true, A16>(p, grid, smem, stream)
-              : launch_one<T, 4, false, A16>(p, grid, smem, stream);
+        return pg ? launch_one<T, 8, true, A16>(p, grid, smem, max_smem, stream)
+                  : launch_one<T, 8, false, A16>(p, grid, smem, max_smem, stream);
+    return pg ? launch_one<T, 4, true, A16>(p, grid, smem, max_smem, stream)
+              : launch_one<T, 4, false, A16>(p, grid, smem, max_smem, stream);
 }
 
 }  // namespace
@@ -456,13 +455,15 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     if (a.bits != 8 && a.bits != 4) return cudaErrorInvalidValue;
     const int chunk_elems = (a.bits == 8) ? 16 : 32;
     if (a.K % chunk_elems != 0) return cudaErrorInvalidValue;
-    if (g_max_smem == 0) {
-        int dev = 0, v = 0;
+    int max_smem = 0;
+    {
+        int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            e = g_max_smem.get(dev, [dev](int& v) {
+                return cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            }, &max_smem);
         if (e != cudaSuccess) return e;
-        g_max_smem = v;
     }
     Params p{};
     p.x = a.x;
@@ -509,7 +510,7 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     p.bar_off = p.sw_off + sw_bytes;
     const int bar_bytes = 2 * kMaxStages * 8 + kConsumerWarps * 4 + 32;  // + abort flag, 2 barriers
     p.stage_off = (p.bar_off + bar_bytes + 127) & ~127;
-    const int budget = (g_max_smem / 2 - 1024) - p.stage_off;
+    const int budget = (max_smem / 2 - 1024) - p.stage_off;
     int ns = budget / p.stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
     if (ns > max_stages_needed) ns = max_stages_needed;
@@ -517,10 +518,12 @@ cudaError_t launch_gemv(const GemvArgs& a, int num_sms, cudaStream_t stream) {
     p.num_stages = ns;
     const int smem = p.stage_off + ns * p.stage_bytes;
     if (a.a16)
-        return a.x_bf16 ? launch_bits<__nv_bfloat16, true>(p, a.bits, pg, grid, smem, stream)
-                        : launch_bits<__half, true>(p, a.bits, pg, grid, smem, stream);
-    return a.x_bf16 ? launch_bits<__nv_bfloat16, false>(p, a.bits, pg, grid, smem, stream)
-                    : launch_bits<__half, false>(p, a.bits, pg, grid, smem, stream);
+        return a.x_bf16
+                   ? launch_bits<__nv_bfloat16, true>(p, a.bits, pg, grid, smem, max_smem, stream)
+                   : launch_bits<__half, true>(p, a.bits, pg, grid, smem, max_smem, stream);
+    return a.x_bf16
+               ? launch_bits<__nv_bfloat16, false>(p, a.bits, pg, grid, smem, max_smem, stream)
+               : launch_bits<__half, false>(p, a.bits, pg, grid, smem, max_smem, stream);
 }
 
 }  // namespace cider

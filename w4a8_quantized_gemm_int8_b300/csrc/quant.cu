@@ -12,6 +12,7 @@
 #include <cstdint>
 
 #include "device_common.cuh"
+#include "host_once.h"
 #include "kernels.h"
 
 namespace cider {
@@ -493,6 +494,43 @@ cudaError_t launch_quant_groups(const void* src, ElemType src_type, int64_t rows
                                  out, scales, num_sms, stream);
 }
 
+namespace {
+
+// Largest sort buffer of the clipped quantizer: groups of up to 16384
+// elements, padded to a power of two, 4 bytes each.
+constexpr int kPctMaxSmem = 16384 * 4;
+
+template <typename T, QuantOut OUT>
+cudaError_t launch_pct_out(const T* p, int64_t rows, int64_t K, int64_t gs, int qmax, double pct,
+                           int npad, size_t smem, void* out, float* scales, int64_t items,
+                           cudaStream_t stream) {
+    auto kern = quant_groups_pct_kernel<T, OUT>;
+    // Opt in once per device to the largest buffer any call needs, so that
+    // concurrent calls with different group sizes never lower it.
+    static PerDevice<int> attr;
+    const cudaError_t e = attr.get([&](int&) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kPctMaxSmem);
+    });
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)items, 256, smem, stream>>>(p, rows, K, gs, qmax, pct, npad, out, scales);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_pct(const T* p, int64_t rows, int64_t K, int64_t gs, int qmax, double pct,
+                       int npad, size_t smem, QuantOut out_kind, void* out, float* scales,
+                       int64_t items, cudaStream_t stream) {
+    if (smem > (size_t)kPctMaxSmem) return cudaErrorInvalidValue;
+    if (out_kind == QuantOut::kInt8)
+        return launch_pct_out<T, QuantOut::kInt8>(p, rows, K, gs, qmax, pct, npad, smem, out,
+                                                  scales, items, stream);
+    return launch_pct_out<T, QuantOut::kInt4>(p, rows, K, gs, qmax, pct, npad, smem, out, scales,
+                                              items, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_quant_groups_pct(const void* src, ElemType src_type, int64_t rows, int64_t K,
                                     int64_t gs, int qmax, double pct, QuantOut out_kind,
                                     void* out, float* scales, cudaStream_t stream) {
@@ -504,26 +542,12 @@ cudaError_t launch_quant_groups_pct(const void* src, ElemType src_type, int64_t 
     int npad = 1;
     while (npad < gs) npad <<= 1;
     const size_t smem = (size_t)npad * 4;
-    if (src_type == ElemType::kBF16) {
-        const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(src);
-        auto k8 = quant_groups_pct_kernel<__nv_bfloat16, QuantOut::kInt8>;
-        auto k4 = quant_groups_pct_kernel<__nv_bfloat16, QuantOut::kInt4>;
-        auto kern = (out_kind == QuantOut::kInt8) ? k8 : k4;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<(unsigned)items, 256, smem, stream>>>(p, rows, K, gs, qmax, pct, npad, out, scales);
-        return cudaGetLastError();
-    }
-    const __half* p = static_cast<const __half*>(src);
-    auto k8 = quant_groups_pct_kernel<__half, QuantOut::kInt8>;
-    auto k4 = quant_groups_pct_kernel<__half, QuantOut::kInt4>;
-    auto kern = (out_kind == QuantOut::kInt8) ? k8 : k4;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<(unsigned)items, 256, smem, stream>>>(p, rows, K, gs, qmax, pct, npad, out, scales);
-    return cudaGetLastError();
+    if (src_type == ElemType::kBF16)
+        return launch_pct<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(src), rows, K, gs,
+                                         qmax, pct, npad, smem, out_kind, out, scales, items,
+                                         stream);
+    return launch_pct<__half>(static_cast<const __half*>(src), rows, K, gs, qmax, pct, npad, smem,
+                              out_kind, out, scales, items, stream);
 }
 
 cudaError_t launch_widen_i8(const int8_t* src, int64_t n, __half* dst, int num_sms,

@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include "device_common.cuh"
+#include "host_once.h"
 #include "kernels.h"
 
 namespace cider {
@@ -26,23 +27,19 @@ __global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, unsigned long lon
     }
 }
 
-constexpr int kMaxDevices = 64;
-unsigned long long* g_status_ptr[kMaxDevices] = {};
+PerDevice<unsigned long long*> g_status_ptr;
 }  // namespace
 
 cudaError_t device_status_ptr(unsigned long long** ptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (g_status_ptr[dev] == nullptr) {
+    return g_status_ptr.get(dev, [](unsigned long long*& v) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_status_word);
-        if (e != cudaSuccess) return e;
-        g_status_ptr[dev] = static_cast<unsigned long long*>(p);
-    }
-    *ptr = g_status_ptr[dev];
-    return cudaSuccess;
+        const cudaError_t r = cudaGetSymbolAddress(&p, g_status_word);
+        v = static_cast<unsigned long long*>(p);
+        return r;
+    }, ptr);
 }
 
 cudaError_t read_and_clear_device_status(unsigned long long* value, cudaStream_t stream) {
