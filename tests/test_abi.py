@@ -98,3 +98,40 @@ def test_clipped_weight_prep_checks_precede_cuda(lib):
     assert lib.cider_quantize_weight_clipped(p, 0, 4, 64, 0, 5, 99.9, p, p, None) == 1
     assert lib.cider_quantize_weight_clipped(None, 0, 4, 64, 0, 8, 99.9, p, p, None) == 1
     assert lib.cider_quantize_weight_clipped(p, 0, 4, 64, 60, 8, 99.9, p, p, None) == 2
+
+
+_C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "cider.h"
+
+int main(void) {
+    /* host-only calls: version, status strings, workspace sizing, and the
+       argument checks that answer before any CUDA call */
+    size_t ws = cider_workspace_bytes(4096, 10240, 2560, 8, 0);
+    cider_status st = cider_w8a8_gemm_pc(NULL, 4, 8, 16, NULL, NULL, NULL, NULL, 0, NULL);
+    printf("%d %s %zu %d\n", cider_abi_version(), cider_status_string(CIDER_OK), ws, (int)st);
+    return st == CIDER_ERR_INVALID_ARG ? 0 : 1;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """The header compiles as C99 (no C++ or CUDA types in the signatures),
+    and a C program links against the library and calls it."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(_C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(cider.LIB_PATH)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-lcider", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == lib.cider_abi_version()
+    assert int(out[-2]) == lib.cider_workspace_bytes(4096, 10240, 2560, 8, 0)
+    assert int(out[-1]) == cider.CIDER_ERR_INVALID_ARG
