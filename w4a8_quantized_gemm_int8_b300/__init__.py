@@ -133,6 +133,8 @@ def workspace_bytes(M: int, N: int, K: int, bits: int = 8, group_size: int = 0) 
 def _workspace(nbytes: int, device) -> torch.Tensor | None:
     """A per-device workspace buffer, grown on demand (stream-ordered reuse:
     calls on one stream may share it)."""
+    if torch.device(device).type != "cuda":
+        raise ValueError("the layer's tensors must be CUDA tensors")
     if nbytes == 0:
         return None
     key = torch.device(device).index
