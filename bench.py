@@ -65,6 +65,9 @@ def parse_args():
                     help="run only the M = 1 GEMV leg (a small command for profilers)")
     ap.add_argument("--step-only", action="store_true",
                     help="run only the M = 4096 step (a small command for profilers)")
+    ap.add_argument("--small-step", action="store_true",
+                    help="run only the few-token per-channel call (M = 128, the single-SM "
+                         "engine): a small command for profilers")
     ap.add_argument("--configs", action="store_true",
                     help="time every workload of the config list (M sweeps, per-group, W4A8, "
                          "decoder layer) through the public calls; one JSON line")
@@ -762,12 +765,51 @@ def run_cider(args):
         dist.destroy_process_group()
 
 
+def run_small_step(args):
+    """The few-token per-channel public call alone (M = 128, N10240 K2560;
+    the single-SM engine): seeded codes and activations made on the GPU,
+    `warmup` calls, then `steps` calls timed with CUDA events. Prints the mean
+    call time. Small enough to run under a profiler."""
+    import torch
+    import w4a8_quantized_gemm_int8_b300 as cider
+    torch.cuda.set_device(0)
+    cider.load_library()
+    dev = torch.device("cuda:0")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    m = 128
+    x = torch.randn(m, K, generator=gen, device=dev).half()
+    wq = torch.randint(-127, 128, (N, K), generator=gen, device=dev, dtype=torch.int8)
+    s_w = torch.rand(N, generator=gen, device=dev) * 0.01 + 0.001
+    y = torch.empty(m, N, dtype=torch.float16, device=dev)
+    ws = torch.empty(max(1, cider.workspace_bytes(m, N, K, 8, 0)), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(args.warmup):
+        cider.w8a8_linear(x, wq, s_w, 0, out=y, ws=ws)
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        cider.w8a8_linear(x, wq, s_w, 0, out=y, ws=ws)
+        b.record(stream)
+    torch.cuda.synchronize()
+    st, site = cider.device_status()
+    assert st == cider.CIDER_OK, f"device status {st} at {site:#x}"
+    us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+    print(json.dumps({"small_step_us": us, "M": m, "N": N, "K": K,
+                      "TOPS": 2.0 * m * N * K / (us * 1e-6) / 1e12}))
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.configs:
         run_configs(args)
+    elif args.small_step:
+        run_small_step(args)
     else:
         run_cider(args)
 
