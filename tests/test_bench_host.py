@@ -31,3 +31,58 @@ def test_clock_held_low_without_reason_is_rejected():
 def test_missing_record_rejects_nothing():
     assert not bench.clocks_rejected(None)
     assert not bench.clocks_rejected({"error": "no NVML samples"})
+
+
+class _FakeNvml:
+    """Stands in for libnvidia-ml: a fixed SM clock and clock-event reason
+    mask, written through the ctypes pointers the sampler passes."""
+
+    def __init__(self, clocks, reasons):
+        self.clocks = list(clocks)
+        self.reasons = reasons
+        self.i = 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, ptr):
+        ptr._obj.value = self.clocks[min(self.i, len(self.clocks) - 1)]
+        self.i += 1
+        return 0
+
+    def reasons_fn(self, h, ptr):
+        ptr._obj.value = self.reasons
+        return 0
+
+
+def _sample(monkeypatch, clocks, reasons):
+    import time
+    fake = _FakeNvml(clocks, reasons)
+    s = bench.ClockSampler(0)
+    monkeypatch.setattr(s, "_open", lambda: (fake, None, 2032, fake.reasons_fn))
+    s.start()
+    time.sleep(0.05)
+    return s.stop()
+
+
+def test_sampler_reports_median_clock_and_decodes_reason_bits(monkeypatch):
+    info = _sample(monkeypatch, [2032], 0x4 | 0x40)
+    assert info["sm_mhz"] == 2032 and info["sm_max_mhz"] == 2032
+    assert info["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert info["samples"] >= 1 and info["source"] == "nvml"
+    assert bench.clocks_rejected(info)
+
+
+def test_sampler_without_reasons_keeps_the_run(monkeypatch):
+    info = _sample(monkeypatch, [2032], 0)
+    assert info["reasons"] == [] and not bench.clocks_rejected(info)
+
+
+def test_sampler_without_nvml_reports_the_error(monkeypatch):
+    s = bench.ClockSampler(0)
+
+    def no_nvml():
+        raise OSError("libnvidia-ml.so.1: cannot open shared object file")
+
+    monkeypatch.setattr(s, "_open", no_nvml)
+    s.start()
+    info = s.stop()
+    assert "error" in info and "libnvidia-ml" in info["error"]
+    assert not bench.clocks_rejected(info)
