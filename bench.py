@@ -705,9 +705,17 @@ def run_cider(args):
         oracle.build()
         x_np, wq_np, sw_np = cpu_inputs()
         rows = size_oracle_sample(x_np, wq_np, sw_np, args.cpu_seconds)
-        cpu_tops, cpu_dt = oracle_tops(x_np, wq_np, sw_np, rows)
+        # A host fast enough to finish the whole workload well inside the
+        # target repeats it (at most 16 passes), so the figure rests on about
+        # cpu_seconds of CPU work either way.
+        passes, cpu_dt = 0, 0.0
+        while passes == 0 or (passes < 16 and cpu_dt < 0.8 * args.cpu_seconds):
+            cpu_dt += oracle_tops(x_np, wq_np, sw_np, rows)[1]
+            passes += 1
+        cpu_tops = 2.0 * passes * rows * N * K / cpu_dt / 1e12
+        reps = f", {passes} passes" if passes > 1 else ""
         cpu = {"value": cpu_tops, "unit": "TOPS", "cores": oracle.get_threads(), "kind": "oracle",
-               "sample": f"{rows} of {M} token rows, full N={N}, K={K} ({cpu_dt:.1f} s)"}
+               "sample": f"{rows} of {M} token rows, full N={N}, K={K}{reps} ({cpu_dt:.1f} s)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
