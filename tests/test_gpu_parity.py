@@ -275,6 +275,29 @@ def test_w4a8_layer(M, N, K, gs):
     assert_f16_within_1ulp(host(y), ref, f"w4 gs{gs}")
 
 
+@pytest.mark.parametrize("cls,gs", [("W8A8Linear", 0), ("W8A8Linear", 64), ("W4A8Linear", 0),
+                                    ("W4A8Linear", 128)])
+def test_layer_classes_match_oracle(cls, gs):
+    """The layer-level names: from_weights prepares the weights on the GPU and
+    a call flattens leading dimensions into tokens (2 x 65 here, the pair
+    engine) or runs the GEMV for one token; outputs match the oracle's on the
+    same weights."""
+    M, N, K = 130, 300, 1024
+    x, w = _layer_inputs(M, N, K, seed=7 + gs)
+    layer = getattr(cider, cls).from_weights(cuda(torch.from_numpy(w)), gs)
+    if cls == "W8A8Linear":
+        wq, s = oracle.quantize_weight_int8(w, gs)
+        ref = oracle.w8a8_linear(x, wq, s, gs)
+    else:
+        wq, s = oracle.pack_weight_int4(w, gs)
+        ref = oracle.w4a8_linear(x, wq, s, gs)
+    y = layer(cuda(torch.from_numpy(x)).reshape(2, 65, K))
+    assert tuple(y.shape) == (2, 65, N)
+    assert_f16_within_1ulp(host(y).reshape(M, N), ref, cls)
+    y1 = layer(cuda(torch.from_numpy(x[:1])))
+    assert_f16_within_1ulp(host(y1), ref[:1], cls + " one token")
+
+
 def test_layer_edge_rows():
     """All-zero tokens, a single non-zero, exact-scale rows, overflow to inf."""
     M, N, K = 6, 64, 128

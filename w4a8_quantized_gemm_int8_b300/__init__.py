@@ -494,3 +494,99 @@ def column_parallel_w8a8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Te
     else:  # more ranks than 128-channel tiles: nothing to compute here
         y = torch.empty((x.shape[0], 0), dtype=torch.float16, device=x.device)
     return y if world == 1 else gather_columns(y, N, world, group=group)
+
+
+# ---------------------------------------------------------------------------
+# the pages' layer-level names (Cider README, "Layer-level API" and
+# "Low-Level API"), over the calls above
+# ---------------------------------------------------------------------------
+
+def is_available() -> bool:
+    """True when the library loads and a B300-class GPU (compute capability
+    10.3, the target of the library's sm_103a kernels) is visible."""
+    try:
+        load_library()
+    except (OSError, RuntimeError):
+        return False
+    return torch.cuda.is_available() and torch.cuda.get_device_capability() == (10, 3)
+
+
+def perchannel_linear(x: torch.Tensor, w_int8: torch.Tensor, scale: torch.Tensor,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    """Per-channel W8A8 linear layer: w8a8_linear with group size 0."""
+    return w8a8_linear(x, w_int8, scale, 0, out=out)
+
+
+class _QuantLinear(torch.nn.Module):
+    """A linear layer without bias over pre-quantized weights: x [..., K]
+    (fp16 or bf16) -> y [..., N] in x's dtype through `linear` (leading
+    dimensions flattened into tokens; one token runs the GEMV)."""
+
+    bits = 8
+
+    def __init__(self, weights: torch.Tensor, scale_w: torch.Tensor, group_size: int = 0,
+                 in_features: int | None = None, out_features: int | None = None):
+        super().__init__()
+        N = weights.shape[0]
+        K = weights.shape[1] * (8 // self.bits)
+        if in_features is not None and in_features != K:
+            raise ValueError(f"in_features {in_features} != weight columns {K}")
+        if out_features is not None and out_features != N:
+            raise ValueError(f"out_features {out_features} != weight rows {N}")
+        if group_size < 0 or (group_size and K % group_size):
+            raise ValueError(f"group_size {group_size} does not divide in_features {K}")
+        want_scales = (N,) if group_size == 0 else (N, K // group_size)
+        if tuple(scale_w.shape) != want_scales:
+            raise ValueError(f"scale_w must have shape {want_scales}, got {tuple(scale_w.shape)}")
+        self.in_features, self.out_features, self.group_size = K, N, group_size
+        self.register_buffer("weight", weights)
+        self.register_buffer("scale_w", scale_w)
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        if x.shape[-1] != self.in_features:
+            raise ValueError(f"x has {x.shape[-1]} features, the layer {self.in_features}")
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, self.in_features)
+        if x2.shape[0] == 0:
+            return x.new_empty(*lead, self.out_features)
+        y = linear(x2.contiguous(), self.weight, self.scale_w, self.bits, self.group_size)
+        return y.reshape(*lead, self.out_features)
+
+    def extra_repr(self) -> str:
+        return (f"in_features={self.in_features}, out_features={self.out_features}, "
+                f"group_size={self.group_size}")
+
+
+class W8A8Linear(_QuantLinear):
+    """INT8 weights [N, K] (w_int8) with per-channel (group_size 0, scale_w
+    [N]) or per-group (scale_w [N, K/group_size]) scales; activations
+    quantized per token inside the call."""
+
+    bits = 8
+
+    def __init__(self, w_int8: torch.Tensor, scale_w: torch.Tensor, group_size: int = 0,
+                 in_features: int | None = None, out_features: int | None = None):
+        super().__init__(w_int8, scale_w, group_size, in_features, out_features)
+
+    @classmethod
+    def from_weights(cls, W: torch.Tensor, group_size: int = 0) -> "W8A8Linear":
+        """Quantizes fp16 weights W [N, K] (on the GPU) and builds the layer."""
+        wq, s = quantize_weight_int8(W, group_size)
+        return cls(wq, s, group_size)
+
+
+class W4A8Linear(_QuantLinear):
+    """Packed INT4 weights [N, K/2] (two codes per byte) with per-column
+    (group_size 0) or per-group scales; activations quantized per token."""
+
+    bits = 4
+
+    def __init__(self, packed_w4: torch.Tensor, scale_w: torch.Tensor, group_size: int = 0,
+                 in_features: int | None = None, out_features: int | None = None):
+        super().__init__(packed_w4, scale_w, group_size, in_features, out_features)
+
+    @classmethod
+    def from_weights(cls, W: torch.Tensor, group_size: int = 0) -> "W4A8Linear":
+        """Quantizes and packs fp16 weights W [N, K] (on the GPU) and builds the layer."""
+        wp, s = pack_weight_int4(W, group_size)
+        return cls(wp, s, group_size)
