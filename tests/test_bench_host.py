@@ -86,3 +86,26 @@ def test_sampler_without_nvml_reports_the_error(monkeypatch):
     info = s.stop()
     assert "error" in info and "libnvidia-ml" in info["error"]
     assert not bench.clocks_rejected(info)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the CPU oracle on a bounded sample) prints
+    one JSON line with the keys of the benchmark contract."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                          "--warmup", "0"], cwd=root, env=env, check=True, capture_output=True,
+                         text=True, timeout=600).stdout.strip().splitlines()
+    line = json.loads(out[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "TOPS"
+    assert line["config"]["workload"] == bench.WORKLOAD
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
