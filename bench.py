@@ -352,6 +352,7 @@ def run_configs(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
+    bf16_peak, hbm_peak, peak_src = peaks()
 
     def inputs(M, N, K, bits, gs, n_out):
         x = torch.randn(M, K, generator=gen, device=dev)
@@ -403,8 +404,11 @@ def run_configs(args):
         G = 1 if gs == 0 else K // gs
         res = {"M": M, "N": N, "K": K, "bits": bits, "gs": gs, "us": round(t * 1e6, 2),
                "TOPS": round(2.0 * M * N * K / t / 1e12, 1)}
-        if M == 1:
+        if M == 1:  # HBM-bound: algorithmic bytes over the measured copy bandwidth
             res["GB/s"] = round((wbytes + 4 * N * G + 2 * K + 2 * N) / t / 1e9, 1)
+            res["frac"] = round(res["GB/s"] / hbm_peak, 3)
+        else:  # tensor-bound: the whole call's flops over the measured dense f16 rate
+            res["frac"] = round(res["TOPS"] / bf16_peak, 3)
         del sets, ws
         return res
 
@@ -441,7 +445,9 @@ def run_configs(args):
                                   "fused": {"linears": fused, "total_us": round(fused_us, 2),
                                             "TOPS": round(tot_ops / (fused_us * 1e-6) / 1e12, 1)}}
     print(json.dumps({"configs": out, "steps": args.steps, "warmup": args.warmup,
-                      "timing": "CUDA events per call, inputs rotating over sets > 3x L2"}))
+                      "timing": "CUDA events per call, inputs rotating over sets > 3x L2",
+                      "frac": f"of {peak_src} peaks: {bf16_peak} TFLOP/s dense bf16/fp16 "
+                              f"(M > 1), {hbm_peak} GB/s HBM copy (M = 1)"}))
 
 
 def run_cider(args):
