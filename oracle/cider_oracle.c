@@ -23,8 +23,7 @@
  *    INT4 to INT8 before the matrix product.
  *  - "min-max" scale (absmax), README section "LLM Quantization" note.
  *
- * Readings taken where the pages are silent (each one is listed in the
- * design notes of the repository):
+ * Readings taken where the pages are silent:
  *  - scale = absmax / qmax in fp32 (qmax = 127 for INT8, 7 for INT4), one
  *    IEEE division, round to nearest even;
  *  - code = clamp(rint(x / scale), -qmax, qmax): IEEE fp32 division, then
