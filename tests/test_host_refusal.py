@@ -53,3 +53,40 @@ def test_missing_library_raises(monkeypatch, tmp_path):
         cider.load_library()
     with pytest.raises(RuntimeError, match="missing"):
         cider.quantize_act(x)
+
+
+# Shapes that disagree with the activations' K or the output's [M, N] are
+# refused before any device work (a kernel would read or write past the
+# tensor's end otherwise).
+BAD_SHAPES = {
+    "w8a8_short_weight_rows": lambda: cider.w8a8_linear(x, wq[:, :K - 16], s_pc),
+    "w8a8_pc_scale_count": lambda: cider.w8a8_linear(x, wq, torch.ones(N - 1)),
+    "w8a8_pg_scale_count": lambda: cider.w8a8_linear(x, wq, torch.ones(N, 2), 64),
+    "w8a8_group_not_dividing_K": lambda: cider.w8a8_linear(x, wq, s_pg, 48),
+    "w8a8_out_shape": lambda: cider.w8a8_linear(x, wq, s_pc,
+                                                out=torch.empty(M, N - 8, dtype=torch.float16)),
+    "w4a8_unpacked_weight": lambda: cider.w4a8_linear(x, wq.view(torch.uint8), s_pg, 64),
+    "linear_bits": lambda: cider.linear(x, wq, s_pc, bits=2),
+    "linear_int4_columns": lambda: cider.linear(x, wq.view(torch.uint8), s_pc, bits=4),
+    "noalloc_out_shape": lambda: cider.w8a8_linear_noalloc(
+        x, wq, s_pc, torch.empty(M + 1, N, dtype=torch.float16)),
+    "gemv_weight_columns": lambda: cider.int8_gemv(torch.zeros(K + 16, dtype=torch.float16),
+                                                   wq, s_pc),
+    "gemv_out_shape": lambda: cider.int8_gemv(x[0], wq, s_pc,
+                                              out=torch.empty(1, N, dtype=torch.float16)),
+    "a16_scale_count": lambda: cider.a16_gemv(x[0], wq, s_pg, 8, 32),
+    "act_image_buffer": lambda: cider.act_image(x, torch.empty(M, K - 8, dtype=torch.float16)),
+    "weight_image_columns": lambda: cider.weight_image(wq, K + 16),
+    "gemm_images_scales": lambda: cider.gemm_images(
+        torch.empty(M, K, dtype=torch.float16), torch.ones(M), torch.empty(N, K,
+                                                                           dtype=torch.float16),
+        torch.ones(N + 1)),
+    "raw_gemm_codes": lambda: cider.raw_gemm_s32(torch.zeros(M, K - 16, dtype=torch.int8), wq, K),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BAD_SHAPES))
+def test_mismatched_shapes_are_refused(name):
+    with pytest.raises(ValueError) as e:
+        BAD_SHAPES[name]()
+    assert "CUDA" not in str(e.value), "refused for the device, not the shape"

@@ -123,6 +123,35 @@ def _dev(t: torch.Tensor, dtype, name: str, ndim: int | None = None) -> int:
     return t.data_ptr()
 
 
+def _check_weights(K: int, N: int, w: torch.Tensor, s_w: torch.Tensor, bits: int,
+                   group_size: int) -> None:
+    """The weights and scales must match the activations' K: the kernels read
+    N x K codes (N x K/2 bytes packed) and the scale table the group size
+    implies, so a smaller tensor would be read past its end."""
+    if bits not in (8, 4):
+        raise ValueError(f"bits must be 8 or 4, got {bits}")
+    if w.dim() != 2 or w.shape[0] != N:
+        raise ValueError(f"w must be 2-D with {N} rows, got shape {tuple(w.shape)}")
+    if bits == 4 and K % 2:
+        raise ValueError(f"packed INT4 weights need an even K, got {K}")
+    cols = K if bits == 8 else K // 2
+    if w.shape[1] != cols:
+        raise ValueError(f"w has {w.shape[1]} columns; K = {K} with {bits}-bit codes "
+                         f"needs {cols}")
+    if group_size < 0 or (group_size and K % group_size):
+        raise ValueError(f"group_size {group_size} must be 0 or a divisor of K = {K}")
+    want = N if group_size == 0 else N * (K // group_size)
+    if s_w.numel() != want:
+        raise ValueError(f"s_w has {s_w.numel()} scales, {want} expected "
+                         f"([N] per channel or [N, K/group_size] per group)")
+
+
+def _check_out(out: torch.Tensor | None, shape: tuple, name: str = "out") -> None:
+    """A caller's output tensor must have exactly the shape the call writes."""
+    if out is not None and tuple(out.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(out.shape)}")
+
+
 _ws_cache: dict = {}
 
 
@@ -197,6 +226,8 @@ def w8a8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor, group_size
     the GEMV inside the library."""
     M, K = x.shape
     N = wq.shape[0]
+    _check_weights(K, N, wq, s_w, 8, group_size)
+    _check_out(out, (M, N))
     y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=x.device)
     need = workspace_bytes(M, N, K, 8, group_size)
     buf = ws if ws is not None else _workspace(need, x.device)
@@ -229,6 +260,8 @@ def linear(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
         raise ValueError(f"out_dtype must be float16 or bfloat16, got {out_dtype}")
     M, K = x.shape
     N = w.shape[0]
+    _check_weights(K, N, w, s_w, bits, group_size)
+    _check_out(out, (M, N))
     y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=x.device)
     need = workspace_bytes(M, N, K, bits, group_size)
     buf = ws if ws is not None else _workspace(need, x.device)
@@ -253,6 +286,8 @@ def a16_gemv(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
     out_dtype = out_dtype or xv.dtype
     K = xv.numel()
     N = w.shape[0]
+    _check_weights(K, N, w, s_w, bits, group_size)
+    _check_out(out, (N,))
     y = out if out is not None else torch.empty((N,), dtype=out_dtype, device=x.device)
     wdt = torch.int8 if bits == 8 else torch.uint8
     st = load_library().cider_a16_gemv(
@@ -305,6 +340,8 @@ def w8a8_linear_noalloc(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
     overlap on the GPU race). ``out`` (fp16 [M,N]) must be provided."""
     M, K = x.shape
     N = wq.shape[0]
+    _check_weights(K, N, wq, s_w, 8, 0)
+    _check_out(out, (M, N))
     st = load_library().cider_w8a8_gemm_pc_noalloc(
         _dev(x, torch.float16, "x", 2), M, N, K, _dev(wq, torch.int8, "wq", 2),
         _dev(s_w, torch.float32, "s_w"), _dev(out, torch.float16, "out", 2), _stream())
@@ -317,6 +354,8 @@ def w4a8_linear(x: torch.Tensor, wp: torch.Tensor, s_w: torch.Tensor, group_size
     """W4A8 linear layer with packed INT4 weights wp [N, K/2]."""
     M, K = x.shape
     N = wp.shape[0]
+    _check_weights(K, N, wp, s_w, 4, group_size)
+    _check_out(out, (M, N))
     y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=x.device)
     need = workspace_bytes(M, N, K, 4, group_size)
     buf = ws if ws is not None else _workspace(need, x.device)
@@ -336,6 +375,8 @@ def int8_gemv(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8
     xv = x.reshape(-1)
     K = xv.numel()
     N = w.shape[0]
+    _check_weights(K, N, w, s_w, bits, group_size)
+    _check_out(out, (N,))
     y = out if out is not None else torch.empty((N,), dtype=torch.float16, device=x.device)
     wdt = torch.int8 if bits == 8 else torch.uint8
     st = load_library().cider_int8_gemv(
@@ -350,6 +391,8 @@ def act_image(x: torch.Tensor, a_img: torch.Tensor | None = None,
     """Stage 1 of the GEMM path: x fp16 [M,K] -> (codes as fp16 integers
     [M,K], s_a fp32 [M])."""
     M, K = x.shape
+    _check_out(a_img, (M, K), "a_img")
+    _check_out(s_a, (M,), "s_a")
     a_img = a_img if a_img is not None else torch.empty((M, K), dtype=torch.float16,
                                                         device=x.device)
     s_a = s_a if s_a is not None else torch.empty((M,), dtype=torch.float32, device=x.device)
@@ -362,6 +405,11 @@ def act_image(x: torch.Tensor, a_img: torch.Tensor | None = None,
 def weight_image(w: torch.Tensor, K: int, bits: int = 8, b_img: torch.Tensor | None = None):
     """Stage 2: INT8 [N,K] or packed INT4 [N,K/2] codes -> fp16 integers [N,K]."""
     N = w.shape[0]
+    if bits not in (8, 4) or w.dim() != 2 or w.shape[1] != (K if bits == 8 else K // 2) \
+            or (bits == 4 and K % 2):
+        raise ValueError(f"w of shape {tuple(w.shape)} does not hold {bits}-bit codes of "
+                         f"K = {K}")
+    _check_out(b_img, (N, K), "b_img")
     b_img = b_img if b_img is not None else torch.empty((N, K), dtype=torch.float16,
                                                         device=w.device)
     wdt = torch.int8 if bits == 8 else torch.uint8
@@ -376,6 +424,9 @@ def gemm_images(a_img: torch.Tensor, s_a: torch.Tensor, b_img: torch.Tensor,
     """Stage 3: tensor-core GEMM + fused dequant on the fp16 code images."""
     M, K = a_img.shape
     N = b_img.shape[0]
+    _check_out(s_a, (M,), "s_a")
+    _check_weights(K, N, b_img, s_w, 8, group_size)  # the fp16 image is [N, K]
+    _check_out(out, (M, N))
     y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=a_img.device)
     _check("cider_gemm_images", load_library().cider_gemm_images(
         _dev(a_img, torch.float16, "a_img", 2), _dev(s_a, torch.float32, "s_a"),
@@ -391,6 +442,13 @@ def raw_gemm_s32(q: torch.Tensor, w: torch.Tensor, K: int, bits: int = 8,
     [M,N,K/gs] per-group partials."""
     M = q.shape[0]
     N = w.shape[0]
+    if q.dim() != 2 or q.shape[1] != K:
+        raise ValueError(f"q must be [M, {K}], got shape {tuple(q.shape)}")
+    if bits not in (8, 4) or w.dim() != 2 or w.shape[1] != (K if bits == 8 else K // 2):
+        raise ValueError(f"w of shape {tuple(w.shape)} does not hold {bits}-bit codes of "
+                         f"K = {K}")
+    if group_size < 0 or (group_size and K % group_size):
+        raise ValueError(f"group_size {group_size} must be 0 or a divisor of K = {K}")
     G = 1 if group_size == 0 else K // group_size
     out = torch.empty((M, N) if group_size == 0 else (M, N, G), dtype=torch.int32,
                       device=q.device)
