@@ -25,7 +25,10 @@
  *    computes y[M,N] = x[M,K] . W^T.
  *  - Unless a comment says "host", every pointer is a device pointer owned
  *    by the caller; the library never allocates, frees, or keeps them.
- *    Pointers must be 16-byte aligned.
+ *    Pointers must be 16-byte aligned. Each buffer must hold at least the
+ *    elements its comment states for the sizes passed (the library sees
+ *    only pointers and cannot check this; the Python binding checks tensor
+ *    shapes before every call).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
  *    only enqueue work on it and return without synchronizing, except
  *    cider_device_status, which synchronizes the stream.
