@@ -298,6 +298,37 @@ def test_layer_classes_match_oracle(cls, gs):
     assert_f16_within_1ulp(host(y1), ref[:1], cls + " one token")
 
 
+def test_empty_inputs_give_empty_outputs():
+    """No tokens (M = 0) or no output channels (N = 0): every call returns an
+    empty result of the right shape and type and launches nothing."""
+    M, N, K = 4, 64, 256
+    x, w = _layer_inputs(M, N, K, seed=3)
+    xd = cuda(torch.from_numpy(x))
+    wq, s = oracle.quantize_weight_int8(w, 0)
+    wqd, sd = cuda(torch.from_numpy(wq)), cuda(torch.from_numpy(s))
+    wg, sg = oracle.quantize_weight_int8(w, 64)
+    wp, s4 = oracle.pack_weight_int4(w, 0)
+    cases = {
+        "pc": (cider.w8a8_linear(xd[:0], wqd, sd), (0, N), torch.float16),
+        "pg": (cider.w8a8_linear(xd[:0], cuda(torch.from_numpy(wg)), cuda(torch.from_numpy(sg)),
+                                 64), (0, N), torch.float16),
+        "w4": (cider.w4a8_linear(xd[:0], cuda(torch.from_numpy(wp)), cuda(torch.from_numpy(s4))),
+               (0, N), torch.float16),
+        "bf16": (cider.linear(xd[:0].bfloat16(), wqd, sd), (0, N), torch.bfloat16),
+        "no channels": (cider.w8a8_linear(xd, wqd[:0], sd[:0]), (M, 0), torch.float16),
+        "gemv": (cider.int8_gemv(xd[0], wqd[:0], sd[:0]), (0,), torch.float16),
+        "a16": (cider.a16_gemv(xd[0], wqd[:0], sd[:0]), (0,), torch.float16),
+        "quant": (cider.quantize_act(xd[:0])[0], (0, K), torch.int8),
+        "quant bf16": (cider.quantize_act_any(xd[:0].bfloat16())[1], (0,), torch.float32),
+        "weights": (cider.quantize_weight_int8(cuda(torch.from_numpy(w[:0])), 64)[1], (0, K // 64),
+                    torch.float32),
+        "int4": (cider.pack_weight_int4(cuda(torch.from_numpy(w[:0])))[0], (0, K // 2),
+                 torch.uint8),
+    }
+    for name, (y, shape, dtype) in cases.items():
+        assert tuple(y.shape) == shape and y.dtype == dtype, name
+
+
 def test_layer_edge_rows():
     """All-zero tokens, a single non-zero, exact-scale rows, overflow to inf."""
     M, N, K = 6, 64, 128

@@ -184,8 +184,12 @@ def quantize_act(x: torch.Tensor):
     M, K = x.shape
     q = torch.empty((M, K), dtype=torch.int8, device=x.device)
     s = torch.empty((M,), dtype=torch.float32, device=x.device)
-    _check("cider_quantize_act", load_library().cider_quantize_act(
-        _dev(x, torch.float16, "x", 2), M, K, q.data_ptr(), s.data_ptr(), _stream()))
+    lib = load_library()
+    xp = _dev(x, torch.float16, "x", 2)
+    if M == 0:  # no tokens: nothing to compute
+        return q, s
+    _check("cider_quantize_act", lib.cider_quantize_act(
+        xp, M, K, q.data_ptr(), s.data_ptr(), _stream()))
     return q, s
 
 
@@ -196,9 +200,12 @@ def quantize_weight_int8(w: torch.Tensor, group_size: int = 0):
     wq = torch.empty((N, K), dtype=torch.int8, device=w.device)
     shape = (N,) if group_size == 0 else (N, K // group_size)
     s = torch.empty(shape, dtype=torch.float32, device=w.device)
-    _check("cider_quantize_weight_int8", load_library().cider_quantize_weight_int8(
-        _dev(w, torch.float16, "w", 2), N, K, group_size, wq.data_ptr(), s.data_ptr(),
-        _stream()))
+    lib = load_library()
+    wp = _dev(w, torch.float16, "w", 2)
+    if N == 0:  # no output channels: nothing to compute
+        return wq, s
+    _check("cider_quantize_weight_int8", lib.cider_quantize_weight_int8(
+        wp, N, K, group_size, wq.data_ptr(), s.data_ptr(), _stream()))
     return wq, s
 
 
@@ -209,9 +216,12 @@ def pack_weight_int4(w: torch.Tensor, group_size: int = 0):
     wp = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
     shape = (N,) if group_size == 0 else (N, K // group_size)
     s = torch.empty(shape, dtype=torch.float32, device=w.device)
-    _check("cider_pack_weight_int4", load_library().cider_pack_weight_int4(
-        _dev(w, torch.float16, "w", 2), N, K, group_size, wp.data_ptr(), s.data_ptr(),
-        _stream()))
+    lib = load_library()
+    wd = _dev(w, torch.float16, "w", 2)
+    if N == 0:  # no output channels: nothing to compute
+        return wp, s
+    _check("cider_pack_weight_int4", lib.cider_pack_weight_int4(
+        wd, N, K, group_size, wp.data_ptr(), s.data_ptr(), _stream()))
     return wp, s
 
 
@@ -237,6 +247,8 @@ def w8a8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor, group_size
     wp = _dev(wq, torch.int8, "wq", 2)
     sp = _dev(s_w, torch.float32, "s_w")
     yp = _dev(y, torch.float16, "y", 2)
+    if M == 0 or N == 0:  # an empty output: nothing to compute
+        return y
     if group_size == 0:
         st = lib.cider_w8a8_gemm_pc(xp, M, N, K, wp, sp, yp, wsp, wsn, _stream())
         _check("cider_w8a8_gemm_pc", st)
@@ -267,9 +279,13 @@ def linear(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
     buf = ws if ws is not None else _workspace(need, x.device)
     wsp, wsn = (buf.data_ptr(), buf.numel()) if buf is not None else (None, 0)
     wdt = torch.int8 if bits == 8 else torch.uint8
-    st = load_library().cider_linear(
-        _dev(x, x.dtype, "x", 2), _DTYPE_CODES[x.dtype], M, N, K, _dev(w, wdt, "w", 2), bits,
-        _dev(s_w, torch.float32, "s_w"), group_size, _dev(y, out_dtype, "y", 2),
+    lib = load_library()
+    xp, wp = _dev(x, x.dtype, "x", 2), _dev(w, wdt, "w", 2)
+    sp, yp = _dev(s_w, torch.float32, "s_w"), _dev(y, out_dtype, "y", 2)
+    if M == 0 or N == 0:  # an empty output: nothing to compute
+        return y
+    st = lib.cider_linear(
+        xp, _DTYPE_CODES[x.dtype], M, N, K, wp, bits, sp, group_size, yp,
         _DTYPE_CODES[out_dtype], wsp, wsn, _stream())
     _check("cider_linear", st)
     return y
@@ -290,9 +306,13 @@ def a16_gemv(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
     _check_out(out, (N,))
     y = out if out is not None else torch.empty((N,), dtype=out_dtype, device=x.device)
     wdt = torch.int8 if bits == 8 else torch.uint8
-    st = load_library().cider_a16_gemv(
-        _dev(xv, xv.dtype, "x"), _DTYPE_CODES[xv.dtype], K, N, _dev(w, wdt, "w", 2), bits,
-        _dev(s_w, torch.float32, "s_w"), group_size, _dev(y, out_dtype, "y"),
+    lib = load_library()
+    xp, wp = _dev(xv, xv.dtype, "x"), _dev(w, wdt, "w", 2)
+    sp, yp = _dev(s_w, torch.float32, "s_w"), _dev(y, out_dtype, "y")
+    if N == 0:  # no output channels: nothing to compute
+        return y
+    st = lib.cider_a16_gemv(
+        xp, _DTYPE_CODES[xv.dtype], K, N, wp, bits, sp, group_size, yp,
         _DTYPE_CODES[out_dtype], _stream())
     _check("cider_a16_gemv", st)
     return y
@@ -310,9 +330,13 @@ def quantize_weight_clipped(w: torch.Tensor, group_size: int = 0, clip_percentil
     wq = torch.empty((N, K) if bits == 8 else (N, K // 2),
                      dtype=torch.int8 if bits == 8 else torch.uint8, device=w.device)
     s = torch.empty((N,) if group_size == 0 else (N, G), dtype=torch.float32, device=w.device)
-    _check("cider_quantize_weight_clipped", load_library().cider_quantize_weight_clipped(
-        _dev(w, w.dtype, "w", 2), _DTYPE_CODES[w.dtype], N, K, group_size, bits,
-        float(clip_percentile), wq.data_ptr(), s.data_ptr(), _stream()))
+    lib = load_library()
+    wd = _dev(w, w.dtype, "w", 2)
+    if N == 0:  # no output channels: nothing to compute
+        return wq, s
+    _check("cider_quantize_weight_clipped", lib.cider_quantize_weight_clipped(
+        wd, _DTYPE_CODES[w.dtype], N, K, group_size, bits, float(clip_percentile),
+        wq.data_ptr(), s.data_ptr(), _stream()))
     return wq, s
 
 
@@ -324,9 +348,12 @@ def quantize_act_any(x: torch.Tensor):
     M, K = x.shape
     q = torch.empty((M, K), dtype=torch.int8, device=x.device)
     s = torch.empty((M,), dtype=torch.float32, device=x.device)
-    _check("cider_quantize_act_ex", load_library().cider_quantize_act_ex(
-        _dev(x, x.dtype, "x", 2), _DTYPE_CODES[x.dtype], M, K, q.data_ptr(), s.data_ptr(),
-        _stream()))
+    lib = load_library()
+    xp = _dev(x, x.dtype, "x", 2)
+    if M == 0:  # no tokens: nothing to compute
+        return q, s
+    _check("cider_quantize_act_ex", lib.cider_quantize_act_ex(
+        xp, _DTYPE_CODES[x.dtype], M, K, q.data_ptr(), s.data_ptr(), _stream()))
     return q, s
 
 
@@ -342,9 +369,12 @@ def w8a8_linear_noalloc(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
     N = wq.shape[0]
     _check_weights(K, N, wq, s_w, 8, 0)
     _check_out(out, (M, N))
-    st = load_library().cider_w8a8_gemm_pc_noalloc(
-        _dev(x, torch.float16, "x", 2), M, N, K, _dev(wq, torch.int8, "wq", 2),
-        _dev(s_w, torch.float32, "s_w"), _dev(out, torch.float16, "out", 2), _stream())
+    lib = load_library()
+    xp, wp = _dev(x, torch.float16, "x", 2), _dev(wq, torch.int8, "wq", 2)
+    sp, yp = _dev(s_w, torch.float32, "s_w"), _dev(out, torch.float16, "out", 2)
+    if M == 0 or N == 0:  # an empty output: nothing to compute
+        return out
+    st = lib.cider_w8a8_gemm_pc_noalloc(xp, M, N, K, wp, sp, yp, _stream())
     _check("cider_w8a8_gemm_pc_noalloc", st)
     return out
 
@@ -360,10 +390,13 @@ def w4a8_linear(x: torch.Tensor, wp: torch.Tensor, s_w: torch.Tensor, group_size
     need = workspace_bytes(M, N, K, 4, group_size)
     buf = ws if ws is not None else _workspace(need, x.device)
     wsp, wsn = (buf.data_ptr(), buf.numel()) if buf is not None else (None, 0)
-    st = load_library().cider_w4a8_gemm(
-        _dev(x, torch.float16, "x", 2), M, N, K, _dev(wp, torch.uint8, "wp", 2),
-        _dev(s_w, torch.float32, "s_w"), group_size, _dev(y, torch.float16, "y", 2), wsp, wsn,
-        _stream())
+    lib = load_library()
+    xp, wpp = _dev(x, torch.float16, "x", 2), _dev(wp, torch.uint8, "wp", 2)
+    sp, yp = _dev(s_w, torch.float32, "s_w"), _dev(y, torch.float16, "y", 2)
+    if M == 0 or N == 0:  # an empty output: nothing to compute
+        return y
+    st = lib.cider_w4a8_gemm(xp, M, N, K, wpp, sp, group_size, yp, wsp, wsn,
+                                        _stream())
     _check("cider_w4a8_gemm", st)
     return y
 
@@ -379,9 +412,12 @@ def int8_gemv(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8
     _check_out(out, (N,))
     y = out if out is not None else torch.empty((N,), dtype=torch.float16, device=x.device)
     wdt = torch.int8 if bits == 8 else torch.uint8
-    st = load_library().cider_int8_gemv(
-        _dev(xv, torch.float16, "x"), K, N, _dev(w, wdt, "w", 2), _dev(s_w, torch.float32, "s_w"),
-        bits, group_size, _dev(y, torch.float16, "y"), _stream())
+    lib = load_library()
+    xp, wp = _dev(xv, torch.float16, "x"), _dev(w, wdt, "w", 2)
+    sp, yp = _dev(s_w, torch.float32, "s_w"), _dev(y, torch.float16, "y")
+    if N == 0:  # no output channels: nothing to compute
+        return y
+    st = lib.cider_int8_gemv(xp, K, N, wp, sp, bits, group_size, yp, _stream())
     _check("cider_int8_gemv", st)
     return y
 
