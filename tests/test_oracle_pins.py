@@ -266,6 +266,28 @@ def test_epilogue_pg_order_and_exact_case():
     assert oracle.epilogue_pg(P2, sw, 2.0 ** -20) == np.float16(np.float32(16777218.0) * 2.0 ** -20).view(np.uint16)
 
 
+def test_epilogue_pg_rounds_each_product_then_each_sum():
+    """Per-group reading (README "Quantization": each group's int32 partial
+    rescaled by its weight scale, the rescaled partials summed): every
+    product and every sum is its own binary32 rounding. Hand-worked case:
+    P = [-3, 2531], s_w = [1, 13259 * 2^-23], s_a = 1.
+      group 0: f = 0 + (-3 * 1) = -3 (exact)
+      group 1: 2531 * 13259 = 33558529, so P*s = 33558529 * 2^-23
+               = 4 + 2^-11 + 2^-23; binary32 in [4, 8) has spacing 2^-21,
+               so fl(P*s) = 4 + 2^-11 (the 2^-23 is below half a spacing);
+               f = fl(-3 + 4 + 2^-11) = 1 + 2^-11 (exact)
+      y = fp16(1 + 2^-11): halfway between 1 and 1 + 2^-10, ties to even
+          -> 1.0 (0x3C00).
+    A fused multiply-add, or any wider accumulator, keeps the 2^-23 and
+    rounds 1 + 2^-11 + 2^-23 up to 1 + 2^-10 (0x3C01) instead."""
+    P = np.array([-3, 2531], np.int32)
+    sw = np.array([1.0, 13259 * 2.0 ** -23], np.float32)
+    assert 2531 * 13259 == 33558529 == (4 << 23) + (1 << 12) + 1
+    assert oracle.epilogue_pg(P, sw, 1.0) == 0x3C00
+    fused = np.float16(np.float32(-3.0 + 2531.0 * float(sw[1])))  # exact in float64
+    assert fused.view(np.uint16) == 0x3C01
+
+
 def test_pg_with_one_group_equals_pc_for_exact_scales():
     rng = np.random.default_rng(9)
     M, N, K = 5, 7, 128
