@@ -288,6 +288,55 @@ def test_epilogue_pg_rounds_each_product_then_each_sum():
     assert fused.view(np.uint16) == 0x3C01
 
 
+def test_epilogue_pc_multiplies_left_to_right():
+    """README "Quantization", row "Output dequant: C_fp16 = C_int32 * s_act *
+    s_weight", read left to right, each product rounded to binary32.
+    Hand-worked: acc = 2275, s_act = 1 + 2^-12 = 4097/4096,
+    s_weight = 1 + 35 * 2^-12 = 4131/4096.
+      t = 2275 * 4097/4096 = 9320675/4096 (exact: binary32 spacing in
+          [2048, 4096) is 2^-12)
+      t * s_weight = 9400319.44 * 2^-12, rounded to 9400319 * 2^-12
+          = 2294.99976; fp16 spacing there is 2, the midpoint 2295 is not
+          reached -> 2294.0 (0x687B).
+    The scales multiplied first: 4097 * 4131 = 16924707, an odd count of
+    2^-24, halfway between binary32 neighbours; ties to even give
+    16924708 * 2^-24; then 2275 times that rounds to exactly 2295, an fp16
+    tie that rounds to even -> 2296.0 (0x687C)."""
+    assert 4097 * 4131 == 16924707
+    assert oracle.epilogue_pc(2275, 1 + 2.0 ** -12, 1 + 35 * 2.0 ** -12) == 0x687B
+
+
+def test_epilogue_pg_sums_groups_in_ascending_order():
+    """Groups summed in ascending order, each sum rounded. Hand-worked:
+    P = [8392704, 1, 1] (8392704 = 2^23 + 2^12), s_w = [2, 1, 1],
+    s_act = 2^-14.
+      ascending: f = 2^24 + 2^13 (exact); adding 1 is a tie between
+          binary32 neighbours 2 apart and rounds to the even one, so f stays
+          2^24 + 2^13, twice; y = fp16((2^24 + 2^13) * 2^-14) = fp16(1024.5),
+          an fp16 tie -> 1024.0 (0x6400).
+    In descending order the two 1s add to 2 first and 2^24 + 2^13 + 2 is
+    exact, so y = fp16(1024.5 + 2^-13) = 1025.0 (0x6401)."""
+    P = np.array([8392704, 1, 1], np.int32)
+    sw = np.array([2.0, 1.0, 1.0], np.float32)
+    assert oracle.epilogue_pg(P, sw, 2.0 ** -14) == 0x6400
+
+
+def test_epilogue_pg_applies_token_scale_once_at_the_end():
+    """The token scale multiplies the finished group sum (README "Output
+    dequant" row: C_int32 * s_act * s_weight, with the per-group sum in place
+    of C_int32 * s_weight). Hand-worked: P = [986, 4093], s_w = [1, 1],
+    s_act = 1 + 25 * 2^-12 = 4121/4096.
+      f = 986 + 4093 = 5079 (exact); 5079 * 4121/4096 = 10465279.5 * 2^-11,
+      a binary32 tie (spacing 2^-11 in [4096, 8192)) -> 10465280 * 2^-11 =
+      5110, itself an fp16 tie between 5108 and 5112 -> 5112.0 (0x6CFE).
+    Scaling each group before the sum gives 992.018066 + 4117.981445 =
+    5109.99951, below the midpoint -> 5108.0 (0x6CFD)."""
+    P = np.array([986, 4093], np.int32)
+    sw = np.array([1.0, 1.0], np.float32)
+    assert 5079 * 4121 == 2 * 10465279 + 1 and 10465280 * 2.0 ** -11 == 5110.0
+    assert oracle.epilogue_pg(P, sw, 1 + 25 * 2.0 ** -12) == 0x6CFE
+
+
 def test_pg_with_one_group_equals_pc_for_exact_scales():
     rng = np.random.default_rng(9)
     M, N, K = 5, 7, 128
