@@ -2,10 +2,13 @@
 such mistake planted in a copy of cider_oracle.c (a reordered product, a
 reciprocal for a division, ties away from zero, a dropped term, swapped
 nibbles, a wrong index, a different accumulation order...), built on the
-CPU, and the pin suite must fail against it. One mistake is not listed: a
-min-max clamp at -128 instead of -127 cannot change any code (|x / s| stays
-below 127.5 for every finite input, subnormal bf16 scales included), so no
-test can tell it apart. No GPU needed."""
+CPU, and the pin suite must fail against it. Two mistakes are not listed
+because no input can tell them apart from the oracle: a min-max clamp at
+-128 instead of -127 (|x / s| stays below 127.5 for every finite input,
+subnormal bf16 scales included), and sending binary32 values above 65520
+instead of from 65520 to the fp16 overflow branch (65520 itself rounds to
+even on the ordinary path, carries out of the top binade and also gives
+infinity). No GPU needed."""
 import os
 import subprocess
 import sys
@@ -57,6 +60,20 @@ M = [
  ("int4_qmax_8", "            s_w[n * G + g] = quantize_block(w + n * K + g * gs, gs, 7.0f, codes + g * gs);", "            s_w[n * G + g] = quantize_block(w + n * K + g * gs, gs, 8.0f, codes + g * gs);"),
  ("weight_group_index", "            s_w[n * G + g] = quantize_block(w + n * K + g * gs, gs, 127.0f, wq + n * K + g * gs);", "            s_w[g * N + n] = quantize_block(w + n * K + g * gs, gs, 127.0f, wq + n * K + g * gs);"),
  ("bf16_input_as_half", "    return dtype == ORACLE_BF16 ? oracle_bf16_to_float(v) : oracle_half_to_float(v);", "    return oracle_half_to_float(v);"),
+ ("pct_sort_descending", "    return (x > y) - (x < y);", "    return (x < y) - (x > y);"),
+ ("pct_no_saturation", "        float r = rintf(elem_to_float(v[k], dtype) / scale);\n        if (r > qmax)\n            r = qmax;", "        float r = rintf(elem_to_float(v[k], dtype) / scale);\n        if (r > 1000.0f)\n            r = qmax;"),
+ ("absmax_signed", "        float a = fabsf(elem_to_float(v[k], dtype));\n        if (a > absmax)", "        float a = elem_to_float(v[k], dtype);\n        if (a > absmax)"),
+ ("layer_weights_reversed", "                    acc += (int32_t)q[k] * (int32_t)wrow[k];", "                    acc += (int32_t)q[k] * (int32_t)wrow[K - 1 - k];"),
+ ("gemm_weight_row_reversed", "                    acc += (int32_t)q[m * K + k] * (int32_t)wq[n * K + k];", "                    acc += (int32_t)q[m * K + k] * (int32_t)wq[(N - 1 - n) * K + k];"),
+ ("half_exponent_bias", "        mag = ldexpf((float)(frac | 0x400), expo - 25); /* 1.frac * 2^(expo-15) */", "        mag = ldexpf((float)(frac | 0x400), expo - 24); /* 1.frac * 2^(expo-15) */"),
+ ("int4_groups_overwrite", "            s_w[n * G + g] = quantize_block(w + n * K + g * gs, gs, 7.0f, codes + g * gs);", "            s_w[n * G + g] = quantize_block(w + n * K + g * gs, gs, 7.0f, codes);"),
+ ("weight_qmax_126", "            s_w[n * G + g] = quantize_block(w + n * K + g * gs, gs, 127.0f, wq + n * K + g * gs);", "            s_w[n * G + g] = quantize_block(w + n * K + g * gs, gs, 126.0f, wq + n * K + g * gs);"),
+ ("zero_row_code_one", "    if (absmax == 0.0f) {\n        for (int64_t k = 0; k < n; ++k)\n            out[k] = 0;\n        return 0.0f;\n    }\n    float scale = absmax / qmax;", "    if (absmax == 0.0f) {\n        for (int64_t k = 0; k < n; ++k)\n            out[k] = 1;\n        return 0.0f;\n    }\n    float scale = absmax / qmax;"),
+ ("pc_output_always_half", "    t = t * s_weight;\n    return float_to_elem(t, y_dtype);", "    t = t * s_weight;\n    return oracle_float_to_half(t);"),
+ ("half_subnormal_floor", "    if (unbiased < -14)\n        unbiased = -14;", "    if (unbiased < -15)\n        unbiased = -15;"),
+ ("bf16_carry", "        if (n >= 256.0) {        /* rounding carried into the next binade */\n            n = 128.0;\n            expo += 1;\n        }", "        if (n > 256.0) {        /* rounding carried into the next binade */\n            n = 128.0;\n            expo += 1;\n        }"),
+ ("a16_group_scale_index", "            total += (double)s_w[n * G + g] * part;", "            total += (double)s_w[n * G] * part;"),
+ ("pct_interp_weight", "(h - (double)i) * ((double)q[i + 1] - (double)q[i])", "(1.0 - (h - (double)i)) * ((double)q[i + 1] - (double)q[i])"),
 ]
 
 
