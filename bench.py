@@ -373,7 +373,7 @@ def run_configs(args):
         for _ in range(n_sets):
             x, wq, s = inputs(M, N, K, bits, gs, n_out)
             sets.append((x, wq, s, torch.empty((M, N), dtype=torch.float16, device=dev)))
-        ws = torch.empty(max(1, cider.workspace_bytes(M, N, K, bits, gs)), dtype=torch.uint8,
+        ws = torch.empty(max(1, cider.workspace_bytes(M, N, K, group_size=gs, bits=bits)), dtype=torch.uint8,
                          device=dev)
 
         def call(i):
@@ -488,7 +488,7 @@ def run_cider(args):
     b_img = torch.empty((N, K), dtype=torch.float16, device=dev)
     y = torch.empty((M, N), dtype=torch.float16, device=dev)
     y_staged = torch.empty_like(y)
-    ws = torch.empty(cider.workspace_bytes(M, N, K, 8, 0), dtype=torch.uint8, device=dev)
+    ws = torch.empty(cider.workspace_bytes(M, N, K, group_size=0, bits=8), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
@@ -624,7 +624,7 @@ def run_cider(args):
     y_h = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(2)]
     x_d = [torch.empty_like(x) for _ in range(2)]
     y_d = [torch.empty_like(y) for _ in range(2)]
-    ws = torch.empty(cider.workspace_bytes(M, N, K, 8, 0), dtype=torch.uint8, device=dev)
+    ws = torch.empty(cider.workspace_bytes(M, N, K, group_size=0, bits=8), dtype=torch.uint8, device=dev)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
     def ev():
@@ -801,7 +801,7 @@ def run_small_step(args):
     wq = torch.randint(-127, 128, (N, K), generator=gen, device=dev, dtype=torch.int8)
     s_w = torch.rand(N, generator=gen, device=dev) * 0.01 + 0.001
     y = torch.empty(m, N, dtype=torch.float16, device=dev)
-    ws = torch.empty(max(1, cider.workspace_bytes(m, N, K, 8, 0)), dtype=torch.uint8,
+    ws = torch.empty(max(1, cider.workspace_bytes(m, N, K, group_size=0, bits=8)), dtype=torch.uint8,
                      device=dev)
     for _ in range(args.warmup):
         cider.w8a8_linear(x, wq, s_w, 0, out=y, ws=ws)

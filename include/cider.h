@@ -65,7 +65,7 @@ typedef enum cider_status {
     CIDER_ERR_WORKSPACE = 5    /* workspace pointer missing or smaller than required */
 } cider_status;
 
-#define CIDER_ABI_VERSION 2
+#define CIDER_ABI_VERSION 3
 
 /* Element types of activations and layer outputs (README roadmap: automatic
  * dtype handling, float16 / bfloat16). Both convert exactly to fp32; an
@@ -74,7 +74,7 @@ typedef enum cider_status {
 #define CIDER_DTYPE_BF16 1
 
 /* Human-readable name of a status code (static string, never NULL). */
-CIDER_API const char* cider_status_string(int status);
+CIDER_API const char* cider_status_string(cider_status status);
 
 /* CIDER_ABI_VERSION of the built library. */
 CIDER_API int cider_abi_version(void);
@@ -132,14 +132,16 @@ CIDER_API cider_status cider_quantize_weight_clipped(const void* w, int32_t w_dt
                                                      float* s_w, void* stream);
 
 /*
- * Bytes of device workspace the GEMM calls below need for this problem
- * (bits 8 or 4). The workspace holds the fp16 operand images of the
- * quantized activations and weights and the per-token scales, and for
- * group_size > 0 a group-major copy of the per-group weight scales. Returns
- * 0 when M == 1 (the GEMV path needs none) and on invalid sizes (including a
- * group_size that does not divide K).
+ * Bytes of device workspace the GEMM calls below need for this problem:
+ * group_size 0 (per channel) or the per-group size, then bits 8 or 4 (the
+ * order of the layer calls' own arguments). The workspace holds the fp16
+ * operand images of the quantized activations and weights and the per-token
+ * scales, and for group_size > 0 a group-major copy of the per-group weight
+ * scales. Returns 0 when M == 1 (the GEMV path needs none) and on invalid
+ * sizes (including a group_size that does not divide K).
  */
-CIDER_API size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bits, int32_t group_size);
+CIDER_API size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group_size,
+                                       int32_t bits);
 
 /*
  * W8A8 per-channel linear layer: quantize x per token, int32 GEMM with wq,
@@ -148,7 +150,7 @@ CIDER_API size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t 
  * matmul_fused_dequant), "Quantization" table.
  *   x_f16 [M,K] fp16; wq [N,K] int8; s_w [N] fp32; y_f16 [M,N] fp16 out;
  *   ws / ws_bytes: device workspace of at least
- *   cider_workspace_bytes(M, N, K, 8, 0) bytes (may be NULL if that is 0).
+ *   cider_workspace_bytes(M, N, K, 0, 8) bytes (may be NULL if that is 0).
  * K % 16 == 0. M == 1 runs the GEMV (same results).
  */
 CIDER_API cider_status cider_w8a8_gemm_pc(const void* x_f16, int64_t M, int64_t N, int64_t K,
@@ -180,18 +182,6 @@ CIDER_API cider_status cider_w4a8_gemm(const void* x_f16, int64_t M, int64_t N, 
                              const uint8_t* wp, const float* s_w, int32_t group_size, void* y_f16,
                              void* ws, size_t ws_bytes, void* stream);
 
-/*
- * M = 1 INT8 GEMV (README "Metal Kernel Pipeline", "Decode (M = 1)").
- * Computes exactly the GEMM's function at M = 1: the single token is
- * quantized per token to INT8, products are exact int32, then the same
- * per-channel or per-group epilogue.
- *   x_f16 [K] fp16; w: int8 [N,K] (bits 8) or packed uint8 [N, K/2]
- *   (bits 4); s_w [N] or [N, K/gs]; y_f16 [N] fp16 out.
- * K <= 16384; bits 8: K % 16 == 0, group_size 0 or a multiple of 16
- * dividing K (at most 32 chunks of 16 per group, a power of two);
- * bits 4: K % 32 == 0, group_size 0 or a multiple of 32 likewise.
- * Needs no workspace.
- */
 /*
  * The linear layer for either activation / output element type: as
  * cider_w8a8_gemm_pc (bits 8, group_size 0), cider_w8a8_gemm_pg (bits 8,
@@ -230,6 +220,18 @@ CIDER_API cider_status cider_a16_gemv(const void* x, int32_t x_dtype, int64_t K,
                                       const void* w, int32_t bits, const float* s_w,
                                       int32_t group_size, void* y, int32_t y_dtype, void* stream);
 
+/*
+ * M = 1 INT8 GEMV (README "Metal Kernel Pipeline", "Decode (M = 1)").
+ * Computes exactly the GEMM's function at M = 1: the single token is
+ * quantized per token to INT8, products are exact int32, then the same
+ * per-channel or per-group epilogue.
+ *   x_f16 [K] fp16; w: int8 [N,K] (bits 8) or packed uint8 [N, K/2]
+ *   (bits 4); s_w [N] or [N, K/gs]; y_f16 [N] fp16 out.
+ * K <= 16384; bits 8: K % 16 == 0, group_size 0 or a multiple of 16
+ * dividing K (at most 32 chunks of 16 per group, a power of two);
+ * bits 4: K % 32 == 0, group_size 0 or a multiple of 32 likewise.
+ * Needs no workspace.
+ */
 CIDER_API cider_status cider_int8_gemv(const void* x_f16, int64_t K, int64_t N, const void* w,
                              const float* s_w, int32_t bits, int32_t group_size, void* y_f16,
                              void* stream);
@@ -290,7 +292,7 @@ CIDER_API cider_status cider_gemm_images(const void* a_img, const float* s_a, co
  * engine on pre-quantized codes, for the bit-exact INT32 contract.
  *   q [M,K] int8; w int8 [N,K] (bits 8) or packed [N, K/2] (bits 4);
  *   out int32: [M,N] totals for group_size 0, else per-group partials
- *   [M, N, K/group_size]. Workspace as cider_workspace_bytes(max(M,2), ...).
+ *   [M, N, K/group_size]. Workspace as cider_workspace_bytes(max(M,2), N, K, 0, bits).
  */
 CIDER_API cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int64_t N, int64_t K,
                                  int32_t bits, int32_t group_size, int32_t* out, void* ws,

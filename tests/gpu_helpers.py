@@ -13,14 +13,23 @@ def f16_ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return np.abs(oa - ob)
 
 
-def assert_f16_within_1ulp(gpu: np.ndarray, ref: np.ndarray, what: str = "") -> int:
+def assert_f16_within_1ulp(gpu: np.ndarray, ref: np.ndarray, what: str = "",
+                           identical: bool = True) -> int:
     """The acceptance bar for fp16 outputs: at most 1 ulp from the oracle.
-    Returns the number of outputs that are not bit-identical."""
+    The kernels perform the oracle's operations in the oracle's order, so by
+    default every output must also be bit-identical (the count of outputs
+    that are not is reported in the message). Returns that count."""
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
     d = f16_ulp_distance(gpu, ref)
     bad = np.argwhere(d > 1)
     assert bad.size == 0, (f"{what}: {len(bad)} outputs beyond 1 ulp, first at {bad[0].tolist()}: "
                            f"gpu={gpu[tuple(bad[0])]} oracle={ref[tuple(bad[0])]}")
-    return int((d != 0).sum())
+    n_diff = int((d != 0).sum())
+    if identical:
+        first = np.argwhere(d != 0)[:1].tolist()
+        assert n_diff == 0, (f"{what}: {n_diff} of {d.size} outputs 1 ulp from the oracle "
+                             f"(not bit-identical), first at {first}")
+    return n_diff
 
 
 def cuda(t: torch.Tensor) -> torch.Tensor:

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert cider.abi_version() == 2
+    assert cider.abi_version() == 3
     for code, name in [(0, "CIDER_OK"), (1, "CIDER_ERR_INVALID_ARG"),
                        (2, "CIDER_ERR_UNSUPPORTED"), (3, "CIDER_ERR_CUDA"),
                        (4, "CIDER_ERR_TIMEOUT"), (5, "CIDER_ERR_WORKSPACE"), (99, "CIDER_ERR_UNKNOWN")]:
@@ -53,9 +53,9 @@ def test_workspace_bytes(lib):
     assert n >= 2 * 4096 * 2560 + 4 * 4096 + 2 * 10240 * 2560
     assert n % 256 == 0
     # per-group: plus the group-major copy of the scales
-    g = cider.workspace_bytes(4096, 2560, 10240, 8, 64)
+    g = cider.workspace_bytes(4096, 2560, 10240, group_size=64, bits=8)
     assert g >= 2 * 4096 * 10240 + 4 * 4096 + 2 * 2560 * 10240 + 4 * 2560 * (10240 // 64)
-    assert cider.workspace_bytes(4096, 2560, 10240, 8, 100) == 0  # 100 does not divide K
+    assert cider.workspace_bytes(4096, 2560, 10240, group_size=100, bits=8) == 0  # 100 does not divide K
 
 
 def test_null_and_size_checks_precede_cuda(lib):
@@ -108,9 +108,12 @@ _C_PROGRAM = r"""
 int main(void) {
     /* host-only calls: version, status strings, workspace sizing, and the
        argument checks that answer before any CUDA call */
-    size_t ws = cider_workspace_bytes(4096, 10240, 2560, 8, 0);
+    /* arguments in the documented order: M, N, K, group_size, bits */
+    size_t ws = cider_workspace_bytes(4096, 10240, 2560, 0, 8);
+    size_t ws_pg = cider_workspace_bytes(4096, 2560, 10240, 64, 4);
     cider_status st = cider_w8a8_gemm_pc(NULL, 4, 8, 16, NULL, NULL, NULL, NULL, 0, NULL);
-    printf("%d %s %zu %d\n", cider_abi_version(), cider_status_string(CIDER_OK), ws, (int)st);
+    printf("%d %s %zu %zu %d\n", cider_abi_version(), cider_status_string(CIDER_OK), ws, ws_pg,
+           (int)st);
     return st == CIDER_ERR_INVALID_ARG ? 0 : 1;
 }
 """
@@ -133,5 +136,7 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
                     "-L", libdir, "-lcider", f"-Wl,-rpath,{libdir}"], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
     assert int(out[0]) == lib.cider_abi_version()
-    assert int(out[-2]) == lib.cider_workspace_bytes(4096, 10240, 2560, 8, 0)
+    assert int(out[-3]) == cider.workspace_bytes(4096, 10240, 2560, group_size=0, bits=8)
+    assert int(out[-2]) == cider.workspace_bytes(4096, 2560, 10240, group_size=64, bits=4)
+    assert int(out[-2]) > int(out[-3]) > 0
     assert int(out[-1]) == cider.CIDER_ERR_INVALID_ARG

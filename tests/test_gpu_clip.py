@@ -30,3 +30,20 @@ def test_clipped_weight_prep_bitexact(N, K, bits, gs, pct, wdt):
     qo, so = oracle.quantize_weight_clipped(wo, gs, pct, bits, w_dtype=wdt)
     assert np.array_equal(host(s).view(np.uint32), np.asarray(so).view(np.uint32))
     assert np.array_equal(host(q), qo)
+
+
+@pytest.mark.parametrize("bits,gs", [(8, 0), (8, 64), (4, 128)])
+def test_clipped_blocks_whose_percentile_is_zero(bits, gs):
+    """Blocks where more than p % of |w| is zero: the clip is 0, so the scale
+    is 0 and every code 0, non-zero weights included (the oracle's pinned
+    reading); the other blocks keep their ordinary clipped codes."""
+    N, K = 64, 1024
+    w = synth.weights(N, K, synth.generator(71 + gs)).float().numpy()
+    keep = np.random.default_rng(5).random((N, K)) < 0.3
+    keep[: N // 2] = True  # half the rows stay dense
+    wh = np.where(keep, w, 0.0).astype(np.float16)
+    q, s = cider.quantize_weight_clipped(cuda(torch.from_numpy(wh)), gs, 50.0, bits)
+    qo, so = oracle.quantize_weight_clipped(wh, gs, 50.0, bits)
+    assert (np.asarray(so)[N // 2:] == 0).all()  # the sparse rows' blocks clip to 0
+    assert np.array_equal(host(s).view(np.uint32), np.asarray(so).view(np.uint32))
+    assert np.array_equal(host(q), qo)

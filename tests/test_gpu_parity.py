@@ -440,3 +440,51 @@ def test_gemv_equals_gemm_row(gs):
     # the public GEMM entry point at M == 1 takes the GEMV
     y1 = host(cider.w8a8_linear(xd[5:6].contiguous(), wd, sd, gs))
     assert np.array_equal(y1.view(np.uint16), y[5:6].view(np.uint16))
+
+
+@pytest.mark.parametrize("prep,bits,gs", [("int8", 8, 0), ("int8", 8, 64), ("int4", 4, 128),
+                                          ("clipped", 8, 0), ("clipped", 4, 128)])
+def test_gpu_weight_prep_then_decode_without_sync(prep, bits, gs):
+    """A weight-preparation call followed at once, on the same stream and with
+    no synchronization, by an M = 1 call that reads those weights: the
+    decode kernel may start early (programmatic dependent launch) but must
+    read the weights and scales only after the preparation has finished. The
+    weight buffers first hold other codes, so an early read would show."""
+    lib = cider.load_library()
+    N, K = 10240, 2560
+    x, w = _layer_inputs(1, N, K, seed=900 + bits + gs)
+    if prep == "clipped":
+        wq_ref, s_ref = oracle.quantize_weight_clipped(w, gs, 99.9, bits)
+    elif bits == 8:
+        wq_ref, s_ref = oracle.quantize_weight_int8(w, gs)
+    else:
+        wq_ref, s_ref = oracle.pack_weight_int4(w, gs)
+    ref = (oracle.w8a8_linear(x, wq_ref, s_ref, gs) if bits == 8
+           else oracle.w4a8_linear(x, wq_ref, s_ref, gs))
+    xd, wd = cuda(torch.from_numpy(x)), cuda(torch.from_numpy(w))
+    G = 1 if gs == 0 else K // gs
+    wq = torch.full((N, K if bits == 8 else K // 2), 0x11, dtype=torch.int8 if bits == 8
+                    else torch.uint8, device="cuda")
+    s = torch.full((N,) if gs == 0 else (N, G), 1e-3, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream().cuda_stream
+    for route in ("gemv", "layer"):
+        wq.fill_(0x11)
+        s.fill_(1e-3)
+        if prep == "clipped":
+            st = lib.cider_quantize_weight_clipped(wd.data_ptr(), 0, N, K, gs, bits, 99.9,
+                                                   wq.data_ptr(), s.data_ptr(), stream)
+        elif bits == 8:
+            st = lib.cider_quantize_weight_int8(wd.data_ptr(), N, K, gs, wq.data_ptr(),
+                                                s.data_ptr(), stream)
+        else:
+            st = lib.cider_pack_weight_int4(wd.data_ptr(), N, K, gs, wq.data_ptr(),
+                                            s.data_ptr(), stream)
+        assert st == cider.CIDER_OK
+        if route == "gemv":
+            y = cider.int8_gemv(xd, wq, s, bits=bits, group_size=gs)
+        else:
+            y = cider.linear(xd, wq, s, bits=bits, group_size=gs)
+        got = host(y).reshape(-1)
+        assert np.array_equal(got.view(np.uint16), ref.reshape(-1).view(np.uint16)), route
+        assert np.array_equal(host(wq), wq_ref) and np.array_equal(host(s), s_ref)

@@ -73,6 +73,8 @@ M = [
  ("half_subnormal_floor", "    if (unbiased < -14)\n        unbiased = -14;", "    if (unbiased < -15)\n        unbiased = -15;"),
  ("bf16_carry", "        if (n >= 256.0) {        /* rounding carried into the next binade */\n            n = 128.0;\n            expo += 1;\n        }", "        if (n > 256.0) {        /* rounding carried into the next binade */\n            n = 128.0;\n            expo += 1;\n        }"),
  ("a16_group_scale_index", "            total += (double)s_w[n * G + g] * part;", "            total += (double)s_w[n * G] * part;"),
+ ("pct_zero_clip_saturates", "    if (clip == 0.0f) {\n        for (int64_t k = 0; k < n; ++k)\n            out[k] = 0;",
+                             "    if (clip == 0.0f) {\n        for (int64_t k = 0; k < n; ++k)\n            out[k] = (int8_t)(elem_to_float(v[k], dtype) > 0.0f ? qmax : elem_to_float(v[k], dtype) < 0.0f ? -qmax : 0.0f);"),
  ("pct_interp_weight", "(h - (double)i) * ((double)q[i + 1] - (double)q[i])", "(1.0 - (h - (double)i)) * ((double)q[i + 1] - (double)q[i])"),
 ]
 

@@ -572,3 +572,22 @@ def test_clip_percentile_hand_example():
     wq, s = oracle.quantize_weight_clipped(w, 0, 50.0, 8)
     assert s[0] == np.float32(1.5) / np.float32(127.0)
     assert wq.tolist() == [[0, 85, -127, 127, 0, -127, 127, 0]]
+
+
+def test_clip_zero_block_gives_zero_scale_and_zero_codes():
+    """Reading (the pages are silent): when the p-th percentile of a block's
+    |w| is 0 (more than p % of its entries are zero), the block's scale is 0
+    and EVERY code is 0, non-zero weights included - the rule min-max applies
+    to an all-zero block. The other plausible reading, saturating the
+    non-zero weights to +-qmax (w / 0 = +-inf, clamped), fails here.
+    Sorted |w| = [0, 0, 0, 0, 0, 0, 3, 5]: p = 50 sits at position 3.5 -> 0;
+    p = 80 at 5.6 -> 0 + 0.6 * (3 - 0) = 1.8, a non-zero clip (contrast)."""
+    w = np.array([[0, 0, 3, 0, 0, -5, 0, 0]], np.float16)
+    wq, s = oracle.quantize_weight_clipped(w, 0, 50.0, 8)
+    assert s.view(np.uint32)[0] == 0
+    assert wq.tolist() == [[0, 0, 0, 0, 0, 0, 0, 0]]
+    wp, s4 = oracle.quantize_weight_clipped(w, 0, 50.0, 4)
+    assert s4[0] == 0.0 and wp.tolist() == [[0x88, 0x88, 0x88, 0x88]]  # nibble 8 = code 0
+    wq, s = oracle.quantize_weight_clipped(w, 0, 80.0, 8)
+    assert s[0] == np.float32(1.8) / np.float32(127.0)
+    assert wq.tolist() == [[0, 0, 127, 0, 0, -127, 0, 0]]

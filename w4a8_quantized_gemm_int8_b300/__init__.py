@@ -155,8 +155,9 @@ def _check_out(out: torch.Tensor | None, shape: tuple, name: str = "out") -> Non
 _ws_cache: dict = {}
 
 
-def workspace_bytes(M: int, N: int, K: int, bits: int = 8, group_size: int = 0) -> int:
-    return int(load_library().cider_workspace_bytes(M, N, K, bits, group_size))
+def workspace_bytes(M: int, N: int, K: int, group_size: int = 0, bits: int = 8) -> int:
+    """cider_workspace_bytes: arguments in the C order (M, N, K, group_size, bits)."""
+    return int(load_library().cider_workspace_bytes(M, N, K, group_size, bits))
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor | None:
@@ -239,7 +240,7 @@ def w8a8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor, group_size
     _check_weights(K, N, wq, s_w, 8, group_size)
     _check_out(out, (M, N))
     y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=x.device)
-    need = workspace_bytes(M, N, K, 8, group_size)
+    need = workspace_bytes(M, N, K, group_size=group_size, bits=8)
     buf = ws if ws is not None else _workspace(need, x.device)
     wsp, wsn = (buf.data_ptr(), buf.numel()) if buf is not None else (None, 0)
     lib = load_library()
@@ -275,7 +276,7 @@ def linear(x: torch.Tensor, w: torch.Tensor, s_w: torch.Tensor, bits: int = 8,
     _check_weights(K, N, w, s_w, bits, group_size)
     _check_out(out, (M, N))
     y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=x.device)
-    need = workspace_bytes(M, N, K, bits, group_size)
+    need = workspace_bytes(M, N, K, group_size=group_size, bits=bits)
     buf = ws if ws is not None else _workspace(need, x.device)
     wsp, wsn = (buf.data_ptr(), buf.numel()) if buf is not None else (None, 0)
     wdt = torch.int8 if bits == 8 else torch.uint8
@@ -387,7 +388,7 @@ def w4a8_linear(x: torch.Tensor, wp: torch.Tensor, s_w: torch.Tensor, group_size
     _check_weights(K, N, wp, s_w, 4, group_size)
     _check_out(out, (M, N))
     y = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=x.device)
-    need = workspace_bytes(M, N, K, 4, group_size)
+    need = workspace_bytes(M, N, K, group_size=group_size, bits=4)
     buf = ws if ws is not None else _workspace(need, x.device)
     wsp, wsn = (buf.data_ptr(), buf.numel()) if buf is not None else (None, 0)
     lib = load_library()
@@ -488,7 +489,7 @@ def raw_gemm_s32(q: torch.Tensor, w: torch.Tensor, K: int, bits: int = 8,
     G = 1 if group_size == 0 else K // group_size
     out = torch.empty((M, N) if group_size == 0 else (M, N, G), dtype=torch.int32,
                       device=q.device)
-    need = workspace_bytes(max(M, 2), N, K, bits, group_size)
+    need = workspace_bytes(max(M, 2), N, K, group_size=group_size, bits=bits)
     buf = _workspace(need, q.device)
     wdt = torch.int8 if bits == 8 else torch.uint8
     st = load_library().cider_test_gemm_s32(

@@ -78,10 +78,14 @@ bool valid_dtype(int32_t d) { return d == CIDER_DTYPE_F16 || d == CIDER_DTYPE_BF
 
 ElemType elem(int32_t d) { return d == CIDER_DTYPE_BF16 ? ElemType::kBF16 : ElemType::kF16; }
 
-// Shared body of the layer entry points (x / y element types: CIDER_DTYPE_*).
-cider_status gemm_common(const void* x, int32_t x_dtype, int64_t M, int64_t N, int64_t K,
-                         const void* w, int bits, const float* s_w, int32_t gs, void* y,
-                         int32_t y_dtype, void* ws, size_t ws_bytes, cudaStream_t stream) {
+}  // namespace
+
+// Shared body of the layer entry points (x / y element types: CIDER_DTYPE_*);
+// declared in kernels.h.
+cider_status cider::linear_call(const void* x, int32_t x_dtype, int64_t M, int64_t N, int64_t K,
+                                const void* w, int bits, const float* s_w, int32_t gs, void* y,
+                                int32_t y_dtype, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                bool route_m1_to_gemv) {
     if (!valid_dtype(x_dtype) || !valid_dtype(y_dtype)) return CIDER_ERR_INVALID_ARG;
     if (!x || !w || !s_w || !y) return CIDER_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || gs < 0) return CIDER_ERR_INVALID_ARG;
@@ -93,7 +97,7 @@ cider_status gemm_common(const void* x, int32_t x_dtype, int64_t M, int64_t N, i
     cider_status st = num_sms(&sms);
     if (st != CIDER_OK) return st;
 
-    if (M == 1) {  // decode: the GEMV computes the same function
+    if (M == 1 && route_m1_to_gemv) {  // decode: the GEMV computes the same function
         if (K > 16384 || !valid_group(gs, K, bits == 8 ? 16 : 32)) return CIDER_ERR_UNSUPPORTED;
         unsigned long long* status = nullptr;
         if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
@@ -138,11 +142,20 @@ cider_status gemm_common(const void* x, int32_t x_dtype, int64_t M, int64_t N, i
     return from_cuda(launch_gemm(a, sms, stream));
 }
 
+namespace {
+
+cider_status gemm_common(const void* x, int32_t x_dtype, int64_t M, int64_t N, int64_t K,
+                         const void* w, int bits, const float* s_w, int32_t gs, void* y,
+                         int32_t y_dtype, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    return linear_call(x, x_dtype, M, N, K, w, bits, s_w, gs, y, y_dtype, ws, ws_bytes, stream,
+                       true);
+}
+
 }  // namespace
 
 extern "C" {
 
-const char* cider_status_string(int status) {
+const char* cider_status_string(cider_status status) {
     switch (status) {
         case CIDER_OK: return "CIDER_OK";
         case CIDER_ERR_INVALID_ARG: return "CIDER_ERR_INVALID_ARG";
@@ -216,7 +229,7 @@ cider_status cider_quantize_weight_clipped(const void* w, int32_t w_dtype, int64
                                              s_w, static_cast<cudaStream_t>(stream)));
 }
 
-size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t bits, int32_t group_size) {
+size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group_size, int32_t bits) {
     if (M <= 1 || N <= 0 || K <= 0 || (bits != 8 && bits != 4)) return 0;
     if (group_size < 0 || (group_size > 0 && K % group_size != 0)) return 0;
     return workspace_bytes(M, N, K, group_size);

@@ -190,6 +190,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no data returned, no completion
+// to wait for). src 16-byte aligned, bytes a multiple of 16. Safe ahead of a
+// dependency wait: L2 is the point of coherence, so a later read after the
+// wait still sees every write of the preceding kernel.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -10,9 +10,10 @@
 // HBM, so the kernel is built to keep as many bytes in flight as HBM needs.
 // Two CTAs per SM, each owning a contiguous slice of weight rows (row-major
 // weights make the slice one contiguous byte range). Weights and their scales
-// are never written by the kernel just before a GEMV, so the producer warp
-// starts ahead of the wait on that kernel (programmatic dependent launch):
-// it stages the per-channel scales of its rows, then issues bulk
+// may be written by the kernel just before a GEMV (a weight-preparation
+// call), so ahead of the wait on that kernel (programmatic dependent launch)
+// the producer warp only prefetches its slice into L2; after the wait it
+// stages the per-channel scales of its rows, then issues bulk
 // asynchronous copies (cp.async.bulk, mbarrier completion) of whole groups of
 // rows into a ring of shared-memory stages - one at once, the rest as soon as
 // the consumers hold x (so x's load does not queue behind the copies); for
@@ -208,6 +209,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
     float* sw_s = reinterpret_cast<float*>(smem + p.sw_off);
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
+        // Ahead of the dependency wait the CTA's weight slice (and staged
+        // per-group scales) is only prefetched into L2, which returns no data:
+        // the preceding kernel in the stream may be the one writing the
+        // weights (a weight-preparation call), so every read that lands in
+        // shared memory or registers comes after griddepcontrol.wait.
+        if (lane == 0) {
+            const uint8_t* src = p.w + (int64_t)n0 * p.row_bytes;
+            for (int s = 0; s < nst; ++s) {
+                const int rows = min(R, nrows - s * R);
+                bulk_prefetch_l2(src + (int64_t)s * R * p.row_bytes, (uint32_t)rows * p.row_bytes);
+            }
+            if (p.scales_staged && nrows > 0)
+                bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.s_w) + (int64_t)n0 * p.G * 4,
+                                 (uint32_t)nrows * p.G * 4);
+        }
+        grid_dep_wait();
         // Per-channel scales of the CTA's rows first: a small latency-bound
         // load that must not queue behind the bulk copies.
         if (!PG && p.sw_in_smem)
@@ -253,11 +270,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params p) {
     }
 
     // -------------------- per-token quantization of x ------------------------
-    // The producer's copies of weights (and staged per-group scales) above may
-    // start before the preceding kernel in the stream has finished
-    // (programmatic dependent launch): weights are never written by the
-    // kernel just before a GEMV. x, per-channel scales and y are touched only
-    // after this wait.
+    // Only the producer's L2 prefetch may run before the preceding kernel in
+    // the stream has finished (programmatic dependent launch); x, weights,
+    // scales and y are read or written only after this wait.
     grid_dep_wait();
     grid_dep_launch();
     {

@@ -7,7 +7,19 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/cider.h"
+
 namespace cider {
+
+// The quantized linear layer behind every layer entry point: argument
+// checks, workspace carving (ws / ws_bytes: at least cider_workspace_bytes
+// of the problem, else CIDER_ERR_WORKSPACE), then the kernels on `stream`.
+// M == 1 runs the GEMV when route_m1_to_gemv is set, the tensor-core GEMM
+// otherwise (the same results either way). x / y types: CIDER_DTYPE_*.
+cider_status linear_call(const void* x, int32_t x_dtype, int64_t M, int64_t N, int64_t K,
+                         const void* w, int bits, const float* s_w, int32_t gs, void* y,
+                         int32_t y_dtype, void* ws, size_t ws_bytes, cudaStream_t stream,
+                         bool route_m1_to_gemv);
 
 // Launches `kern` with programmatic stream serialization: it may be scheduled
 // while the preceding kernel in the stream is still running (that kernel

@@ -19,12 +19,15 @@
 // per device, with that device current, by the first call on that device;
 // that first call should therefore happen before any stream capture.
 //
-// Every call overwrites the parts of the array it reads (the kernels write
-// the operand images and scales before the GEMM reads them, and rows beyond
-// M are zero-filled by the tensor loads, not read from the array), so stale
-// contents from an earlier call never matter. Calls whose execution overlaps
-// on the GPU (different streams, or different host threads) share the array
-// and race: serialize them.
+// The call is cider_w8a8_gemm_pc's own layer body (the same checks, the same
+// workspace layout and the same kernels) with the array as its workspace;
+// only M == 1 differs: it runs the tensor-core GEMM instead of the GEMV (the
+// same results). Every call overwrites the parts of the array it reads (the
+// kernels write the operand images and scales before the GEMM reads them,
+// and rows beyond M are zero-filled by the tensor loads, not read from the
+// array), so stale contents from an earlier call never matter. Calls whose
+// execution overlaps on the GPU (different streams, or different host
+// threads) share the array and race: serialize them.
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <mutex>
@@ -35,15 +38,13 @@
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+static_assert(kStaticScratchBytes == CIDER_STATIC_SCRATCH_BYTES, "size stated in cider.h");
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
-
-constexpr size_t round256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 // Device address of the array on the current device (looked up once).
 cider_status scratch_address(void** out) {
@@ -61,69 +62,21 @@ cider_status scratch_address(void** out) {
     return CIDER_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" cider_status cider_w8a8_gemm_pc_noalloc(const void* x_f16, int64_t M, int64_t N,
                                                    int64_t K, const int8_t* wq, const float* s_w,
                                                    void* y_f16, void* stream) {
-    using namespace cider;
     if (!x_f16 || !wq || !s_w || !y_f16) return CIDER_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0) return CIDER_ERR_INVALID_ARG;
-    if (K % 16 != 0) return CIDER_ERR_UNSUPPORTED;
-    if (!aligned16(x_f16) || !aligned16(wq) || !aligned16(s_w) || !aligned16(y_f16))
-        return CIDER_ERR_UNSUPPORTED;
-    if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return CIDER_ERR_UNSUPPORTED;
-    // Layout inside the array: a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K]
-    // fp16 (only for the SM-pair engine; the single-SM engine reads wq itself).
-    const bool img = gemm_uses_pair(M);
-    const size_t a_bytes = round256((size_t)M * K * 2);
-    const size_t s_bytes = round256((size_t)M * 4);
-    const size_t b_bytes = img ? round256((size_t)N * K * 2) : 0;
-    if (a_bytes + s_bytes + b_bytes > kStaticScratchBytes) return CIDER_ERR_WORKSPACE;
-
+    // Problems whose scratch exceeds the array are refused before the
+    // address lookup (the layer body checks the size again, M == 1 included).
+    if (M > 1 && cider_workspace_bytes(M, N, K, 0, 8) > kStaticScratchBytes)
+        return CIDER_ERR_WORKSPACE;
     void* base = nullptr;
-    cider_status st = scratch_address(&base);
+    const cider_status st = scratch_address(&base);
     if (st != CIDER_OK) return st;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return CIDER_ERR_CUDA;
-    unsigned long long* status = nullptr;
-    if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
-
-    uint8_t* p = static_cast<uint8_t*>(base);
-    __half* a_img = reinterpret_cast<__half*>(p);
-    float* s_a = reinterpret_cast<float*>(p + a_bytes);
-    __half* b_img = img ? reinterpret_cast<__half*>(p + a_bytes + s_bytes) : nullptr;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    cudaError_t e = launch_operand_images(x_f16, ElemType::kF16, M, K,
-                                          img ? wq : nullptr, 8, N, a_img, s_a, b_img, nullptr,
-                                          nullptr, 1, sms, s);
-    if (e == cudaSuccess) {
-        GemmArgs a{};
-        a.a_img = a_img;
-        a.b_img = b_img;
-        a.b_raw = img ? nullptr : wq;
-        a.b_bits = 8;
-        a.M = M;
-        a.N = N;
-        a.K = K;
-        a.group_size = 0;
-        a.s_a = s_a;
-        a.s_w = s_w;
-        a.out = y_f16;
-        a.mode = GemmMode::kPcF16;
-        a.timeout_ns = kWaitTimeoutNs;
-        a.status = status;
-        e = launch_gemm(a, sms, s);
-    }
-    if (e == cudaSuccess) return CIDER_OK;
-    if (e == cudaErrorInvalidValue) {
-        cudaGetLastError();
-        return CIDER_ERR_UNSUPPORTED;
-    }
-    return CIDER_ERR_CUDA;
+    return cider::linear_call(x_f16, CIDER_DTYPE_F16, M, N, K, wq, 8, s_w, 0, y_f16,
+                              CIDER_DTYPE_F16, base, kStaticScratchBytes,
+                              static_cast<cudaStream_t>(stream), false);
 }
