@@ -135,10 +135,12 @@ CIDER_API cider_status cider_quantize_weight_clipped(const void* w, int32_t w_dt
  * Bytes of device workspace the GEMM calls below need for this problem:
  * group_size 0 (per channel) or the per-group size, then bits 8 or 4 (the
  * order of the layer calls' own arguments). The workspace holds the fp16
- * operand images of the quantized activations and weights and the per-token
- * scales, and for group_size > 0 a group-major copy of the per-group weight
- * scales. Returns 0 when M == 1 (the GEMV path needs none) and on invalid
- * sizes (including a group_size that does not divide K).
+ * image of the quantized activations (the codes as exact fp16 integers) and
+ * the per-token scales; for M > 128, except for INT8 per-group layers (whose
+ * weights are widened on chip), an fp16 image of the weight codes; and for
+ * per-group layers that read one, a group-major copy of the weight scales.
+ * Returns 0 when M == 1 (the GEMV path needs none) and on invalid sizes
+ * (including a group_size that does not divide K).
  */
 CIDER_API size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group_size,
                                        int32_t bits);

@@ -49,12 +49,19 @@ def test_workspace_bytes(lib):
     assert cider.workspace_bytes(1, 10240, 2560) == 0   # GEMV path
     assert cider.workspace_bytes(0, 16, 16) == 0
     assert cider.workspace_bytes(4, 16, 16, bits=3) == 0
+    # per channel, SM pairs: activation image, token scales, fp16 weight image
     n = cider.workspace_bytes(4096, 10240, 2560)
-    assert n >= 2 * 4096 * 2560 + 4 * 4096 + 2 * 10240 * 2560
+    assert n == 2 * 4096 * 2560 + 4 * 4096 + 2 * 10240 * 2560
     assert n % 256 == 0
-    # per-group: plus the group-major copy of the scales
+    # INT8 per group, SM pairs: the weights are widened on chip (no image)
     g = cider.workspace_bytes(4096, 2560, 10240, group_size=64, bits=8)
-    assert g >= 2 * 4096 * 10240 + 4 * 4096 + 2 * 2560 * 10240 + 4 * 2560 * (10240 // 64)
+    assert g == 2 * 4096 * 10240 + 4 * 4096
+    # W4A8 per group, SM pairs: weight image and a group-major copy of the scales
+    w4 = cider.workspace_bytes(4096, 2560, 10240, group_size=128, bits=4)
+    assert w4 == 2 * 4096 * 10240 + 4 * 4096 + 2 * 2560 * 10240 + 4 * 2560 * (10240 // 128)
+    # few tokens, per group: activation image and the group-major scale copy
+    s = cider.workspace_bytes(64, 2560, 10240, group_size=64, bits=8)
+    assert s == 2 * 64 * 10240 + 256 + 4 * 2560 * (10240 // 64)
     assert cider.workspace_bytes(4096, 2560, 10240, group_size=100, bits=8) == 0  # 100 does not divide K
 
 

@@ -41,19 +41,36 @@ cider_status from_cuda(cudaError_t e) {
 struct Workspace {
     __half* a_img;
     float* s_a;
-    __half* b_img;
-    float* s_wT;  // per-group scales, group-major (per-group modes only)
+    __half* b_img;  // fp16 weight image (SM-pair engine, image path only)
+    float* s_wT;    // per-group scales, group-major (per-group, engines that read it)
 };
 
-// a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K] fp16 (SM-pair engine only;
-// the single-SM engine reads the raw weight codes) | s_wT [K/gs, N] fp32 (gs > 0)
-size_t workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t gs = 0) {
-    const size_t b = gemm_uses_pair(M) ? align256((size_t)N * K * 2) : 0;
-    const size_t t = gs > 0 ? align256((size_t)(K / gs) * N * 4) : 0;
+// Weight operand of the SM-pair engine (M > 128): INT8 per-group layers take
+// the raw codes, widened on chip into tensor memory (gemm_tw.cu); the other
+// layers take an fp16 weight image written by the operand-image launch
+// (gemm_tc2.cu). Measured on B300 at M = 4096 (public call): per-group gs 64
+// 370 us raw against 493 us with the image, gs 128 296 against 315; per
+// channel 205 against 160 and W4A8 gs 128 (M = 8192) 542 against 443 - the
+// 192-token tiles of the raw engine leave its MMA thread too little slack.
+bool pair_uses_image(int64_t M, int64_t gs, int bits) {
+    return gemm_uses_pair(M) && !(gs > 0 && bits == 8);
+}
+
+// Group-major scale copy: read by the single-SM engine and by the image
+// pair kernel in per-group mode.
+bool uses_scales_t(int64_t M, int64_t gs, int bits) {
+    return gs > 0 && (!gemm_uses_pair(M) || pair_uses_image(M, gs, bits));
+}
+
+// a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K] fp16 (image path) |
+// s_wT [K/gs, N] fp32 (uses_scales_t)
+size_t workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t gs, int bits) {
+    const size_t b = pair_uses_image(M, gs, bits) ? align256((size_t)N * K * 2) : 0;
+    const size_t t = uses_scales_t(M, gs, bits) ? align256((size_t)(K / gs) * N * 4) : 0;
     return align256((size_t)M * K * 2) + align256((size_t)M * 4) + b + t;
 }
 
-Workspace carve(void* ws, int64_t M, int64_t N, int64_t K, int64_t gs = 0) {
+Workspace carve(void* ws, int64_t M, int64_t N, int64_t K, int64_t gs, int bits) {
     uint8_t* p = static_cast<uint8_t*>(ws);
     Workspace w;
     w.a_img = reinterpret_cast<__half*>(p);
@@ -61,11 +78,11 @@ Workspace carve(void* ws, int64_t M, int64_t N, int64_t K, int64_t gs = 0) {
     w.s_a = reinterpret_cast<float*>(p);
     p += align256((size_t)M * 4);
     w.b_img = nullptr;
-    if (gemm_uses_pair(M)) {
+    if (pair_uses_image(M, gs, bits)) {
         w.b_img = reinterpret_cast<__half*>(p);
         p += align256((size_t)N * K * 2);
     }
-    w.s_wT = gs > 0 ? reinterpret_cast<float*>(p) : nullptr;
+    w.s_wT = uses_scales_t(M, gs, bits) ? reinterpret_cast<float*>(p) : nullptr;
     return w;
 }
 
@@ -108,18 +125,19 @@ cider_status cider::linear_call(const void* x, int32_t x_dtype, int64_t M, int64
     // A group's partial sum must stay exact in the tensor core's fp32
     // accumulator: at most 1024 products of magnitude <= 127^2.
     if (!valid_group(gs, K, 64) || gs > 1024) return CIDER_ERR_UNSUPPORTED;
-    const size_t need = workspace_bytes(M, N, K, gs);
+    const size_t need = workspace_bytes(M, N, K, gs, bits);
     if (!ws || ws_bytes < need) return CIDER_ERR_WORKSPACE;
     if (!aligned16(ws)) return CIDER_ERR_UNSUPPORTED;
     unsigned long long* status = nullptr;
     if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
 
-    // SM-pair engine: fp16 images of both operands. Single-SM engine (few
-    // tokens): activation image only; the GEMM widens the raw weight codes.
-    Workspace wsp = carve(ws, M, N, K, gs);
+    // The activation image (fp16 codes and token scales), and the fp16
+    // weight image where the engine takes one, in one launch; the other
+    // engines widen the raw weight codes on chip.
+    Workspace wsp = carve(ws, M, N, K, gs, bits);
     const bool img = wsp.b_img != nullptr;
-    cudaError_t e = launch_operand_images(x, elem(x_dtype), M, K, img ? w : nullptr,
-                                          bits, N, wsp.a_img, wsp.s_a, wsp.b_img, s_w, wsp.s_wT,
+    cudaError_t e = launch_operand_images(x, elem(x_dtype), M, K, img ? w : nullptr, bits, N,
+                                          wsp.a_img, wsp.s_a, wsp.b_img, s_w, wsp.s_wT,
                                           gs > 0 ? K / gs : 1, sms, stream);
     if (e != cudaSuccess) return from_cuda(e);
     GemmArgs a{};
@@ -232,7 +250,7 @@ cider_status cider_quantize_weight_clipped(const void* w, int32_t w_dtype, int64
 size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group_size, int32_t bits) {
     if (M <= 1 || N <= 0 || K <= 0 || (bits != 8 && bits != 4)) return 0;
     if (group_size < 0 || (group_size > 0 && K % group_size != 0)) return 0;
-    return workspace_bytes(M, N, K, group_size);
+    return workspace_bytes(M, N, K, group_size, bits);
 }
 
 cider_status cider_w8a8_gemm_pc(const void* x_f16, int64_t M, int64_t N, int64_t K,
@@ -386,7 +404,7 @@ cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int6
         return CIDER_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(w) || !aligned16(out)) return CIDER_ERR_UNSUPPORTED;
     const int64_t Mw = M < 2 ? 2 : M;
-    if (!ws || ws_bytes < workspace_bytes(Mw, N, K)) return CIDER_ERR_WORKSPACE;
+    if (!ws || ws_bytes < workspace_bytes(Mw, N, K, group_size, bits)) return CIDER_ERR_WORKSPACE;
     if (!aligned16(ws)) return CIDER_ERR_UNSUPPORTED;
     int sms = 0;
     cider_status st = num_sms(&sms);
@@ -394,7 +412,7 @@ cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int6
     unsigned long long* status = nullptr;
     if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    Workspace wsp = carve(ws, Mw, N, K);
+    Workspace wsp = carve(ws, Mw, N, K, group_size, bits);
     cudaError_t e = launch_widen_i8(q, M * K, wsp.a_img, sms, s);
     if (e != cudaSuccess) return from_cuda(e);
     if (wsp.b_img) {

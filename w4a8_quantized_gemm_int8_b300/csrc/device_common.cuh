@@ -154,6 +154,45 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Like mbar_try_wait, but the thread may be suspended in hardware for up to
+// suspend_ns while the phase is incomplete (it resumes when the phase
+// completes or the time runs out), instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait_bounded for threads off the critical issue path: while the phase
+// is incomplete the thread sleeps in hardware (up to suspend_ns per try)
+// rather than spinning, leaving its scheduler's issue slots to the warps
+// that feed the tensor core. Same bound, abort and reporting rules.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity,
+                                                        uint64_t timeout_ns,
+                                                        volatile int* abort,
+                                                        unsigned long long* status,
+                                                        uint32_t site,
+                                                        uint32_t suspend_ns = 2000) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, suspend_ns)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            report_device_error(status, kDevTimeout, site);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // Drain wait: like mbar_wait_bounded but does not give up when *abort is
 // raised (used after an abort, to let copies or MMAs already issued by this
 // CTA complete before it releases shared or tensor memory). Bounded by

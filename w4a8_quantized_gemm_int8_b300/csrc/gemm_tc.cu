@@ -747,6 +747,13 @@ CUresult encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, ui
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
+CUresult encode_tmap_u8_2d_swizzled(CUtensorMap* map, const void* base, uint64_t rows,
+                                    uint64_t cols, uint32_t box_rows, uint32_t box_cols,
+                                    CUtensorMapSwizzle swizzle) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, box_rows, box_cols,
+                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
 cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     using namespace gemm1;
     if (a.M <= 0 || a.N <= 0 || a.K <= 0 || a.K % 16 != 0) return cudaErrorInvalidValue;

@@ -714,7 +714,12 @@ bool gemm_uses_pair(int64_t M) {
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream) {
-    if (gemm_uses_pair(a.M) && a.b_img) return launch_gemm_tc_pair(a, num_sms, stream);
+    if (gemm_uses_pair(a.M)) {
+        // Raw weight codes: widened on chip into tensor memory; an fp16
+        // weight image (cider_gemm_images): read as it is.
+        if (a.b_raw) return launch_gemm_tw(a, num_sms, stream);
+        if (a.b_img) return launch_gemm_tc_pair(a, num_sms, stream);
+    }
     return launch_gemm_tc(a, num_sms, stream);
 }
 

@@ -1,0 +1,788 @@
+// INT8 x INT8 -> INT32 GEMM with fused dequant on a pair of SMs, the weight
+// codes widened on chip into tensor memory (no weight image in HBM).
+//
+// What it computes (Cider README, "Metal Kernel Pipeline" and
+// "Quantization"; W4A8 per the "Modes" table, "Unpack -> TensorOps"):
+// acc[m,n] = sum_k q[m,k] * wq[n,k] exactly in int32, then
+//   per-channel: y = fp16(((float)acc * s_a[m]) * s_w[n])
+//   per-group:   f = sum over groups g, ascending, of (float)P_g * s_w[n,g]; y = fp16(f * s_a[m])
+// on exact fp16 images of the codes with tcgen05 kind::f16 (sm_103a has no
+// integer MMA kind) and an fp32 tensor-memory accumulator folded into int32
+// every <= 1024 k (every group in per-group mode), where every partial sum is
+// an exact integer.
+//
+// Roles are swapped relative to a token-major GEMM: the weights are the MMA's
+// A operand (M = 256 output channels per SM pair, 128 per CTA) and the tokens
+// its B operand (N = 192 tokens per pair tile, 96 loaded by each CTA). The
+// tensor core reads A from tensor memory, so the weights never need an fp16
+// copy in shared or global memory: TMA stages each CTA's raw codes (INT8
+// [N,K], or packed INT4 [N,K/2]) as 128 rows x one 64-k block, and four
+// converter warps (one per TMEM lane quadrant; thread = weight row) widen
+// them to exact fp16 pairs with byte permutes and one fp16 subtraction and
+// write them with tcgen05.st into one of four 32-column A stages in TMEM. The
+// activations come from the fp16 code image of the per-token quantization
+// (K-major, 128-byte swizzle) as B. The even CTA's MMA thread issues
+// tcgen05.mma.cta_group::2 (M 256, N 192, K 16) with A in both CTAs' tensor
+// memory and B in both CTAs' shared memory, into two 192-column fp32
+// accumulators per CTA (lane = output channel, column = token). Measured on
+// B300: this MMA runs at full rate (96 cycles per instruction), the same as
+// with A in shared memory, but each tcgen05.mma costs the issuing thread
+// about 55 cycles and each tcgen05.commit about 60, so a k-block (four MMAs,
+// 384 cycles) carries exactly one barrier wait and one commit: the token
+// bytes and the converters' arrivals complete one "full" barrier, and one
+// commit per k-block frees both its shared-memory stage and its A stage.
+//
+// Epilogue (8 warps: each one TMEM lane quadrant, i.e. 32 output channels,
+// and half of the tile's 192 tokens): segment folds as in the token-major
+// kernels; the final dequant writes 32 tokens x 32 channels per step through
+// shared-memory staging and a TMA store. Persistent over tiles (token tile
+// fastest, so concurrent clusters share weight tiles in L2). Every mbarrier
+// wait is bounded.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+#include <cstring>
+
+#include "device_common.cuh"
+#include "host_once.h"
+#include "kernels.h"
+
+namespace cider {
+namespace gemmw {
+
+constexpr int BW = 128;           // weight rows per CTA (MMA M = 256 per pair)
+constexpr int BT = 192;           // tokens per pair tile (MMA N); each CTA loads BT / 2
+constexpr int BK = 64;            // k per block: one 128-byte swizzle row of fp16 tokens
+constexpr int KB_PER_STAGE = 1;   // 64-k blocks per stage (the MMA loop assumes 1)
+constexpr int SK = BK * KB_PER_STAGE;
+constexpr int STAGES = 8 / KB_PER_STAGE;    // shared-memory ring (raw weights + tokens)
+constexpr int A_STAGES = 4 / KB_PER_STAGE;  // tensor-memory ring of widened weights
+constexpr int A_STAGE_COLS = SK / 2;  // two fp16 per 32-bit column
+constexpr int NUM_ACC = 2;
+constexpr int ACC_COLS = BT;
+constexpr int A_COL0 = NUM_ACC * ACC_COLS;  // 384
+constexpr int TMEM_COLS = 512;
+static_assert(A_COL0 + A_STAGES * A_STAGE_COLS <= TMEM_COLS, "tensor memory budget");
+constexpr int ACT_BLOCK_BYTES = (BT / 2) * BK * 2;  // one 64-k token block: 12 KB per CTA
+constexpr int ACT_STAGE_BYTES = KB_PER_STAGE * ACT_BLOCK_BYTES;
+constexpr int RAW_STAGE_BYTES = BW * SK;            // 16 KB (INT8; INT4 uses half)
+constexpr int MAX_SEG_KB = 16;    // 16 x 64 = 1024 k per exact fp32 segment
+// Warps 0-3: TMA producer, MMA issuer (and TMEM owner), two idle; warps
+// 4-11: two converter warpgroups, taking alternate k-blocks; warps 12-19:
+// epilogue.
+constexpr int NUM_CONV_GROUPS = 2;
+constexpr int FIRST_EPI_WARP = 4 + 4 * NUM_CONV_GROUPS;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = (FIRST_EPI_WARP + NUM_EPI_WARPS) * 32;
+constexpr int LAUNCH_REGS = 96;
+constexpr int ROLE_REGS = 40;
+// Converter / epilogue register split per weight width (the split ptxas
+// allocates without spills for the per-channel kernels of each width).
+template <int BITS>
+struct Regs {
+    static constexpr int kConv = BITS == 8 ? 56 : 48;
+    static constexpr int kEpi = BITS == 8 ? 160 : 168;
+    static_assert(128 * ROLE_REGS + 128 * NUM_CONV_GROUPS * kConv + 256 * kEpi <=
+                      NUM_THREADS * LAUNCH_REGS,
+                  "register split exceeds the launch allocation");
+};
+constexpr int COLS = BT / 2;      // tokens per epilogue warp
+constexpr int CHUNKS = COLS / 32; // 32-token output rounds per warp
+constexpr int LD = 16;            // columns per TMEM load of the fold
+constexpr int OUT_WARP_BYTES = 32 * 64;  // staging: 32 tokens x 32 channels fp16
+constexpr int SMEM_LIMIT = 232448;
+constexpr uint16_t kPairMask = 0x3;
+
+struct __align__(8) Barriers {
+    // even CTA: stage u's token blocks landed (both CTAs' TMA bytes) and its
+    // weights are in A stage u % A_STAGES (both CTAs' converters arrived):
+    // one producer arrival with the byte count + 4 converter warps x 2 CTAs.
+    uint64_t full[STAGES];
+    // each CTA: the MMAs of stage u completed (one commit, multicast): the
+    // shared-memory stage, and A stage u % A_STAGES, may be refilled.
+    uint64_t empty[STAGES];
+    uint64_t raw_full[STAGES];   // each CTA: its raw weight block landed
+    uint64_t acc_full[NUM_ACC];  // each CTA: accumulator buffer ready
+    uint64_t acc_empty[NUM_ACC]; // even CTA: both CTAs' epilogues drained it (16 warps)
+    uint64_t drain;              // even CTA: MMA drain after an abort
+};
+static_assert(sizeof(Barriers) <= 512, "barrier area");
+static_assert(STAGES % A_STAGES == 0 && STAGES >= A_STAGES, "A stages follow the ring");
+static_assert(SK == 64 || SK == 128, "raw rows of 32 to 128 bytes");
+static_assert(KB_PER_STAGE == 1 && (STAGES & (STAGES - 1)) == 0 &&
+                  (A_STAGES & (A_STAGES - 1)) == 0 && (NUM_ACC & (NUM_ACC - 1)) == 0,
+              "ring arithmetic by masks");
+
+struct SmemLayout {
+    static constexpr int raw_off = 0;
+    static constexpr int act_off = raw_off + STAGES * RAW_STAGE_BYTES;
+    static constexpr int out_off = act_off + STAGES * ACT_STAGE_BYTES;
+    static constexpr int bar_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;
+    static constexpr int misc_off = bar_off + 512;  // tmem base, abort flag
+    static constexpr int bytes = misc_off + 16;
+    static constexpr int alloc_bytes = bytes + 1024;  // runtime 1024-byte alignment slack
+    static_assert(alloc_bytes <= SMEM_LIMIT, "shared memory per block");
+    static_assert(act_off % 1024 == 0 && RAW_STAGE_BYTES % 1024 == 0 &&
+                      ACT_STAGE_BYTES % 1024 == 0,
+                  "swizzled stages must stay 1024-byte aligned");
+};
+
+struct Params {
+    int M, N, K;
+    int bits;        // 8: INT8 codes; 4: packed INT4 (nibble = code + 8)
+    int num_kb;
+    int seg_kb;      // k-blocks per segment (one accumulator buffer)
+    int num_seg;
+    int G;
+    int tiles_t, tiles_w;  // token tiles of BT, weight tiles of 2 * BW
+    const float* s_a;
+    const float* s_w;
+    void* out;
+    int tma_store;   // 16-bit output through tmap_y (N % 8 == 0)
+    int out_bf16;
+    uint64_t timeout_ns;
+    unsigned long long* status;
+};
+
+enum : uint32_t {
+    kSiteProducerEmpty = 0x401,
+    kSiteMmaAccEmpty = 0x403,
+    kSiteMmaFull = 0x404,
+    kSiteConvRaw = 0x406,
+    kSiteConvA = 0x407,
+    kSiteEpiAccFull = 0x408,
+    kSiteDrain = 0x409,
+    kSiteProducerDrain = 0x40a,
+};
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T on both CTAs of the pair, kind::f16.
+__device__ __forceinline__ void mma_pair_a_tmem(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The four MMAs of one 64-k block: D (+)= A[a_tmem + 8k] * B[b_desc + 2k]^T
+// for k = 0..3 (16 k each; B advances 32 bytes within its 128-byte swizzle
+// rows), the first one accumulating only if `accumulate`.
+__device__ __forceinline__ void mma4_pair_a_tmem(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%5], %6, %3, t;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%7], %8, %3, t;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%9], %10, %3, t;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(a_tmem + 8), "l"(b_desc + 2),
+        "r"(a_tmem + 16), "l"(b_desc + 4), "r"(a_tmem + 24), "l"(b_desc + 6)
+        : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes from 32 registers.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// 16 consecutive TMEM columns of this warp's 32 lanes from 16 registers.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Four signed INT8 codes (k order) -> two packed fp16 pairs (exact): the code
+// plus 128 goes under the fp16 exponent of 1024 (0x64 high byte), then
+// 1024 + 128 is subtracted.
+__device__ __forceinline__ void widen_i8x4(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // [c0 + 128, 0x64, c1 + 128, 0x64]
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);  // [c2 + 128, 0x64, c3 + 128, 0x64]
+    const __half2 bias = __float2half2_rn(1152.0f);
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    p01 = *reinterpret_cast<const uint32_t*>(&ha);
+    p23 = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// Eight INT4 codes (one 32-bit word: element 2j in the low nibble of byte j)
+// -> four packed fp16 pairs (exact): nibble under the exponent of 1024, then
+// 1024 + 8 subtracted.
+__device__ __forceinline__ void widen_i4x8(uint32_t w, uint32_t* p) {
+    const uint32_t lo = w & 0x0F0F0F0Fu;         // elements 0, 2, 4, 6
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // elements 1, 3, 5, 7
+    const __half2 bias = __float2half2_rn(1032.0f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        // bytes [lo.bj, hi.bj] -> halves 0x64lo, 0x64hi
+        const uint32_t sel = (uint32_t)j | ((uint32_t)(4 + j) << 8);
+        uint32_t v = (__byte_perm(lo, hi, sel) & 0x00FF00FFu) | 0x64006400u;
+        const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), bias);
+        p[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+template <GemmMode MODE, int BITS>
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
+    gemm_tw_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                   const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_y, const Params p) {
+    constexpr int RAW_ROW = (BITS == 8) ? SK : SK / 2;     // raw bytes of one row and stage
+    constexpr int RAW_BYTES = BW * RAW_ROW;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Barriers* bars = reinterpret_cast<Barriers*>(smem + SmemLayout::bar_off);
+    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+    const int cluster = (int)cluster_id_x();
+    const int nclusters = (int)num_clusters_x();
+    const int num_tiles = p.tiles_t * p.tiles_w;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1 + 4 * 2);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+            mbar_init(smem_u32(&bars->raw_full[s]), 1);
+        }
+        for (int b = 0; b < NUM_ACC; ++b) {
+            mbar_init(smem_u32(&bars->acc_full[b]), 1);
+            mbar_init(smem_u32(&bars->acc_empty[b]), 2 * NUM_EPI_WARPS);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmap_x);
+        prefetch_tmap(&tmap_w);
+        if (p.tma_store) prefetch_tmap(&tmap_y);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_base_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    // Both CTAs' barriers are initialised before any cross-CTA arrive or TMA.
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_base_slot;
+    // Everything above overlaps the tail of the preceding kernel (programmatic
+    // dependent launch); global memory is touched only after this wait.
+    grid_dep_wait();
+    grid_dep_launch();
+
+    if (warp < 4) {
+        setmaxnreg_dec<ROLE_REGS>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------ TMA producer (both CTAs) ----------
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+                const int tt = tile % p.tiles_t, tw = tile / p.tiles_t;
+                const int w_row = tw * (2 * BW) + (int)rank * BW;
+                const int t_row = tt * BT + (int)rank * (BT / 2);
+                for (int ks = 0; ks < p.num_kb; ++ks) {
+                    // The MMAs of the stage's previous use completed: its token
+                    // blocks were read, and so was its raw block (the
+                    // converters arrive on the full barrier the MMA waited on).
+                    if (!mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1, p.timeout_ns,
+                                           abort_flag, p.status, kSiteProducerEmpty))
+                        goto producer_done;
+                    const uint32_t rf = smem_u32(&bars->raw_full[stage]);
+                    mbar_arrive_expect_tx(rf, RAW_BYTES);
+                    tma_load_2d(smem_u32(smem + SmemLayout::raw_off + stage * RAW_STAGE_BYTES),
+                                &tmap_w, rf, ks * RAW_ROW, w_row);
+                    const uint32_t bf_local = smem_u32(&bars->full[stage]);
+                    if (rank == 0) mbar_arrive_expect_tx(bf_local, 2 * ACT_STAGE_BYTES);
+#pragma unroll
+                    for (int j = 0; j < KB_PER_STAGE; ++j)
+                        tma_load_2d_pair(smem_u32(smem + SmemLayout::act_off +
+                                                  stage * ACT_STAGE_BYTES + j * ACT_BLOCK_BYTES),
+                                         &tmap_x, map_to_rank(bf_local, 0), ks * SK + j * BK,
+                                         t_row);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        producer_done:
+            // No copy may still be landing, and no MMA-commit arrive from the
+            // other CTA may still be in flight, when this CTA exits.
+            for (int u = (issued > STAGES ? issued - STAGES : 0); u < issued; ++u) {
+                const uint32_t ph = (uint32_t)(u / STAGES) & 1u;
+                if (!mbar_wait_drain(smem_u32(&bars->raw_full[u % STAGES]), ph, p.timeout_ns) ||
+                    !mbar_wait_drain(smem_u32(&bars->empty[u % STAGES]), ph, p.timeout_ns))
+                    report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
+            }
+        } else if (warp == 1 && lane == 0 && rank == 0) {
+            // ------------------------------ MMA issuer (even CTA) -------------
+            constexpr uint32_t idesc = idesc_f16_f32acc(2 * BW, BT);
+            uint32_t seg_count = 0;
+            bool issued_any = false;
+            // The issuing thread is on the critical path: each tcgen05.mma
+            // costs it ~55 cycles and a k-block's four MMAs run 384 cycles,
+            // so the loop keeps to one barrier wait, one four-MMA issue and
+            // one commit per k-block, with no division.
+            const uint32_t a_base = tmem_base + A_COL0;
+            const uint32_t act_base = smem_u32(smem + SmemLayout::act_off);
+            uint32_t u = 0;  // k-blocks issued (the ring position)
+            for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+                for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.seg_kb, ++seg_count) {
+                    const uint32_t b = seg_count & (NUM_ACC - 1);
+                    const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
+                    if (!mbar_wait_bounded(smem_u32(&bars->acc_empty[b]), acc_phase ^ 1,
+                                           p.timeout_ns, abort_flag, p.status, kSiteMmaAccEmpty))
+                        goto mma_done;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + b * ACC_COLS;
+                    const int kb1 = min(p.num_kb, kb0 + p.seg_kb);
+                    for (int kb = kb0; kb < kb1; ++kb, ++u) {
+                        const uint32_t stage = u & (STAGES - 1);
+                        if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), (u / STAGES) & 1,
+                                               p.timeout_ns, abort_flag, p.status, kSiteMmaFull))
+                            goto mma_done;
+                        tc_fence_after();
+                        mma4_pair_a_tmem(d_tmem, a_base + (u & (A_STAGES - 1)) * A_STAGE_COLS,
+                                         smem_desc_sw128_kmajor(act_base + stage * ACT_STAGE_BYTES),
+                                         idesc, kb > kb0 ? 1u : 0u);
+                        issued_any = true;
+                        // One commit per k-block releases its shared-memory
+                        // stage and its A stage on both CTAs.
+                        tc_commit_pair_multicast(smem_u32(&bars->empty[stage]), kPairMask);
+                    }
+                    tc_commit_pair_multicast(smem_u32(&bars->acc_full[b]), kPairMask);
+                }
+            }
+        mma_done:
+            if (*abort_flag && issued_any) {
+                tc_commit_pair_multicast(smem_u32(&bars->drain), 0x1);
+                if (!mbar_wait_drain(smem_u32(&bars->drain), 0, p.timeout_ns))
+                    report_device_error(p.status, kDevTimeout, kSiteDrain);
+            }
+        }
+    } else if (warp < FIRST_EPI_WARP) {
+        setmaxnreg_dec<Regs<BITS>::kConv>();
+        // ------------------------------ converters (both CTAs) ----------------
+        // Thread = weight row r of the CTA's 128 (TMEM lane r): reads its raw
+        // k-block (swizzled 16-byte chunks), widens it to 32 fp16 pairs and
+        // stores them into the A stage's 32 columns of lane r. Converter
+        // warpgroup cg takes the k-blocks u (in the CTA's running order) with
+        // u % NUM_CONV_GROUPS == cg, so two k-blocks are widened at once.
+        const int q = warp & 3;
+        const int cg = (warp - 4) >> 2;
+        const int r = q * 32 + lane;
+        const int total = ((num_tiles - cluster + nclusters - 1) / nclusters) * p.num_kb;
+        for (int u = cg; u < total; u += NUM_CONV_GROUPS) {
+            const int stage = u % STAGES, astage = u % A_STAGES;
+            const uint32_t phase = (uint32_t)(u / STAGES) & 1u;
+            bool ok = mbar_wait_bounded(smem_u32(&bars->raw_full[stage]), phase, p.timeout_ns,
+                                        abort_flag, p.status, kSiteConvRaw);
+            // A stage u % A_STAGES is free once the MMAs of stage u - A_STAGES
+            // completed.
+            if (u >= A_STAGES) {
+                const int v = u - A_STAGES;
+                ok = ok && mbar_wait_bounded(smem_u32(&bars->empty[v % STAGES]),
+                                             (uint32_t)(v / STAGES) & 1u, p.timeout_ns,
+                                             abort_flag, p.status, kSiteConvA);
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const uint8_t* raw = smem + SmemLayout::raw_off + stage * RAW_STAGE_BYTES;
+            const uint32_t t_a = tmem_base + ((uint32_t)(q * 32) << 16) + A_COL0 +
+                                 astage * A_STAGE_COLS;
+            // Raw rows of RAW_ROW bytes, swizzled by TMA with a span of RAW_ROW:
+            // 16-byte chunk c of row r sits at chunk c ^ ((r >> SH) & (RAW_ROW / 16 - 1)).
+            constexpr int SH = RAW_ROW == 128 ? 0 : RAW_ROW == 64 ? 1 : 2;
+            const int swz = (r >> SH) & (RAW_ROW / 16 - 1);
+#pragma unroll
+            for (int h = 0; h < SK / 32; ++h) {  // 32 k per step: 16 columns
+                uint32_t v[16];
+                if constexpr (BITS == 8) {
+                    uint4 w2[2];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        w2[c] = *reinterpret_cast<const uint4*>(
+                            raw + r * RAW_ROW + (((2 * h + c) ^ swz) << 4));
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const uint4 w = w2[c];
+                        widen_i8x4(w.x, v[8 * c + 0], v[8 * c + 1]);
+                        widen_i8x4(w.y, v[8 * c + 2], v[8 * c + 3]);
+                        widen_i8x4(w.z, v[8 * c + 4], v[8 * c + 5]);
+                        widen_i8x4(w.w, v[8 * c + 6], v[8 * c + 7]);
+                    }
+                } else {
+                    const uint4 w =
+                        *reinterpret_cast<const uint4*>(raw + r * RAW_ROW + ((h ^ swz) << 4));
+                    widen_i4x8(w.x, v + 0);
+                    widen_i4x8(w.y, v + 4);
+                    widen_i4x8(w.z, v + 8);
+                    widen_i4x8(w.w, v + 12);
+                }
+                tmem_st_32x32b_x16(t_a + 16 * h, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            // Relaxed arrival: the tensor-memory stores are ordered for the
+            // MMA thread by the tcgen05 fences around this synchronization,
+            // not by release semantics (a cluster-scope release costs a full
+            // memory barrier per k-block).
+            if (lane == 0)
+                mbar_arrive_cluster_relaxed(map_to_rank(smem_u32(&bars->full[stage]), 0));
+        }
+    } else {
+        setmaxnreg_inc<Regs<BITS>::kEpi>();
+        // ------------------------------ epilogue (both CTAs) ------------------
+        // Warp w (12..19) owns TMEM lanes 32 * (w % 4).. (32 output channels,
+        // one per thread) and the COLS tokens [COLS * half, COLS * half + COLS)
+        // of each accumulator, read 32 at a time.
+        const int ewarp = warp - FIRST_EPI_WARP;
+        const int quad = warp & 3;
+        const int half = ewarp >> 2;
+        uint8_t* stage_out = smem + SmemLayout::out_off + ewarp * OUT_WARP_BYTES;
+        uint32_t seg_count = 0;
+        bool store_pending = false;
+        uint32_t acc[COLS];
+
+        for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+            const int tt = tile % p.tiles_t, tw = tile / p.tiles_t;
+            const int n_base = tw * (2 * BW) + (int)rank * BW + quad * 32;
+            const int n = n_base + lane;                  // this thread's output channel
+            const int m_base = tt * BT + half * COLS;     // the warp's first token
+            // This thread's scales: per-channel s_w[n], or group g's s_w[n, g]
+            // (the next group's prefetched one group ahead).
+            float sw_next = 0.0f;
+            if (p.s_w != nullptr && n < p.N) sw_next = __ldg(p.s_w + (int64_t)n * p.G);
+            if constexpr (MODE == GemmMode::kPgF16) {
+#pragma unroll
+                for (int j = 0; j < COLS; ++j) acc[j] = 0u;  // f = +0 before the first group
+            }
+            for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
+                const uint32_t b = seg_count % NUM_ACC;
+                const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
+                const bool last_seg = (seg == p.num_seg - 1);
+                float sw = sw_next;
+                if constexpr (MODE == GemmMode::kPgF16) {
+                    if (seg + 1 < p.num_seg && n < p.N)
+                        sw_next = __ldg(p.s_w + (int64_t)n * p.G + seg + 1);
+                }
+                {
+                    const bool ok = mbar_wait_bounded(smem_u32(&bars->acc_full[b]), acc_phase,
+                                                      p.timeout_ns, abort_flag, p.status,
+                                                      kSiteEpiAccFull);
+                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                }
+                tc_fence_after();
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                       b * ACC_COLS + half * COLS;
+                {
+                    uint32_t va[LD], vb[LD];
+                    tmem_ld_32x32b_x16_ptr(t_row, va);
+                    tmem_wait_ld_16(va);
+#pragma unroll
+                    for (int ch = 0; ch < COLS / LD; ++ch) {
+                        uint32_t* v = (ch & 1) ? vb : va;
+                        uint32_t* vn = (ch & 1) ? va : vb;
+                        if (ch + 1 < COLS / LD) tmem_ld_32x32b_x16_ptr(t_row + (ch + 1) * LD, vn);
+                        const int c0 = ch * LD;
+                        if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
+                            // Exact fp32 integers -> int32: the fast conversion holds
+                            // below 2^22; a warp holding a larger one converts all.
+                            bool big = false;
+#pragma unroll
+                            for (int j = 0; j < LD; ++j)
+                                big |= fabsf(__uint_as_float(v[j])) >= 4194304.0f;
+                            if (__any_sync(0xffffffffu, big)) {
+#pragma unroll
+                                for (int j = 0; j < LD; ++j) {
+                                    const int part = __float2int_rn(__uint_as_float(v[j]));
+                                    acc[c0 + j] = (seg == 0) ? (uint32_t)part
+                                                             : (uint32_t)((int)acc[c0 + j] + part);
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < LD; j += 2) {
+                                    float t0, t1;
+                                    fadd2_rn(t0, t1, __uint_as_float(v[j]),
+                                             __uint_as_float(v[j + 1]), 12582912.0f, 12582912.0f);
+                                    const int p0 = __float_as_int(t0) - 0x4B400000;
+                                    const int p1 = __float_as_int(t1) - 0x4B400000;
+                                    acc[c0 + j] = (seg == 0) ? (uint32_t)p0
+                                                             : (uint32_t)((int)acc[c0 + j] + p0);
+                                    acc[c0 + j + 1] = (seg == 0)
+                                                          ? (uint32_t)p1
+                                                          : (uint32_t)((int)acc[c0 + j + 1] + p1);
+                                }
+                            }
+                        } else if constexpr (MODE == GemmMode::kPgF16) {
+                            // f = f + fl(P_g * s_g), both roundings kept (ascending
+                            // g; f starts at +0). Scalar products: a packed multiply
+                            // whose only use is a packed add is contracted into a
+                            // fused multiply-add.
+#pragma unroll
+                            for (int j = 0; j < LD; j += 2) {
+                                const float q0 = __fmul_rn(__uint_as_float(v[j]), sw);
+                                const float q1 = __fmul_rn(__uint_as_float(v[j + 1]), sw);
+                                float r0, r1;
+                                fadd2_rn(r0, r1, __uint_as_float(acc[c0 + j]),
+                                         __uint_as_float(acc[c0 + j + 1]), q0, q1);
+                                acc[c0 + j] = __float_as_uint(r0);
+                                acc[c0 + j + 1] = __float_as_uint(r1);
+                            }
+                        } else {  // kRawPgS32: this group's partials, straight out
+                            if (n < p.N) {
+#pragma unroll
+                                for (int j = 0; j < LD; ++j) {
+                                    const int m = m_base + c0 + j;
+                                    if (m < p.M)
+                                        static_cast<int32_t*>(p.out)[((int64_t)m * p.N + n) * p.G +
+                                                                     seg] =
+                                            __float2int_rn(__uint_as_float(v[j]));
+                                }
+                            }
+                        }
+                        if (ch + 1 < COLS / LD) tmem_wait_ld_16(vn);
+                    }
+                }
+                // This warp's reads of the buffer are complete: release it on
+                // the even CTA's barrier (a relaxed arrival: it orders no
+                // memory writes).
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster_relaxed(map_to_rank(smem_u32(&bars->acc_empty[b]), 0));
+
+                if (last_seg) {
+                    if constexpr (MODE == GemmMode::kRawS32) {
+                        if (n < p.N) {
+#pragma unroll
+                            for (int j = 0; j < COLS; ++j) {
+                                const int m = m_base + j;
+                                if (m < p.M)
+                                    static_cast<int32_t*>(p.out)[(int64_t)m * p.N + n] =
+                                        (int)acc[j];
+                            }
+                        }
+                    } else if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kPgF16) {
+                        bool big = false;
+                        if constexpr (MODE == GemmMode::kPcF16) {
+#pragma unroll
+                            for (int j = 0; j < COLS; ++j) {
+                                const int a = (int)acc[j];
+                                big |= (a >= 4194304 || a <= -4194304);
+                            }
+                        }
+                        const bool slow_cvt = __any_sync(0xffffffffu, big);
+                        // Rounds of 32 tokens: dequant, stage [token][channel],
+                        // TMA store (or direct stores).
+#pragma unroll
+                        for (int ch = 0; ch < CHUNKS; ++ch) {
+                            const int mt = m_base + ch * 32 + lane;  // lane's token of the round
+                            const float sa_lane = (mt < p.M) ? __ldg(p.s_a + mt) : 0.0f;
+                            uint32_t yv[16];  // token pairs (2j, 2j + 1), 16 bits each
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                const int c = ch * 32 + j;
+                                const float sa0 = __shfl_sync(0xffffffffu, sa_lane, j);
+                                const float sa1 = __shfl_sync(0xffffffffu, sa_lane, j + 1);
+                                float y0, y1;
+                                if constexpr (MODE == GemmMode::kPcF16) {
+                                    const float f0 = slow_cvt ? __int2float_rn((int)acc[c])
+                                                              : small_int_to_float((int)acc[c]);
+                                    const float f1 = slow_cvt ? __int2float_rn((int)acc[c + 1])
+                                                              : small_int_to_float((int)acc[c + 1]);
+                                    float t0, t1;
+                                    fmul2_rn(t0, t1, f0, f1, sa0, sa1);
+                                    fmul2_rn(y0, y1, t0, t1, sw, sw);
+                                } else {
+                                    fmul2_rn(y0, y1, __uint_as_float(acc[c]),
+                                             __uint_as_float(acc[c + 1]), sa0, sa1);
+                                }
+                                yv[j / 2] = pack2_rn(y0, y1, p.out_bf16 != 0);
+                            }
+                            if (p.tma_store) {
+                                // The staging buffer is free once the previous
+                                // store from it has been read out.
+                                if (store_pending && lane == 0) bulk_wait_group_read0();
+                                __syncwarp();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    *reinterpret_cast<uint16_t*>(stage_out + j * 64 + lane * 2) =
+                                        (uint16_t)(yv[j / 2] >> (16 * (j & 1)));
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&tmap_y, smem_u32(stage_out), n_base,
+                                                 m_base + ch * 32);
+                                    bulk_commit_group();
+                                }
+                                store_pending = true;
+                            } else if (n < p.N) {
+                                uint16_t* out = static_cast<uint16_t*>(p.out);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    const int m = m_base + ch * 32 + j;
+                                    if (m < p.M)
+                                        out[(int64_t)m * p.N + n] =
+                                            (uint16_t)(yv[j / 2] >> (16 * (j & 1)));
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    epi_done:
+        // Every output store has completed before the CTA exits.
+        if (store_pending && lane == 0) bulk_wait_group0();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // Neither CTA leaves (or frees tensor memory) while the other may still
+    // arrive on its barriers or the MMAs may still read or write its tensor
+    // memory.
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace gemmw
+
+namespace {
+
+template <GemmMode MODE, int BITS>
+cudaError_t launch_tw_mode(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty,
+                           const gemmw::Params& p, int num_sms, cudaStream_t stream) {
+    using namespace gemmw;
+    auto kern = gemm_tw_kernel<MODE, BITS>;
+    // Once per device: the register count the role split assumes, the
+    // shared-memory opt-in, and how many pairs fit on the GPU at once.
+    static PerDevice<int> max_clusters_of;
+    int max_clusters = 0;
+    const cudaError_t e = max_clusters_of.get([&](int& n) {
+        cudaFuncAttributes fa;
+        cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+        if (r != cudaSuccess) return r;
+        if (fa.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SmemLayout::alloc_bytes);
+        if (r != cudaSuccess) return r;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = SmemLayout::alloc_bytes;
+        cfg.numAttrs = 0;  // the kernel's compile-time cluster shape (2, 1, 1) applies
+        r = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (r != cudaSuccess) return r;
+        return n > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+    }, &max_clusters);
+    if (e != cudaSuccess) return e;
+    const int tiles = p.tiles_t * p.tiles_w;
+    const int clusters = tiles < max_clusters ? tiles : max_clusters;
+    return launch_pdl(kern, 2 * clusters, NUM_THREADS, SmemLayout::alloc_bytes, stream, tx, tw, ty,
+                      p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+    using namespace gemmw;
+    if (a.M <= 0 || a.N <= 0 || a.K <= 0 || a.K % 16 != 0) return cudaErrorInvalidValue;
+    if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2)
+        return cudaErrorInvalidValue;
+    if (!a.b_raw || (a.b_bits != 8 && a.b_bits != 4)) return cudaErrorInvalidValue;
+    if (a.b_bits == 4 && a.K % 32 != 0) return cudaErrorInvalidValue;
+    const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
+    CUtensorMap tx, tw, ty;
+    const uint64_t row_bytes = a.b_bits == 8 ? (uint64_t)a.K : (uint64_t)a.K / 2;
+    const uint32_t raw_row = a.b_bits == 8 ? SK : SK / 2;  // bytes of one row per stage
+    if (encode_tmap_f16_kmajor(&tx, a.a_img, a.M, a.K, BT / 2, BK) != CUDA_SUCCESS ||
+        encode_tmap_u8_2d_swizzled(&tw, a.b_raw, a.N, row_bytes, BW,
+                                   raw_row, raw_row == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                            : raw_row == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                            : CU_TENSOR_MAP_SWIZZLE_32B) !=
+            CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // 16-bit output through TMA stores of 32 channels x 32 tokens when the
+    // row pitch allows it (a multiple of 16 bytes); direct stores otherwise.
+    const bool f16_out = (a.mode == GemmMode::kPcF16 || a.mode == GemmMode::kPgF16);
+    const bool tma_store = f16_out && (a.N % 8 == 0) &&
+                           (reinterpret_cast<uintptr_t>(a.out) % 16 == 0);
+    memset(&ty, 0, sizeof(ty));
+    if (tma_store && encode_tmap_f16_2d(&ty, a.out, a.M, a.N, 32, 32,
+                                        CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    Params p{};
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.bits = a.b_bits;
+    p.num_kb = (p.K + BK - 1) / BK;
+    if (per_group) {
+        if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
+            return cudaErrorInvalidValue;
+        if (a.group_size / BK > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
+        p.seg_kb = a.group_size / BK;
+        p.G = p.K / a.group_size;
+    } else {
+        const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        p.seg_kb = (p.num_kb + nseg - 1) / nseg;
+        p.G = 1;
+    }
+    p.num_seg = (p.num_kb + p.seg_kb - 1) / p.seg_kb;
+    p.tiles_t = (p.M + BT - 1) / BT;
+    p.tiles_w = (p.N + 2 * BW - 1) / (2 * BW);
+    p.s_a = a.s_a;
+    p.s_w = a.s_w;
+    p.out = a.out;
+    p.tma_store = tma_store ? 1 : 0;
+    p.out_bf16 = a.out_bf16;
+    p.timeout_ns = a.timeout_ns;
+    p.status = a.status;
+    // Launched for INT8 per-group layers (and their raw int32 test mode): the
+    // layer call routes every other layer to the fp16-image pair kernel, which
+    // measured faster for them.
+    if (a.b_bits != 8) return cudaErrorInvalidValue;
+    if (a.mode == GemmMode::kPgF16)
+        return launch_tw_mode<GemmMode::kPgF16, 8>(tx, tw, ty, p, num_sms, stream);
+    if (a.mode == GemmMode::kRawPgS32)
+        return launch_tw_mode<GemmMode::kRawPgS32, 8>(tx, tw, ty, p, num_sms, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace cider

@@ -109,6 +109,10 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm_tc(const GemmArgs& args, int num_sms, cudaStream_t stream);
+// Same function on SM pairs with the raw weight codes (b_raw) widened on chip
+// into tensor memory, where the tensor core reads them as its A operand; no
+// weight image. For M > 128.
+cudaError_t launch_gemm_tw(const GemmArgs& args, int num_sms, cudaStream_t stream);
 // Same function on SM pairs (cta_group::2, 256 x 256 tiles); for M > 128.
 cudaError_t launch_gemm_tc_pair(const GemmArgs& args, int num_sms, cudaStream_t stream);
 // Picks the engine for the problem: SM pairs for M > 128, single SMs otherwise
@@ -149,6 +153,12 @@ CUresult encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t rows, u
 // Host-side encoder for a 2D byte tile map (unswizzled).
 CUresult encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                            uint32_t box_rows, uint32_t box_cols);
+
+// Host-side encoder for a 2D byte tile map with the given swizzle (the box's
+// row of bytes must equal the swizzle span for the 32/64/128-byte modes).
+CUresult encode_tmap_u8_2d_swizzled(CUtensorMap* map, const void* base, uint64_t rows,
+                                    uint64_t cols, uint32_t box_rows, uint32_t box_cols,
+                                    CUtensorMapSwizzle swizzle);
 
 // Host-side encoder for a 2D fp16 K-major tile map with 128-byte swizzle.
 CUresult encode_tmap_f16_kmajor(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
