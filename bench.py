@@ -44,9 +44,8 @@ METRIC = "W8A8 GEMM TOPS & % INT8 peak at M=4096; M=1 INT8 GEMV HBM GB/s"
 WORKLOAD = "w8a8_per_channel_linear_M4096_N10240_K2560"
 FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + write) of one launch of the pair GEMM at this workload,
-# from the ncu capture summarised in profiles/; reset to None whenever the
-# kernel changes until it is captured again. None: the epilogue gained the
-# bf16-output option after the last capture, which measured 128.6 MB.
+# from its ncu capture; reset to None whenever the kernel changes until it
+# is captured again.
 GEMM_DRAM_BYTES_PER_LAUNCH = None
 # dram__bytes_read.sum + dram__bytes_write.sum of one cold gemv_kernel<8, false> launch at
 # N10240 K2560 (ncu; the algorithmic bytes are 26.28 MB).
@@ -69,11 +68,16 @@ def parse_args():
     ap.add_argument("--small-step", action="store_true",
                     help="run only the few-token per-channel call (M = 128, the single-SM "
                          "engine): a small command for profilers")
+    ap.add_argument("--layer", type=int, nargs=5, metavar=("M", "N", "K", "BITS", "GS"),
+                    help="run only the public layer call of this shape (seeded inputs made "
+                         "on the GPU): a small command for profilers")
     ap.add_argument("--configs", action="store_true",
                     help="time every workload of the config list (M sweeps, per-group, W4A8, "
                          "decoder layer) through the public calls; one JSON line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave the per-config sweep out of the headline line")
     return ap.parse_args()
 
 
@@ -92,6 +96,19 @@ def peaks():
         return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
     except Exception:
         return 1800.0, 6400.0, "fallback"
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (for the CPU-baseline record)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
 
 
 class ClockSampler:
@@ -263,7 +280,7 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "mode": "per-channel",
                    "sample_rows": rows},
         "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu": cpu_model()},
         "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -333,26 +350,123 @@ def gemv_leg(args, x, wq, s_w, y_row0, stream):
     if y_row0 is not None:
         for t in ys:
             assert torch.equal(t.view(torch.int16), y_row0.view(torch.int16)), "graph GEMV"
+    # The same two measurements of a plain streaming read of the same bytes
+    # (a measurement kernel launched as the GEMV is): the ceiling a GEMV of
+    # this size can reach with this timing.
+    sink = torch.empty(4096, dtype=torch.int32, device=dev)
+    for i in range(n_copies):
+        cider.read_bytes(wq_copies[i], sink)
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e5 * args.steps))
+    for i, (a, b) in enumerate(rev):
+        a.record(stream)
+        cider.read_bytes(wq_copies[i % n_copies], sink)
+        b.record(stream)
+    torch.cuda.synchronize()
+    read_standalone = statistics.mean([a.elapsed_time(b) for a, b in rev]) / 1e3
+    rgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        cider.read_bytes(wq_copies[0], sink)
+        side.synchronize()
+        with torch.cuda.graph(rgraph, stream=side):
+            for i in range(n_copies):
+                cider.read_bytes(wq_copies[i], sink)
+    torch.cuda.synchronize()
+    rgraph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        rgraph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    read_sequence = a.elapsed_time(b) / 1e3 / (reps * n_copies)
     del wq_copies
-    return standalone, sequence, n_copies
+    return standalone, sequence, n_copies, read_standalone, read_sequence
 
 
-def run_configs(args):
+def gemv_sequence(args, N_, K_, dev, stream, seed=1):
+    """CUDA-graph decode sequence of per-channel INT8 GEMVs of one shape over
+    weight copies that together exceed 3x L2: mean time per launch (s)."""
+    import torch
+    import w4a8_quantized_gemm_int8_b300 as cider
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_copies = (3 * l2) // (N_ * K_) + 2
+    x1 = (torch.randn(K_, generator=gen, device=dev)).half()
+    ws = [torch.randint(-127, 128, (N_, K_), generator=gen, device=dev, dtype=torch.int8)
+          for _ in range(n_copies)]
+    s_w = torch.rand(N_, generator=gen, device=dev) * 0.01 + 1e-3
+    ys = [torch.empty((N_,), dtype=torch.float16, device=dev) for _ in range(n_copies)]
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        cider.int8_gemv(x1, ws[0], s_w, 8, 0, out=ys[0])
+        side.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(n_copies):
+                cider.int8_gemv(x1, ws[i], s_w, 8, 0, out=ys[i])
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(3, args.steps // n_copies)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    del ws
+    return a.elapsed_time(b) / 1e3 / (reps * n_copies), n_copies
+
+
+def int8_mma_rate(dev, stream) -> float:
+    """INT8 tensor rate (TOPS) of a register-only loop of the legacy
+    mma.sync.m16n8k32 s8 instruction on every SM (a measurement kernel of the
+    library): the "% INT8 peak" denominator (sm_103a has no integer kind of
+    tcgen05.mma). Best of three timed launches."""
+    import torch
+    import w4a8_quantized_gemm_int8_b300 as cider
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = 8 * sms, 2048
+    ops = blocks * 4 * 8 * iters * 8192
+    cider.int8_mma_loop(blocks, 64)
+    best = float("inf")
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        cider.int8_mma_loop(blocks, iters)
+        b.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) / 1e3)
+    return ops / best / 1e12
+
+
+def config_sweep(args, check: bool):
     """Every workload shape of the operator configs, timed through the public
     calls (quant + GEMM + dequant per call; the GEMV for M = 1). Inputs are
     drawn on the GPU from a seeded generator (timing does not depend on the
     values), in sets rotated so that together they exceed 3x L2. Times are
-    CUDA-event means over `steps` calls after `warmup`."""
+    CUDA-event means over `steps` calls after `warmup`.
+
+    Returns (results, samples): with `check`, samples holds, per case, a few
+    token rows of x and 64 sampled output channels (their weight rows and
+    scales, and the GPU's outputs there), for the CPU-baseline leg to
+    recompute with the oracle (check_samples)."""
     import torch
     import w4a8_quantized_gemm_int8_b300 as cider
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda:0")
-    cider.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
-    bf16_peak, hbm_peak, peak_src = peaks()
+    bf16_peak, hbm_peak, _ = peaks()
+    samples = []
 
     def inputs(M, N, K, bits, gs, n_out):
         x = torch.randn(M, K, generator=gen, device=dev)
@@ -365,7 +479,7 @@ def run_configs(args):
             wq, s = cider.pack_weight_int4(w, gs)
         return x, wq, s
 
-    def time_case(M, N, K, bits, gs, n_out=4, a16=False):
+    def time_case(key, M, N, K, bits, gs, n_out=4, a16=False):
         wbytes = N * K if bits == 8 else N * K // 2
         per_set = 2 * M * K + wbytes + 2 * M * N
         n_sets = max(1, min(8, -(-3 * l2 // per_set) + 1))
@@ -373,8 +487,8 @@ def run_configs(args):
         for _ in range(n_sets):
             x, wq, s = inputs(M, N, K, bits, gs, n_out)
             sets.append((x, wq, s, torch.empty((M, N), dtype=torch.float16, device=dev)))
-        ws = torch.empty(max(1, cider.workspace_bytes(M, N, K, group_size=gs, bits=bits)), dtype=torch.uint8,
-                         device=dev)
+        ws = torch.empty(max(1, cider.workspace_bytes(M, N, K, group_size=gs, bits=bits)),
+                         dtype=torch.uint8, device=dev)
 
         def call(i):
             x, wq, s, y = sets[i % n_sets]
@@ -409,24 +523,33 @@ def run_configs(args):
             res["frac"] = round(res["GB/s"] / hbm_peak, 3)
         else:  # tensor-bound: the whole call's flops over the measured dense f16 rate
             res["frac"] = round(res["TOPS"] / bf16_peak, 3)
+        if check:
+            # the last call's set: rows first, middle, last; 64 seeded channels
+            x, wq, s, y = sets[(max(args.warmup, n_sets) + args.steps - 1) % n_sets]
+            rows = sorted({0, M // 2, M - 1})
+            cols = torch.randperm(N, generator=gen, device=dev)[:min(64, N)].sort().values
+            samples.append({"key": key, "case": res, "a16": a16, "bits": bits, "gs": gs,
+                            "x": x[rows].cpu(), "w": wq[cols].cpu(), "s": s[cols].cpu(),
+                            "y": y[rows][:, cols].cpu()})
         del sets, ws
         return res
 
-    out = {"per_channel_N10240_K2560": [time_case(m, 10240, 2560, 8, 0)
-                                        for m in (1, 128, 1024, 4096, 8192)]}
+    out = {"per_channel_N10240_K2560": [time_case("per_channel_N10240_K2560", m, 10240, 2560,
+                                                  8, 0) for m in (1, 128, 1024, 4096, 8192)]}
     for gs in (64, 128):
-        out[f"per_group{gs}_N2560_K10240"] = [time_case(m, 2560, 10240, 8, gs)
-                                              for m in (1, 128, 1024, 4096, 8192)]
+        key = f"per_group{gs}_N2560_K10240"
+        out[key] = [time_case(key, m, 2560, 10240, 8, gs) for m in (1, 128, 1024, 4096, 8192)]
     for (n, k) in ((10240, 2560), (2560, 10240)):
-        out[f"w4a8_gs128_N{n}_K{k}"] = [time_case(m, n, k, 4, 128) for m in (1, 1024, 8192)]
+        key = f"w4a8_gs128_N{n}_K{k}"
+        out[key] = [time_case(key, m, n, k, 4, 128) for m in (1, 1024, 8192)]
     # The A16 decode product (activations unquantized, weights dequantized).
-    out["a16_decode_M1"] = [dict(time_case(1, n, k, b, g, a16=True), mode="a16")
+    out["a16_decode_M1"] = [dict(time_case("a16_decode_M1", 1, n, k, b, g, a16=True), mode="a16")
                             for (n, k, b, g) in ((10240, 2560, 8, 0), (2560, 10240, 8, 64),
                                                  (10240, 2560, 4, 128))]
     import synth
     layer = []
     for name, K_, N_ in synth.DECODER_LAYER:
-        r = time_case(2048, N_, K_, 8, 0, n_out=max(1, round(K_ * 0.01)))
+        r = time_case("decoder_layer", 2048, N_, K_, 8, 0, n_out=max(1, round(K_ * 0.01)))
         r["linear"] = name
         layer.append(r)
     tot_us = sum(r["us"] for r in layer)
@@ -436,15 +559,64 @@ def run_configs(args):
     fused = []
     for name, K_, N_ in (("qkv", 4096, 6144), ("o", 4096, 4096), ("gate_up", 4096, 24576),
                          ("down", 12288, 4096)):
-        r = time_case(2048, N_, K_, 8, 0, n_out=max(1, round(K_ * 0.01)))
+        r = time_case("decoder_layer_fused", 2048, N_, K_, 8, 0, n_out=max(1, round(K_ * 0.01)))
         r["linear"] = name
         fused.append(r)
     fused_us = sum(r["us"] for r in fused)
     out["decoder_layer_M2048"] = {"linears": layer, "total_us": round(tot_us, 2),
                                   "TOPS": round(tot_ops / (tot_us * 1e-6) / 1e12, 1),
+                                  "frac": round(tot_ops / (tot_us * 1e-6) / 1e12 / bf16_peak, 3),
                                   "fused": {"linears": fused, "total_us": round(fused_us, 2),
                                             "TOPS": round(tot_ops / (fused_us * 1e-6) / 1e12, 1)}}
-    print(json.dumps({"configs": out, "steps": args.steps, "warmup": args.warmup,
+    return out, samples
+
+
+def check_samples(samples) -> dict:
+    """CPU-baseline leg: the oracle recomputes each sampled block of outputs
+    from the same inputs and codes. Quantized layers must be bit-identical;
+    the A16 product (a floating-point sum) must lie within its derived error
+    bound. Marks each case with "oracle": "match" / "MISMATCH"; returns a
+    summary."""
+    import numpy as np
+    import oracle
+    n_match = n = 0
+    for sm in samples:
+        x = sm["x"].numpy()
+        w, s = sm["w"].numpy(), sm["s"].numpy()
+        y = sm["y"].numpy()
+        if sm["a16"]:
+            K = x.shape[1]
+            G = 1 if sm["gs"] == 0 else K // sm["gs"]
+            ref = oracle.a16_gemv(x[0], w, s, sm["bits"], sm["gs"])
+            codes = (w.astype(np.float64) if sm["bits"] == 8
+                     else oracle.unpack_int4(w, K).astype(np.float64))
+            sc = np.repeat(np.abs(s.astype(np.float64).reshape(len(w), G)), K // G, axis=1)
+            E = (K + 2) * 2.0 ** -24 * ((np.abs(codes) * sc) @ np.abs(x[0].astype(np.float64)))
+            mag = np.maximum(np.abs(ref) + E, 2.0 ** -14)
+            ulp = 2.0 ** (np.floor(np.log2(mag)) - 10)
+            ok = bool(np.all(np.abs(y[0].astype(np.float64) - ref) <= 0.5 * ulp + E))
+        else:
+            fn = oracle.w8a8_linear if sm["bits"] == 8 else oracle.w4a8_linear
+            ref = fn(x, w, s, sm["gs"])
+            ok = bool(np.array_equal(ref.view(np.uint16), y.view(np.uint16)))
+        sm["case"]["oracle"] = "match" if ok else "MISMATCH"
+        n += 1
+        n_match += ok
+    return {"cases": n, "match": n_match,
+            "sample": "per case: token rows first, middle, last x 64 seeded output channels"}
+
+
+def run_configs(args):
+    """The config sweep alone: one JSON line."""
+    import torch
+    import w4a8_quantized_gemm_int8_b300 as cider
+    torch.cuda.set_device(0)
+    cider.load_library()
+    bf16_peak, hbm_peak, peak_src = peaks()
+    out, samples = config_sweep(args, check=not args.no_cpu_baseline)
+    summary = check_samples(samples) if samples else None
+    print(json.dumps({"configs": out, "oracle_check": summary, "steps": args.steps,
+                      "warmup": args.warmup,
                       "timing": "CUDA events per call, inputs rotating over sets > 3x L2",
                       "frac": f"of {peak_src} peaks: {bf16_peak} TFLOP/s dense bf16/fp16 "
                               f"(M > 1), {hbm_peak} GB/s HBM copy (M = 1)"}))
@@ -476,7 +648,7 @@ def run_cider(args):
     wq, s_w = cider.quantize_weight_int8(li.w.to(dev), 0)  # offline prep, untimed
     stream = torch.cuda.current_stream()
     if args.gemv_only:
-        gemv_s, gemv_seq_s, n_copies = gemv_leg(args, x, wq, s_w, None, stream)
+        gemv_s, gemv_seq_s, n_copies, _, _ = gemv_leg(args, x, wq, s_w, None, stream)
         if rank == 0:
             nb = N * K + 4 * N + 2 * K + 2 * N
             print(json.dumps({"gemv_us": gemv_s * 1e6, "sequence_us": gemv_seq_s * 1e6,
@@ -609,10 +781,14 @@ def run_cider(args):
     achieved = flops / gemm_s / 1e12
 
     # ---- M = 1 decode GEMV on the same weights (HBM stream) ----------------
-    gemv_s, gemv_seq_s, n_copies = gemv_leg(args, x, wq, s_w, y[0], stream)
+    gemv_s, gemv_seq_s, n_copies, read_s, read_seq_s = gemv_leg(args, x, wq, s_w, y[0], stream)
     gemv_bytes = N * K + 4 * N + 2 * K + 2 * N
     gemv_gbs = gemv_bytes / gemv_s / 1e9
     gemv_seq_gbs = gemv_bytes / gemv_seq_s / 1e9
+    # The fused gate|up projection of an 8B-class decoder (K 4096 -> 12288 + 12288).
+    gu_N, gu_K = 24576, 4096
+    gu_s, gu_copies = gemv_sequence(args, gu_N, gu_K, dev, stream)
+    gu_bytes = gu_N * gu_K + 4 * gu_N + 2 * gu_K + 2 * gu_N
 
     # ---- end to end through the public call, host buffers ------------------
     # Steps run as a serving loop runs them: the copy-in of step i + 1 and the
@@ -683,24 +859,12 @@ def run_cider(args):
     sus_clock_info = sus_clocks.stop()
     sus_s = max_over_ranks(s0.elapsed_time(s1) / 1e3 / n_sus)
     value = world * flops / mean_step_s / 1e12
-    # ---- INT8 library rate on this GPU (context for "% INT8 peak") ----------
-    int8_lib = None
-    try:
-        a8 = torch.randint(-127, 128, (8192, 8192), dtype=torch.int8, device=dev)
-        b8 = torch.randint(-127, 128, (8192, 8192), dtype=torch.int8, device=dev).t()
-        for _ in range(3):
-            torch._int_mm(a8, b8)
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        s0.record(stream)
-        for _ in range(10):
-            torch._int_mm(a8, b8)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        int8_lib = 2.0 * 8192 ** 3 / (s0.elapsed_time(s1) / 10 / 1e3) / 1e12
-        del a8, b8
-    except Exception as exc:  # the library may not offer INT8 GEMM here
-        int8_lib = f"unavailable: {type(exc).__name__}"
+    # ---- the INT8 tensor rate of this GPU (the "% INT8 peak" denominator) ---
+    int8_rate = int8_mma_rate(dev, stream)
+
+    # ---- every workload of the config list (compact) -----------------------
+    sweep = (None if (args.no_configs or rank != 0)
+             else config_sweep(args, check=not args.no_cpu_baseline))
 
     if rank != 0:
         return
@@ -721,7 +885,11 @@ def run_cider(args):
         cpu_tops = 2.0 * passes * rows * N * K / cpu_dt / 1e12
         reps = f", {passes} passes" if passes > 1 else ""
         cpu = {"value": cpu_tops, "unit": "TOPS", "cores": oracle.get_threads(), "kind": "oracle",
-               "sample": f"{rows} of {M} token rows, full N={N}, K={K}{reps} ({cpu_dt:.1f} s)"}
+               "sample": f"{rows} of {M} token rows, full N={N}, K={K}{reps} ({cpu_dt:.1f} s)",
+               "cpu": cpu_model()}
+        # The same leg recomputes the sampled outputs of every config case.
+        if sweep is not None:
+            cpu["config_check"] = check_samples(sweep[1])
 
     line = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
@@ -743,16 +911,15 @@ def run_cider(args):
                      "traffic": GEMM_DRAM_BYTES_PER_LAUNCH,
                      "traffic_source": (
                          "ncu dram__bytes_read.sum + dram__bytes_write.sum, one cold-cache "
-                         "launch (profiles/gemm_tc2_kernel_pc_M4096_N10240_K2560.md)"
+                         "launch of `python bench.py --step-only`"
                          if GEMM_DRAM_BYTES_PER_LAUNCH is not None else
-                         "none for the current kernel: it changed (bf16-output option) after "
-                         "the last capture, which measured 128.6 MB per launch "
-                         "(profiles/gemm_tc2_kernel_pc_M4096_N10240_K2560.md)"),
+                         "none: the kernel changed after its last ncu capture"),
                      "kernel": "gemm_tc2_kernel<kPcF16> (SM pairs, cta_group::2)",
                      "peak_source": f"{peak_src} dense bf16 burst; fp16 nominal rate equal"},
-        "int8_peak": {"torch_int_mm_8192_tops": int8_lib,
-                      "value_pct": (100.0 * value / int8_lib
-                                    if isinstance(int8_lib, float) else None)},
+        "int8_peak": {"value": int8_rate, "unit": "TOPS",
+                      "source": "register-only loop of mma.sync.m16n8k32 s8 on every SM, run "
+                                "by this bench (sm_103a has no integer tcgen05.mma kind)",
+                      "value_pct": 100.0 * value / int8_rate},
         "gemv": {"value": gemv_gbs, "unit": "GB/s", "us": gemv_s * 1e6, "M": 1, "N": N, "K": K,
                  "bytes": gemv_bytes, "kernel": "gemv_kernel<8, false>",
                  "l2": f"cold: {n_copies} rotating weight copies ({n_copies * N * K >> 20} MiB > 3x L2)",
@@ -761,12 +928,23 @@ def run_cider(args):
                               "unit": "GB/s", "frac": gemv_gbs / hbm_peak,
                               "traffic": GEMV_DRAM_BYTES_PER_LAUNCH,
                               "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write."
-                                                "sum, one cold launch (profiles/gemv_kernel_pc_"
-                                                "M1_N10240_K2560.md)"},
+                                                "sum, one cold launch of `python bench.py "
+                                                "--gemv-only`"},
                  "sequence": {"value": gemv_seq_gbs, "unit": "GB/s", "us": gemv_seq_s * 1e6,
                               "timing": f"CUDA graph of {n_copies} back-to-back GEMVs (one per "
                                         "weight copy), total time / launches",
-                              "frac": gemv_seq_gbs / hbm_peak}},
+                              "frac": gemv_seq_gbs / hbm_peak},
+                 "read_ceiling": {
+                     "standalone_us": read_s * 1e6, "sequence_us": read_seq_s * 1e6,
+                     "standalone_GB/s": N * K / read_s / 1e9,
+                     "sequence_GB/s": N * K / read_seq_s / 1e9,
+                     "what": "a plain streaming read of the same weight copies, launched and "
+                             "timed like the GEMV (standalone and CUDA-graph sequence)"},
+                 "gate_up_decode": {
+                     "N": gu_N, "K": gu_K, "us": gu_s * 1e6, "GB/s": gu_bytes / gu_s / 1e9,
+                     "frac": gu_bytes / gu_s / 1e9 / hbm_peak,
+                     "timing": f"CUDA graph of {gu_copies} back-to-back GEMVs of the fused "
+                               "gate|up projection (K 4096 -> 2 x 12288), total / launches"}},
         "sustained": {"value": world * flops / sus_s / 1e12, "unit": "TOPS",
                       "seconds": sus_s * n_sus, "steps": n_sus, "ms_per_step": sus_s * 1e3,
                       "clocks": sus_clock_info},
@@ -775,6 +953,7 @@ def run_cider(args):
                 "timing": "steps pipelined on three streams (copy-in, layer, copy-out), "
                           "total time / steps"},
         "cpu_baseline": cpu,
+        "configs": sweep[0] if sweep is not None else None,
         "gpu_launches": 2 * args.steps,
         "clocks": clock_info,
         "impl": "cider",
@@ -784,11 +963,12 @@ def run_cider(args):
         dist.destroy_process_group()
 
 
-def run_small_step(args):
-    """The few-token per-channel public call alone (M = 128, N10240 K2560;
-    the single-SM engine): seeded codes and activations made on the GPU,
-    `warmup` calls, then `steps` calls timed with CUDA events. Prints the mean
-    call time. Small enough to run under a profiler."""
+def run_layer(args, m, n, k, bits, gs):
+    """One public layer call of shape (m, n, k, bits, gs) alone: seeded codes,
+    scales and activations made on the GPU, `warmup` calls, then `steps`
+    calls timed with CUDA events. Prints the mean call time. Small enough to
+    run under a profiler (--small-step: m = 128 per channel at N10240 K2560,
+    the single-SM engine)."""
     import torch
     import w4a8_quantized_gemm_int8_b300 as cider
     torch.cuda.set_device(0)
@@ -796,29 +976,32 @@ def run_small_step(args):
     dev = torch.device("cuda:0")
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
-    m = 128
-    x = torch.randn(m, K, generator=gen, device=dev).half()
-    wq = torch.randint(-127, 128, (N, K), generator=gen, device=dev, dtype=torch.int8)
-    s_w = torch.rand(N, generator=gen, device=dev) * 0.01 + 0.001
-    y = torch.empty(m, N, dtype=torch.float16, device=dev)
-    ws = torch.empty(max(1, cider.workspace_bytes(m, N, K, group_size=0, bits=8)), dtype=torch.uint8,
-                     device=dev)
+    G = 1 if gs == 0 else k // gs
+    x = torch.randn(m, k, generator=gen, device=dev).half()
+    w = torch.randint(-127, 128, (n, k if bits == 8 else k // 2), generator=gen, device=dev,
+                      dtype=torch.int8)
+    if bits == 4:
+        w = w.view(torch.uint8)
+    s_w = torch.rand((n, G) if gs else (n,), generator=gen, device=dev) * 0.01 + 0.001
+    y = torch.empty(m, n, dtype=torch.float16, device=dev)
+    ws = torch.empty(max(1, cider.workspace_bytes(m, n, k, group_size=gs, bits=bits)),
+                     dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
-        cider.w8a8_linear(x, wq, s_w, 0, out=y, ws=ws)
+        cider.linear(x, w, s_w, bits, gs, out=y, ws=ws)
     stream = torch.cuda.current_stream()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     torch.cuda.synchronize()
     for a, b in evs:
         a.record(stream)
-        cider.w8a8_linear(x, wq, s_w, 0, out=y, ws=ws)
+        cider.linear(x, w, s_w, bits, gs, out=y, ws=ws)
         b.record(stream)
     torch.cuda.synchronize()
     st, site = cider.device_status()
     assert st == cider.CIDER_OK, f"device status {st} at {site:#x}"
     us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
-    print(json.dumps({"small_step_us": us, "M": m, "N": N, "K": K,
-                      "TOPS": 2.0 * m * N * K / (us * 1e-6) / 1e12}))
+    print(json.dumps({"layer_us": us, "M": m, "N": n, "K": k, "bits": bits, "gs": gs,
+                      "TOPS": 2.0 * m * n * k / (us * 1e-6) / 1e12}))
 
 
 def main():
@@ -828,7 +1011,9 @@ def main():
     elif args.configs:
         run_configs(args)
     elif args.small_step:
-        run_small_step(args)
+        run_layer(args, 128, N, K, 8, 0)
+    elif args.layer:
+        run_layer(args, *args.layer)
     else:
         run_cider(args)
 

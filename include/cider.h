@@ -301,6 +301,28 @@ CIDER_API cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64
                                  size_t ws_bytes, void* stream);
 
 /*
+ * Measurement hook, not for users: the INT8 tensor rate available to a
+ * register-only loop of the legacy mma.sync.m16n8k32 s8 instruction (sm_103a
+ * has no integer kind of tcgen05.mma), the denominator the benchmark uses
+ * for "% INT8 peak". Launches `blocks` blocks of 4 warps; each warp executes
+ * 8 * iters MMAs of 16 x 8 x 32 products (8192 operations each), so the call
+ * performs blocks * 4 * 8 * iters * 8192 operations. sink: blocks * 128
+ * int32 (device), written with a fold of the accumulators.
+ */
+CIDER_API cider_status cider_test_int8_mma_loop(int32_t blocks, int64_t iters, int32_t* sink,
+                                               void* stream);
+
+/*
+ * Measurement hook, not for users: a plain streaming read of `bytes` bytes
+ * at src (device, 16-byte aligned, bytes a multiple of 16), launched as the
+ * GEMV is (two blocks per SM, programmatic dependent launch), the ceiling a
+ * decode GEMV of the same bytes is compared with. sink: 2 * (number of SMs)
+ * uint32 (device).
+ */
+CIDER_API cider_status cider_test_read_bytes(const void* src, int64_t bytes, uint32_t* sink,
+                                            void* stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the device status word of the
  * current device. Returns CIDER_ERR_TIMEOUT if a bounded device-side wait
  * (mbarrier poll) gave up since the last read, CIDER_OK otherwise. If

@@ -28,6 +28,7 @@ ABI_FUNCTIONS = (
     "cider_w8a8_gemm_pc_noalloc",
     "cider_act_image", "cider_weight_image", "cider_gemm_images",
     "cider_test_gemm_s32", "cider_device_status", "cider_test_wait_timeout",
+    "cider_test_int8_mma_loop", "cider_test_read_bytes",
 )
 
 CIDER_OK = 0
@@ -85,6 +86,8 @@ def load_library():
             "cider_test_gemm_s32": ([p, p, i64, i64, i64, i32, i32, p, p, sz, p], ctypes.c_int),
             "cider_device_status": ([p, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
             "cider_test_wait_timeout": ([i64, p], ctypes.c_int),
+            "cider_test_int8_mma_loop": ([i32, i64, p, p], ctypes.c_int),
+            "cider_test_read_bytes": ([p, i64, p, p], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -516,6 +519,24 @@ def wait_timeout_probe(timeout_ns: int) -> None:
 # ---------------------------------------------------------------------------
 # linears that read the same input (q/k/v, gate/up): one call
 # ---------------------------------------------------------------------------
+
+def int8_mma_loop(blocks: int, iters: int, device="cuda") -> torch.Tensor:
+    """Measurement hook: `blocks` x 4 warps, each 8 * iters legacy INT8 MMAs
+    (8192 operations each); returns the sink tensor (time it with events)."""
+    sink = torch.empty(blocks * 128, dtype=torch.int32, device=device)
+    _check("cider_test_int8_mma_loop",
+           load_library().cider_test_int8_mma_loop(blocks, iters, sink.data_ptr(), _stream()))
+    return sink
+
+
+def read_bytes(t: torch.Tensor, sink: torch.Tensor) -> None:
+    """Measurement hook: a plain streaming read of t's bytes, launched as the
+    GEMV is; sink: uint32/int32 of at least 2 x (number of SMs) elements."""
+    nbytes = t.numel() * t.element_size()
+    _dev(t, t.dtype, "t")
+    _check("cider_test_read_bytes",
+           load_library().cider_test_read_bytes(t.data_ptr(), nbytes, sink.data_ptr(), _stream()))
+
 
 def concat_linears(weights):
     """Offline, at weight-prep time: stacks the weight rows and scale rows of

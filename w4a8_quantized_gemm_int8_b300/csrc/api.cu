@@ -438,6 +438,22 @@ cider_status cider_test_gemm_s32(const int8_t* q, const void* w, int64_t M, int6
     return from_cuda(launch_gemm(a, sms, s));
 }
 
+cider_status cider_test_int8_mma_loop(int32_t blocks, int64_t iters, int32_t* sink,
+                                      void* stream) {
+    if (blocks <= 0 || iters <= 0 || !sink) return CIDER_ERR_INVALID_ARG;
+    return from_cuda(launch_int8_mma_loop(blocks, iters, sink, static_cast<cudaStream_t>(stream)));
+}
+
+cider_status cider_test_read_bytes(const void* src, int64_t bytes, uint32_t* sink, void* stream) {
+    if (!src || !sink || bytes <= 0) return CIDER_ERR_INVALID_ARG;
+    if (bytes % 16 != 0 || !aligned16(src)) return CIDER_ERR_UNSUPPORTED;
+    int sms = 0;
+    cider_status st = num_sms(&sms);
+    if (st != CIDER_OK) return st;
+    return from_cuda(launch_read_bytes(src, bytes, 2 * sms, sink,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 cider_status cider_device_status(void* stream, uint32_t* site) {
     unsigned long long v = 0;
     if (read_and_clear_device_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess)

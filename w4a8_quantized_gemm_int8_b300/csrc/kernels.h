@@ -140,6 +140,15 @@ struct GemvArgs {
 
 cudaError_t launch_gemv(const GemvArgs& args, int num_sms, cudaStream_t stream);
 
+// ---- measurement kernels (benchmark test hooks) ----------------------------
+// `blocks` blocks of 4 warps, each warp 8 x iters mma.sync.m16n8k32 s8
+// instructions (8192 operations each); sink: blocks * 128 int32.
+cudaError_t launch_int8_mma_loop(int blocks, int64_t iters, int32_t* sink, cudaStream_t stream);
+// Streaming read of `bytes` (a multiple of 16, src 16-byte aligned) by `grid`
+// blocks of 512 threads, launched like the GEMV; sink: grid words.
+cudaError_t launch_read_bytes(const void* src, int64_t bytes, int grid, uint32_t* sink,
+                              cudaStream_t stream);
+
 // ---- device status --------------------------------------------------------
 // Address of the current device's status word (looked up once per device).
 cudaError_t device_status_ptr(unsigned long long** ptr);
