@@ -46,7 +46,7 @@ FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + write) of one launch of the pair GEMM at this workload,
 # from its ncu capture; reset to None whenever the kernel changes until it
 # is captured again.
-GEMM_DRAM_BYTES_PER_LAUNCH = None
+GEMM_DRAM_BYTES_PER_LAUNCH = 127.87e6  # 74.06 MB read + 53.81 MB written
 # dram__bytes_read.sum + dram__bytes_write.sum of one cold gemv_kernel<8, false> launch at
 # N10240 K2560 (ncu; the algorithmic bytes are 26.28 MB).
 GEMV_DRAM_BYTES_PER_LAUNCH = 26.30e6
@@ -518,6 +518,8 @@ def config_sweep(args, check: bool):
         G = 1 if gs == 0 else K // gs
         res = {"M": M, "N": N, "K": K, "bits": bits, "gs": gs, "us": round(t * 1e6, 2),
                "TOPS": round(2.0 * M * N * K / t / 1e12, 1)}
+        if a16:
+            res["mode"] = "a16"
         if M == 1:  # HBM-bound: algorithmic bytes over the measured copy bandwidth
             res["GB/s"] = round((wbytes + 4 * N * G + 2 * K + 2 * N) / t / 1e9, 1)
             res["frac"] = round(res["GB/s"] / hbm_peak, 3)
@@ -543,7 +545,7 @@ def config_sweep(args, check: bool):
         key = f"w4a8_gs128_N{n}_K{k}"
         out[key] = [time_case(key, m, n, k, 4, 128) for m in (1, 1024, 8192)]
     # The A16 decode product (activations unquantized, weights dequantized).
-    out["a16_decode_M1"] = [dict(time_case("a16_decode_M1", 1, n, k, b, g, a16=True), mode="a16")
+    out["a16_decode_M1"] = [time_case("a16_decode_M1", 1, n, k, b, g, a16=True)
                             for (n, k, b, g) in ((10240, 2560, 8, 0), (2560, 10240, 8, 64),
                                                  (10240, 2560, 4, 128))]
     import synth
