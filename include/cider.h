@@ -137,10 +137,14 @@ CIDER_API cider_status cider_quantize_weight_clipped(const void* w, int32_t w_dt
  * order of the layer calls' own arguments). The workspace holds the fp16
  * image of the quantized activations (the codes as exact fp16 integers) and
  * the per-token scales; for M > 128, except for INT8 per-group layers (whose
- * weights are widened on chip), an fp16 image of the weight codes; and for
- * per-group layers that read one, a group-major copy of the weight scales.
- * Returns 0 when M == 1 (the GEMV path needs none) and on invalid sizes
- * (including a group_size that does not divide K).
+ * weights are widened on chip), an fp16 image of the weight codes; for
+ * per-group layers that read one, a group-major copy of the weight scales;
+ * and for per-channel layers of at most 128 tokens, whose k-blocks are
+ * shared out evenly among the SMs, int32 partial output tiles (up to
+ * 2 * 160 tiles of 128 columns and min(M rounded up to 32, 128) rows) that
+ * a fix-up launch sums exactly. Returns 0 when M == 1 (the GEMV path needs
+ * none) and on invalid sizes (including a group_size that does not divide
+ * K).
  */
 CIDER_API size_t cider_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t group_size,
                                        int32_t bits);

@@ -59,6 +59,13 @@ def test_workspace_bytes(lib):
     # W4A8 per group, SM pairs: weight image and a group-major copy of the scales
     w4 = cider.workspace_bytes(4096, 2560, 10240, group_size=128, bits=4)
     assert w4 == 2 * 4096 * 10240 + 4 * 4096 + 2 * 2560 * 10240 + 4 * 2560 * (10240 // 128)
+    # few-token per-channel layers: activation image, token scales and the
+    # stream-K partial tiles (2 per CTA, at most 160 CTAs, rows M rounded up to 32)
+    a256 = lambda v: (v + 255) // 256 * 256
+    assert cider.workspace_bytes(128, 10240, 2560) == \
+        a256(128 * 2560 * 2) + a256(128 * 4) + a256(160 * 2 * 128 * 128 * 4)
+    assert cider.workspace_bytes(40, 10240, 2560, bits=4) == \
+        a256(40 * 2560 * 2) + a256(40 * 4) + a256(160 * 2 * 64 * 128 * 4)
     # few tokens, per group: activation image and the group-major scale copy
     s = cider.workspace_bytes(64, 2560, 10240, group_size=64, bits=8)
     assert s == 2 * 64 * 10240 + 256 + 4 * 2560 * (10240 // 64)

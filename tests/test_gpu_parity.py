@@ -252,6 +252,30 @@ def test_w8a8_pc_layer(M, N, K):
     assert_f16_within_1ulp(host(y), ref, "pc")
 
 
+# Per-channel layers of at most 128 tokens share the k-blocks of all tiles
+# evenly among the SMs (stream-K): these shapes give CTAs whose runs cross a
+# tile boundary, tiles summed from two or three CTAs' int32 partials, and
+# runs from 1 to about 20 k-blocks, so segments of 15 and 16 k-blocks too.
+SK_SHAPES = [(32, 5120, 4096), (77, 2560, 8192), (128, 1280, 2560), (9, 10240, 1024)]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("M,N,K", SK_SHAPES)
+def test_pc_layer_stream_k(M, N, K, bits):
+    x, w = _layer_inputs(M, N, K, seed=M + K + bits)
+    if bits == 8:
+        wq, s = oracle.quantize_weight_int8(w, 0)
+        y = cider.w8a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                              cuda(torch.from_numpy(s)), 0)
+        ref = oracle.w8a8_linear(x, wq, s, 0)
+    else:
+        wq, s = oracle.pack_weight_int4(w, 0)
+        y = cider.w4a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                              cuda(torch.from_numpy(s)), 0)
+        ref = oracle.w4a8_linear(x, wq, s, 0)
+    assert_f16_within_1ulp(host(y), ref, f"stream-K w{bits}")
+
+
 @pytest.mark.parametrize("gs", [64, 128])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (3, 300, 1024), (130, 264, 2560),
                                    (5, 260, 1152)])

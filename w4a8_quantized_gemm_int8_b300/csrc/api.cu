@@ -43,6 +43,7 @@ struct Workspace {
     float* s_a;
     __half* b_img;  // fp16 weight image (SM-pair engine, image path only)
     float* s_wT;    // per-group scales, group-major (per-group, engines that read it)
+    int32_t* sk_part;  // stream-K partial tiles (single-SM engine, per channel)
 };
 
 // Weight operand of the SM-pair engine (M > 128): INT8 per-group layers take
@@ -62,12 +63,17 @@ bool uses_scales_t(int64_t M, int64_t gs, int bits) {
     return gs > 0 && (!gemm_uses_pair(M) || pair_uses_image(M, gs, bits));
 }
 
+// Per-channel layers on the single-SM engine split the k-blocks of all
+// tiles evenly over the SMs (stream-K) and need its scratch.
+bool uses_stream_k(int64_t M, int64_t gs) { return gs == 0 && !gemm_uses_pair(M); }
+
 // a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K] fp16 (image path) |
-// s_wT [K/gs, N] fp32 (uses_scales_t)
+// s_wT [K/gs, N] fp32 (uses_scales_t) | stream-K partial tiles (uses_stream_k)
 size_t workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t gs, int bits) {
     const size_t b = pair_uses_image(M, gs, bits) ? align256((size_t)N * K * 2) : 0;
     const size_t t = uses_scales_t(M, gs, bits) ? align256((size_t)(K / gs) * N * 4) : 0;
-    return align256((size_t)M * K * 2) + align256((size_t)M * 4) + b + t;
+    const size_t sk = uses_stream_k(M, gs) ? align256(stream_k_part_bytes(M)) : 0;
+    return align256((size_t)M * K * 2) + align256((size_t)M * 4) + b + t + sk;
 }
 
 Workspace carve(void* ws, int64_t M, int64_t N, int64_t K, int64_t gs, int bits) {
@@ -82,7 +88,12 @@ Workspace carve(void* ws, int64_t M, int64_t N, int64_t K, int64_t gs, int bits)
         w.b_img = reinterpret_cast<__half*>(p);
         p += align256((size_t)N * K * 2);
     }
-    w.s_wT = uses_scales_t(M, gs, bits) ? reinterpret_cast<float*>(p) : nullptr;
+    w.s_wT = nullptr;
+    if (uses_scales_t(M, gs, bits)) {
+        w.s_wT = reinterpret_cast<float*>(p);
+        p += align256((size_t)(K / gs) * N * 4);
+    }
+    w.sk_part = uses_stream_k(M, gs) ? reinterpret_cast<int32_t*>(p) : nullptr;
     return w;
 }
 
@@ -157,6 +168,7 @@ cider_status cider::linear_call(const void* x, int32_t x_dtype, int64_t M, int64
     a.timeout_ns = kWaitTimeoutNs;
     a.status = status;
     a.out_bf16 = (y_dtype == CIDER_DTYPE_BF16);
+    a.sk_part = wsp.sk_part;
     return from_cuda(launch_gemm(a, sms, stream));
 }
 

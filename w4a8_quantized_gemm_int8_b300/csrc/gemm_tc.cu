@@ -45,12 +45,26 @@ namespace gemm1 {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int MAX_STAGES = 8;
-constexpr int NUM_CONV_WARPS = 2;
+static_assert(BK == 64, "a k-block is four MMAs of 16 k");
+constexpr int MAX_STAGES = 8;       // operand stages (activation + fp16 weight tiles)
+constexpr int MAX_RAW_STAGES = 24;  // raw weight-code stages
+constexpr int RAW_AB_STAGES = 4;    // operand stages when the weights arrive raw
+// Warps 0-3: TMA producers (warp 0: weight codes, or both operands from an
+// image; warp 2: activation tiles when the weights arrive raw), MMA issuer
+// and TMEM owner (warp 1); warps 4-7: weight converters (one warpgroup);
+// warps 8-15: epilogue.
+constexpr int NUM_CONV_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_EPI_THREADS = NUM_EPI_WARPS * 32;
-constexpr int NUM_ROLE_THREADS = 128;  // TMA warp, MMA warp, two converter warps
-constexpr int NUM_THREADS = NUM_ROLE_THREADS + NUM_EPI_THREADS;
+constexpr int FIRST_EPI_WARP = 8;
+constexpr int NUM_THREADS = FIRST_EPI_WARP * 32 + NUM_EPI_THREADS;
+constexpr int LAUNCH_REGS = 128;
+constexpr int ROLE_REGS = 56;
+constexpr int CONV_REGS = 80;
+constexpr int EPI_REGS = 184;
+static_assert(128 * ROLE_REGS + 128 * CONV_REGS + NUM_EPI_THREADS * EPI_REGS <=
+                  NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
 constexpr int TMEM_COLS = 512;    // all of TMEM: 512 / BN fp32 accumulators
 constexpr int MAX_ACC = 8;
 constexpr int MAX_SEG_KB = 16;    // 16 x 64 = 1024 k per exact fp32 segment
@@ -82,36 +96,49 @@ struct Cfg {
     static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes + kRawBytes;
     static constexpr int kScaleFloats = kScaleDepth * kGroups * kCols;  // per epilogue warp
     static constexpr int kFixedBytes = NUM_EPI_WARPS * OUT_WARP_BYTES +
-                                       NUM_EPI_WARPS * kScaleFloats * 4 + 512 + 16 + 1024;
-    static constexpr int kStages = (SMEM_LIMIT - kFixedBytes) / kStageBytes < MAX_STAGES
-                                       ? (SMEM_LIMIT - kFixedBytes) / kStageBytes
-                                       : MAX_STAGES;
+                                       NUM_EPI_WARPS * kScaleFloats * 4 + 1024 + 16 + 1024;
+    static constexpr int kABBytes = A_STAGE_BYTES + kBStageBytes;
+    static constexpr int kAvail = SMEM_LIMIT - kFixedBytes;
+    // Image weights: one ring of operand stages, as deep as fits. Raw codes:
+    // the operand ring stays short (its tiles come from L2 or are written on
+    // chip) and the rest of shared memory holds raw-code stages, so that
+    // enough weight bytes are in flight from HBM per SM; with one ring for
+    // everything (five stages) a few-token layer ran at a fixed number of
+    // microseconds per k-block whatever the code width or token count.
+    static constexpr int kStages = kRaw ? RAW_AB_STAGES
+                                        : (kAvail / kABBytes < MAX_STAGES ? kAvail / kABBytes
+                                                                          : MAX_STAGES);
+    static constexpr int kRawFit = kRaw ? (kAvail - kStages * kABBytes) / kRawBytes : 0;
+    static constexpr int kRawStages = kRawFit < MAX_RAW_STAGES ? kRawFit : MAX_RAW_STAGES;
     static_assert(kNumAcc >= 2 && kNumAcc <= MAX_ACC && kChunks >= 1, "tile width");
     static_assert(kStages >= 4, "pipeline depth");
+    static_assert(!kRaw || kRawStages >= 4, "raw pipeline depth");
 };
 
 struct __align__(8) Barriers {
     uint64_t full[MAX_STAGES];       // TMA of the activation (and image weight) tiles
-    uint64_t raw_full[MAX_STAGES];   // TMA of the raw weight tile
     uint64_t conv_full[MAX_STAGES];  // converters wrote the fp16 weight tile
     uint64_t empty[MAX_STAGES];      // the MMAs reading the stage completed
+    uint64_t raw_full[MAX_RAW_STAGES];   // TMA of a raw weight tile
+    uint64_t raw_empty[MAX_RAW_STAGES];  // the converters took the raw tile into registers
     uint64_t acc_full[MAX_ACC];
     uint64_t acc_empty[MAX_ACC];
     uint64_t drain;
 };
-static_assert(sizeof(Barriers) <= 512, "barrier area");
+static_assert(sizeof(Barriers) <= 1024, "barrier area");
 
 template <int BSRC, int BN>
 struct SmemLayout {
     using C = Cfg<BSRC, BN>;
     static constexpr int STAGES = C::kStages;
+    static constexpr int RAW_STAGES = C::kRawStages;
     static constexpr int a_off = 0;
     static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
     static constexpr int raw_off = b_off + STAGES * C::kBStageBytes;
-    static constexpr int out_off = raw_off + STAGES * C::kRawBytes;
+    static constexpr int out_off = raw_off + RAW_STAGES * C::kRawBytes;
     static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;
     static constexpr int bar_off = scale_off + NUM_EPI_WARPS * C::kScaleFloats * 4;
-    static constexpr int misc_off = bar_off + 512;  // tmem base, abort
+    static constexpr int misc_off = bar_off + 1024;  // tmem base, abort
     static constexpr int bytes = misc_off + 16;
     static constexpr int alloc_bytes = bytes + 1024;  // runtime 1024-byte alignment slack
     static_assert(alloc_bytes <= SMEM_LIMIT, "shared memory per block");
@@ -123,7 +150,7 @@ struct Params {
     int num_kb;   // k-blocks of 64
     int seg_kb;   // k-blocks per segment
     int num_seg;  // segments per tile
-    int group_kb; // k-blocks per group (per-group; = seg_kb for per-channel)
+    int group_kb; // k-blocks per group (per-group; MAX_SEG_KB, no split, per-channel)
     int G;        // columns of s_w (1 for per-channel)
     int tiles_m, tiles_n;
     const float* s_a;
@@ -134,6 +161,14 @@ struct Params {
     int out_bf16;   // output elements are bfloat16 instead of fp16
     uint64_t timeout_ns;
     unsigned long long* status;
+    // Stream-K (per-channel modes): the tiles' num_kb-long k-block runs form
+    // `units` units, CTA c takes units [c * units / grid, (c + 1) * units /
+    // grid). A tile that several CTAs share is left to the fix-up kernel:
+    // each stores its int32 partial of the tile in `part`.
+    int streamk;
+    int64_t units;
+    int32_t* part;  // [grid][2][BN / 4][part_rows][4] int32
+    int part_rows;
 };
 
 // Wait sites recorded in the device status word on a timeout.
@@ -146,7 +181,83 @@ enum : uint32_t {
     kSiteProducerDrain = 0x106,
     kSiteConvRaw = 0x107,
     kSiteMmaConv = 0x108,
+    kSiteConvEmpty = 0x109,
 };
+
+// A CTA's work item: k-blocks [kb0, kb1) of one tile.
+struct Work {
+    int tile, kb0, kb1;
+};
+
+// The items of this CTA, in order: whole tiles blockIdx.x, + gridDim.x, ...;
+// or with stream-K its run of units, cut at tile boundaries.
+struct WorkIter {
+    int64_t u, uend;
+    int tile, num_tiles, nk;
+    bool sk;
+    __device__ __forceinline__ WorkIter(const Params& p, int num_tiles_)
+        : tile((int)blockIdx.x), num_tiles(num_tiles_), nk(p.num_kb), sk(p.streamk != 0) {
+        u = sk ? (int64_t)blockIdx.x * p.units / gridDim.x : 0;
+        uend = sk ? ((int64_t)blockIdx.x + 1) * p.units / gridDim.x : 0;
+    }
+    __device__ __forceinline__ bool next(Work& w) {
+        if (sk) {
+            if (u >= uend) return false;
+            w.tile = (int)(u / nk);
+            w.kb0 = (int)(u - (int64_t)w.tile * nk);
+            const int64_t left = uend - u;
+            w.kb1 = (left < (int64_t)(nk - w.kb0)) ? w.kb0 + (int)left : nk;
+            u += w.kb1 - w.kb0;
+            return true;
+        }
+        if (tile >= num_tiles) return false;
+        w.tile = tile;
+        w.kb0 = 0;
+        w.kb1 = nk;
+        tile += gridDim.x;
+        return true;
+    }
+};
+
+// The stream-K CTA whose units include unit u (ranges as in WorkIter).
+__device__ __forceinline__ int sk_cta_of_unit(int64_t u, int64_t units, int grid) {
+    return (int)(((u + 1) * grid + units - 1) / units) - 1;
+}
+
+// Segments of an item: per-group, the tile's fixed segments (items are whole
+// tiles); per-channel, the item's k-blocks in equal runs of at most
+// MAX_SEG_KB.
+template <GemmMode MODE>
+__device__ __forceinline__ void item_segments(const Params& p, const Work& w, int& seg_kb,
+                                              int& nseg) {
+    if constexpr (MODE == GemmMode::kPgF16 || MODE == GemmMode::kRawPgS32) {
+        seg_kb = p.seg_kb;
+        nseg = p.num_seg;
+    } else {
+        const int len = w.kb1 - w.kb0;
+        const int n = (len + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        seg_kb = (len + n - 1) / n;
+        nseg = (len + seg_kb - 1) / seg_kb;
+    }
+}
+
+// The four MMAs of one k-block (4 x 16 k; both operands advance 32 bytes
+// within their 128-byte swizzle rows, 2 in descriptor units), issued from one
+// asm block; the first accumulates only if `accumulate`.
+__device__ __forceinline__ void mma4_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, t;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "l"(a_desc + 2), "l"(b_desc + 2),
+        "l"(a_desc + 4), "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
+        : "memory");
+}
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int& tn) {
     tm = tile % tiles_m;
@@ -203,13 +314,14 @@ __device__ __forceinline__ void widen_piece(const uint4 raw, uint8_t* tile, int 
 }
 
 template <GemmMode MODE, int BSRC, int BN>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __maxnreg__(LAUNCH_REGS)
     gemm_tc1_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_y, const Params p) {
     using Layout = SmemLayout<BSRC, BN>;
     using C = Cfg<BSRC, BN>;
     constexpr int STAGES = Layout::STAGES;
+    constexpr int RAW_STAGES = Layout::RAW_STAGES > 0 ? Layout::RAW_STAGES : 1;
     constexpr int NUM_ACC = C::kNumAcc;
     constexpr int COLS = C::kCols;
     constexpr int SD = C::kScaleDepth;
@@ -228,9 +340,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
-            mbar_init(smem_u32(&bars->raw_full[s]), 1);
             mbar_init(smem_u32(&bars->conv_full[s]), NUM_CONV_WARPS);
             mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int r = 0; r < RAW_STAGES; ++r) {
+            mbar_init(smem_u32(&bars->raw_full[r]), 1);
+            mbar_init(smem_u32(&bars->raw_empty[r]), NUM_CONV_WARPS);
         }
         for (int b = 0; b < NUM_ACC; ++b) {
             mbar_init(smem_u32(&bars->acc_full[b]), 1);
@@ -256,51 +371,80 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     grid_dep_wait();
     grid_dep_launch();
 
-    if (warp == 0) {
-        // ------------------------------ TMA producer --------------------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int issued = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                int tm, tn;
-                tile_coords(tile, p.tiles_m, tm, tn);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1, p.timeout_ns,
-                                           abort_flag, p.status, kSiteProducerEmpty))
-                        goto producer_done;
-                    const uint32_t fb = smem_u32(&bars->full[stage]);
-                    mbar_arrive_expect_tx(fb, C::kFullTx);
-                    tma_load_2d(smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES), &tmap_a,
-                                fb, kb * BK, tm * BM);
-                    if constexpr (C::kRaw) {
-                        const uint32_t rb = smem_u32(&bars->raw_full[stage]);
-                        mbar_arrive_expect_tx(rb, C::kRawBytes);
-                        tma_load_2d(smem_u32(smem + Layout::raw_off + stage * C::kRawBytes),
-                                    &tmap_b, rb, kb * C::kRawRowBytes, tn * BN);
-                    } else {
-                        tma_load_2d(smem_u32(smem + Layout::b_off + stage * C::kBStageBytes),
-                                    &tmap_b, fb, kb * BK, tn * BN);
-                    }
-                    ++issued;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
+    if (warp < 4) setmaxnreg_dec<ROLE_REGS>();
+    if ((C::kRaw ? warp == 2 : warp == 0) && lane == 0) {
+        // -------------------- TMA producer: operand stages --------------------
+        // The activation tile of each k-block, and with an image its fp16
+        // weight tile too, into the operand stage the MMAs of the k-block read.
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        WorkIter it(p, num_tiles);
+        Work w;
+        while (it.next(w)) {
+            int tm, tn;
+            tile_coords(w.tile, p.tiles_m, tm, tn);
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                if (!mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1, p.timeout_ns,
+                                       abort_flag, p.status, kSiteProducerEmpty))
+                    goto producer_done;
+                const uint32_t fb = smem_u32(&bars->full[stage]);
+                mbar_arrive_expect_tx(fb, C::kFullTx);
+                tma_load_2d(smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES), &tmap_a, fb,
+                            kb * BK, tm * BM);
+                if constexpr (!C::kRaw)
+                    tma_load_2d(smem_u32(smem + Layout::b_off + stage * C::kBStageBytes), &tmap_b,
+                                fb, kb * BK, tn * BN);
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
                 }
             }
-        producer_done:
-            if (*abort_flag) {
-                // Let every tile load already issued land before the CTA exits:
-                // the last use u of each stage completes phase u / STAGES.
-                for (int u = (issued > STAGES ? issued - STAGES : 0); u < issued; ++u) {
-                    const uint32_t par = (uint32_t)(u / STAGES) & 1u;
-                    bool ok = mbar_wait_drain(smem_u32(&bars->full[u % STAGES]), par, p.timeout_ns);
-                    if (C::kRaw)
-                        ok = mbar_wait_drain(smem_u32(&bars->raw_full[u % STAGES]), par,
-                                             p.timeout_ns) && ok;
-                    if (!ok) report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
+        }
+    producer_done:
+        if (*abort_flag) {
+            // Let every load already issued land before the CTA exits: the
+            // last use u of each stage completes phase u / STAGES.
+            for (int u = (issued > STAGES ? issued - STAGES : 0); u < issued; ++u) {
+                const uint32_t par = (uint32_t)(u / STAGES) & 1u;
+                if (!mbar_wait_drain(smem_u32(&bars->full[u % STAGES]), par, p.timeout_ns))
+                    report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
+            }
+        }
+    } else if (C::kRaw && warp == 0 && lane == 0) {
+        // -------------------- TMA producer: raw weight codes -----------------
+        // Runs up to RAW_STAGES k-blocks ahead of the converters.
+        int rstage = 0;
+        uint32_t rphase = 0;
+        int issued = 0;
+        WorkIter it(p, num_tiles);
+        Work w;
+        while (it.next(w)) {
+            int tm, tn;
+            tile_coords(w.tile, p.tiles_m, tm, tn);
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                if (!mbar_wait_bounded(smem_u32(&bars->raw_empty[rstage]), rphase ^ 1,
+                                       p.timeout_ns, abort_flag, p.status, kSiteProducerEmpty))
+                    goto raw_producer_done;
+                const uint32_t rb = smem_u32(&bars->raw_full[rstage]);
+                mbar_arrive_expect_tx(rb, C::kRawBytes);
+                tma_load_2d(smem_u32(smem + Layout::raw_off + rstage * C::kRawBytes), &tmap_b, rb,
+                            kb * C::kRawRowBytes, tn * BN);
+                ++issued;
+                if (++rstage == RAW_STAGES) {
+                    rstage = 0;
+                    rphase ^= 1;
                 }
+            }
+        }
+    raw_producer_done:
+        if (*abort_flag) {
+            for (int u = (issued > RAW_STAGES ? issued - RAW_STAGES : 0); u < issued; ++u) {
+                const uint32_t par = (uint32_t)(u / RAW_STAGES) & 1u;
+                if (!mbar_wait_drain(smem_u32(&bars->raw_full[u % RAW_STAGES]), par,
+                                     p.timeout_ns))
+                    report_device_error(p.status, kDevTimeout, kSiteProducerDrain);
             }
         }
     } else if (warp == 1) {
@@ -311,21 +455,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             uint32_t seg_count = 0;
             bool issued_any = false;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
+            WorkIter it(p, num_tiles);
+            Work w;
+            while (it.next(w)) {
+                int seg_kb, nseg;
+                item_segments<MODE>(p, w, seg_kb, nseg);
+                for (int seg = 0; seg < nseg; ++seg, ++seg_count) {
                     const uint32_t b = seg_count % NUM_ACC;
                     const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
                     if (!mbar_wait_bounded(smem_u32(&bars->acc_empty[b]), acc_phase ^ 1,
                                            p.timeout_ns, abort_flag, p.status, kSiteMmaAccEmpty))
                         goto mma_done;
                     tc_fence_after();
-                    const int kb0 = seg * p.seg_kb;
-                    const int kb1 = min(p.num_kb, kb0 + p.seg_kb);
+                    const int kb0 = w.kb0 + seg * seg_kb;
+                    const int kb1 = min(w.kb1, kb0 + seg_kb);
+                    // Group j of the segment accumulates into its own BN
+                    // columns; gpos is the k-block's position in its group.
+                    uint32_t d_tmem = tmem_base + b * C::kBufCols;
+                    int gpos = 0;
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        // Group j of the segment accumulates into its own BN columns.
-                        const int j = (kb - kb0) / p.group_kb;
-                        const int gkb0 = kb0 + j * p.group_kb;
-                        const uint32_t d_tmem = tmem_base + b * C::kBufCols + j * BN;
                         if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, p.timeout_ns,
                                                abort_flag, p.status, kSiteMmaFull))
                             goto mma_done;
@@ -334,15 +482,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                p.timeout_ns, abort_flag, p.status, kSiteMmaConv))
                             goto mma_done;
                         tc_fence_after();
-                        const uint64_t adesc = smem_desc_sw128_kmajor(
-                            smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES));
-                        const uint64_t bdesc = smem_desc_sw128_kmajor(
-                            smem_u32(smem + Layout::b_off + stage * C::kBStageBytes));
-#pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) {
-                            // +32 bytes along K per 16-element step (encoded >> 4).
-                            tc_mma_f16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                                       (kb > gkb0 || k > 0) ? 1u : 0u);
+                        mma4_f16(d_tmem,
+                                 smem_desc_sw128_kmajor(
+                                     smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES)),
+                                 smem_desc_sw128_kmajor(
+                                     smem_u32(smem + Layout::b_off + stage * C::kBStageBytes)),
+                                 idesc, gpos > 0 ? 1u : 0u);
+                        if (++gpos == p.group_kb) {
+                            gpos = 0;
+                            d_tmem += BN;
                         }
                         issued_any = true;
                         tc_commit(smem_u32(&bars->empty[stage]));
@@ -363,6 +511,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else if (warp < 4) {
+        // idle role warps
+    } else if (warp < FIRST_EPI_WARP) {
+        setmaxnreg_dec<CONV_REGS>();
         // ------------------------- weight converters --------------------------
         // A stage's raw tile is BN rows of kRawRowBytes, i.e. PPR 16-byte
         // pieces per row; piece pc covers row pc / PPR, fp16 chunks from
@@ -371,32 +522,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr int PPR = C::kRawRowBytes / 16;
             constexpr int CPP = 8 / PPR;
             constexpr int PER_THREAD = BN * PPR / (32 * NUM_CONV_WARPS);
-            const int ct = (warp - 2) * 32 + lane;
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+            static_assert(PER_THREAD >= 1 && PER_THREAD * 32 * NUM_CONV_WARPS == BN * PPR,
+                          "converter work split");
+            const int ct = (warp - 4) * 32 + lane;
+            int stage = 0, rstage = 0;
+            uint32_t phase = 0, rphase = 0;
+            WorkIter it(p, num_tiles);
+            Work w;
+            while (it.next(w)) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     {
-                        const bool ok = mbar_wait_bounded(smem_u32(&bars->raw_full[stage]), phase,
-                                                          p.timeout_ns, abort_flag, p.status,
-                                                          kSiteConvRaw);
+                        const bool ok = mbar_wait_bounded(smem_u32(&bars->raw_full[rstage]),
+                                                          rphase, p.timeout_ns, abort_flag,
+                                                          p.status, kSiteConvRaw);
                         if (!__all_sync(0xffffffffu, ok)) goto conv_done;
                     }
-                    const uint4* raw =
-                        reinterpret_cast<const uint4*>(smem + Layout::raw_off + stage * C::kRawBytes);
+                    const uint4* raw = reinterpret_cast<const uint4*>(
+                        smem + Layout::raw_off + rstage * C::kRawBytes);
                     uint8_t* tile_b = smem + Layout::b_off + stage * C::kBStageBytes;
                     uint4 pcs[PER_THREAD];
 #pragma unroll
                     for (int i = 0; i < PER_THREAD; ++i) pcs[i] = raw[ct + i * 32 * NUM_CONV_WARPS];
+                    {
+                        // The fp16 tile of this operand stage is free once the
+                        // MMAs of its previous k-block completed.
+                        const bool ok = mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1,
+                                                          p.timeout_ns, abort_flag, p.status,
+                                                          kSiteConvEmpty);
+                        if (!__all_sync(0xffffffffu, ok)) goto conv_done;
+                    }
 #pragma unroll
                     for (int i = 0; i < PER_THREAD; ++i) {
                         const int pc = ct + i * 32 * NUM_CONV_WARPS;
                         widen_piece<BSRC>(pcs[i], tile_b, pc / PPR, (pc % PPR) * CPP);
                     }
-                    // Make the generic-proxy writes visible to the tensor core.
+                    // Order this warp's generic-proxy accesses before the
+                    // async proxy's: its fp16 writes before the tensor core's
+                    // reads, its reads of the raw stage (consumed above) before
+                    // the next copy into it. Then release both stages.
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&bars->conv_full[stage]));
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bars->raw_empty[rstage]));
+                        mbar_arrive(smem_u32(&bars->conv_full[stage]));
+                    }
+                    if (++rstage == RAW_STAGES) {
+                        rstage = 0;
+                        rphase ^= 1;
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -406,12 +579,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         conv_done:;
         }
     } else {
+        setmaxnreg_inc<EPI_REGS>();
         // ------------------------------ epilogue ------------------------------
-        // Warp w (4..11) owns TMEM lanes 32 * (w % 4) .. +31 (its 32 token
+        // Warp w (8..15) owns TMEM lanes 32 * (w % 4) .. +31 (its 32 token
         // rows; a warp may only access its own lane quadrant) and the COLS
         // columns [COLS * half, COLS * half + COLS) of the tile, read 32 at a
         // time.
-        const int ewarp = warp - 4;
+        const int ewarp = warp - FIRST_EPI_WARP;
         const int quad = warp & 3;
         const int half = ewarp >> 2;
         uint8_t* stage_out = smem + Layout::out_off + ewarp * OUT_WARP_BYTES;
@@ -424,12 +598,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int GS = C::kGroups;
         constexpr int SET = GS * COLS;  // floats per use: [group][column]
         float* wsc = scales + ewarp * C::kScaleFloats;
-        int f_tile = blockIdx.x, f_seg = kPerSegScales ? 0 : p.num_seg - 1;  // next use to fetch
+        // Next use to fetch: item fw, segment f_seg of it (per-group).
+        WorkIter f_it(p, num_tiles);
+        Work fw;
+        bool f_ok = f_it.next(fw);
+        int f_seg = 0;
         uint32_t f_slot = 0, u_slot = 0;
         auto fetch_next = [&]() {
-            if (f_tile < num_tiles) {
+            if (f_ok) {
                 int tm, tn;
-                tile_coords(f_tile, p.tiles_m, tm, tn);
+                tile_coords(fw.tile, p.tiles_m, tm, tn);
                 float* dst = wsc + f_slot * SET;
 #pragma unroll
                 for (int j = 0; j < GS; ++j) {
@@ -450,8 +628,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (kPerSegScales && f_seg + 1 < p.num_seg) {
                     ++f_seg;
                 } else {
-                    f_seg = kPerSegScales ? 0 : p.num_seg - 1;
-                    f_tile += gridDim.x;
+                    f_seg = 0;
+                    f_ok = f_it.next(fw);
                 }
             }
             cp_async_commit();  // possibly empty: one group per use keeps the count
@@ -461,21 +639,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t seg_count = 0;
         bool store_pending = false;
         uint32_t acc[COLS];  // int32 running sum (per-channel) or fp32 running sum (per-group)
+        bool first_item = true;  // stream-K: partial slot 0 for the first item, 1 after
 
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        WorkIter it(p, num_tiles);
+        Work w;
+        while (it.next(w)) {
             int tm, tn;
-            tile_coords(tile, p.tiles_m, tm, tn);
+            tile_coords(w.tile, p.tiles_m, tm, tn);
             const int m_base = tm * BM + quad * 32;
             const int m = m_base + lane;
             const int n_w = tn * BN + half * COLS;
+            int seg_kb, nseg;
+            item_segments<MODE>(p, w, seg_kb, nseg);
+            (void)seg_kb;
             if constexpr (MODE == GemmMode::kPgF16) {
 #pragma unroll
                 for (int j = 0; j < COLS; ++j) acc[j] = 0u;  // f = +0 before the first group
             }
-            for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
+            for (int seg = 0; seg < nseg; ++seg, ++seg_count) {
                 const uint32_t b = seg_count % NUM_ACC;
                 const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
-                const bool last_seg = (seg == p.num_seg - 1);
+                const bool last_seg = (seg == nseg - 1);
                 const bool uses_scales = kPerSegScales || last_seg;
                 const float* sc = wsc + u_slot * SET;
                 if (uses_scales) {
@@ -566,7 +750,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[b]));
 
-                if (last_seg) {
+                bool emit = last_seg;
+                if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
+                    if (last_seg && p.streamk && (w.kb0 != 0 || w.kb1 != p.num_kb)) {
+                        // ---- stream-K: a tile shared with other CTAs ----
+                        // Only this CTA's int32 partial of its rows and columns
+                        // is stored; the fix-up kernel sums the partials and
+                        // writes the output. A partial tile is [BN / 4]
+                        // [part_rows] runs of four columns, so that the 32 lanes
+                        // (32 rows) of a warp store 512 contiguous bytes.
+                        const int r = quad * 32 + lane;
+                        const int slot = first_item ? 0 : 1;
+                        if (r < p.part_rows) {
+                            int4* dst = reinterpret_cast<int4*>(p.part) +
+                                        (((int64_t)blockIdx.x * 2 + slot) * (BN / 4) +
+                                         half * (COLS / 4)) * p.part_rows + r;
+#pragma unroll
+                            for (int j = 0; j < COLS; j += 4)
+                                dst[(j / 4) * p.part_rows] =
+                                    make_int4((int)acc[j], (int)acc[j + 1], (int)acc[j + 2],
+                                              (int)acc[j + 3]);
+                        }
+                        emit = false;
+                    }
+                }
+                if (emit) {
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c) {
                         const uint32_t* ac = acc + c * 32;
@@ -642,6 +850,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (uses_scales) u_slot = (u_slot + 1 == SD) ? 0 : u_slot + 1;
             }
+            first_item = false;
         }
     epi_done:
         cp_async_wait_all();
@@ -655,6 +864,133 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stream-K fix-up: every tile that several CTAs shared gets the sum of their
+// int32 partials (exact, any order) and the layer's epilogue, computed as in
+// the GEMM epilogue: y = fp16((float(acc) * s_a[m]) * s_w[n]) (or the raw
+// int32 sums). One CTA per 32 rows and 64 columns of a tile: lane = row,
+// warp w sums the runs of four columns w and w + 8 of its half; rows are
+// then written from shared memory, 2 columns per lane.
+// ---------------------------------------------------------------------------
+struct FixArgs {
+    const int32_t* part;
+    int part_rows;
+    int64_t units;
+    int grid;  // CTAs of the GEMM launch
+    int num_kb;
+    int tiles_m;
+    int M, N;
+    const float* s_a;
+    const float* s_w;
+    void* out;
+    int out_bf16;
+    int raw_s32;
+};
+
+constexpr int FIX_THREADS = 256;
+constexpr int FIX_STRIDE = 65;  // words per staged row (64 + 1: conflict-free columns)
+// Contributors of one tile: at most grid / tiles + 2 CTAs share it.
+constexpr int FIX_MAX_CONTRIB = kStreamKMaxCtas + 2;
+static_assert(FIX_MAX_CONTRIB <= FIX_THREADS, "one thread per contributor");
+
+__global__ void __launch_bounds__(FIX_THREADS) sk_fixup_kernel(const FixArgs f) {
+    __shared__ uint32_t stage[32 * FIX_STRIDE];
+    __shared__ const int4* base[FIX_MAX_CONTRIB];  // each contributor's partial tile
+    grid_dep_wait();
+    grid_dep_launch();
+    const int chunks = f.part_rows / 32;
+    const int half = blockIdx.x & 1;
+    const int tile = (blockIdx.x >> 1) / chunks, chunk = (blockIdx.x >> 1) % chunks;
+    const int64_t u0 = (int64_t)tile * f.num_kb;
+    const int c_first = sk_cta_of_unit(u0, f.units, f.grid);
+    const int c_last = sk_cta_of_unit(u0 + f.num_kb - 1, f.units, f.grid);
+    if (c_first == c_last) return;  // one CTA did the whole tile and wrote it
+    const int nc = c_last - c_first + 1;
+    if ((int)threadIdx.x < nc) {
+        // The tile is CTA c's first item (slot 0) exactly when c's run starts
+        // inside it, else its last (slot 1).
+        const int c = c_first + (int)threadIdx.x;
+        const int64_t c_start = (int64_t)c * f.units / f.grid;
+        const int slot = (c_start / f.num_kb == tile) ? 0 : 1;
+        base[threadIdx.x] =
+            reinterpret_cast<const int4*>(f.part) + ((int64_t)c * 2 + slot) * 32 * f.part_rows;
+    }
+    __syncthreads();
+    int tm, tn;
+    tile_coords(tile, f.tiles_m, tm, tn);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = chunk * 32 + lane;  // row within the tile
+    const int m = tm * BM + r;
+    const float sa = (!f.raw_s32 && m < f.M) ? __ldg(f.s_a + m) : 0.0f;
+    // All contributors' loads of this thread's two column runs are issued
+    // together (contributors outermost, four at a time), so that the sums
+    // wait for about one load latency per four contributors.
+    int acc[2][4] = {};
+#pragma unroll 4
+    for (int i = 0; i < nc; ++i) {
+        const int4* b = base[i] + r;
+        int4 v[2];
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass)
+            v[pass] = __ldcg(b + (int64_t)(half * 16 + warp + 8 * pass) * f.part_rows);
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            acc[pass][0] += v[pass].x;
+            acc[pass][1] += v[pass].y;
+            acc[pass][2] += v[pass].z;
+            acc[pass][3] += v[pass].w;
+        }
+    }
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int cl = warp + 8 * pass;  // run within the half: columns 4 cl .. 4 cl + 3
+        const int a0 = acc[pass][0], a1 = acc[pass][1], a2 = acc[pass][2], a3 = acc[pass][3];
+        uint32_t* row = stage + lane * FIX_STRIDE;
+        if (f.raw_s32) {
+            row[4 * cl] = (uint32_t)a0;
+            row[4 * cl + 1] = (uint32_t)a1;
+            row[4 * cl + 2] = (uint32_t)a2;
+            row[4 * cl + 3] = (uint32_t)a3;
+        } else {
+            const int n = tn * 128 + half * 64 + 4 * cl;
+            const float w0 = (n < f.N) ? __ldg(f.s_w + n) : 0.0f;
+            const float w1 = (n + 1 < f.N) ? __ldg(f.s_w + n + 1) : 0.0f;
+            const float w2 = (n + 2 < f.N) ? __ldg(f.s_w + n + 2) : 0.0f;
+            const float w3 = (n + 3 < f.N) ? __ldg(f.s_w + n + 3) : 0.0f;
+            const bool bf16 = f.out_bf16 != 0;
+            row[2 * cl] = pack2_rn(__fmul_rn(__fmul_rn(__int2float_rn(a0), sa), w0),
+                                   __fmul_rn(__fmul_rn(__int2float_rn(a1), sa), w1), bf16);
+            row[2 * cl + 1] = pack2_rn(__fmul_rn(__fmul_rn(__int2float_rn(a2), sa), w2),
+                                       __fmul_rn(__fmul_rn(__int2float_rn(a3), sa), w3), bf16);
+        }
+    }
+    __syncthreads();
+    // Warp w writes rows w, w + 8, w + 16, w + 24 of the chunk; lane l
+    // columns 2 l, 2 l + 1 of the half (int32: 4 l' .. 4 l' + 3 per pass).
+    for (int i = warp; i < 32; i += 8) {
+        const int mm = tm * BM + chunk * 32 + i;
+        if (mm >= f.M) break;
+        const uint32_t* row = stage + i * FIX_STRIDE;
+        if (f.raw_s32) {
+            int32_t* out = static_cast<int32_t*>(f.out) + (int64_t)mm * f.N;
+            for (int j = lane; j < 64; j += 32) {
+                const int n = tn * 128 + half * 64 + j;
+                if (n < f.N) out[n] = (int32_t)row[j];
+            }
+        } else {
+            uint16_t* out = static_cast<uint16_t*>(f.out) + (int64_t)mm * f.N;
+            const int n0 = tn * 128 + half * 64 + 2 * lane;
+            const uint32_t h01 = row[lane];
+            if (n0 + 1 < f.N && (f.N & 1) == 0) {
+                *reinterpret_cast<uint32_t*>(out + n0) = h01;
+            } else {
+                if (n0 < f.N) out[n0] = (uint16_t)(h01 & 0xFFFFu);
+                if (n0 + 1 < f.N) out[n0 + 1] = (uint16_t)(h01 >> 16);
+            }
+        }
     }
 }
 
@@ -700,8 +1036,14 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
                         const gemm1::Params& p, int grid, cudaStream_t stream) {
     using Layout = gemm1::SmemLayout<BSRC, BN>;
     auto kern = gemm1::gemm_tc1_kernel<MODE, BSRC, BN>;
-    static PerDevice<int> attr;  // the shared-memory opt-in, once per device
+    // Once per device: the register count the warp-role split assumes, and the
+    // shared-memory opt-in.
+    static PerDevice<int> attr;
     const cudaError_t e = attr.get([&](int&) {
+        cudaFuncAttributes fa;
+        cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+        if (r != cudaSuccess) return r;
+        if (fa.numRegs != gemm1::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Layout::alloc_bytes);
     });
@@ -800,7 +1142,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     } else {
         const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
         p.seg_kb = (p.num_kb + nseg - 1) / nseg;
-        p.group_kb = p.seg_kb;
+        // No group split inside a segment: a stream-K item's segments may be
+        // longer than those of a whole tile, never longer than MAX_SEG_KB.
+        p.group_kb = MAX_SEG_KB;
         p.G = 1;
     }
     p.num_seg = (p.num_kb + p.seg_kb - 1) / p.seg_kb;
@@ -815,10 +1159,43 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     p.timeout_ns = a.timeout_ns;
     p.status = a.status;
     const int tiles = p.tiles_m * p.tiles_n;
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    if (bsrc == 8) return launch_src<8>(a.mode, ta, tb, ty, p, grid, stream);
-    if (bsrc == 4) return launch_src<4>(a.mode, ta, tb, ty, p, grid, stream);
-    return launch_src<0>(a.mode, ta, tb, ty, p, grid, stream);
+    int grid = tiles < num_sms ? tiles : num_sms;
+    // Stream-K when whole tiles would leave SMs idle (fewer tiles than SMs,
+    // or a last partial wave): every CTA takes an equal run of k-blocks.
+    const bool per_channel = (a.mode == GemmMode::kPcF16 || a.mode == GemmMode::kRawS32);
+    if (per_channel && a.sk_part != nullptr && tiles % num_sms != 0 && tiles < 8 * num_sms &&
+        p.num_kb >= 2) {
+        p.streamk = 1;
+        p.units = (int64_t)tiles * p.num_kb;
+        int g = num_sms < kStreamKMaxCtas ? num_sms : kStreamKMaxCtas;
+        if ((int64_t)g > p.units) g = (int)p.units;
+        grid = g;
+        p.part = a.sk_part;
+        p.part_rows = (int)stream_k_part_rows(a.M);
+    }
+    cudaError_t e;
+    if (bsrc == 8)
+        e = launch_src<8>(a.mode, ta, tb, ty, p, grid, stream);
+    else if (bsrc == 4)
+        e = launch_src<4>(a.mode, ta, tb, ty, p, grid, stream);
+    else
+        e = launch_src<0>(a.mode, ta, tb, ty, p, grid, stream);
+    if (e != cudaSuccess || !p.streamk) return e;
+    FixArgs f{};
+    f.part = p.part;
+    f.part_rows = p.part_rows;
+    f.units = p.units;
+    f.grid = grid;
+    f.num_kb = p.num_kb;
+    f.tiles_m = p.tiles_m;
+    f.M = p.M;
+    f.N = p.N;
+    f.s_a = p.s_a;
+    f.s_w = p.s_w;
+    f.out = p.out;
+    f.out_bf16 = p.out_bf16;
+    f.raw_s32 = (a.mode == GemmMode::kRawS32) ? 1 : 0;
+    return launch_pdl(sk_fixup_kernel, tiles * (p.part_rows / 32) * 2, FIX_THREADS, 0, stream, f);
 }
 
 }  // namespace cider

@@ -135,6 +135,7 @@ struct Params {
     int num_seg;
     int G;
     int tiles_t, tiles_w;  // token tiles of BT, weight tiles of 2 * BW
+    int w_fastest;         // tile order (tile_coords)
     const float* s_a;
     const float* s_w;
     void* out;
@@ -154,6 +155,19 @@ enum : uint32_t {
     kSiteDrain = 0x409,
     kSiteProducerDrain = 0x40a,
 };
+
+// Tile order: weight tiles fastest when the activation image is the larger
+// operand (concurrent clusters then share token tiles, and the activations
+// are read from DRAM about once), token tiles fastest otherwise.
+__device__ __forceinline__ void tile_coords(const Params& p, int tile, int& tt, int& tw) {
+    if (p.w_fastest) {
+        tw = tile % p.tiles_w;
+        tt = tile / p.tiles_w;
+    } else {
+        tt = tile % p.tiles_t;
+        tw = tile / p.tiles_t;
+    }
+}
 
 // D[tmem] (+)= A[tmem] * B[smem desc]^T on both CTAs of the pair, kind::f16.
 __device__ __forceinline__ void mma_pair_a_tmem(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -306,7 +320,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             uint32_t phase = 0;
             int issued = 0;
             for (int tile = cluster; tile < num_tiles; tile += nclusters) {
-                const int tt = tile % p.tiles_t, tw = tile / p.tiles_t;
+                int tt, tw;
+                tile_coords(p, tile, tt, tw);
                 const int w_row = tw * (2 * BW) + (int)rank * BW;
                 const int t_row = tt * BT + (int)rank * (BT / 2);
                 for (int ks = 0; ks < p.num_kb; ++ks) {
@@ -476,7 +491,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
         uint32_t acc[COLS];
 
         for (int tile = cluster; tile < num_tiles; tile += nclusters) {
-            const int tt = tile % p.tiles_t, tw = tile / p.tiles_t;
+            int tt, tw;
+            tile_coords(p, tile, tt, tw);
             const int n_base = tw * (2 * BW) + (int)rank * BW + quad * 32;
             const int n = n_base + lane;                  // this thread's output channel
             const int m_base = tt * BT + half * COLS;     // the warp's first token
@@ -767,6 +783,7 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     p.num_seg = (p.num_kb + p.seg_kb - 1) / p.seg_kb;
     p.tiles_t = (p.M + BT - 1) / BT;
     p.tiles_w = (p.N + 2 * BW - 1) / (2 * BW);
+    p.w_fastest = (2.0 * (double)p.M > (a.b_bits == 8 ? 1.0 : 0.5) * (double)p.N) ? 1 : 0;
     p.s_a = a.s_a;
     p.s_w = a.s_w;
     p.out = a.out;

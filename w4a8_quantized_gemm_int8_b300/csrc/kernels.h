@@ -106,7 +106,19 @@ struct GemmArgs {
     const void* b_raw;
     int b_bits;
     int out_bf16;  // fp16-output modes: write bfloat16 instead of fp16
+    // Stream-K scratch of the single-SM engine (per-channel modes; NULL:
+    // whole tiles per CTA): int32 partial tiles [kStreamKMaxCtas][2][32]
+    // [stream_k_part_rows(M)][4], summed by a fix-up launch after the GEMM.
+    int32_t* sk_part;
 };
+
+// Stream-K sizing: at most kStreamKMaxCtas CTAs share the k-blocks of all
+// tiles; each keeps at most two partial tiles (its first and its last).
+constexpr int kStreamKMaxCtas = 160;
+inline int64_t stream_k_part_rows(int64_t M) { return M >= 128 ? 128 : (M + 31) / 32 * 32; }
+inline size_t stream_k_part_bytes(int64_t M) {
+    return (size_t)kStreamKMaxCtas * 2 * (size_t)stream_k_part_rows(M) * 128 * 4;
+}
 
 cudaError_t launch_gemm_tc(const GemmArgs& args, int num_sms, cudaStream_t stream);
 // Same function on SM pairs with the raw weight codes (b_raw) widened on chip

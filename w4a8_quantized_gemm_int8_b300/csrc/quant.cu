@@ -405,6 +405,18 @@ cudaError_t launch_rows_reg_t(const T* src, int64_t rows, int64_t K, int qmax, v
     const int64_t cap = (int64_t)num_sms * 8;  // 8 resident blocks of 256 threads per SM
     const int g1 = (int)std::min<int64_t>((rows + 7) / 8, cap);
     const int g8 = (int)std::min<int64_t>(rows, cap);
+    // Few rows: a block of eight warps per row (see launch_images_t).
+    if (rows <= (int64_t)num_sms * 4) {
+        if (nvec <= 256 * 2)
+            return launch_pdl(quant_rows_reg_kernel<T, OUT, 2, 8>, g8, 256, 0, stream, src, rows,
+                              K, qmax, out, scales);
+        if (nvec <= 256 * 4)
+            return launch_pdl(quant_rows_reg_kernel<T, OUT, 4, 8>, g8, 256, 0, stream, src, rows,
+                              K, qmax, out, scales);
+        if (nvec <= 256 * 8)
+            return launch_pdl(quant_rows_reg_kernel<T, OUT, 8, 8>, g8, 256, 0, stream, src, rows,
+                              K, qmax, out, scales);
+    }
     if (nvec <= 32 * 4)
         return launch_pdl(quant_rows_reg_kernel<T, OUT, 4, 1>, g1, 256, 0, stream, src, rows, K,
                           qmax, out, scales);
@@ -579,6 +591,14 @@ cudaError_t launch_images_t(const ImagesArgs& a0, int64_t nvec, int num_sms, cud
     };
     const int64_t g1 = std::min<int64_t>((a.M + 7) / 8, (int64_t)num_sms * 3);
     const int64_t g8 = std::min<int64_t>(a.M, (int64_t)num_sms * 4);
+    // Few rows: a block of eight warps per row, so that the rows' loads are
+    // spread over many SMs (one warp per row left most SMs idle and took
+    // about 7 us at 128 x 2560).
+    if (a.M <= (int64_t)num_sms * 4) {
+        if (nvec <= 256 * 2) return go(operand_images_kernel<T, 2, 8, BITS>, g8);
+        if (nvec <= 256 * 4) return go(operand_images_kernel<T, 4, 8, BITS>, g8);
+        if (nvec <= 256 * 8) return go(operand_images_kernel<T, 8, 8, BITS>, g8);
+    }
     if (nvec <= 32 * 4) return go(operand_images_kernel<T, 4, 1, BITS>, g1);
     if (nvec <= 32 * 8) return go(operand_images_kernel<T, 8, 1, BITS>, g1);
     if (nvec <= 32 * 12) return go(operand_images_kernel<T, 12, 1, BITS>, g1);
