@@ -1,5 +1,6 @@
-// INT8 x INT8 -> INT32 GEMM with fused dequant, one SM per tile: the engine
-// for few tokens (M <= 128), and the tensor-map encoders both engines use.
+// INT8 x INT8 -> INT32 GEMM with fused dequant on single SMs (cta_group::1
+// MMAs): the engine for few tokens (M <= 128), and the tensor-map encoders
+// the engines use.
 //
 // What it computes (Cider README, sections "Metal Kernel Pipeline" and
 // "Quantization"): acc[m,n] = sum_k q[m,k] * wq[n,k] exactly in int32, then
@@ -13,23 +14,35 @@
 // product is an integer of magnitude <= 127^2 and every partial sum over at
 // most 1024 consecutive k an integer below 127^2 * 1024 < 2^24, exact in
 // fp32. K is cut into segments of at most 1024 (per-channel) or of one group
-// (per-group); each segment accumulates into one of eight TMEM buffers, and
+// (per-group); each segment accumulates into one of the TMEM buffers, and
 // the epilogue folds it (exact fp32 integer -> int32 and add, or rescale and
 // add in fp32 in ascending group order) while the tensor core fills the others.
 //
-// Shape for few tokens: one CTA per 128-token tile of 128 output channels
-// (per-channel; 80 tiles at N = 10240) or 64 (per-group), persistent over
-// tiles. With few tokens the weights are nearly all of the bytes, so they
-// are read as their raw codes (INT8 [N,K] or packed INT4 [N,K/2]) and
-// widened to exact fp16 on chip: TMA stages the raw bytes and two converter
-// warps write the 128-byte-swizzled fp16 operand tile that the tensor core
-// reads; no weight image is written to memory. (An fp16 weight image is
-// accepted too.) Warp 0 issues TMA, warp 1 owns TMEM and issues MMAs
-// (128 x BN x 16), warps 2-3 convert, warps 4..11 are the epilogue: each owns
-// one TMEM lane quadrant and half of the tile's columns, reads them 32 at a
-// time, and writes fp16 output through 64-byte-swizzled staging and TMA
-// stores. Weight scales are fetched by cp.async several segments ahead.
-// Every wait is bounded.
+// Shape for few tokens: tiles of 128 tokens x 128 output channels
+// (per-channel) or 64 (per-group). With few tokens the weights are nearly
+// all of the bytes, so they are read as their raw codes (INT8 [N,K] or
+// packed INT4 [N,K/2]) and widened to exact fp16 on chip: TMA stages the raw
+// bytes in a deep ring of their own (up to 24 stages) and a warpgroup of
+// converter warps writes the 128-byte-swizzled fp16 operand tile that the
+// tensor core reads, in a short ring of operand stages beside the
+// activation tiles; no weight image is written to memory. (An fp16 weight
+// image is accepted too.) Warp 0 issues the raw-code TMA (or, with an image,
+// all of it), warp 2 the activation TMA, warp 1 owns TMEM and issues the
+// MMAs (128 x BN x 16, the four of a k-block in one go), warps 4-7 convert,
+// warps 8-15 are the epilogue: each owns one TMEM lane quadrant and half of
+// the tile's columns, reads them 32 at a time, and writes fp16 output
+// through 64-byte-swizzled staging and TMA stores. Weight scales are
+// fetched by cp.async several segments ahead. Every wait is bounded.
+//
+// Work split: per-group layers give whole tiles to CTAs (persistent over
+// tiles). Per-channel layers with fewer tiles than SMs, or a ragged last
+// wave, use stream-K: the tiles' k-blocks in tile order are cut into one
+// equal run per CTA (80 tiles x 40 k-blocks on 148 SMs: 21 or 22 k-blocks
+// each), so a CTA works on the end of one tile and the start of the next;
+// a tile shared by several CTAs is stored by each as an exact int32 partial
+// and summed, in any order, by a fix-up launch that applies the epilogue.
+// Per-group layers cannot be split that way: their result is a rounded fp32
+// sum over the groups in ascending order.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cstdint>
