@@ -84,13 +84,19 @@ constexpr int MAX_SEG_KB = 16;    // 16 x 64 = 1024 k per exact fp32 segment
 constexpr int OUT_WARP_BYTES = 32 * 32 * 2;  // one 32 x 32 fp16 store box per warp
 constexpr int SMEM_LIMIT = 232448;           // opt-in shared memory per block
 
+// Groups per TMEM buffer: per-group tiles of 64 columns hold 4, of 128
+// columns 2 (two buffers of 256 columns); per-channel tiles 1.
+__host__ __device__ constexpr int tile_groups(GemmMode mode, int bn) {
+    return (mode == GemmMode::kPgF16 || mode == GemmMode::kRawPgS32) ? (bn == 64 ? 4 : 2) : 1;
+}
+
 // Per-instantiation shape. BSRC: weight operand source, 0 = fp16 image (TMA
 // straight into the operand tile), 8 / 4 = raw INT8 / packed INT4 codes
 // widened on chip. BN: tile width in output channels. An MMA of 128 rows
 // costs the same issue time for any N up to 128, so per-channel tiles are
 // 128 wide; per-group tiles stay 64 wide so that a short K (few tiles) still
 // spreads over the SMs and the per-group fold stays light.
-template <int BSRC, int BN>
+template <int BSRC, int BN, int GROUPS>
 struct Cfg {
     static constexpr bool kRaw = BSRC != 0;
     static constexpr int kCols = BN / 2;        // columns per epilogue warp
@@ -98,7 +104,7 @@ struct Cfg {
     // Per-group tiles hold kGroups groups' partials side by side in one TMEM
     // buffer (one accumulator of BN columns per group), so the tensor core and
     // the epilogue hand over once per kGroups groups, not once per group.
-    static constexpr int kGroups = (BN == 64) ? 4 : 1;
+    static constexpr int kGroups = GROUPS;
     static constexpr int kBufCols = kGroups * BN;
     static constexpr int kNumAcc = TMEM_COLS / kBufCols;
     static constexpr int kScaleDepth = 2;  // scale sets (one per segment) in flight per warp
@@ -140,9 +146,9 @@ struct __align__(8) Barriers {
 };
 static_assert(sizeof(Barriers) <= 1024, "barrier area");
 
-template <int BSRC, int BN>
+template <int BSRC, int BN, int GROUPS>
 struct SmemLayout {
-    using C = Cfg<BSRC, BN>;
+    using C = Cfg<BSRC, BN, GROUPS>;
     static constexpr int STAGES = C::kStages;
     static constexpr int RAW_STAGES = C::kRawStages;
     static constexpr int a_off = 0;
@@ -331,8 +337,9 @@ __global__ void __maxnreg__(LAUNCH_REGS)
     gemm_tc1_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_y, const Params p) {
-    using Layout = SmemLayout<BSRC, BN>;
-    using C = Cfg<BSRC, BN>;
+    constexpr int GROUPS_ = tile_groups(MODE, BN);
+    using Layout = SmemLayout<BSRC, BN, GROUPS_>;
+    using C = Cfg<BSRC, BN, GROUPS_>;
     constexpr int STAGES = Layout::STAGES;
     constexpr int RAW_STAGES = Layout::RAW_STAGES > 0 ? Layout::RAW_STAGES : 1;
     constexpr int NUM_ACC = C::kNumAcc;
@@ -1047,7 +1054,7 @@ CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_by
 template <GemmMode MODE, int BSRC, int BN>
 cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                         const gemm1::Params& p, int grid, cudaStream_t stream) {
-    using Layout = gemm1::SmemLayout<BSRC, BN>;
+    using Layout = gemm1::SmemLayout<BSRC, BN, gemm1::tile_groups(MODE, BN)>;
     auto kern = gemm1::gemm_tc1_kernel<MODE, BSRC, BN>;
     // Once per device: the register count the warp-role split assumes, and the
     // shared-memory opt-in.
@@ -1066,18 +1073,22 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 
 // Per-channel modes run 128-wide tiles, per-group modes 64-wide ones.
 template <int BSRC>
-cudaError_t launch_src(GemmMode mode, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t launch_src(GemmMode mode, int bn, const CUtensorMap& ta, const CUtensorMap& tb,
                        const CUtensorMap& ty, const gemm1::Params& p, int grid,
                        cudaStream_t stream) {
     switch (mode) {
         case GemmMode::kPcF16:
             return launch_mode<GemmMode::kPcF16, BSRC, 128>(ta, tb, ty, p, grid, stream);
         case GemmMode::kPgF16:
-            return launch_mode<GemmMode::kPgF16, BSRC, 64>(ta, tb, ty, p, grid, stream);
+            return bn == 128
+                       ? launch_mode<GemmMode::kPgF16, BSRC, 128>(ta, tb, ty, p, grid, stream)
+                       : launch_mode<GemmMode::kPgF16, BSRC, 64>(ta, tb, ty, p, grid, stream);
         case GemmMode::kRawS32:
             return launch_mode<GemmMode::kRawS32, BSRC, 128>(ta, tb, ty, p, grid, stream);
         case GemmMode::kRawPgS32:
-            return launch_mode<GemmMode::kRawPgS32, BSRC, 64>(ta, tb, ty, p, grid, stream);
+            return bn == 128
+                       ? launch_mode<GemmMode::kRawPgS32, BSRC, 128>(ta, tb, ty, p, grid, stream)
+                       : launch_mode<GemmMode::kRawPgS32, BSRC, 64>(ta, tb, ty, p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -1119,7 +1130,16 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     if (bsrc == 0 && !a.b_img) return cudaErrorInvalidValue;
     if (bsrc == 4 && a.K % 32 != 0) return cudaErrorInvalidValue;
     const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
-    const int BN = per_group ? 64 : 128;  // tile width of the mode's kernel
+    // Tile width: 128 per channel. Per group (whole tiles per CTA): an M128
+    // MMA costs the same for N = 64 and N = 128, so 128-wide tiles are taken
+    // when they need fewer waves over the SMs (N = 10240: 80 tiles in one
+    // wave against 160 in two), else 64-wide ones (less work per tile).
+    int BN = 128;
+    if (per_group) {
+        const int64_t w128 = ((a.N + 127) / 128 * ((a.M + BM - 1) / BM) + num_sms - 1) / num_sms;
+        const int64_t w64 = ((a.N + 63) / 64 * ((a.M + BM - 1) / BM) + num_sms - 1) / num_sms;
+        BN = (w128 < w64) ? 128 : 64;
+    }
     CUtensorMap ta, tb, ty;
     if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
@@ -1150,7 +1170,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
             return cudaErrorInvalidValue;
         p.group_kb = a.group_size / BK;
         if (p.group_kb > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
-        p.seg_kb = p.group_kb * Cfg<0, 64>::kGroups;  // groups per segment of the per-group kernel
+        p.seg_kb = p.group_kb * tile_groups(a.mode, BN);  // groups per segment
         p.G = p.K / a.group_size;
     } else {
         const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
@@ -1188,11 +1208,11 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     }
     cudaError_t e;
     if (bsrc == 8)
-        e = launch_src<8>(a.mode, ta, tb, ty, p, grid, stream);
+        e = launch_src<8>(a.mode, BN, ta, tb, ty, p, grid, stream);
     else if (bsrc == 4)
-        e = launch_src<4>(a.mode, ta, tb, ty, p, grid, stream);
+        e = launch_src<4>(a.mode, BN, ta, tb, ty, p, grid, stream);
     else
-        e = launch_src<0>(a.mode, ta, tb, ty, p, grid, stream);
+        e = launch_src<0>(a.mode, BN, ta, tb, ty, p, grid, stream);
     if (e != cudaSuccess || !p.streamk) return e;
     FixArgs f{};
     f.part = p.part;
