@@ -720,6 +720,10 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream) {
         if (a.b_raw) return launch_gemm_tw(a, num_sms, stream);
         if (a.b_img) return launch_gemm_tc_pair(a, num_sms, stream);
     }
+    // Few tokens on raw codes: SM pairs with the weights as the MMA's M side
+    // where they fill the GPU (CIDER_GEMM_ENGINE=single keeps one SM per CTA).
+    if (engine_override() != 1 && gemm_tw_takes_few_tokens(a, num_sms))
+        return launch_gemm_tw(a, num_sms, stream);
     return launch_gemm_tc(a, num_sms, stream);
 }
 

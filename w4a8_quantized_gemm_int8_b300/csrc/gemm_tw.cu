@@ -40,6 +40,7 @@
 // wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 
@@ -51,7 +52,8 @@ namespace cider {
 namespace gemmw {
 
 constexpr int BW = 128;           // weight rows per CTA (MMA M = 256 per pair)
-constexpr int BT = 192;           // tokens per pair tile (MMA N); each CTA loads BT / 2
+constexpr int BT_MANY = 192;      // tokens per pair tile (MMA N) for many tokens
+constexpr int BT_FEW = 128;       // ... and for at most 128 tokens; each CTA loads BT / 2
 constexpr int BK = 64;            // k per block: one 128-byte swizzle row of fp16 tokens
 constexpr int KB_PER_STAGE = 1;   // 64-k blocks per stage (the MMA loop assumes 1)
 constexpr int SK = BK * KB_PER_STAGE;
@@ -59,12 +61,7 @@ constexpr int STAGES = 8 / KB_PER_STAGE;    // shared-memory ring (raw weights +
 constexpr int A_STAGES = 4 / KB_PER_STAGE;  // tensor-memory ring of widened weights
 constexpr int A_STAGE_COLS = SK / 2;  // two fp16 per 32-bit column
 constexpr int NUM_ACC = 2;
-constexpr int ACC_COLS = BT;
-constexpr int A_COL0 = NUM_ACC * ACC_COLS;  // 384
 constexpr int TMEM_COLS = 512;
-static_assert(A_COL0 + A_STAGES * A_STAGE_COLS <= TMEM_COLS, "tensor memory budget");
-constexpr int ACT_BLOCK_BYTES = (BT / 2) * BK * 2;  // one 64-k token block: 12 KB per CTA
-constexpr int ACT_STAGE_BYTES = KB_PER_STAGE * ACT_BLOCK_BYTES;
 constexpr int RAW_STAGE_BYTES = BW * SK;            // 16 KB (INT8; INT4 uses half)
 constexpr int MAX_SEG_KB = 16;    // 16 x 64 = 1024 k per exact fp32 segment
 // Warps 0-3: TMA producer, MMA issuer (and TMEM owner), two idle; warps
@@ -86,8 +83,6 @@ struct Regs {
                       NUM_THREADS * LAUNCH_REGS,
                   "register split exceeds the launch allocation");
 };
-constexpr int COLS = BT / 2;      // tokens per epilogue warp
-constexpr int CHUNKS = COLS / 32; // 32-token output rounds per warp
 constexpr int LD = 16;            // columns per TMEM load of the fold
 constexpr int OUT_WARP_BYTES = 32 * 64;  // staging: 32 tokens x 32 channels fp16
 constexpr int SMEM_LIMIT = 232448;
@@ -108,12 +103,27 @@ struct __align__(8) Barriers {
 };
 static_assert(sizeof(Barriers) <= 512, "barrier area");
 static_assert(STAGES % A_STAGES == 0 && STAGES >= A_STAGES, "A stages follow the ring");
+
+// Shapes that depend on the token tile BT.
+template <int BT>
+struct Tile {
+    static constexpr int ACC_COLS = BT;
+    static constexpr int A_COL0 = NUM_ACC * ACC_COLS;  // 384 for BT 192
+    static_assert(A_COL0 + A_STAGES * A_STAGE_COLS <= TMEM_COLS, "tensor memory budget");
+    static constexpr int ACT_BLOCK_BYTES = (BT / 2) * BK * 2;  // one 64-k token block per CTA
+    static constexpr int ACT_STAGE_BYTES = KB_PER_STAGE * ACT_BLOCK_BYTES;
+    static constexpr int COLS = BT / 2;       // tokens per epilogue warp
+    static constexpr int CHUNKS = COLS / 32;  // 32-token output rounds per warp
+    static_assert(COLS % 32 == 0 && COLS % LD == 0, "epilogue rounds");
+};
 static_assert(SK == 64 || SK == 128, "raw rows of 32 to 128 bytes");
 static_assert(KB_PER_STAGE == 1 && (STAGES & (STAGES - 1)) == 0 &&
                   (A_STAGES & (A_STAGES - 1)) == 0 && (NUM_ACC & (NUM_ACC - 1)) == 0,
               "ring arithmetic by masks");
 
+template <int BT>
 struct SmemLayout {
+    static constexpr int ACT_STAGE_BYTES = Tile<BT>::ACT_STAGE_BYTES;
     static constexpr int raw_off = 0;
     static constexpr int act_off = raw_off + STAGES * RAW_STAGE_BYTES;
     static constexpr int out_off = act_off + STAGES * ACT_STAGE_BYTES;
@@ -136,6 +146,15 @@ struct Params {
     int G;
     int tiles_t, tiles_w;  // token tiles of BT, weight tiles of 2 * BW
     int w_fastest;         // tile order (tile_coords)
+    // Stream-K (per-channel, one token tile): the tiles' k-blocks in tile
+    // order form `units` units; pair c takes [c * units / pairs, (c + 1) *
+    // units / pairs). A tile several pairs share is stored by each CTA as an
+    // int32 partial [part_rows tokens][BW channels] in `part` (slot 0: the
+    // pair's first item, 1: its last) and summed by sk_fixup_pair_kernel.
+    int streamk;
+    int64_t units;
+    int32_t* part;
+    int part_rows;
     const float* s_a;
     const float* s_w;
     void* out;
@@ -155,6 +174,60 @@ enum : uint32_t {
     kSiteDrain = 0x409,
     kSiteProducerDrain = 0x40a,
 };
+
+// A pair's work item: k-blocks [kb0, kb1) of one tile.
+struct Work {
+    int tile, kb0, kb1;
+};
+
+// The items of this pair, in order: whole tiles cluster, + nclusters, ...;
+// or with stream-K (kernels built with SK) its run of units, cut at tile
+// boundaries.
+template <bool SK>
+struct WorkIter {
+    int64_t u, uend;
+    int tile, num_tiles, step, nk;
+    bool sk;
+    __device__ __forceinline__ WorkIter(const Params& p, int cluster, int nclusters, int num_tiles_)
+        : tile(cluster), num_tiles(num_tiles_), step(nclusters), nk(p.num_kb),
+          sk(SK && p.streamk != 0) {
+        u = sk ? (int64_t)cluster * p.units / nclusters : 0;
+        uend = sk ? ((int64_t)cluster + 1) * p.units / nclusters : 0;
+    }
+    __device__ __forceinline__ bool next(Work& w) {
+        if (SK && sk) {
+            if (u >= uend) return false;
+            w.tile = (int)(u / nk);
+            w.kb0 = (int)(u - (int64_t)w.tile * nk);
+            const int64_t left = uend - u;
+            w.kb1 = (left < (int64_t)(nk - w.kb0)) ? w.kb0 + (int)left : nk;
+            u += w.kb1 - w.kb0;
+            return true;
+        }
+        if (tile >= num_tiles) return false;
+        w.tile = tile;
+        w.kb0 = 0;
+        w.kb1 = nk;
+        tile += step;
+        return true;
+    }
+};
+
+// Segments of an item: per-group, one group each (items are whole tiles);
+// per-channel, the item's k-blocks in equal runs of at most MAX_SEG_KB.
+template <GemmMode MODE>
+__device__ __forceinline__ void item_segments(const Params& p, const Work& w, int& seg_kb,
+                                              int& nseg) {
+    if constexpr (MODE == GemmMode::kPgF16 || MODE == GemmMode::kRawPgS32) {
+        seg_kb = p.seg_kb;
+        nseg = p.num_seg;
+    } else {
+        const int len = w.kb1 - w.kb0;
+        const int n = (len + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        seg_kb = (len + n - 1) / n;
+        nseg = (len + seg_kb - 1) / seg_kb;
+    }
+}
 
 // Tile order: weight tiles fastest when the activation image is the larger
 // operand (concurrent clusters then share token tiles, and the activations
@@ -260,13 +333,24 @@ __device__ __forceinline__ void widen_i4x8(uint32_t w, uint32_t* p) {
     }
 }
 
-template <GemmMode MODE, int BITS>
+template <GemmMode MODE, int BITS, int BT>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     gemm_tw_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_y, const Params p) {
+    using SmemLayout = gemmw::SmemLayout<BT>;
+    constexpr int ACC_COLS = Tile<BT>::ACC_COLS;
+    constexpr int A_COL0 = Tile<BT>::A_COL0;
+    constexpr int ACT_BLOCK_BYTES = Tile<BT>::ACT_BLOCK_BYTES;
+    constexpr int ACT_STAGE_BYTES = Tile<BT>::ACT_STAGE_BYTES;
+    constexpr int COLS = Tile<BT>::COLS;
+    constexpr int CHUNKS = Tile<BT>::CHUNKS;
     constexpr int RAW_ROW = (BITS == 8) ? SK : SK / 2;     // raw bytes of one row and stage
     constexpr int RAW_BYTES = BW * RAW_ROW;
+    // Stream-K is built into the few-token per-channel kernels only.
+    constexpr bool kStreamK =
+        (BT == BT_FEW) && (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32);
+    using WorkIter = gemmw::WorkIter<kStreamK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -319,12 +403,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
-            for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+            WorkIter it(p, cluster, nclusters, num_tiles);
+            Work wk;
+            while (it.next(wk)) {
                 int tt, tw;
-                tile_coords(p, tile, tt, tw);
+                tile_coords(p, wk.tile, tt, tw);
                 const int w_row = tw * (2 * BW) + (int)rank * BW;
                 const int t_row = tt * BT + (int)rank * (BT / 2);
-                for (int ks = 0; ks < p.num_kb; ++ks) {
+                for (int ks = wk.kb0; ks < wk.kb1; ++ks) {
                     // The MMAs of the stage's previous use completed: its token
                     // blocks were read, and so was its raw block (the
                     // converters arrive on the full barrier the MMA waited on).
@@ -371,8 +457,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             const uint32_t a_base = tmem_base + A_COL0;
             const uint32_t act_base = smem_u32(smem + SmemLayout::act_off);
             uint32_t u = 0;  // k-blocks issued (the ring position)
-            for (int tile = cluster; tile < num_tiles; tile += nclusters) {
-                for (int kb0 = 0; kb0 < p.num_kb; kb0 += p.seg_kb, ++seg_count) {
+            WorkIter it(p, cluster, nclusters, num_tiles);
+            Work wk;
+            while (it.next(wk)) {
+                int seg_kb, nseg;
+                item_segments<MODE>(p, wk, seg_kb, nseg);
+                (void)nseg;
+                for (int kb0 = wk.kb0; kb0 < wk.kb1; kb0 += seg_kb, ++seg_count) {
                     const uint32_t b = seg_count & (NUM_ACC - 1);
                     const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
                     if (!mbar_wait_bounded(smem_u32(&bars->acc_empty[b]), acc_phase ^ 1,
@@ -380,7 +471,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                         goto mma_done;
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + b * ACC_COLS;
-                    const int kb1 = min(p.num_kb, kb0 + p.seg_kb);
+                    const int kb1 = min(wk.kb1, kb0 + seg_kb);
                     for (int kb = kb0; kb < kb1; ++kb, ++u) {
                         const uint32_t stage = u & (STAGES - 1);
                         if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), (u / STAGES) & 1,
@@ -416,7 +507,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
         const int q = warp & 3;
         const int cg = (warp - 4) >> 2;
         const int r = q * 32 + lane;
-        const int total = ((num_tiles - cluster + nclusters - 1) / nclusters) * p.num_kb;
+        // The pair's k-blocks, in the order the producer loads them.
+        const int total =
+            (kStreamK && p.streamk) ? (int)(((int64_t)cluster + 1) * p.units / nclusters -
+                              (int64_t)cluster * p.units / nclusters)
+                      : ((num_tiles - cluster + nclusters - 1) / nclusters) * p.num_kb;
         for (int u = cg; u < total; u += NUM_CONV_GROUPS) {
             const int stage = u % STAGES, astage = u % A_STAGES;
             const uint32_t phase = (uint32_t)(u / STAGES) & 1u;
@@ -488,11 +583,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
         uint8_t* stage_out = smem + SmemLayout::out_off + ewarp * OUT_WARP_BYTES;
         uint32_t seg_count = 0;
         bool store_pending = false;
+        bool first_item = true;  // stream-K: partial slot 0 for the first item, 1 after
         uint32_t acc[COLS];
 
-        for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+        WorkIter it(p, cluster, nclusters, num_tiles);
+        Work wk;
+        while (it.next(wk)) {
             int tt, tw;
-            tile_coords(p, tile, tt, tw);
+            tile_coords(p, wk.tile, tt, tw);
+            int seg_kb, nseg;
+            item_segments<MODE>(p, wk, seg_kb, nseg);
+            (void)seg_kb;
             const int n_base = tw * (2 * BW) + (int)rank * BW + quad * 32;
             const int n = n_base + lane;                  // this thread's output channel
             const int m_base = tt * BT + half * COLS;     // the warp's first token
@@ -504,13 +605,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
 #pragma unroll
                 for (int j = 0; j < COLS; ++j) acc[j] = 0u;  // f = +0 before the first group
             }
-            for (int seg = 0; seg < p.num_seg; ++seg, ++seg_count) {
+            for (int seg = 0; seg < nseg; ++seg, ++seg_count) {
                 const uint32_t b = seg_count % NUM_ACC;
                 const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
-                const bool last_seg = (seg == p.num_seg - 1);
+                const bool last_seg = (seg == nseg - 1);
                 float sw = sw_next;
                 if constexpr (MODE == GemmMode::kPgF16) {
-                    if (seg + 1 < p.num_seg && n < p.N)
+                    if (seg + 1 < nseg && n < p.N)
                         sw_next = __ldg(p.s_w + (int64_t)n * p.G + seg + 1);
                 }
                 {
@@ -599,7 +700,26 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                 if (lane == 0)
                     mbar_arrive_cluster_relaxed(map_to_rank(smem_u32(&bars->acc_empty[b]), 0));
 
-                if (last_seg) {
+                bool emit = last_seg;
+                if constexpr (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32) {
+                    if (kStreamK && last_seg && p.streamk && (wk.kb0 != 0 || wk.kb1 != p.num_kb)) {
+                        // A tile shared with other pairs: this CTA's int32
+                        // partial, [token][channel] (a warp stores 32
+                        // consecutive channels of a token: 128 bytes); the
+                        // fix-up launch sums the partials and writes y.
+                        const int slot = first_item ? 0 : 1;
+                        int32_t* dst = p.part +
+                                       ((int64_t)blockIdx.x * 2 + slot) * p.part_rows * BW +
+                                       quad * 32 + lane;
+#pragma unroll
+                        for (int j = 0; j < COLS; ++j) {
+                            const int mt = half * COLS + j;  // token within the tile
+                            if (mt < p.part_rows) dst[(int64_t)mt * BW] = (int)acc[j];
+                        }
+                        emit = false;
+                    }
+                }
+                if (emit) {
                     if constexpr (MODE == GemmMode::kRawS32) {
                         if (n < p.N) {
 #pragma unroll
@@ -678,6 +798,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                     }
                 }
             }
+            first_item = false;
         }
     epi_done:
         // Every output store has completed before the CTA exits.
@@ -697,15 +818,116 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Stream-K fix-up of the pair kernel (one token tile, tiles_t == 1): every
+// weight tile that several pairs shared gets, in each of its two 128-channel
+// halves, the sum of the pairs' int32 partials (exact, any order) and the
+// per-channel epilogue y = fp16((float(acc) * s_a[m]) * s_w[n]) computed as
+// in the GEMM epilogue (or the raw int32 sums). One CTA per 32 tokens x 64
+// channels: warp w takes tokens w, w + 8, w + 16, w + 24, lane l channels
+// 2 l and 2 l + 1 (8-byte loads; a warp reads and writes whole runs).
+// ---------------------------------------------------------------------------
+struct FixArgs {
+    const int32_t* part;
+    int part_rows;
+    int64_t units;
+    int pairs;  // clusters of the GEMM launch
+    int num_kb;
+    int M, N;
+    const float* s_a;
+    const float* s_w;
+    void* out;
+    int out_bf16;
+    int raw_s32;
+};
+
+constexpr int FIX_THREADS = 256;
+constexpr int FIX_MAX_CONTRIB = kStreamKMaxCtas / 2 + 2;  // pairs sharing one tile
+constexpr int64_t kStreamKMinGainKb = 24;
+
+// The stream-K pair whose units include unit u (ranges as in WorkIter).
+__device__ __forceinline__ int sk_pair_of_unit(int64_t u, int64_t units, int pairs) {
+    return (int)(((u + 1) * pairs + units - 1) / units) - 1;
+}
+
+__global__ void __launch_bounds__(FIX_THREADS) sk_fixup_pair_kernel(const FixArgs f) {
+    __shared__ const int2* base[FIX_MAX_CONTRIB];  // each contributor's partial half-tile
+    grid_dep_wait();
+    grid_dep_launch();
+    const int chunks = f.part_rows / 32;
+    const int half = blockIdx.x & 1;
+    const int chunk = (blockIdx.x >> 1) % chunks;
+    const int t128 = (blockIdx.x >> 1) / chunks;  // 128-channel tile: pair tile t128 / 2
+    const int tw = t128 >> 1, rank = t128 & 1;
+    const int64_t u0 = (int64_t)tw * f.num_kb;
+    const int p_first = sk_pair_of_unit(u0, f.units, f.pairs);
+    const int p_last = sk_pair_of_unit(u0 + f.num_kb - 1, f.units, f.pairs);
+    if (p_first == p_last) return;  // one pair did the whole tile and wrote it
+    const int nc = p_last - p_first + 1;
+    if ((int)threadIdx.x < nc) {
+        // The tile is pair c's first item (slot 0) exactly when c's run starts
+        // inside it, else its last (slot 1).
+        const int c = p_first + (int)threadIdx.x;
+        const int64_t c_start = (int64_t)c * f.units / f.pairs;
+        const int slot = (c_start / f.num_kb == tw) ? 0 : 1;
+        base[threadIdx.x] = reinterpret_cast<const int2*>(
+            f.part + ((int64_t)(2 * c + rank) * 2 + slot) * f.part_rows * BW + half * 64);
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int acc[4][2] = {};
+#pragma unroll 4
+    for (int i = 0; i < nc; ++i) {
+        int2 v[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            v[r] = __ldcg(base[i] + (int64_t)(chunk * 32 + warp + 8 * r) * (BW / 2) + lane);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            acc[r][0] += v[r].x;
+            acc[r][1] += v[r].y;
+        }
+    }
+    const int n = tw * (2 * BW) + rank * BW + half * 64 + 2 * lane;
+    float w0 = 0.0f, w1 = 0.0f;
+    if (!f.raw_s32) {
+        if (n < f.N) w0 = __ldg(f.s_w + n);
+        if (n + 1 < f.N) w1 = __ldg(f.s_w + n + 1);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int m = chunk * 32 + warp + 8 * r;
+        if (m >= f.M) break;
+        if (f.raw_s32) {
+            int32_t* out = static_cast<int32_t*>(f.out) + (int64_t)m * f.N;
+            if (n < f.N) out[n] = acc[r][0];
+            if (n + 1 < f.N) out[n + 1] = acc[r][1];
+        } else {
+            const float sa = __ldg(f.s_a + m);
+            const uint32_t h = pack2_rn(__fmul_rn(__fmul_rn(__int2float_rn(acc[r][0]), sa), w0),
+                                        __fmul_rn(__fmul_rn(__int2float_rn(acc[r][1]), sa), w1),
+                                        f.out_bf16 != 0);
+            uint16_t* out = static_cast<uint16_t*>(f.out) + (int64_t)m * f.N;
+            if (n + 1 < f.N && (f.N & 1) == 0) {
+                *reinterpret_cast<uint32_t*>(out + n) = h;
+            } else {
+                if (n < f.N) out[n] = (uint16_t)(h & 0xFFFFu);
+                if (n + 1 < f.N) out[n + 1] = (uint16_t)(h >> 16);
+            }
+        }
+    }
+}
+
 }  // namespace gemmw
 
 namespace {
 
-template <GemmMode MODE, int BITS>
+template <GemmMode MODE, int BITS, int BT>
 cudaError_t launch_tw_mode(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty,
-                           const gemmw::Params& p, int num_sms, cudaStream_t stream) {
+                           gemmw::Params p, int32_t* sk_part, int num_sms, cudaStream_t stream) {
     using namespace gemmw;
-    auto kern = gemm_tw_kernel<MODE, BITS>;
+    using SmemLayout = gemmw::SmemLayout<BT>;
+    auto kern = gemm_tw_kernel<MODE, BITS, BT>;
     // Once per device: the register count the role split assumes, the
     // shared-memory opt-in, and how many pairs fit on the GPU at once.
     static PerDevice<int> max_clusters_of;
@@ -729,12 +951,64 @@ cudaError_t launch_tw_mode(const CUtensorMap& tx, const CUtensorMap& tw, const C
     }, &max_clusters);
     if (e != cudaSuccess) return e;
     const int tiles = p.tiles_t * p.tiles_w;
-    const int clusters = tiles < max_clusters ? tiles : max_clusters;
-    return launch_pdl(kern, 2 * clusters, NUM_THREADS, SmemLayout::alloc_bytes, stream, tx, tw, ty,
-                      p);
+    int clusters = tiles < max_clusters ? tiles : max_clusters;
+    // Stream-K (per-channel, one token tile): every pair takes an equal run of
+    // k-blocks, when that shortens the longest pair's run by at least
+    // kStreamKMinGainKb k-blocks (the partial stores and the fix-up launch
+    // cost about as much as 24 k-blocks of a pair: measured at M = 128, whole
+    // tiles win at N10240 K2560, 40 tiles on 74 pairs, 40 against 22
+    // k-blocks; stream-K wins at N2560 K10240 and at N28672 K8192).
+    const bool per_channel = (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32);
+    if (per_channel && sk_part != nullptr && p.tiles_t == 1 && p.num_kb >= 2) {
+        const int64_t units = (int64_t)tiles * p.num_kb;
+        int g = max_clusters < kStreamKMaxCtas / 2 ? max_clusters : kStreamKMaxCtas / 2;
+        if ((int64_t)g > units) g = (int)units;
+        const int64_t dp_kb = (int64_t)((tiles + clusters - 1) / clusters) * p.num_kb;
+        const int64_t sk_kb = (units + g - 1) / g;
+        if (dp_kb - sk_kb >= kStreamKMinGainKb) {
+            p.streamk = 1;
+            p.units = units;
+            clusters = g;
+            p.part = sk_part;
+            p.part_rows = (int)stream_k_part_rows(p.M);
+        }
+    }
+    cudaError_t r = launch_pdl(kern, 2 * clusters, NUM_THREADS, SmemLayout::alloc_bytes, stream,
+                               tx, tw, ty, p);
+    if (r != cudaSuccess || !p.streamk) return r;
+    FixArgs f{};
+    f.part = p.part;
+    f.part_rows = p.part_rows;
+    f.units = p.units;
+    f.pairs = clusters;
+    f.num_kb = p.num_kb;
+    f.M = p.M;
+    f.N = p.N;
+    f.s_a = p.s_a;
+    f.s_w = p.s_w;
+    f.out = p.out;
+    f.out_bf16 = p.out_bf16;
+    f.raw_s32 = (MODE == GemmMode::kRawS32) ? 1 : 0;
+    return launch_pdl(sk_fixup_pair_kernel, 2 * tiles * (p.part_rows / 32) * 2, FIX_THREADS, 0,
+                      stream, f);
 }
 
 }  // namespace
+
+bool gemm_tw_takes_few_tokens(const GemmArgs& a, int num_sms) {
+    using namespace gemmw;
+    if (a.M > BT_FEW || a.b_raw == nullptr || (a.b_bits != 8 && a.b_bits != 4)) return false;
+    if (a.mode == GemmMode::kPcF16) return true;
+    if (a.mode != GemmMode::kPgF16) return false;
+    // Per group (whole tiles only): when the pairs' tiles occupy at least as
+    // many SMs as the single-SM engine's (N = 10240: 80 and 80; N = 2560: 20
+    // against 40).
+    const int64_t pair_ctas = 2 * std::min<int64_t>((a.N + 2 * BW - 1) / (2 * BW), num_sms / 2);
+    const int64_t t128 = (a.N + 127) / 128, t64 = (a.N + 63) / 64;
+    const int64_t single_tiles =
+        ((t128 + num_sms - 1) / num_sms < (t64 + num_sms - 1) / num_sms) ? t128 : t64;
+    return pair_ctas >= std::min<int64_t>(single_tiles, num_sms);
+}
 
 cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     using namespace gemmw;
@@ -744,6 +1018,9 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     if (!a.b_raw || (a.b_bits != 8 && a.b_bits != 4)) return cudaErrorInvalidValue;
     if (a.b_bits == 4 && a.K % 32 != 0) return cudaErrorInvalidValue;
     const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
+    // Token tile: 128 for at most 128 tokens (one tile), else 192.
+    const bool few = a.M <= BT_FEW;
+    const int BT = few ? BT_FEW : BT_MANY;
     CUtensorMap tx, tw, ty;
     const uint64_t row_bytes = a.b_bits == 8 ? (uint64_t)a.K : (uint64_t)a.K / 2;
     const uint32_t raw_row = a.b_bits == 8 ? SK : SK / 2;  // bytes of one row per stage
@@ -791,14 +1068,30 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     p.out_bf16 = a.out_bf16;
     p.timeout_ns = a.timeout_ns;
     p.status = a.status;
-    // Launched for INT8 per-group layers (and their raw int32 test mode): the
+    // Many tokens: INT8 per-group layers (and their raw int32 test mode); the
     // layer call routes every other layer to the fp16-image pair kernel, which
-    // measured faster for them.
+    // measured faster for them. Few tokens: per-channel (with stream-K) and
+    // per-group layers, INT8 or INT4 (gemm_tw_takes_few_tokens).
+    if (few) {
+        if (a.mode == GemmMode::kPcF16)
+            return a.b_bits == 8 ? launch_tw_mode<GemmMode::kPcF16, 8, BT_FEW>(
+                                       tx, tw, ty, p, a.sk_part, num_sms, stream)
+                                 : launch_tw_mode<GemmMode::kPcF16, 4, BT_FEW>(
+                                       tx, tw, ty, p, a.sk_part, num_sms, stream);
+        if (a.mode == GemmMode::kPgF16)
+            return a.b_bits == 8 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW>(
+                                       tx, tw, ty, p, nullptr, num_sms, stream)
+                                 : launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW>(
+                                       tx, tw, ty, p, nullptr, num_sms, stream);
+        return cudaErrorInvalidValue;
+    }
     if (a.b_bits != 8) return cudaErrorInvalidValue;
     if (a.mode == GemmMode::kPgF16)
-        return launch_tw_mode<GemmMode::kPgF16, 8>(tx, tw, ty, p, num_sms, stream);
+        return launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY>(tx, tw, ty, p, nullptr, num_sms,
+                                                             stream);
     if (a.mode == GemmMode::kRawPgS32)
-        return launch_tw_mode<GemmMode::kRawPgS32, 8>(tx, tw, ty, p, num_sms, stream);
+        return launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY>(tx, tw, ty, p, nullptr, num_sms,
+                                                                stream);
     return cudaErrorInvalidValue;
 }
 

@@ -125,6 +125,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& args, int num_sms, cudaStream_t strea
 // into tensor memory, where the tensor core reads them as its A operand; no
 // weight image. For M > 128.
 cudaError_t launch_gemm_tw(const GemmArgs& args, int num_sms, cudaStream_t stream);
+// True when launch_gemm_tw is the better engine for a problem of at most 128
+// tokens (raw INT8 / INT4 codes; per-channel, or per-group when its pair
+// tiles occupy at least as many SMs as the single-SM engine's tiles).
+bool gemm_tw_takes_few_tokens(const GemmArgs& args, int num_sms);
 // Same function on SM pairs (cta_group::2, 256 x 256 tiles); for M > 128.
 cudaError_t launch_gemm_tc_pair(const GemmArgs& args, int num_sms, cudaStream_t stream);
 // Picks the engine for the problem: SM pairs for M > 128, single SMs otherwise
