@@ -77,8 +77,10 @@ def _inputs(M, N, K, seed):
     return li.x.numpy(), li.w.numpy()
 
 
+# The last two take stream-K on SM pairs for per-channel layers (their
+# partial tiles live in the guarded workspace).
 SHAPES = [(130, 257, 1088), (200, 8, 2560), (3, 300, 192), (4, 40, 80), (257, 136, 512),
-          (1, 1000, 2560)]
+          (1, 1000, 2560), (32, 1280, 8192), (77, 2500, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

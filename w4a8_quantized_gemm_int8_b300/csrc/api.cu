@@ -43,28 +43,30 @@ struct Workspace {
     float* s_a;
     __half* b_img;  // fp16 weight image (SM-pair engine, image path only)
     float* s_wT;    // per-group scales, group-major (per-group, engines that read it)
-    int32_t* sk_part;  // stream-K partial tiles (single-SM engine, per channel)
+    int32_t* sk_part;  // stream-K partial tiles (M <= 128, per channel)
 };
 
 // Weight operand of the SM-pair engine (M > 128): INT8 per-group layers take
 // the raw codes, widened on chip into tensor memory (gemm_tw.cu); the other
 // layers take an fp16 weight image written by the operand-image launch
 // (gemm_tc2.cu). Measured on B300 at M = 4096 (public call): per-group gs 64
-// 370 us raw against 493 us with the image, gs 128 296 against 315; per
-// channel 205 against 160 and W4A8 gs 128 (M = 8192) 542 against 443 - the
-// 192-token tiles of the raw engine leave its MMA thread too little slack.
+// 362 us raw against 493 us with the image, gs 128 295 against 315; per
+// channel 200 against 160 and W4A8 gs 128 (M = 8192) 537 against 442 - the
+// raw engine widens each weight k-block once per 192-token tile, the image
+// once per call. Layers of at most 128 tokens always take raw codes.
 bool pair_uses_image(int64_t M, int64_t gs, int bits) {
     return gemm_uses_pair(M) && !(gs > 0 && bits == 8);
 }
 
 // Group-major scale copy: read by the single-SM engine and by the image
-// pair kernel in per-group mode.
+// pair kernel in per-group mode (for M <= 128 allocated whichever engine
+// the launch picks).
 bool uses_scales_t(int64_t M, int64_t gs, int bits) {
     return gs > 0 && (!gemm_uses_pair(M) || pair_uses_image(M, gs, bits));
 }
 
-// Per-channel layers on the single-SM engine split the k-blocks of all
-// tiles evenly over the SMs (stream-K) and need its scratch.
+// Per-channel layers of at most 128 tokens may split the k-blocks of all
+// tiles over the SMs or SM pairs (stream-K) and need its scratch.
 bool uses_stream_k(int64_t M, int64_t gs) { return gs == 0 && !gemm_uses_pair(M); }
 
 // a_img [M,K] fp16 | s_a [M] fp32 | b_img [N,K] fp16 (image path) |

@@ -1,6 +1,8 @@
 // INT8 x INT8 -> INT32 GEMM with fused dequant on single SMs (cta_group::1
-// MMAs): the engine for few tokens (M <= 128), and the tensor-map encoders
-// the engines use.
+// MMAs): a few-token engine (M <= 128; the layer call takes it for the
+// per-group layers whose pair tiles would fill fewer SMs, and for every
+// few-token layer under CIDER_GEMM_ENGINE=single), and the tensor-map
+// encoders the engines use.
 //
 // What it computes (Cider README, sections "Metal Kernel Pipeline" and
 // "Quantization"): acc[m,n] = sum_k q[m,k] * wq[n,k] exactly in int32, then
@@ -35,8 +37,8 @@
 // fetched by cp.async several segments ahead. Every wait is bounded.
 //
 // Work split: per-group layers give whole tiles to CTAs (persistent over
-// tiles). Per-channel layers with fewer tiles than SMs, or a ragged last
-// wave, use stream-K: the tiles' k-blocks in tile order are cut into one
+// tiles). Per-channel layers use stream-K when it shortens the longest
+// CTA's run by at least 12 k-blocks: the tiles' k-blocks in tile order are cut into one
 // equal run per CTA (80 tiles x 40 k-blocks on 148 SMs: 21 or 22 k-blocks
 // each), so a CTA works on the end of one tile and the start of the next;
 // a tile shared by several CTAs is stored by each as an exact int32 partial

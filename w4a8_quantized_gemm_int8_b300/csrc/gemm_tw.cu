@@ -13,7 +13,8 @@
 //
 // Roles are swapped relative to a token-major GEMM: the weights are the MMA's
 // A operand (M = 256 output channels per SM pair, 128 per CTA) and the tokens
-// its B operand (N = 192 tokens per pair tile, 96 loaded by each CTA). The
+// its B operand (N = 192 tokens per pair tile for many tokens, 96 loaded by
+// each CTA; 128 for at most 128 tokens). The
 // tensor core reads A from tensor memory, so the weights never need an fp16
 // copy in shared or global memory: TMA stages each CTA's raw codes (INT8
 // [N,K], or packed INT4 [N,K/2]) as 128 rows x one 64-k block, and four
@@ -35,9 +36,12 @@
 // Epilogue (8 warps: each one TMEM lane quadrant, i.e. 32 output channels,
 // and half of the tile's 192 tokens): segment folds as in the token-major
 // kernels; the final dequant writes 32 tokens x 32 channels per step through
-// shared-memory staging and a TMA store. Persistent over tiles (token tile
-// fastest, so concurrent clusters share weight tiles in L2). Every mbarrier
-// wait is bounded.
+// shared-memory staging and a TMA store. Persistent over tiles (the faster
+// tile index chosen so that concurrent clusters share the larger operand in
+// L2). Few tokens: per-channel layers may instead cut the k-blocks of all
+// tiles into one equal run per pair (stream-K); a tile shared by pairs is
+// stored by each CTA as an int32 partial and summed by
+// sk_fixup_pair_kernel. Every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <algorithm>

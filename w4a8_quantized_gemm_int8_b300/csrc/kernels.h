@@ -101,14 +101,15 @@ struct GemmArgs {
     GemmMode mode;
     uint64_t timeout_ns;
     unsigned long long* status;  // device status word
-    // Raw weight codes instead of b_img (single-SM engine only): INT8 [N, K]
-    // (b_bits 8) or packed INT4 [N, K/2] (b_bits 4), widened on chip.
+    // Raw weight codes instead of b_img: INT8 [N, K] (b_bits 8) or packed
+    // INT4 [N, K/2] (b_bits 4), widened on chip.
     const void* b_raw;
     int b_bits;
     int out_bf16;  // fp16-output modes: write bfloat16 instead of fp16
-    // Stream-K scratch of the single-SM engine (per-channel modes; NULL:
-    // whole tiles per CTA): int32 partial tiles [kStreamKMaxCtas][2][32]
-    // [stream_k_part_rows(M)][4], summed by a fix-up launch after the GEMM.
+    // Stream-K scratch for per-channel layers of at most 128 tokens (NULL:
+    // whole tiles per CTA): per CTA two int32 partial tiles of
+    // stream_k_part_rows(M) x 128 (single-SM engine: [2][32][rows][4]; SM
+    // pairs: [2][rows][128]), summed by a fix-up launch after the GEMM.
     int32_t* sk_part;
 };
 
@@ -123,7 +124,9 @@ inline size_t stream_k_part_bytes(int64_t M) {
 cudaError_t launch_gemm_tc(const GemmArgs& args, int num_sms, cudaStream_t stream);
 // Same function on SM pairs with the raw weight codes (b_raw) widened on chip
 // into tensor memory, where the tensor core reads them as its A operand; no
-// weight image. For M > 128.
+// weight image. INT8 per-group layers of more than 128 tokens (192-token
+// tiles), and the few-token layers gemm_tw_takes_few_tokens picks (128-token
+// tiles).
 cudaError_t launch_gemm_tw(const GemmArgs& args, int num_sms, cudaStream_t stream);
 // True when launch_gemm_tw is the better engine for a problem of at most 128
 // tokens (raw INT8 / INT4 codes; per-channel, or per-group when its pair
@@ -131,11 +134,13 @@ cudaError_t launch_gemm_tw(const GemmArgs& args, int num_sms, cudaStream_t strea
 bool gemm_tw_takes_few_tokens(const GemmArgs& args, int num_sms);
 // Same function on SM pairs (cta_group::2, 256 x 256 tiles); for M > 128.
 cudaError_t launch_gemm_tc_pair(const GemmArgs& args, int num_sms, cudaStream_t stream);
-// Picks the engine for the problem: SM pairs for M > 128, single SMs otherwise
-// (CIDER_GEMM_ENGINE=single|pair in the environment overrides).
+// Picks the engine for the problem: SM pairs for M > 128; for M <= 128 the
+// raw-code pair kernel where gemm_tw_takes_few_tokens says so, single SMs
+// otherwise (CIDER_GEMM_ENGINE=single|pair in the environment overrides:
+// single keeps every M <= 128 problem on single SMs).
 cudaError_t launch_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
-// The engine launch_gemm takes for M tokens: true = SM pairs (needs b_img),
-// false = single SMs (takes raw weight codes).
+// True when launch_gemm takes an M > 128 engine (fp16 weight image, or raw
+// codes for INT8 per-group); false for the few-token engines (raw codes).
 bool gemm_uses_pair(int64_t M);
 
 // ---- M = 1 GEMV (quantizes x per CTA, int32 dot products, same epilogue) ----
