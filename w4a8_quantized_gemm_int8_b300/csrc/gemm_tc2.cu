@@ -72,7 +72,8 @@ template <int BN, int GPB>
 struct Cfg {
     static constexpr int kGroups = GPB;            // groups side by side in one buffer
     static constexpr int kBufCols = kGroups * BN;  // one TMEM accumulator buffer
-    static constexpr int kNumAcc = TMEM_COLS / kBufCols;  // buffers in flight
+    // Buffers in flight: the largest power of two that fits TMEM.
+    static constexpr int kNumAcc = TMEM_COLS / kBufCols >= 4 ? 4 : TMEM_COLS / kBufCols >= 2 ? 2 : 1;
     static constexpr int kCols = BN / 2;           // columns per epilogue warp and group
     static constexpr int kChunks = kCols / 32;     // 32-column TMEM loads per warp and group
     static constexpr int kScaleSet = kGroups * kCols;  // scale floats per warp and segment
@@ -84,9 +85,9 @@ struct Cfg {
     static constexpr int kStages = (SMEM_LIMIT - kFixedBytes) / kStageBytes < MAX_STAGES
                                        ? (SMEM_LIMIT - kFixedBytes) / kStageBytes
                                        : MAX_STAGES;
-    static_assert(kNumAcc * kBufCols == TMEM_COLS && kNumAcc >= 2 && kNumAcc <= MAX_ACC &&
-                      (kNumAcc & (kNumAcc - 1)) == 0,
-                  "accumulator buffers fill TMEM");
+    static_assert(kNumAcc * kBufCols <= TMEM_COLS && kNumAcc >= 2 && kNumAcc <= MAX_ACC &&
+                      (kNumAcc & (kNumAcc - 1)) == 0 && kCols % 32 == 0,
+                  "accumulator buffers fit TMEM");
     static_assert(kStages >= 4, "pipeline depth");
 };
 
@@ -636,7 +637,22 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
         return cudaErrorInvalidValue;
     const bool per_group = (a.mode == GemmMode::kPgF16 || a.mode == GemmMode::kRawPgS32);
     // Tile width and groups per accumulator buffer of the mode's kernel.
-    const int BN = per_group ? PG_BN : 256;
+    // Per-channel tiles are 256 wide, or 192 when that takes no more waves
+    // over the pairs: a 192-wide tile costs about 0.9 of a 256-wide one
+    // (measured; an N = 192 MMA issues close to its execution time), so it
+    // pays only where the 256-wide tiles leave a ragged last wave. Measured
+    // (public call): M = 1024 at N10240 K2560 (216 against 160 tiles, 3
+    // waves of 74 pairs either way) 69.8 -> 67.7 us, M = 256 42.8 -> 41.1;
+    // the gate|up shape M2048 N24576 (14 waves against 11) 306 -> 352 us,
+    // so it stays 256 wide.
+    int BN = per_group ? PG_BN : 256;
+    if (a.mode == GemmMode::kPcF16) {
+        const int64_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+        const int64_t tm = (a.M + 2 * BM - 1) / (2 * BM);
+        const int64_t waves256 = (tm * ((a.N + 255) / 256) + pairs - 1) / pairs;
+        const int64_t waves192 = (tm * ((a.N + 191) / 192) + pairs - 1) / pairs;
+        if (waves192 <= waves256) BN = 192;
+    }
     const int GS = per_group ? PG_GPB : 1;
     CUtensorMap ta, tb, ty;
     if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS ||
@@ -683,7 +699,9 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     p.status = a.status;
     switch (a.mode) {
         case GemmMode::kPcF16:
-            return launch_pair_mode<GemmMode::kPcF16, 256, 1>(ta, tb, ty, p, num_sms, stream);
+            return BN == 192
+                       ? launch_pair_mode<GemmMode::kPcF16, 192, 1>(ta, tb, ty, p, num_sms, stream)
+                       : launch_pair_mode<GemmMode::kPcF16, 256, 1>(ta, tb, ty, p, num_sms, stream);
         case GemmMode::kPgF16:
             return launch_pair_mode<GemmMode::kPgF16, PG_BN, PG_GPB>(ta, tb, ty, p, num_sms,
                                                                      stream);
