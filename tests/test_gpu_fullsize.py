@@ -81,7 +81,7 @@ def test_w8a8_pg_full_size(M, gs):
 
 
 @pytest.mark.parametrize("N,K", [(10240, 2560), (2560, 10240)])
-@pytest.mark.parametrize("M", [1, 1024, 8192])
+@pytest.mark.parametrize("M", [1, 128, 1024, 8192])
 def test_w4a8_full_size(M, N, K):
     wp, s, wpd, sd = _prepared(N, K, 4, 128, 300 + N)
     x = _acts(M, K, 3000 + M + N)

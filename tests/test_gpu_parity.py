@@ -276,6 +276,27 @@ def test_pc_layer_stream_k(M, N, K, bits):
     assert_f16_within_1ulp(host(y), ref, f"stream-K w{bits}")
 
 
+# Per-group layers of at most 128 tokens whose SM-pair tiles fill as many
+# SMs as single-SM tiles would (wide layers) run on SM pairs with 128-token
+# tiles, the weights widened into tensor memory.
+@pytest.mark.parametrize("bits,gs", [(8, 64), (8, 128), (4, 128), (4, 64)])
+@pytest.mark.parametrize("M", [128, 37])
+def test_pg_few_token_layer_on_pairs(M, bits, gs):
+    N, K = 10240, 1024
+    x, w = _layer_inputs(M, N, K, seed=M + gs + bits)
+    if bits == 8:
+        wq, s = oracle.quantize_weight_int8(w, gs)
+        y = cider.w8a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                              cuda(torch.from_numpy(s)), gs)
+        ref = oracle.w8a8_linear(x, wq, s, gs)
+    else:
+        wq, s = oracle.pack_weight_int4(w, gs)
+        y = cider.w4a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                              cuda(torch.from_numpy(s)), gs)
+        ref = oracle.w4a8_linear(x, wq, s, gs)
+    assert_f16_within_1ulp(host(y), ref, f"few-token pg{gs} w{bits} on pairs")
+
+
 @pytest.mark.parametrize("gs", [64, 128])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (3, 300, 1024), (130, 264, 2560),
                                    (5, 260, 1152)])
