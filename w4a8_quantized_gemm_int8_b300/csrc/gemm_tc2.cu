@@ -20,7 +20,9 @@
 // stage barrier; the MMA commits arrive on both CTAs' barriers (multicast);
 // both CTAs' epilogue warps release an accumulator buffer on the even CTA's
 // barrier. Persistent: each cluster walks the tile list with a stride of the
-// number of clusters. Every mbarrier wait is bounded.
+// number of clusters. Per-channel tiles may be 256 x 192 instead (N = 192
+// MMAs), when that needs no more waves over the pairs (the launcher's
+// rule). Every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cstdint>

@@ -132,7 +132,8 @@ cudaError_t launch_gemm_tw(const GemmArgs& args, int num_sms, cudaStream_t strea
 // tokens (raw INT8 / INT4 codes; per-channel, or per-group when its pair
 // tiles occupy at least as many SMs as the single-SM engine's tiles).
 bool gemm_tw_takes_few_tokens(const GemmArgs& args, int num_sms);
-// Same function on SM pairs (cta_group::2, 256 x 256 tiles); for M > 128.
+// Same function on SM pairs (cta_group::2, 256 x 256 tiles, or 256 x 192 for
+// per-channel layers where that takes no more waves); for M > 128.
 cudaError_t launch_gemm_tc_pair(const GemmArgs& args, int num_sms, cudaStream_t stream);
 // Picks the engine for the problem: SM pairs for M > 128; for M <= 128 the
 // raw-code pair kernel where gemm_tw_takes_few_tokens says so, single SMs
