@@ -66,8 +66,9 @@ def parse_args():
     ap.add_argument("--step-only", action="store_true",
                     help="run only the M = 4096 step (a small command for profilers)")
     ap.add_argument("--small-step", action="store_true",
-                    help="run only the few-token per-channel call (M = 128, the single-SM "
-                         "engine): a small command for profilers")
+                    help="run only the few-token per-channel call (M = 128: the SM-pair "
+                         "few-token engine, or the single-SM one with CIDER_GEMM_ENGINE=single): "
+                         "a small command for profilers")
     ap.add_argument("--layer", type=int, nargs=5, metavar=("M", "N", "K", "BITS", "GS"),
                     help="run only the public layer call of this shape (seeded inputs made "
                          "on the GPU): a small command for profilers")
@@ -970,7 +971,7 @@ def run_layer(args, m, n, k, bits, gs):
     scales and activations made on the GPU, `warmup` calls, then `steps`
     calls timed with CUDA events. Prints the mean call time. Small enough to
     run under a profiler (--small-step: m = 128 per channel at N10240 K2560,
-    the single-SM engine)."""
+    the few-token engine)."""
     import torch
     import w4a8_quantized_gemm_int8_b300 as cider
     torch.cuda.set_device(0)
