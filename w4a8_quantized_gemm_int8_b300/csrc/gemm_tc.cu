@@ -94,10 +94,10 @@ __host__ __device__ constexpr int tile_groups(GemmMode mode, int bn) {
 
 // Per-instantiation shape. BSRC: weight operand source, 0 = fp16 image (TMA
 // straight into the operand tile), 8 / 4 = raw INT8 / packed INT4 codes
-// widened on chip. BN: tile width in output channels. An MMA of 128 rows
-// costs the same issue time for any N up to 128, so per-channel tiles are
-// 128 wide; per-group tiles stay 64 wide so that a short K (few tiles) still
-// spreads over the SMs and the per-group fold stays light.
+// widened on chip. BN: tile width in output channels. An MMA of M128 x N64
+// holds the issuing thread almost as long as one of N128 (56 against 65
+// cycles on B300), so per-channel tiles are 128 wide; per-group tiles are
+// 128 or 64 wide (the launcher's wave rule).
 template <int BSRC, int BN, int GROUPS>
 struct Cfg {
     static constexpr bool kRaw = BSRC != 0;
