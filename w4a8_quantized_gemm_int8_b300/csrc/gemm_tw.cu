@@ -219,7 +219,7 @@ struct WorkIter {
 
 // Segments of an item: per-group, one group each (items are whole tiles);
 // per-channel, the item's k-blocks in equal runs of at most MAX_SEG_KB.
-template <GemmMode MODE>
+template <GemmMode MODE, int MAX_SEG>
 __device__ __forceinline__ void item_segments(const Params& p, const Work& w, int& seg_kb,
                                               int& nseg) {
     if constexpr (MODE == GemmMode::kPgF16 || MODE == GemmMode::kRawPgS32) {
@@ -227,7 +227,7 @@ __device__ __forceinline__ void item_segments(const Params& p, const Work& w, in
         nseg = p.num_seg;
     } else {
         const int len = w.kb1 - w.kb0;
-        const int n = (len + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        const int n = (len + MAX_SEG - 1) / MAX_SEG;
         seg_kb = (len + n - 1) / n;
         nseg = (len + seg_kb - 1) / seg_kb;
     }
@@ -346,15 +346,33 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     constexpr int ACC_COLS = Tile<BT>::ACC_COLS;
     constexpr int A_COL0 = Tile<BT>::A_COL0;
     constexpr int ACT_BLOCK_BYTES = Tile<BT>::ACT_BLOCK_BYTES;
-    constexpr int ACT_STAGE_BYTES = Tile<BT>::ACT_STAGE_BYTES;
+    constexpr int ACT_STAGE_BYTES_1 = Tile<BT>::ACT_STAGE_BYTES;  // one 64-k block
     constexpr int COLS = Tile<BT>::COLS;
     constexpr int CHUNKS = Tile<BT>::CHUNKS;
-    constexpr int RAW_ROW = (BITS == 8) ? SK : SK / 2;     // raw bytes of one row and stage
-    constexpr int RAW_BYTES = BW * RAW_ROW;
     // Stream-K is built into the few-token per-channel kernels only.
     constexpr bool kStreamK =
         (BT == BT_FEW) && (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32);
     using WorkIter = gemmw::WorkIter<kStreamK>;
+    // Those kernels also take two 64-k blocks per stage: one barrier wait and
+    // one commit per eight MMAs. (tcgen05.mma holds its issuing thread until
+    // the tensor core takes it, so every wait, commit and loop step of the
+    // MMA thread adds to the time of a k-block.) Their "k-blocks" in Params
+    // (num_kb, segments, stream-K units) count stages of 128 k.
+    constexpr int KPS = kStreamK ? 2 : 1;
+    constexpr int SK = BK * KPS;                  // k per stage
+    constexpr int STAGES = 8 / KPS;               // the same shared-memory bytes
+    constexpr int A_STAGES = 4 / KPS;             // the same tensor-memory columns
+    constexpr int A_STAGE_COLS = SK / 2;
+    constexpr int RAW_STAGE_BYTES = BW * SK;
+    constexpr int MAX_SEG = MAX_SEG_KB / KPS;
+    constexpr int ACT_STAGE_BYTES = KPS * ACT_STAGE_BYTES_1;
+    constexpr int RAW_ROW = (BITS == 8) ? SK : SK / 2;  // raw bytes of one row and stage
+    constexpr int RAW_BYTES = BW * RAW_ROW;
+    static_assert(ACT_STAGE_BYTES == KPS * ACT_BLOCK_BYTES, "token blocks per stage");
+    static_assert(STAGES * RAW_STAGE_BYTES == gemmw::STAGES * gemmw::RAW_STAGE_BYTES &&
+                      STAGES * ACT_STAGE_BYTES == gemmw::STAGES * ACT_STAGE_BYTES_1 &&
+                      A_STAGES * A_STAGE_COLS == gemmw::A_STAGES * gemmw::A_STAGE_COLS,
+                  "the stage rings keep their byte and column budgets");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -428,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                     const uint32_t bf_local = smem_u32(&bars->full[stage]);
                     if (rank == 0) mbar_arrive_expect_tx(bf_local, 2 * ACT_STAGE_BYTES);
 #pragma unroll
-                    for (int j = 0; j < KB_PER_STAGE; ++j)
+                    for (int j = 0; j < KPS; ++j)
                         tma_load_2d_pair(smem_u32(smem + SmemLayout::act_off +
                                                   stage * ACT_STAGE_BYTES + j * ACT_BLOCK_BYTES),
                                          &tmap_x, map_to_rank(bf_local, 0), ks * SK + j * BK,
@@ -465,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             Work wk;
             while (it.next(wk)) {
                 int seg_kb, nseg;
-                item_segments<MODE>(p, wk, seg_kb, nseg);
+                item_segments<MODE, MAX_SEG>(p, wk, seg_kb, nseg);
                 (void)nseg;
                 for (int kb0 = wk.kb0; kb0 < wk.kb1; kb0 += seg_kb, ++seg_count) {
                     const uint32_t b = seg_count & (NUM_ACC - 1);
@@ -482,9 +500,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                                                p.timeout_ns, abort_flag, p.status, kSiteMmaFull))
                             goto mma_done;
                         tc_fence_after();
-                        mma4_pair_a_tmem(d_tmem, a_base + (u & (A_STAGES - 1)) * A_STAGE_COLS,
-                                         smem_desc_sw128_kmajor(act_base + stage * ACT_STAGE_BYTES),
-                                         idesc, kb > kb0 ? 1u : 0u);
+#pragma unroll
+                        for (int j = 0; j < KPS; ++j)
+                            mma4_pair_a_tmem(
+                                d_tmem, a_base + (u & (A_STAGES - 1)) * A_STAGE_COLS + 32 * j,
+                                smem_desc_sw128_kmajor(act_base + stage * ACT_STAGE_BYTES +
+                                                       j * ACT_BLOCK_BYTES),
+                                idesc, (kb > kb0 || j > 0) ? 1u : 0u);
                         issued_any = true;
                         // One commit per k-block releases its shared-memory
                         // stage and its A stage on both CTAs.
@@ -596,7 +618,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             int tt, tw;
             tile_coords(p, wk.tile, tt, tw);
             int seg_kb, nseg;
-            item_segments<MODE>(p, wk, seg_kb, nseg);
+            item_segments<MODE, MAX_SEG>(p, wk, seg_kb, nseg);
             (void)seg_kb;
             const int n_base = tw * (2 * BW) + (int)rank * BW + quad * 32;
             const int n = n_base + lane;                  // this thread's output channel
@@ -962,14 +984,16 @@ cudaError_t launch_tw_mode(const CUtensorMap& tx, const CUtensorMap& tw, const C
     // cost about as much as 24 k-blocks of a pair: measured at M = 128, whole
     // tiles win at N10240 K2560, 40 tiles on 74 pairs, 40 against 22
     // k-blocks; stream-K wins at N2560 K10240 and at N28672 K8192).
+    // (p.num_kb counts stages of two k-blocks in these kernels.)
     const bool per_channel = (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32);
+    const int kps = (BT == BT_FEW && per_channel) ? 2 : 1;
     if (per_channel && sk_part != nullptr && p.tiles_t == 1 && p.num_kb >= 2) {
         const int64_t units = (int64_t)tiles * p.num_kb;
         int g = max_clusters < kStreamKMaxCtas / 2 ? max_clusters : kStreamKMaxCtas / 2;
         if ((int64_t)g > units) g = (int)units;
         const int64_t dp_kb = (int64_t)((tiles + clusters - 1) / clusters) * p.num_kb;
         const int64_t sk_kb = (units + g - 1) / g;
-        if (dp_kb - sk_kb >= kStreamKMinGainKb) {
+        if ((dp_kb - sk_kb) * kps >= kStreamKMinGainKb) {
             p.streamk = 1;
             p.units = units;
             clusters = g;
@@ -1025,9 +1049,12 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     // Token tile: 128 for at most 128 tokens (one tile), else 192.
     const bool few = a.M <= BT_FEW;
     const int BT = few ? BT_FEW : BT_MANY;
+    // k-blocks per stage of the kernel launched: two for the few-token
+    // per-channel kernels, one otherwise.
+    const int kps = (few && !per_group) ? 2 : 1;
     CUtensorMap tx, tw, ty;
     const uint64_t row_bytes = a.b_bits == 8 ? (uint64_t)a.K : (uint64_t)a.K / 2;
-    const uint32_t raw_row = a.b_bits == 8 ? SK : SK / 2;  // bytes of one row per stage
+    const uint32_t raw_row = (a.b_bits == 8 ? SK : SK / 2) * kps;  // bytes of one row per stage
     if (encode_tmap_f16_kmajor(&tx, a.a_img, a.M, a.K, BT / 2, BK) != CUDA_SUCCESS ||
         encode_tmap_u8_2d_swizzled(&tw, a.b_raw, a.N, row_bytes, BW,
                                    raw_row, raw_row == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -1057,7 +1084,10 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         p.seg_kb = a.group_size / BK;
         p.G = p.K / a.group_size;
     } else {
-        const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        // In stages of kps k-blocks; segments of at most MAX_SEG_KB k-blocks.
+        p.num_kb = (p.num_kb + kps - 1) / kps;
+        const int max_seg = MAX_SEG_KB / kps;
+        const int nseg = (p.num_kb + max_seg - 1) / max_seg;
         p.seg_kb = (p.num_kb + nseg - 1) / nseg;
         p.G = 1;
     }
