@@ -337,7 +337,7 @@ __device__ __forceinline__ void widen_i4x8(uint32_t w, uint32_t* p) {
     }
 }
 
-template <GemmMode MODE, int BITS, int BT>
+template <GemmMode MODE, int BITS, int BT, int KPS_>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     gemm_tw_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
@@ -353,12 +353,16 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     constexpr bool kStreamK =
         (BT == BT_FEW) && (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32);
     using WorkIter = gemmw::WorkIter<kStreamK>;
-    // Those kernels also take two 64-k blocks per stage: one barrier wait and
-    // one commit per eight MMAs. (tcgen05.mma holds its issuing thread until
-    // the tensor core takes it, so every wait, commit and loop step of the
-    // MMA thread adds to the time of a k-block.) Their "k-blocks" in Params
-    // (num_kb, segments, stream-K units) count stages of 128 k.
-    constexpr int KPS = kStreamK ? 2 : 1;
+    // KPS 64-k blocks per stage: two for the few-token per-channel kernels
+    // and for per-group layers whose groups are whole stages (a multiple of
+    // 128 k), one otherwise. With two, the MMA thread waits and commits once
+    // per eight MMAs (tcgen05.mma holds its issuing thread until the tensor
+    // core takes it, so every wait, commit and loop step of that thread adds
+    // to the time of a k-block), and the "k-blocks" of Params (num_kb,
+    // segments, stream-K units) count stages of 128 k.
+    constexpr int KPS = KPS_;
+    static_assert(KPS == 1 || KPS == 2, "one or two k-blocks per stage");
+    static_assert(!kStreamK || KPS == 2, "the stream-K kernels take two k-blocks per stage");
     constexpr int SK = BK * KPS;                  // k per stage
     constexpr int STAGES = 8 / KPS;               // the same shared-memory bytes
     constexpr int A_STAGES = 4 / KPS;             // the same tensor-memory columns
@@ -948,12 +952,12 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_pair_kernel(const FixArg
 
 namespace {
 
-template <GemmMode MODE, int BITS, int BT>
+template <GemmMode MODE, int BITS, int BT, int KPS>
 cudaError_t launch_tw_mode(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty,
                            gemmw::Params p, int32_t* sk_part, int num_sms, cudaStream_t stream) {
     using namespace gemmw;
     using SmemLayout = gemmw::SmemLayout<BT>;
-    auto kern = gemm_tw_kernel<MODE, BITS, BT>;
+    auto kern = gemm_tw_kernel<MODE, BITS, BT, KPS>;
     // Once per device: the register count the role split assumes, the
     // shared-memory opt-in, and how many pairs fit on the GPU at once.
     static PerDevice<int> max_clusters_of;
@@ -986,7 +990,7 @@ cudaError_t launch_tw_mode(const CUtensorMap& tx, const CUtensorMap& tw, const C
     // k-blocks; stream-K wins at N2560 K10240 and at N28672 K8192).
     // (p.num_kb counts stages of two k-blocks in these kernels.)
     const bool per_channel = (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32);
-    const int kps = (BT == BT_FEW && per_channel) ? 2 : 1;
+    const int kps = KPS;
     if (per_channel && sk_part != nullptr && p.tiles_t == 1 && p.num_kb >= 2) {
         const int64_t units = (int64_t)tiles * p.num_kb;
         int g = max_clusters < kStreamKMaxCtas / 2 ? max_clusters : kStreamKMaxCtas / 2;
@@ -1050,8 +1054,11 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     const bool few = a.M <= BT_FEW;
     const int BT = few ? BT_FEW : BT_MANY;
     // k-blocks per stage of the kernel launched: two for the few-token
-    // per-channel kernels, one otherwise.
-    const int kps = (few && !per_group) ? 2 : 1;
+    // per-channel kernels and for groups of a multiple of 128 k, else one.
+    const int kps = (few && !per_group) ||
+                            (per_group && a.group_size > 0 && a.group_size % (2 * BK) == 0)
+                        ? 2
+                        : 1;
     CUtensorMap tx, tw, ty;
     const uint64_t row_bytes = a.b_bits == 8 ? (uint64_t)a.K : (uint64_t)a.K / 2;
     const uint32_t raw_row = (a.b_bits == 8 ? SK : SK / 2) * kps;  // bytes of one row per stage
@@ -1081,7 +1088,8 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
             return cudaErrorInvalidValue;
         if (a.group_size / BK > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
-        p.seg_kb = a.group_size / BK;
+        p.num_kb = (p.num_kb + kps - 1) / kps;  // stages (a group is a whole number of them)
+        p.seg_kb = a.group_size / BK / kps;
         p.G = p.K / a.group_size;
     } else {
         // In stages of kps k-blocks; segments of at most MAX_SEG_KB k-blocks.
@@ -1108,24 +1116,34 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     // per-group layers, INT8 or INT4 (gemm_tw_takes_few_tokens).
     if (few) {
         if (a.mode == GemmMode::kPcF16)
-            return a.b_bits == 8 ? launch_tw_mode<GemmMode::kPcF16, 8, BT_FEW>(
+            return a.b_bits == 8 ? launch_tw_mode<GemmMode::kPcF16, 8, BT_FEW, 2>(
                                        tx, tw, ty, p, a.sk_part, num_sms, stream)
-                                 : launch_tw_mode<GemmMode::kPcF16, 4, BT_FEW>(
+                                 : launch_tw_mode<GemmMode::kPcF16, 4, BT_FEW, 2>(
                                        tx, tw, ty, p, a.sk_part, num_sms, stream);
-        if (a.mode == GemmMode::kPgF16)
-            return a.b_bits == 8 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW>(
-                                       tx, tw, ty, p, nullptr, num_sms, stream)
-                                 : launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW>(
-                                       tx, tw, ty, p, nullptr, num_sms, stream);
+        if (a.mode == GemmMode::kPgF16) {
+            if (a.b_bits == 8)
+                return kps == 2 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW, 2>(
+                                      tx, tw, ty, p, nullptr, num_sms, stream)
+                                : launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW, 1>(
+                                      tx, tw, ty, p, nullptr, num_sms, stream);
+            return kps == 2 ? launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW, 2>(
+                                  tx, tw, ty, p, nullptr, num_sms, stream)
+                            : launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW, 1>(
+                                  tx, tw, ty, p, nullptr, num_sms, stream);
+        }
         return cudaErrorInvalidValue;
     }
     if (a.b_bits != 8) return cudaErrorInvalidValue;
     if (a.mode == GemmMode::kPgF16)
-        return launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY>(tx, tw, ty, p, nullptr, num_sms,
-                                                             stream);
+        return kps == 2 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY, 2>(tx, tw, ty, p, nullptr,
+                                                                          num_sms, stream)
+                        : launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY, 1>(tx, tw, ty, p, nullptr,
+                                                                          num_sms, stream);
     if (a.mode == GemmMode::kRawPgS32)
-        return launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY>(tx, tw, ty, p, nullptr, num_sms,
-                                                                stream);
+        return kps == 2 ? launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY, 2>(
+                              tx, tw, ty, p, nullptr, num_sms, stream)
+                        : launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY, 1>(
+                              tx, tw, ty, p, nullptr, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 
