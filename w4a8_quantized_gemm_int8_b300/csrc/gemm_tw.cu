@@ -337,7 +337,7 @@ __device__ __forceinline__ void widen_i4x8(uint32_t w, uint32_t* p) {
     }
 }
 
-template <GemmMode MODE, int BITS, int BT, int KPS_>
+template <GemmMode MODE, int BITS, int BT, int KPS_, int GPS>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     gemm_tw_kernel(const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_w,
@@ -362,6 +362,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     // segments, stream-K units) count stages of 128 k.
     constexpr int KPS = KPS_;
     static_assert(KPS == 1 || KPS == 2, "one or two k-blocks per stage");
+    // GPS = 2: per-group layers of one k-block per group with two k-blocks
+    // per stage, i.e. two groups per stage, each into its own accumulator
+    // buffer; Params count stages in num_kb and groups in num_seg.
+    static_assert(GPS == 1 || (GPS == 2 && KPS == 2 &&
+                               (MODE == GemmMode::kPgF16 || MODE == GemmMode::kRawPgS32)),
+                  "two groups per stage: per-group kernels with two k-blocks per stage");
     static_assert(!kStreamK || KPS == 2, "the stream-K kernels take two k-blocks per stage");
     constexpr int SK = BK * KPS;                  // k per stage
     constexpr int STAGES = 8 / KPS;               // the same shared-memory bytes
@@ -485,7 +491,41 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
             uint32_t u = 0;  // k-blocks issued (the ring position)
             WorkIter it(p, cluster, nclusters, num_tiles);
             Work wk;
-            while (it.next(wk)) {
+            if constexpr (GPS == 2) {
+                // Whole tiles; stage st holds the groups 2 st and 2 st + 1 (an
+                // odd count leaves the last stage's second block, zero-filled
+                // by TMA, without a group).
+                while (it.next(wk)) {
+                    for (int st = wk.kb0; st < wk.kb1; ++st, ++u) {
+                        const uint32_t stage = u & (STAGES - 1);
+                        if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), (u / STAGES) & 1,
+                                               p.timeout_ns, abort_flag, p.status, kSiteMmaFull))
+                            goto mma_done;
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            if (2 * st + j >= p.G) break;
+                            const uint32_t b = seg_count & (NUM_ACC - 1);
+                            const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
+                            if (!mbar_wait_bounded(smem_u32(&bars->acc_empty[b]), acc_phase ^ 1,
+                                                   p.timeout_ns, abort_flag, p.status,
+                                                   kSiteMmaAccEmpty))
+                                goto mma_done;
+                            tc_fence_after();
+                            mma4_pair_a_tmem(
+                                tmem_base + b * ACC_COLS,
+                                a_base + (u & (A_STAGES - 1)) * A_STAGE_COLS + 32 * j,
+                                smem_desc_sw128_kmajor(act_base + stage * ACT_STAGE_BYTES +
+                                                       j * ACT_BLOCK_BYTES),
+                                idesc, 0u);
+                            issued_any = true;
+                            tc_commit_pair_multicast(smem_u32(&bars->acc_full[b]), kPairMask);
+                            ++seg_count;
+                        }
+                        tc_commit_pair_multicast(smem_u32(&bars->empty[stage]), kPairMask);
+                    }
+                }
+            }
+            while (GPS == 1 && it.next(wk)) {
                 int seg_kb, nseg;
                 item_segments<MODE, MAX_SEG>(p, wk, seg_kb, nseg);
                 (void)nseg;
@@ -952,12 +992,12 @@ __global__ void __launch_bounds__(FIX_THREADS) sk_fixup_pair_kernel(const FixArg
 
 namespace {
 
-template <GemmMode MODE, int BITS, int BT, int KPS>
+template <GemmMode MODE, int BITS, int BT, int KPS, int GPS = 1>
 cudaError_t launch_tw_mode(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty,
                            gemmw::Params p, int32_t* sk_part, int num_sms, cudaStream_t stream) {
     using namespace gemmw;
     using SmemLayout = gemmw::SmemLayout<BT>;
-    auto kern = gemm_tw_kernel<MODE, BITS, BT, KPS>;
+    auto kern = gemm_tw_kernel<MODE, BITS, BT, KPS, GPS>;
     // Once per device: the register count the role split assumes, the
     // shared-memory opt-in, and how many pairs fit on the GPU at once.
     static PerDevice<int> max_clusters_of;
@@ -1055,10 +1095,15 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     const int BT = few ? BT_FEW : BT_MANY;
     // k-blocks per stage of the kernel launched: two for the few-token
     // per-channel kernels and for groups of a multiple of 128 k, else one.
-    const int kps = (few && !per_group) ||
-                            (per_group && a.group_size > 0 && a.group_size % (2 * BK) == 0)
-                        ? 2
-                        : 1;
+    // Per-group layers of 64-k groups take two groups per stage (gps 2);
+    // other group sizes that are not a multiple of 128 k keep one k-block
+    // per stage.
+    const int kps =
+        (few && !per_group) ||
+                (per_group && (a.group_size == BK || a.group_size % (2 * BK) == 0))
+            ? 2
+            : 1;
+    const int gps = (per_group && a.group_size == BK) ? 2 : 1;
     CUtensorMap tx, tw, ty;
     const uint64_t row_bytes = a.b_bits == 8 ? (uint64_t)a.K : (uint64_t)a.K / 2;
     const uint32_t raw_row = (a.b_bits == 8 ? SK : SK / 2) * kps;  // bytes of one row per stage
@@ -1088,9 +1133,10 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
             return cudaErrorInvalidValue;
         if (a.group_size / BK > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
-        p.num_kb = (p.num_kb + kps - 1) / kps;  // stages (a group is a whole number of them)
-        p.seg_kb = a.group_size / BK / kps;
+        p.num_kb = (p.num_kb + kps - 1) / kps;  // stages
         p.G = p.K / a.group_size;
+        // Segments (one per group): whole stages, or half a stage with gps 2.
+        p.seg_kb = gps == 2 ? 1 : a.group_size / BK / kps;
     } else {
         // In stages of kps k-blocks; segments of at most MAX_SEG_KB k-blocks.
         p.num_kb = (p.num_kb + kps - 1) / kps;
@@ -1099,7 +1145,7 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         p.seg_kb = (p.num_kb + nseg - 1) / nseg;
         p.G = 1;
     }
-    p.num_seg = (p.num_kb + p.seg_kb - 1) / p.seg_kb;
+    p.num_seg = gps == 2 ? p.G : (p.num_kb + p.seg_kb - 1) / p.seg_kb;
     p.tiles_t = (p.M + BT - 1) / BT;
     p.tiles_w = (p.N + 2 * BW - 1) / (2 * BW);
     p.w_fastest = (2.0 * (double)p.M > (a.b_bits == 8 ? 1.0 : 0.5) * (double)p.N) ? 1 : 0;
@@ -1122,28 +1168,36 @@ cudaError_t launch_gemm_tw(const GemmArgs& a, int num_sms, cudaStream_t stream) 
                                        tx, tw, ty, p, a.sk_part, num_sms, stream);
         if (a.mode == GemmMode::kPgF16) {
             if (a.b_bits == 8)
-                return kps == 2 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW, 2>(
+                return kps == 1 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW, 1>(
                                       tx, tw, ty, p, nullptr, num_sms, stream)
-                                : launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW, 1>(
-                                      tx, tw, ty, p, nullptr, num_sms, stream);
-            return kps == 2 ? launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW, 2>(
+                       : gps == 2 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW, 2, 2>(
+                                        tx, tw, ty, p, nullptr, num_sms, stream)
+                                  : launch_tw_mode<GemmMode::kPgF16, 8, BT_FEW, 2>(
+                                        tx, tw, ty, p, nullptr, num_sms, stream);
+            return kps == 1 ? launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW, 1>(
                                   tx, tw, ty, p, nullptr, num_sms, stream)
-                            : launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW, 1>(
-                                  tx, tw, ty, p, nullptr, num_sms, stream);
+                   : gps == 2 ? launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW, 2, 2>(
+                                    tx, tw, ty, p, nullptr, num_sms, stream)
+                              : launch_tw_mode<GemmMode::kPgF16, 4, BT_FEW, 2>(
+                                    tx, tw, ty, p, nullptr, num_sms, stream);
         }
         return cudaErrorInvalidValue;
     }
     if (a.b_bits != 8) return cudaErrorInvalidValue;
     if (a.mode == GemmMode::kPgF16)
-        return kps == 2 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY, 2>(tx, tw, ty, p, nullptr,
+        return kps == 1 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY, 1>(tx, tw, ty, p, nullptr,
                                                                           num_sms, stream)
-                        : launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY, 1>(tx, tw, ty, p, nullptr,
-                                                                          num_sms, stream);
+               : gps == 2 ? launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY, 2, 2>(
+                                tx, tw, ty, p, nullptr, num_sms, stream)
+                          : launch_tw_mode<GemmMode::kPgF16, 8, BT_MANY, 2>(tx, tw, ty, p, nullptr,
+                                                                            num_sms, stream);
     if (a.mode == GemmMode::kRawPgS32)
-        return kps == 2 ? launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY, 2>(
+        return kps == 1 ? launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY, 1>(
                               tx, tw, ty, p, nullptr, num_sms, stream)
-                        : launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY, 1>(
-                              tx, tw, ty, p, nullptr, num_sms, stream);
+               : gps == 2 ? launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY, 2, 2>(
+                                tx, tw, ty, p, nullptr, num_sms, stream)
+                          : launch_tw_mode<GemmMode::kRawPgS32, 8, BT_MANY, 2>(
+                                tx, tw, ty, p, nullptr, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 
