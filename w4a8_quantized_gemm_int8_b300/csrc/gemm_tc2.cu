@@ -70,7 +70,7 @@ constexpr int PG_GPB = 1;
 //   BN 128, GPB 2 (two buffers):   475 / 382 us
 //   BN 128, GPB 1 (four buffers):  551 / 420 us
 // and at M = 1024 and 8192 the launched shape is the fastest of the three.
-template <int BN, int GPB>
+template <int BN, int GPB, int KPS = 1>
 struct Cfg {
     static constexpr int kGroups = GPB;            // groups side by side in one buffer
     static constexpr int kBufCols = kGroups * BN;  // one TMEM accumulator buffer
@@ -80,8 +80,9 @@ struct Cfg {
     static constexpr int kChunks = kCols / 32;     // 32-column TMEM loads per warp and group
     static constexpr int kScaleSet = kGroups * kCols;  // scale floats per warp and segment
     static constexpr int kBStageBytes = (BN / 2) * BK * 2;
-    static constexpr int kStageTx = 2 * (A_STAGE_BYTES + kBStageBytes);  // both CTAs
-    static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes;
+    // A stage holds KPS 64-k blocks of A and of B.
+    static constexpr int kStageTx = 2 * KPS * (A_STAGE_BYTES + kBStageBytes);  // both CTAs
+    static constexpr int kStageBytes = KPS * (A_STAGE_BYTES + kBStageBytes);
     static constexpr int kFixedBytes =
         NUM_EPI_WARPS * OUT_WARP_BYTES + NUM_EPI_WARPS * 2 * kScaleSet * 4 + 256 + 16 + 1024;
     static constexpr int kStages = (SMEM_LIMIT - kFixedBytes) / kStageBytes < MAX_STAGES
@@ -90,7 +91,7 @@ struct Cfg {
     static_assert(kNumAcc * kBufCols <= TMEM_COLS && kNumAcc >= 2 && kNumAcc <= MAX_ACC &&
                       (kNumAcc & (kNumAcc - 1)) == 0 && kCols % 32 == 0,
                   "accumulator buffers fit TMEM");
-    static_assert(kStages >= 4, "pipeline depth");
+    static_assert(kStages * KPS >= 6, "pipeline depth (k-blocks in flight)");
 };
 
 struct __align__(8) Barriers {
@@ -102,13 +103,13 @@ struct __align__(8) Barriers {
 };
 static_assert(sizeof(Barriers) <= 256, "barrier area");
 
-template <int BN, int GPB>
+template <int BN, int GPB, int KPS = 1>
 struct SmemLayout {
-    using C = Cfg<BN, GPB>;
+    using C = Cfg<BN, GPB, KPS>;
     static constexpr int STAGES = C::kStages;
     static constexpr int a_off = 0;
-    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
-    static constexpr int out_off = b_off + STAGES * C::kBStageBytes;  // per-warp output staging
+    static constexpr int b_off = a_off + STAGES * KPS * A_STAGE_BYTES;
+    static constexpr int out_off = b_off + STAGES * KPS * C::kBStageBytes;  // per-warp output staging
     // Per epilogue warp: two sets of its columns' weight scales.
     static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;
     static constexpr int bar_off = scale_off + NUM_EPI_WARPS * 2 * C::kScaleSet * 4;
@@ -151,13 +152,39 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int& tm, int&
     tn = tile / tiles_m;
 }
 
-template <GemmMode MODE, int BN, int GPB>
+// The four MMAs of one 64-k block on the pair (both operands advance 32 bytes
+// per 16 k within their 128-byte swizzle rows), issued from one asm block;
+// the first accumulates only if `accumulate`.
+__device__ __forceinline__ void mma4_pair_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %5, %6, %3, t;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %7, %8, %3, t;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %9, %10, %3, t;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "l"(a_desc + 2), "l"(b_desc + 2),
+        "l"(a_desc + 4), "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
+        : "memory");
+}
+
+// KPS: 64-k blocks per stage. With two (per-channel modes), the MMA thread
+// waits and commits once per eight MMAs: tcgen05.mma holds its issuing
+// thread until the tensor core takes it, so every wait, commit and loop step
+// of that thread adds to a k-block's time. Params then count stages in
+// num_kb and seg_kb.
+template <GemmMode MODE, int BN, int GPB, int KPS>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_y, const Params p) {
-    using C = Cfg<BN, GPB>;
-    using SmemLayout = gemm2::SmemLayout<BN, GPB>;
+    static_assert(KPS == 1 || (KPS == 2 && GPB == 1 &&
+                               (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32)),
+                  "two k-blocks per stage: per-channel modes");
+    using C = Cfg<BN, GPB, KPS>;
+    using SmemLayout = gemm2::SmemLayout<BN, GPB, KPS>;
     constexpr int STAGES = SmemLayout::STAGES;
     constexpr int COLS = C::kCols;
     constexpr int GS = C::kGroups;
@@ -225,10 +252,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                     const uint32_t fb_local = smem_u32(&bars->full[stage]);
                     if (rank == 0) mbar_arrive_expect_tx(fb_local, C::kStageTx);
                     const uint32_t fb = map_to_rank(fb_local, 0);
-                    tma_load_2d_pair(smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES),
-                                     &tmap_a, fb, kb * BK, a_row);
-                    tma_load_2d_pair(smem_u32(smem + SmemLayout::b_off + stage * C::kBStageBytes),
-                                     &tmap_b, fb, kb * BK, b_row);
+#pragma unroll
+                    for (int j = 0; j < KPS; ++j) {
+                        tma_load_2d_pair(smem_u32(smem + SmemLayout::a_off +
+                                                  (stage * KPS + j) * A_STAGE_BYTES),
+                                         &tmap_a, fb, (kb * KPS + j) * BK, a_row);
+                        tma_load_2d_pair(smem_u32(smem + SmemLayout::b_off +
+                                                  (stage * KPS + j) * C::kBStageBytes),
+                                         &tmap_b, fb, (kb * KPS + j) * BK, b_row);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -273,14 +305,16 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
                                                abort_flag, p.status, kSiteMmaFull))
                             goto mma_done;
                         tc_fence_after();
-                        const uint64_t adesc = smem_desc_sw128_kmajor(
-                            smem_u32(smem + SmemLayout::a_off + stage * A_STAGE_BYTES));
-                        const uint64_t bdesc = smem_desc_sw128_kmajor(
-                            smem_u32(smem + SmemLayout::b_off + stage * C::kBStageBytes));
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k)
-                            tc_mma_f16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                                            (kb > gkb0 || k > 0) ? 1u : 0u);
+                        for (int j = 0; j < KPS; ++j)
+                            mma4_pair_f16(d_tmem,
+                                          smem_desc_sw128_kmajor(smem_u32(
+                                              smem + SmemLayout::a_off +
+                                              (stage * KPS + j) * A_STAGE_BYTES)),
+                                          smem_desc_sw128_kmajor(smem_u32(
+                                              smem + SmemLayout::b_off +
+                                              (stage * KPS + j) * C::kBStageBytes)),
+                                          idesc, (kb > gkb0 || j > 0) ? 1u : 0u);
                         issued_any = true;
                         tc_commit_pair_multicast(smem_u32(&bars->empty[stage]), kPairMask);
                         if (++stage == STAGES) {
@@ -596,12 +630,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
 
 namespace {
 
-template <GemmMode MODE, int BN, int GPB>
+template <GemmMode MODE, int BN, int GPB, int KPS = 1>
 cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                              const gemm2::Params& p, int num_sms, cudaStream_t stream) {
     using namespace gemm2;
-    using SmemLayout = gemm2::SmemLayout<BN, GPB>;
-    auto kern = gemm_tc2_kernel<MODE, BN, GPB>;
+    using SmemLayout = gemm2::SmemLayout<BN, GPB, KPS>;
+    auto kern = gemm_tc2_kernel<MODE, BN, GPB, KPS>;
     // Once per device: the register count the role/epilogue split assumes,
     // the shared-memory opt-in, and how many pairs fit on the GPU at once
     // (SMs pair up within a GPC).
@@ -682,7 +716,11 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
         p.seg_kb = p.group_kb * GS;
         p.G = p.K / a.group_size;
     } else {
-        const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        // The per-channel kernels take two k-blocks per stage: k-blocks are
+        // counted in stages of 128 k from here on.
+        p.num_kb = (p.num_kb + 1) / 2;
+        const int max_seg = MAX_SEG_KB / 2;
+        const int nseg = (p.num_kb + max_seg - 1) / max_seg;
         p.seg_kb = (p.num_kb + nseg - 1) / nseg;
         p.group_kb = p.seg_kb;
         p.G = 1;
@@ -702,13 +740,15 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
     switch (a.mode) {
         case GemmMode::kPcF16:
             return BN == 192
-                       ? launch_pair_mode<GemmMode::kPcF16, 192, 1>(ta, tb, ty, p, num_sms, stream)
-                       : launch_pair_mode<GemmMode::kPcF16, 256, 1>(ta, tb, ty, p, num_sms, stream);
+                       ? launch_pair_mode<GemmMode::kPcF16, 192, 1, 2>(ta, tb, ty, p, num_sms,
+                                                                       stream)
+                       : launch_pair_mode<GemmMode::kPcF16, 256, 1, 2>(ta, tb, ty, p, num_sms,
+                                                                       stream);
         case GemmMode::kPgF16:
             return launch_pair_mode<GemmMode::kPgF16, PG_BN, PG_GPB>(ta, tb, ty, p, num_sms,
                                                                      stream);
         case GemmMode::kRawS32:
-            return launch_pair_mode<GemmMode::kRawS32, 256, 1>(ta, tb, ty, p, num_sms, stream);
+            return launch_pair_mode<GemmMode::kRawS32, 256, 1, 2>(ta, tb, ty, p, num_sms, stream);
         case GemmMode::kRawPgS32:
             return launch_pair_mode<GemmMode::kRawPgS32, PG_BN, PG_GPB>(ta, tb, ty, p, num_sms,
                                                                         stream);
