@@ -170,7 +170,8 @@ __device__ __forceinline__ void mma4_pair_f16(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
-// KPS: 64-k blocks per stage. With two (per-channel modes), the MMA thread
+// KPS: 64-k blocks per stage. With two (per-channel modes, and per-group
+// modes whose groups are whole stages), the MMA thread
 // waits and commits once per eight MMAs: tcgen05.mma holds its issuing
 // thread until the tensor core takes it, so every wait, commit and loop step
 // of that thread adds to a k-block's time. Params then count stages in
@@ -180,9 +181,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(LAUNCH_REGS)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_y, const Params p) {
-    static_assert(KPS == 1 || (KPS == 2 && GPB == 1 &&
-                               (MODE == GemmMode::kPcF16 || MODE == GemmMode::kRawS32)),
-                  "two k-blocks per stage: per-channel modes");
+    static_assert(KPS == 1 || (KPS == 2 && GPB == 1),
+                  "two k-blocks per stage: one group per accumulator buffer");
     using C = Cfg<BN, GPB, KPS>;
     using SmemLayout = gemm2::SmemLayout<BN, GPB, KPS>;
     constexpr int STAGES = SmemLayout::STAGES;
@@ -690,6 +690,12 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
         if (waves192 <= waves256) BN = 192;
     }
     const int GS = per_group ? PG_GPB : 1;
+    // Per-group layers whose groups are a multiple of 128 k take two k-blocks
+    // per stage as well (one group per accumulator buffer).
+    const int pg_kps = (per_group && PG_GPB == 1 && a.group_size > 0 &&
+                        a.group_size % (2 * BK) == 0)
+                           ? 2
+                           : 1;
     CUtensorMap ta, tb, ty;
     if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS ||
         encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN / 2, BK) != CUDA_SUCCESS)
@@ -713,6 +719,10 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
             return cudaErrorInvalidValue;
         if (a.group_size / BK > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
         p.group_kb = a.group_size / BK;
+        if (pg_kps == 2) {  // groups of a multiple of 128 k: whole stages of two k-blocks
+            p.num_kb = (p.num_kb + 1) / 2;
+            p.group_kb /= 2;
+        }
         p.seg_kb = p.group_kb * GS;
         p.G = p.K / a.group_size;
     } else {
@@ -745,11 +755,17 @@ cudaError_t launch_gemm_tc_pair(const GemmArgs& a, int num_sms, cudaStream_t str
                        : launch_pair_mode<GemmMode::kPcF16, 256, 1, 2>(ta, tb, ty, p, num_sms,
                                                                        stream);
         case GemmMode::kPgF16:
+            if (pg_kps == 2)
+                return launch_pair_mode<GemmMode::kPgF16, PG_BN, 1, 2>(ta, tb, ty, p, num_sms,
+                                                                       stream);
             return launch_pair_mode<GemmMode::kPgF16, PG_BN, PG_GPB>(ta, tb, ty, p, num_sms,
                                                                      stream);
         case GemmMode::kRawS32:
             return launch_pair_mode<GemmMode::kRawS32, 256, 1, 2>(ta, tb, ty, p, num_sms, stream);
         case GemmMode::kRawPgS32:
+            if (pg_kps == 2)
+                return launch_pair_mode<GemmMode::kRawPgS32, PG_BN, 1, 2>(ta, tb, ty, p, num_sms,
+                                                                          stream);
             return launch_pair_mode<GemmMode::kRawPgS32, PG_BN, PG_GPB>(ta, tb, ty, p, num_sms,
                                                                         stream);
     }
