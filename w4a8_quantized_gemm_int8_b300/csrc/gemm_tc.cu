@@ -25,12 +25,14 @@
 // all of the bytes, so they are read as their raw codes (INT8 [N,K] or
 // packed INT4 [N,K/2]) and widened to exact fp16 on chip: TMA stages the raw
 // bytes in a deep ring of their own (up to 24 stages) and a warpgroup of
-// converter warps writes the 128-byte-swizzled fp16 operand tile that the
+// converter warps writes the 128-byte-swizzled fp16 operand tiles that the
 // tensor core reads, in a short ring of operand stages beside the
-// activation tiles; no weight image is written to memory. (An fp16 weight
-// image is accepted too.) Warp 0 issues the raw-code TMA (or, with an image,
-// all of it), warp 2 the activation TMA, warp 1 owns TMEM and issues the
-// MMAs (128 x BN x 16, the four of a k-block in one go), warps 4-7 convert,
+// activation tiles; no weight image is written to memory. Each stage of both
+// rings holds two k-blocks of 64 (one "k-step"), so the MMA thread waits and
+// commits once per 128 k. (An fp16 weight image is accepted too, one k-block
+// per stage.) Warp 0 issues the raw-code TMA (or, with an image, all of it),
+// warp 2 the activation TMA, warp 1 owns TMEM and issues the MMAs
+// (128 x BN x 16, the four of a k-block in one go), warps 4-7 convert,
 // warps 8-15 are the epilogue: each owns one TMEM lane quadrant and half of
 // the tile's columns, reads them 32 at a time, and writes fp16 output
 // through 64-byte-swizzled staging and TMA stores. Weight scales are
@@ -38,9 +40,9 @@
 //
 // Work split: per-group layers give whole tiles to CTAs (persistent over
 // tiles). Per-channel layers use stream-K when it shortens the longest
-// CTA's run by at least 12 k-blocks: the tiles' k-blocks in tile order are cut into one
-// equal run per CTA (80 tiles x 40 k-blocks on 148 SMs: 21 or 22 k-blocks
-// each), so a CTA works on the end of one tile and the start of the next;
+// CTA's run by at least 12 k-blocks: the tiles' k-steps in tile order are cut
+// into one equal run per CTA (80 tiles x 20 k-steps on 148 SMs: 10 or 11
+// k-steps each), so a CTA works on the end of one tile and the start of the next;
 // a tile shared by several CTAs is stored by each as an exact int32 partial
 // and summed, in any order, by a fix-up launch that applies the epilogue.
 // Per-group layers cannot be split that way: their result is a rounded fp32
@@ -63,7 +65,14 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;
 static_assert(BK == 64, "a k-block is four MMAs of 16 k");
 constexpr int MAX_STAGES = 8;       // operand stages (activation + fp16 weight tiles)
 constexpr int MAX_RAW_STAGES = 24;  // raw weight-code stages
-constexpr int RAW_AB_STAGES = 4;    // operand stages when the weights arrive raw
+constexpr int RAW_AB_KB = 4;        // operand k-blocks in flight when the weights arrive raw
+// k-blocks per pipeline stage ("k-step"). With raw weight codes a stage holds
+// two: the MMA thread waits on a stage's barriers and commits it once per
+// 128 k, and that per-stage synchronization, not the tensor core, bounds a
+// tile's k loop (an M128 x N128 x K16 MMA takes about 65 cycles, a k-block's
+// barrier waits, commit and loop several hundred). fp16 images keep one per
+// stage: two would leave fewer than four stages in shared memory.
+__host__ __device__ constexpr int stage_kb(int bsrc) { return bsrc != 0 ? 2 : 1; }
 // Warps 0-3: TMA producers (warp 0: weight codes, or both operands from an
 // image; warp 2: activation tiles when the weights arrive raw), MMA issuer
 // and TMEM owner (warp 1); warps 4-7: weight converters (one warpgroup);
@@ -101,6 +110,7 @@ __host__ __device__ constexpr int tile_groups(GemmMode mode, int bn) {
 template <int BSRC, int BN, int GROUPS>
 struct Cfg {
     static constexpr bool kRaw = BSRC != 0;
+    static constexpr int kKps = stage_kb(BSRC);  // k-blocks per stage
     static constexpr int kCols = BN / 2;        // columns per epilogue warp
     static constexpr int kChunks = kCols / 32;  // 32-column TMEM loads per warp and segment
     // Per-group tiles hold kGroups groups' partials side by side in one TMEM
@@ -110,15 +120,20 @@ struct Cfg {
     static constexpr int kBufCols = kGroups * BN;
     static constexpr int kNumAcc = TMEM_COLS / kBufCols;
     static constexpr int kScaleDepth = 2;  // scale sets (one per segment) in flight per warp
-    static constexpr int kBStageBytes = BN * BK * 2;
-    static constexpr int kRawRowBytes = BSRC == 8 ? BK : BK / 2;  // one k-block of one row
+    // A stage holds kKps k-blocks: activation tiles of A_STAGE_BYTES and fp16
+    // weight tiles of kBBlockBytes, each block's tile a whole swizzled operand.
+    static constexpr int kAStageBytes = kKps * A_STAGE_BYTES;
+    static constexpr int kBBlockBytes = BN * BK * 2;
+    static constexpr int kBStageBytes = kKps * kBBlockBytes;
+    // Raw codes of one row for the kKps k-blocks of a stage (row-major, the
+    // blocks side by side).
+    static constexpr int kRawRowBytes = kKps * (BSRC == 8 ? BK : BK / 2);
     static constexpr int kRawBytes = kRaw ? BN * kRawRowBytes : 0;
-    static constexpr int kFullTx = kRaw ? A_STAGE_BYTES : A_STAGE_BYTES + kBStageBytes;
-    static constexpr int kStageBytes = A_STAGE_BYTES + kBStageBytes + kRawBytes;
+    static constexpr int kFullTx = kRaw ? kAStageBytes : kAStageBytes + kBStageBytes;
     static constexpr int kScaleFloats = kScaleDepth * kGroups * kCols;  // per epilogue warp
     static constexpr int kFixedBytes = NUM_EPI_WARPS * OUT_WARP_BYTES +
                                        NUM_EPI_WARPS * kScaleFloats * 4 + 1024 + 16 + 1024;
-    static constexpr int kABBytes = A_STAGE_BYTES + kBStageBytes;
+    static constexpr int kABBytes = kAStageBytes + kBStageBytes;
     static constexpr int kAvail = SMEM_LIMIT - kFixedBytes;
     // Image weights: one ring of operand stages, as deep as fits. Raw codes:
     // the operand ring stays short (its tiles come from L2 or are written on
@@ -126,14 +141,15 @@ struct Cfg {
     // enough weight bytes are in flight from HBM per SM; with one ring for
     // everything (five stages) a few-token layer ran at a fixed number of
     // microseconds per k-block whatever the code width or token count.
-    static constexpr int kStages = kRaw ? RAW_AB_STAGES
+    static constexpr int kStages = kRaw ? RAW_AB_KB / kKps
                                         : (kAvail / kABBytes < MAX_STAGES ? kAvail / kABBytes
                                                                           : MAX_STAGES);
     static constexpr int kRawFit = kRaw ? (kAvail - kStages * kABBytes) / kRawBytes : 0;
     static constexpr int kRawStages = kRawFit < MAX_RAW_STAGES ? kRawFit : MAX_RAW_STAGES;
     static_assert(kNumAcc >= 2 && kNumAcc <= MAX_ACC && kChunks >= 1, "tile width");
-    static_assert(kStages >= 4, "pipeline depth");
+    static_assert(kStages >= 2 && kStages * kKps >= 4, "pipeline depth");
     static_assert(!kRaw || kRawStages >= 4, "raw pipeline depth");
+    static_assert(kRaw || kKps == 1, "image operands stage one k-block");
 };
 
 struct __align__(8) Barriers {
@@ -154,7 +170,7 @@ struct SmemLayout {
     static constexpr int STAGES = C::kStages;
     static constexpr int RAW_STAGES = C::kRawStages;
     static constexpr int a_off = 0;
-    static constexpr int b_off = a_off + STAGES * A_STAGE_BYTES;
+    static constexpr int b_off = a_off + STAGES * C::kAStageBytes;
     static constexpr int raw_off = b_off + STAGES * C::kBStageBytes;
     static constexpr int out_off = raw_off + RAW_STAGES * C::kRawBytes;
     static constexpr int scale_off = out_off + NUM_EPI_WARPS * OUT_WARP_BYTES;
@@ -168,8 +184,9 @@ struct SmemLayout {
 
 struct Params {
     int M, N, K;
-    int num_kb;   // k-blocks of 64
-    int seg_kb;   // k-blocks per segment
+    int num_kb;   // k-steps (stages of stage_kb(BSRC) k-blocks of 64) per tile
+    int num_blk;  // k-blocks of 64 (the last k-step may hold one block past K)
+    int seg_kb;   // k-steps per segment
     int num_seg;  // segments per tile
     int group_kb; // k-blocks per group (per-group; MAX_SEG_KB, no split, per-channel)
     int G;        // columns of s_w (1 for per-channel)
@@ -182,7 +199,7 @@ struct Params {
     int out_bf16;   // output elements are bfloat16 instead of fp16
     uint64_t timeout_ns;
     unsigned long long* status;
-    // Stream-K (per-channel modes): the tiles' num_kb-long k-block runs form
+    // Stream-K (per-channel modes): the tiles' num_kb-long k-step runs form
     // `units` units, CTA c takes units [c * units / grid, (c + 1) * units /
     // grid). A tile that several CTAs share is left to the fix-up kernel:
     // each stores its int32 partial of the tile in `part`.
@@ -205,7 +222,7 @@ enum : uint32_t {
     kSiteConvEmpty = 0x109,
 };
 
-// A CTA's work item: k-blocks [kb0, kb1) of one tile.
+// A CTA's work item: k-steps [kb0, kb1) of one tile.
 struct Work {
     int tile, kb0, kb1;
 };
@@ -246,17 +263,18 @@ __device__ __forceinline__ int sk_cta_of_unit(int64_t u, int64_t units, int grid
 }
 
 // Segments of an item: per-group, the tile's fixed segments (items are whole
-// tiles); per-channel, the item's k-blocks in equal runs of at most
-// MAX_SEG_KB.
-template <GemmMode MODE>
+// tiles); per-channel, the item's k-steps in equal runs of at most
+// MAX_SEG_KB k-blocks.
+template <GemmMode MODE, int KPS>
 __device__ __forceinline__ void item_segments(const Params& p, const Work& w, int& seg_kb,
                                               int& nseg) {
     if constexpr (MODE == GemmMode::kPgF16 || MODE == GemmMode::kRawPgS32) {
         seg_kb = p.seg_kb;
         nseg = p.num_seg;
     } else {
+        constexpr int MAX_SEG = MAX_SEG_KB / KPS;
         const int len = w.kb1 - w.kb0;
-        const int n = (len + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        const int n = (len + MAX_SEG - 1) / MAX_SEG;
         seg_kb = (len + n - 1) / n;
         nseg = (len + seg_kb - 1) / seg_kb;
     }
@@ -344,6 +362,7 @@ __global__ void __maxnreg__(LAUNCH_REGS)
     using C = Cfg<BSRC, BN, GROUPS_>;
     constexpr int STAGES = Layout::STAGES;
     constexpr int RAW_STAGES = Layout::RAW_STAGES > 0 ? Layout::RAW_STAGES : 1;
+    constexpr int KPS = C::kKps;
     constexpr int NUM_ACC = C::kNumAcc;
     constexpr int COLS = C::kCols;
     constexpr int SD = C::kScaleDepth;
@@ -396,8 +415,9 @@ __global__ void __maxnreg__(LAUNCH_REGS)
     if (warp < 4) setmaxnreg_dec<ROLE_REGS>();
     if ((C::kRaw ? warp == 2 : warp == 0) && lane == 0) {
         // -------------------- TMA producer: operand stages --------------------
-        // The activation tile of each k-block, and with an image its fp16
-        // weight tile too, into the operand stage the MMAs of the k-block read.
+        // The activation tiles of each k-step's k-blocks, and with an image
+        // their fp16 weight tiles too, into the operand stage its MMAs read (a
+        // block past K reads as zeros).
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
@@ -412,11 +432,16 @@ __global__ void __maxnreg__(LAUNCH_REGS)
                     goto producer_done;
                 const uint32_t fb = smem_u32(&bars->full[stage]);
                 mbar_arrive_expect_tx(fb, C::kFullTx);
-                tma_load_2d(smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES), &tmap_a, fb,
-                            kb * BK, tm * BM);
-                if constexpr (!C::kRaw)
-                    tma_load_2d(smem_u32(smem + Layout::b_off + stage * C::kBStageBytes), &tmap_b,
-                                fb, kb * BK, tn * BN);
+#pragma unroll
+                for (int j = 0; j < KPS; ++j) {
+                    tma_load_2d(smem_u32(smem + Layout::a_off + stage * C::kAStageBytes +
+                                         j * A_STAGE_BYTES),
+                                &tmap_a, fb, (kb * KPS + j) * BK, tm * BM);
+                    if constexpr (!C::kRaw)
+                        tma_load_2d(smem_u32(smem + Layout::b_off + stage * C::kBStageBytes +
+                                             j * C::kBBlockBytes),
+                                    &tmap_b, fb, (kb * KPS + j) * BK, tn * BN);
+                }
                 ++issued;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -436,7 +461,8 @@ __global__ void __maxnreg__(LAUNCH_REGS)
         }
     } else if (C::kRaw && warp == 0 && lane == 0) {
         // -------------------- TMA producer: raw weight codes -----------------
-        // Runs up to RAW_STAGES k-blocks ahead of the converters.
+        // Runs up to RAW_STAGES k-steps ahead of the converters; one box per
+        // k-step holds BN rows of its KPS k-blocks' codes.
         int rstage = 0;
         uint32_t rphase = 0;
         int issued = 0;
@@ -481,7 +507,7 @@ __global__ void __maxnreg__(LAUNCH_REGS)
             Work w;
             while (it.next(w)) {
                 int seg_kb, nseg;
-                item_segments<MODE>(p, w, seg_kb, nseg);
+                item_segments<MODE, KPS>(p, w, seg_kb, nseg);
                 for (int seg = 0; seg < nseg; ++seg, ++seg_count) {
                     const uint32_t b = seg_count % NUM_ACC;
                     const uint32_t acc_phase = (seg_count / NUM_ACC) & 1;
@@ -492,7 +518,9 @@ __global__ void __maxnreg__(LAUNCH_REGS)
                     const int kb0 = w.kb0 + seg * seg_kb;
                     const int kb1 = min(w.kb1, kb0 + seg_kb);
                     // Group j of the segment accumulates into its own BN
-                    // columns; gpos is the k-block's position in its group.
+                    // columns; gpos is the k-block's position in its group
+                    // (segments start on group boundaries, and a group may
+                    // end inside a k-step).
                     uint32_t d_tmem = tmem_base + b * C::kBufCols;
                     int gpos = 0;
                     for (int kb = kb0; kb < kb1; ++kb) {
@@ -504,15 +532,22 @@ __global__ void __maxnreg__(LAUNCH_REGS)
                                                p.timeout_ns, abort_flag, p.status, kSiteMmaConv))
                             goto mma_done;
                         tc_fence_after();
-                        mma4_f16(d_tmem,
-                                 smem_desc_sw128_kmajor(
-                                     smem_u32(smem + Layout::a_off + stage * A_STAGE_BYTES)),
-                                 smem_desc_sw128_kmajor(
-                                     smem_u32(smem + Layout::b_off + stage * C::kBStageBytes)),
-                                 idesc, gpos > 0 ? 1u : 0u);
-                        if (++gpos == p.group_kb) {
-                            gpos = 0;
-                            d_tmem += BN;
+#pragma unroll
+                        for (int j = 0; j < KPS; ++j) {
+                            if (KPS == 1 || kb * KPS + j < p.num_blk) {
+                                mma4_f16(d_tmem,
+                                         smem_desc_sw128_kmajor(smem_u32(
+                                             smem + Layout::a_off + stage * C::kAStageBytes +
+                                             j * A_STAGE_BYTES)),
+                                         smem_desc_sw128_kmajor(smem_u32(
+                                             smem + Layout::b_off + stage * C::kBStageBytes +
+                                             j * C::kBBlockBytes)),
+                                         idesc, gpos > 0 ? 1u : 0u);
+                                if (++gpos == p.group_kb) {
+                                    gpos = 0;
+                                    d_tmem += BN;
+                                }
+                            }
                         }
                         issued_any = true;
                         tc_commit(smem_u32(&bars->empty[stage]));
@@ -538,13 +573,16 @@ __global__ void __maxnreg__(LAUNCH_REGS)
         setmaxnreg_dec<CONV_REGS>();
         // ------------------------- weight converters --------------------------
         // A stage's raw tile is BN rows of kRawRowBytes, i.e. PPR 16-byte
-        // pieces per row; piece pc covers row pc / PPR, fp16 chunks from
-        // (pc % PPR) * CPP.
+        // pieces per row, PPK of them per k-block. Block j is widened into its
+        // own fp16 operand tile: its piece pc covers row pc / PPK, raw piece
+        // j * PPK + pc % PPK of the row, fp16 chunks from (pc % PPK) * CPP.
         if constexpr (C::kRaw) {
             constexpr int PPR = C::kRawRowBytes / 16;
-            constexpr int CPP = 8 / PPR;
-            constexpr int PER_THREAD = BN * PPR / (32 * NUM_CONV_WARPS);
-            static_assert(PER_THREAD >= 1 && PER_THREAD * 32 * NUM_CONV_WARPS == BN * PPR,
+            constexpr int PPK = PPR / KPS;
+            constexpr int CPP = 8 / PPK;
+            constexpr int PER_THREAD = BN * PPK / (32 * NUM_CONV_WARPS);
+            static_assert(PPK * KPS == PPR && CPP * PPK == 8, "raw pieces per k-block");
+            static_assert(PER_THREAD >= 1 && PER_THREAD * 32 * NUM_CONV_WARPS == BN * PPK,
                           "converter work split");
             const int ct = (warp - 4) * 32 + lane;
             int stage = 0, rstage = 0;
@@ -561,22 +599,30 @@ __global__ void __maxnreg__(LAUNCH_REGS)
                     }
                     const uint4* raw = reinterpret_cast<const uint4*>(
                         smem + Layout::raw_off + rstage * C::kRawBytes);
-                    uint8_t* tile_b = smem + Layout::b_off + stage * C::kBStageBytes;
-                    uint4 pcs[PER_THREAD];
 #pragma unroll
-                    for (int i = 0; i < PER_THREAD; ++i) pcs[i] = raw[ct + i * 32 * NUM_CONV_WARPS];
-                    {
-                        // The fp16 tile of this operand stage is free once the
-                        // MMAs of its previous k-block completed.
-                        const bool ok = mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1,
-                                                          p.timeout_ns, abort_flag, p.status,
-                                                          kSiteConvEmpty);
-                        if (!__all_sync(0xffffffffu, ok)) goto conv_done;
-                    }
+                    for (int j = 0; j < KPS; ++j) {
+                        uint8_t* tile_b =
+                            smem + Layout::b_off + stage * C::kBStageBytes + j * C::kBBlockBytes;
+                        uint4 pcs[PER_THREAD];
 #pragma unroll
-                    for (int i = 0; i < PER_THREAD; ++i) {
-                        const int pc = ct + i * 32 * NUM_CONV_WARPS;
-                        widen_piece<BSRC>(pcs[i], tile_b, pc / PPR, (pc % PPR) * CPP);
+                        for (int i = 0; i < PER_THREAD; ++i) {
+                            const int pc = ct + i * 32 * NUM_CONV_WARPS;
+                            pcs[i] = raw[(pc / PPK) * PPR + j * PPK + pc % PPK];
+                        }
+                        if (j == 0) {
+                            // The fp16 tiles of this operand stage are free once
+                            // the MMAs of its previous k-step completed.
+                            const bool ok =
+                                mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1,
+                                                  p.timeout_ns, abort_flag, p.status,
+                                                  kSiteConvEmpty);
+                            if (!__all_sync(0xffffffffu, ok)) goto conv_done;
+                        }
+#pragma unroll
+                        for (int i = 0; i < PER_THREAD; ++i) {
+                            const int pc = ct + i * 32 * NUM_CONV_WARPS;
+                            widen_piece<BSRC>(pcs[i], tile_b, pc / PPK, (pc % PPK) * CPP);
+                        }
                     }
                     // Order this warp's generic-proxy accesses before the
                     // async proxy's: its fp16 writes before the tensor core's
@@ -672,7 +718,7 @@ __global__ void __maxnreg__(LAUNCH_REGS)
             const int m = m_base + lane;
             const int n_w = tn * BN + half * COLS;
             int seg_kb, nseg;
-            item_segments<MODE>(p, w, seg_kb, nseg);
+            item_segments<MODE, KPS>(p, w, seg_kb, nseg);
             (void)seg_kb;
             if constexpr (MODE == GemmMode::kPgF16) {
 #pragma unroll
@@ -1142,6 +1188,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         const int64_t w64 = ((a.N + 63) / 64 * ((a.M + BM - 1) / BM) + num_sms - 1) / num_sms;
         BN = (w128 < w64) ? 128 : 64;
     }
+    const int kps = stage_kb(bsrc);
     CUtensorMap ta, tb, ty;
     if (encode_tmap_f16_kmajor(&ta, a.a_img, a.M, a.K, BM, BK) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
@@ -1150,9 +1197,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         rb = encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN, BK);
     } else {
         // Raw codes: row n holds K bytes (INT8) or K / 2 bytes (packed INT4);
-        // a box is one k-block of BN rows, unswizzled.
+        // a box is one k-step (kps k-blocks) of BN rows, unswizzled.
         const uint64_t row_bytes = (bsrc == 8) ? (uint64_t)a.K : (uint64_t)a.K / 2;
-        rb = encode_tmap_u8_2d(&tb, a.b_raw, a.N, row_bytes, BN, bsrc == 8 ? BK : BK / 2);
+        rb = encode_tmap_u8_2d(&tb, a.b_raw, a.N, row_bytes, BN,
+                               (uint32_t)(kps * (bsrc == 8 ? BK : BK / 2)));
     }
     if (rb != CUDA_SUCCESS) return cudaErrorInvalidValue;
     const bool f16_out = (a.mode == GemmMode::kPcF16 || a.mode == GemmMode::kPgF16);
@@ -1166,16 +1214,22 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     p.M = (int)a.M;
     p.N = (int)a.N;
     p.K = (int)a.K;
-    p.num_kb = (p.K + BK - 1) / BK;
+    p.num_blk = (p.K + BK - 1) / BK;
+    p.num_kb = (p.num_blk + kps - 1) / kps;
     if (per_group) {
         if (a.group_size <= 0 || a.group_size % BK != 0 || p.K % a.group_size != 0)
             return cudaErrorInvalidValue;
         p.group_kb = a.group_size / BK;
         if (p.group_kb > MAX_SEG_KB) return cudaErrorInvalidValue;  // exact fp32 partials only
-        p.seg_kb = p.group_kb * tile_groups(a.mode, BN);  // groups per segment
+        // A segment is tile_groups groups (an even count), a whole number of
+        // k-steps.
+        const int seg_blk = p.group_kb * tile_groups(a.mode, BN);
+        if (seg_blk % kps != 0) return cudaErrorInvalidValue;
+        p.seg_kb = seg_blk / kps;
         p.G = p.K / a.group_size;
     } else {
-        const int nseg = (p.num_kb + MAX_SEG_KB - 1) / MAX_SEG_KB;
+        const int max_seg = MAX_SEG_KB / kps;
+        const int nseg = (p.num_kb + max_seg - 1) / max_seg;
         p.seg_kb = (p.num_kb + nseg - 1) / nseg;
         // No group split inside a segment: a stream-K item's segments may be
         // longer than those of a whole tile, never longer than MAX_SEG_KB.
@@ -1196,7 +1250,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
     const int tiles = p.tiles_m * p.tiles_n;
     int grid = tiles < num_sms ? tiles : num_sms;
     // Stream-K when whole tiles would leave SMs idle (fewer tiles than SMs,
-    // or a last partial wave): every CTA takes an equal run of k-blocks.
+    // or a last partial wave): every CTA takes an equal run of k-steps.
     // Taken when it shortens the longest CTA's run by at least 12 k-blocks
     // (about the cost of the partial stores and the fix-up launch here:
     // M128 N10240 K2560 went from 32.3 to 28.9 us with 40 against 22).
@@ -1207,7 +1261,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         if ((int64_t)g > units) g = (int)units;
         const int64_t dp_kb = (int64_t)((tiles + grid - 1) / grid) * p.num_kb;
         const int64_t sk_kb = (units + g - 1) / g;
-        if (dp_kb - sk_kb >= 12) {
+        if ((dp_kb - sk_kb) * kps >= 12) {
             p.streamk = 1;
             p.units = units;
             grid = g;
