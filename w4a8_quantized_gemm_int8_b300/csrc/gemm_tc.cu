@@ -125,10 +125,12 @@ struct Cfg {
     static constexpr int kAStageBytes = kKps * A_STAGE_BYTES;
     static constexpr int kBBlockBytes = BN * BK * 2;
     static constexpr int kBStageBytes = kKps * kBBlockBytes;
-    // Raw codes of one row for the kKps k-blocks of a stage (row-major, the
-    // blocks side by side).
-    static constexpr int kRawRowBytes = kKps * (BSRC == 8 ? BK : BK / 2);
-    static constexpr int kRawBytes = kRaw ? BN * kRawRowBytes : 0;
+    // Raw codes of one row and k-block; a raw stage holds the kKps blocks one
+    // after the other, each BN rows of kRawRowBytes (the converters' reads of
+    // a block then cover contiguous bytes, free of bank conflicts).
+    static constexpr int kRawRowBytes = BSRC == 8 ? BK : BK / 2;
+    static constexpr int kRawBlockBytes = kRaw ? BN * kRawRowBytes : 0;
+    static constexpr int kRawBytes = kKps * kRawBlockBytes;
     static constexpr int kFullTx = kRaw ? kAStageBytes : kAStageBytes + kBStageBytes;
     static constexpr int kScaleFloats = kScaleDepth * kGroups * kCols;  // per epilogue warp
     static constexpr int kFixedBytes = NUM_EPI_WARPS * OUT_WARP_BYTES +
@@ -462,7 +464,7 @@ __global__ void __maxnreg__(LAUNCH_REGS)
     } else if (C::kRaw && warp == 0 && lane == 0) {
         // -------------------- TMA producer: raw weight codes -----------------
         // Runs up to RAW_STAGES k-steps ahead of the converters; one box per
-        // k-step holds BN rows of its KPS k-blocks' codes.
+        // k-block of the k-step, BN rows each.
         int rstage = 0;
         uint32_t rphase = 0;
         int issued = 0;
@@ -477,8 +479,11 @@ __global__ void __maxnreg__(LAUNCH_REGS)
                     goto raw_producer_done;
                 const uint32_t rb = smem_u32(&bars->raw_full[rstage]);
                 mbar_arrive_expect_tx(rb, C::kRawBytes);
-                tma_load_2d(smem_u32(smem + Layout::raw_off + rstage * C::kRawBytes), &tmap_b, rb,
-                            kb * C::kRawRowBytes, tn * BN);
+#pragma unroll
+                for (int j = 0; j < KPS; ++j)
+                    tma_load_2d(smem_u32(smem + Layout::raw_off + rstage * C::kRawBytes +
+                                         j * C::kRawBlockBytes),
+                                &tmap_b, rb, (kb * KPS + j) * C::kRawRowBytes, tn * BN);
                 ++issued;
                 if (++rstage == RAW_STAGES) {
                     rstage = 0;
@@ -572,16 +577,14 @@ __global__ void __maxnreg__(LAUNCH_REGS)
     } else if (warp < FIRST_EPI_WARP) {
         setmaxnreg_dec<CONV_REGS>();
         // ------------------------- weight converters --------------------------
-        // A stage's raw tile is BN rows of kRawRowBytes, i.e. PPR 16-byte
-        // pieces per row, PPK of them per k-block. Block j is widened into its
-        // own fp16 operand tile: its piece pc covers row pc / PPK, raw piece
-        // j * PPK + pc % PPK of the row, fp16 chunks from (pc % PPK) * CPP.
+        // Block j of a raw stage is BN rows of kRawRowBytes, i.e. PPK 16-byte
+        // pieces per row, widened into its own fp16 operand tile: its piece
+        // pc covers row pc / PPK, fp16 chunks from (pc % PPK) * CPP.
         if constexpr (C::kRaw) {
-            constexpr int PPR = C::kRawRowBytes / 16;
-            constexpr int PPK = PPR / KPS;
+            constexpr int PPK = C::kRawRowBytes / 16;
             constexpr int CPP = 8 / PPK;
             constexpr int PER_THREAD = BN * PPK / (32 * NUM_CONV_WARPS);
-            static_assert(PPK * KPS == PPR && CPP * PPK == 8, "raw pieces per k-block");
+            static_assert(CPP * PPK == 8, "raw pieces per k-block");
             static_assert(PER_THREAD >= 1 && PER_THREAD * 32 * NUM_CONV_WARPS == BN * PPK,
                           "converter work split");
             const int ct = (warp - 4) * 32 + lane;
@@ -607,7 +610,7 @@ __global__ void __maxnreg__(LAUNCH_REGS)
 #pragma unroll
                         for (int i = 0; i < PER_THREAD; ++i) {
                             const int pc = ct + i * 32 * NUM_CONV_WARPS;
-                            pcs[i] = raw[(pc / PPK) * PPR + j * PPK + pc % PPK];
+                            pcs[i] = raw[j * (BN * PPK) + pc];
                         }
                         if (j == 0) {
                             // The fp16 tiles of this operand stage are free once
@@ -1197,10 +1200,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int num_sms, cudaStream_t stream) 
         rb = encode_tmap_f16_kmajor(&tb, a.b_img, a.N, a.K, BN, BK);
     } else {
         // Raw codes: row n holds K bytes (INT8) or K / 2 bytes (packed INT4);
-        // a box is one k-step (kps k-blocks) of BN rows, unswizzled.
+        // a box is one k-block of BN rows, unswizzled.
         const uint64_t row_bytes = (bsrc == 8) ? (uint64_t)a.K : (uint64_t)a.K / 2;
-        rb = encode_tmap_u8_2d(&tb, a.b_raw, a.N, row_bytes, BN,
-                               (uint32_t)(kps * (bsrc == 8 ? BK : BK / 2)));
+        rb = encode_tmap_u8_2d(&tb, a.b_raw, a.N, row_bytes, BN, bsrc == 8 ? BK : BK / 2);
     }
     if (rb != CUDA_SUCCESS) return cudaErrorInvalidValue;
     const bool f16_out = (a.mode == GemmMode::kPcF16 || a.mode == GemmMode::kPgF16);
