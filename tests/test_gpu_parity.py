@@ -221,6 +221,20 @@ def test_gemm_s32_group_partials(gs, M, K):
     assert np.array_equal(host(part), oracle.gemm_s32(q, w, gs))
 
 
+@pytest.mark.parametrize("gs,M,K", [(64, 40, 192), (64, 3, 320), (192, 40, 576),
+                                    (192, 7, 1344), (192, 140, 576)])
+def test_gemm_s32_group_partials_odd_blocks(gs, M, K):
+    """Per-group partials where K is an odd number of 64-k blocks (the
+    few-token engine stages two blocks at a time: the last stage holds one
+    block past K) and where a 192-k group ends inside a stage."""
+    N = 200
+    q = _codes((M, K), 13)
+    w = _codes((N, K), 14)
+    part = cider.raw_gemm_s32(cuda(torch.from_numpy(q)), cuda(torch.from_numpy(w)), K,
+                               group_size=gs)
+    assert np.array_equal(host(part), oracle.gemm_s32(q, w, gs))
+
+
 @pytest.mark.parametrize("M,N,K", [(130, 300, 512), (40, 300, 96), (1, 77, 224)])
 def test_gemm_s32_int4_weights(M, N, K):
     q = _codes((M, K), 21)
@@ -307,6 +321,27 @@ def test_w8a8_pg_layer(M, N, K, gs):
                           cuda(torch.from_numpy(s)), gs)
     ref = oracle.w8a8_linear(x, wq, s, gs)
     assert_f16_within_1ulp(host(y), ref, f"pg{gs}")
+
+
+@pytest.mark.parametrize("bits,gs,M,N,K", [(8, 64, 40, 300, 192), (8, 64, 100, 300, 320),
+                                            (8, 192, 7, 300, 576), (8, 192, 77, 520, 1344),
+                                            (8, 192, 130, 264, 576), (4, 64, 40, 300, 192),
+                                            (4, 192, 77, 520, 1344)])
+def test_pg_layer_odd_k_blocks(bits, gs, M, N, K):
+    """Per-group layers whose K is an odd number of 64-k blocks, and 192-k
+    groups that end inside one of the few-token engine's two-block stages."""
+    x, w = _layer_inputs(M, N, K, seed=gs + M + bits)
+    if bits == 8:
+        wq, s = oracle.quantize_weight_int8(w, gs)
+        y = cider.w8a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                              cuda(torch.from_numpy(s)), gs)
+        ref = oracle.w8a8_linear(x, wq, s, gs)
+    else:
+        wq, s = oracle.pack_weight_int4(w, gs)
+        y = cider.w4a8_linear(cuda(torch.from_numpy(x)), cuda(torch.from_numpy(wq)),
+                              cuda(torch.from_numpy(s)), gs)
+        ref = oracle.w4a8_linear(x, wq, s, gs)
+    assert_f16_within_1ulp(host(y), ref, f"pg{gs} w{bits} K{K}")
 
 
 @pytest.mark.parametrize("gs", [0, 128, 64])
