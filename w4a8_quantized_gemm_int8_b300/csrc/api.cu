@@ -60,7 +60,7 @@ bool pair_uses_image(int64_t M, int64_t gs, int bits) {
 
 // Group-major scale copy: read by the single-SM engine and by the image
 // pair kernel in per-group mode (for M <= 128 allocated whichever engine
-// the launch picks).
+// the launch picks; written only when that engine reads it).
 bool uses_scales_t(int64_t M, int64_t gs, int bits) {
     return gs > 0 && (!gemm_uses_pair(M) || pair_uses_image(M, gs, bits));
 }
@@ -144,15 +144,8 @@ cider_status cider::linear_call(const void* x, int32_t x_dtype, int64_t M, int64
     unsigned long long* status = nullptr;
     if (device_status_ptr(&status) != cudaSuccess) return CIDER_ERR_CUDA;
 
-    // The activation image (fp16 codes and token scales), and the fp16
-    // weight image where the engine takes one, in one launch; the other
-    // engines widen the raw weight codes on chip.
     Workspace wsp = carve(ws, M, N, K, gs, bits);
     const bool img = wsp.b_img != nullptr;
-    cudaError_t e = launch_operand_images(x, elem(x_dtype), M, K, img ? w : nullptr, bits, N,
-                                          wsp.a_img, wsp.s_a, wsp.b_img, s_w, wsp.s_wT,
-                                          gs > 0 ? K / gs : 1, sms, stream);
-    if (e != cudaSuccess) return from_cuda(e);
     GemmArgs a{};
     a.a_img = wsp.a_img;
     a.b_img = wsp.b_img;
@@ -171,6 +164,16 @@ cider_status cider::linear_call(const void* x, int32_t x_dtype, int64_t M, int64
     a.status = status;
     a.out_bf16 = (y_dtype == CIDER_DTYPE_BF16);
     a.sk_part = wsp.sk_part;
+    // The group-major scale copy only where the chosen engine reads it.
+    float* s_wT = (wsp.s_wT && gemm_reads_scales_t(a, sms)) ? wsp.s_wT : nullptr;
+    a.s_wT = s_wT;
+    // The activation image (fp16 codes and token scales), and the fp16
+    // weight image where the engine takes one, in one launch; the other
+    // engines widen the raw weight codes on chip.
+    cudaError_t e = launch_operand_images(x, elem(x_dtype), M, K, img ? w : nullptr, bits, N,
+                                          wsp.a_img, wsp.s_a, wsp.b_img, s_w, s_wT,
+                                          gs > 0 ? K / gs : 1, sms, stream);
+    if (e != cudaSuccess) return from_cuda(e);
     return from_cuda(launch_gemm(a, sms, stream));
 }
 

@@ -789,6 +789,14 @@ bool gemm_uses_pair(int64_t M) {
     return engine == 2 || (engine == 0 && M > gemm2::BM);
 }
 
+bool gemm_reads_scales_t(const GemmArgs& a, int num_sms) {
+    if (a.mode != GemmMode::kPgF16) return false;
+    // The same choice as launch_gemm: the raw-code pair kernel reads s_w as
+    // it is; the image pair kernel and the single-SM engine read s_wT.
+    if (gemm_uses_pair(a.M)) return a.b_raw == nullptr && a.b_img != nullptr;
+    return !(engine_override() != 1 && gemm_tw_takes_few_tokens(a, num_sms));
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream) {
     if (gemm_uses_pair(a.M)) {
         // Raw weight codes: widened on chip into tensor memory; an fp16

@@ -143,6 +143,10 @@ cudaError_t launch_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
 // True when launch_gemm takes an M > 128 engine (fp16 weight image, or raw
 // codes for INT8 per-group); false for the few-token engines (raw codes).
 bool gemm_uses_pair(int64_t M);
+// True when the engine launch_gemm picks for `args` reads the group-major
+// scale copy s_wT (per-group layers on the image pair kernel or on single
+// SMs); the raw-code pair kernel reads s_w itself.
+bool gemm_reads_scales_t(const GemmArgs& args, int num_sms);
 
 // ---- M = 1 GEMV (quantizes x per CTA, int32 dot products, same epilogue) ----
 struct GemvArgs {
